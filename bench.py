@@ -1,0 +1,382 @@
+"""Benchmark of the owner-side Muon update on GB300.
+
+One step = one pass of the whole update over a batch of synthetic matrices:
+momentum accumulate + pack + norm, Newton-Schulz (5 steps, quintic), and the
+apply W <- W - lr O, through the C ABI (muon_step).
+
+Default workload: 16 square 1024x1024 bf16 gradients N(0, 0.02^2), fp32
+momentum, bf16 weights (the square case where Gram space gives no reduction).
+Other workloads (--config): c3 (32-layer d=4096 / ffn=14336 model, every
+matrix), c4 (512 mixed small matrices), c5_n<N> (1024 x N, batch 8).
+
+Prints one JSON line (rank 0).  `value` is algorithmic TFLOP/s over all ranks
+(symmetric Gram count 3 s^2 l + (4T - 3) s^3 per matrix), with inputs resident
+in HBM; `e2e` is the same metric with the gradients copied from pinned host
+memory and the updated weights copied back inside the timed region.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    """Roofline denominators: MEASURED_PEAKS.json if present, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            flat = {}
+
+            def walk(x, pre=""):
+                if isinstance(x, dict):
+                    for k, v in x.items():
+                        walk(v, f"{pre}{k}.")
+                elif isinstance(x, (int, float)):
+                    flat[pre[:-1]] = float(x)
+            walk(d)
+            hbm = next((v for k, v in flat.items() if "hbm" in k.lower() and "gb" in k.lower()), None)
+            bf = next((v for k, v in flat.items() if "bf16" in k.lower() and "sustain" not in k.lower()
+                       and "tflop" in k.lower()), None)
+            bfs = next((v for k, v in flat.items() if "bf16" in k.lower() and "sustain" in k.lower()), None)
+            if hbm and bf:
+                return {"hbm_gbs": hbm, "bf16_tflops": bf, "bf16_tflops_sustained": bfs or bf,
+                        "source": "measured"}
+        except Exception:
+            pass
+    return dict(FALLBACK, source="fallback")
+
+
+def make_workload(name: str, device):
+    if name == "c2":
+        return synth.c2(device)
+    if name == "c3":
+        return synth.c3(device)
+    if name == "c4":
+        return synth.c4(device)
+    if name.startswith("c5"):
+        n = int(name.split("_n")[1]) if "_n" in name else 4096
+        return synth.c5(device, n=n)
+    raise SystemExit(f"unknown config {name}")
+
+
+WORKLOAD_DESC = {
+    "c2": "16x square 1024x1024 bf16 grads N(0,0.02^2), fp32 momentum, bf16 W, 5 NS steps quintic",
+    "c3": "Llama-style 32 layers d=4096 ffn=14336 (q,k,v,o 4096^2; gate/up 4096x14336; down 14336x4096), "
+          "bf16 grads N(0,1e-6), fp32 momentum, 5 NS steps",
+    "c4": "512 matrices from {256x1024,512x2048,768x3072}, rank-8 + 1e-4 noise, bf16, 5 NS steps",
+}
+
+
+class Clocks:
+    """Samples nvidia-smi every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.out, _ = self.p.communicate(timeout=5)
+            except Exception:
+                self.p.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (getattr(self, "out", "") or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(work, budget_s=15.0, max_mats=None):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload."""
+    import oracle
+    flops = 0.0
+    done = 0
+    t0 = time.perf_counter()
+    order = list(range(len(work.shapes)))
+    for i in order:
+        if max_mats is not None and done >= max_mats:
+            break
+        g = work.grads[i].detach().to("cpu")
+        w = work.weights[i].detach().to("cpu")
+        m, n = work.shapes[i]
+        oracle.muon_update(w, g, np.zeros((m, n)), work.beta, work.lr, work.steps, work.coeffs)
+        s, l = min(m, n), max(m, n)
+        flops += 3.0 * s * s * l + (4 * work.steps - 3) * float(s) ** 3
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    cores = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max(int(x.get("num_threads", 1)) for x in threadpool_info()) or cores
+    except Exception:
+        pass
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {len(work.shapes)} matrices of the same workload, fp64 numpy, "
+                      f"{dt:.1f} s", "seconds": dt, "matrices": done}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    work = make_workload(args.config, "cpu")
+    steps = []
+    per_step_budget = max(5.0, 60.0 / max(args.steps, 1))
+    for _ in range(args.warmup):
+        cpu_baseline(work, budget_s=1.0, max_mats=1)
+    vals = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        r = cpu_baseline(work, budget_s=per_step_budget)
+        vals.append(r)
+        steps.append(r["seconds"])
+    tot_flops = sum(v["value"] * 1e12 * v["seconds"] for v in vals)
+    tot_s = sum(steps)
+    value = tot_flops / tot_s / 1e12
+    line = {
+        "impl": "reference", "metric": "Muon update TFLOP/s (algorithmic, symmetric Gram count)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_s / max(args.steps, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC.get(args.config, args.config), "name": args.config,
+                   "sample": vals[0]["sample"]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": vals[0]["cores"], "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": time.perf_counter() - t_all,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import newton_schulz_04_gb300 as pkg
+    pkg.load(build_if_missing=True)
+    dev = torch.device("cuda", local)
+    work = make_workload(args.config, dev if args.config == "c3" else "cpu")
+    shapes = work.shapes
+    count = len(shapes)
+    W = [w.to(dev) for w in work.weights]
+    G = [g.to(dev) for g in work.grads]
+    Mo = [torch.zeros(g.shape, dtype=torch.float32, device=dev) for g in G]
+    if args.config != "c3":
+        cpu_work = work
+    else:
+        cpu_work = None
+    ws = pkg.new_workspace(pkg.workspace_bytes(shapes, work.steps, work.dtype), dev)
+    flops_step = work.flop_count()
+    in_bytes = sum(g.numel() * g.element_size() for g in G) + sum(m.numel() * 4 for m in Mo) * 2 + \
+        sum(w.numel() * w.element_size() for w in W) * 2
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if in_bytes < 4 * L2_BYTES else None
+    st = torch.cuda.current_stream(dev)
+
+    def step():
+        pkg.muon_step(W, G, Mo, work.beta, work.lr, work.steps, work.coeffs, "auto", ws, st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert pkg.device_status(ws) == 0
+    # ---- device-resident timing; per-launch events on the same stream
+    times = []
+    pkg.profile_enable(True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        for _ in range(args.steps):
+            if flush is not None:
+                flush.zero_()  # evict L2 between timed steps (outside the events)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            step()
+            b.record(st)
+            times.append((a, b))
+        torch.cuda.synchronize()
+    barrier(world)
+    pkg.profile_enable(False)
+    ms = [a.elapsed_time(b) for a, b in times]
+    recs = pkg.profile_records()
+    assert pkg.device_status(ws) == 0
+    t_total = max_over_ranks(sum(ms) / 1e3, world)
+    ms_step = 1e3 * t_total / args.steps
+    value = world * flops_step * args.steps / t_total / 1e12
+    # dominant kernel kind by time
+    by = {}
+    for k, t, fl, byt in recs:
+        d = by.setdefault(k, [0.0, 0, 0.0, 0.0])
+        d[0] += t
+        d[1] += 1
+        d[2] += fl
+        d[3] += byt
+    dom = max(by, key=lambda k: by[k][0])
+    pk = peaks()
+    tot_launch_ms = sum(v[0] for v in by.values())
+    if dom.startswith("tc") or dom.startswith("simt"):
+        achieved = by[dom][2] / (by[dom][0] / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                "peak_source": pk["source"], "launches": by[dom][1],
+                "avg_launch_ms": by[dom][0] / by[dom][1], "share_of_launch_time": by[dom][0] / tot_launch_ms}
+    else:
+        achieved = by[dom][3] / (by[dom][0] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"],
+                "launches": by[dom][1], "avg_launch_ms": by[dom][0] / by[dom][1],
+                "share_of_launch_time": by[dom][0] / tot_launch_ms}
+    kernels = {k: {"launches": v[1], "ms_total": v[0], "share": v[0] / tot_launch_ms,
+                   "tflops": (v[2] / (v[0] / 1e3) / 1e12) if v[2] else None,
+                   "gbs": (v[3] / (v[0] / 1e3) / 1e9) if v[3] else None} for k, v in by.items()}
+    # ---- end to end through the C ABI with host buffers (pinned)
+    Gh = [g.to("cpu").pin_memory() for g in G]
+    Wh = [torch.empty(w.shape, dtype=w.dtype).pin_memory() for w in W]
+    h2d = sum(g.numel() * g.element_size() for g in Gh)
+    d2h = sum(w.numel() * w.element_size() for w in Wh)
+    e2e_ms = []
+    for it in range(args.warmup + args.steps):
+        if flush is not None:
+            flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for g, gh in zip(G, Gh):
+            g.copy_(gh, non_blocking=True)
+        step()
+        for w, wh in zip(W, Wh):
+            wh.copy_(w, non_blocking=True)
+        b.record(st)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_t = max_over_ranks(sum(e2e_ms) / 1e3, world)
+    e2e_val = world * flops_step * args.steps / e2e_t / 1e12
+    launches_per_step = len(recs) / args.steps
+    line = {
+        "metric": "Muon update TFLOP/s (algorithmic, symmetric Gram count)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC.get(args.config, args.config), "name": args.config,
+                   "matrices_per_gpu": count, "l2": "flushed between timed steps" if flush is not None
+                   else "inputs larger than L2", "parallelism": f"replicas x{world}" if world > 1 else "1 gpu"},
+        "matrices_per_s": world * count * args.steps / t_total,
+        "pct_of_bf16_peak": 100.0 * value / pk["bf16_tflops"],
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "roofline": roof,
+        "kernels": kernels,
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": 1e3 * e2e_t / args.steps},
+        "clocks": clk.summary(),
+        "peaks": pk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and cpu_work is not None:
+        line["cpu_baseline"] = cpu_baseline(cpu_work, budget_s=args.cpu_budget)
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline:
+        small = synth.Workload("c3_sample", [(4096, 4096)], [work.grads[0].cpu()], [work.weights[0].cpu()])
+        line["cpu_baseline"] = cpu_baseline(small, budget_s=args.cpu_budget, max_mats=1)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="c2")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

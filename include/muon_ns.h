@@ -1,0 +1,202 @@
+/*
+ * muon_ns.h -- C ABI of the owner-side Muon update for one NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (for each 2D matrix it is given):
+ *
+ *   M  <- beta * M + G                      momentum accumulate (heavy ball)
+ *   X  =  M, or M^T when rows > cols        short side first
+ *   X0 =  X / (||X||_F + 1e-7)
+ *   repeat `steps` times:                   Newton-Schulz (NS) iteration
+ *       X <- a X + b (X X^T) X + c (X X^T)^2 X
+ *   O  =  X (un-transposed)
+ *   W  <- W - lr * O                        scaled apply
+ *
+ * Sources: DMuon technical summary (gist.science, arXiv 2606.27153), §1
+ * "Definizione del Problema" (NS on momentum-aggregated gradients, the product
+ * X X^T needs the whole matrix) and §2.2 "Iterazione Gram Newton-Schulz
+ * Efficiente" (run the iteration on G = X X^T of the short side, compute only
+ * the lower triangle of the symmetric products, batch matrices of the same
+ * shape).  MatrixFSDP technical summary (gist.science, arXiv 2607.05895),
+ * "Metodologia": the owner of a matrix runs this update locally.  The pages do
+ * not fix the momentum form, the normalisation or the apply; the readings
+ * above are the plainest ones.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers to memory the caller owns
+ *    (e.g. torch tensors).  Arrays of pointers (W, grad, mom) and `shapes`
+ *    are HOST arrays.  The library allocates no device memory: scratch comes
+ *    from the caller's workspace `ws` (size from muon_workspace_bytes).
+ *  - Matrices are dense row-major: element (i, j) of an m x n matrix is at
+ *    offset i*n + j.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the call returns before it completes.
+ *  - Argument errors are detected before anything is launched, so a failed
+ *    call writes nothing.  Nothing throws across the ABI.  The message of the
+ *    last error on the calling thread is returned by muon_last_error().
+ *  - A kernel that waits longer than its bound (about a second) on an
+ *    internal barrier stops, records MUON_ERR_TIMEOUT in the workspace's
+ *    status word and returns; muon_device_status() reports it.
+ *  - NaN and Inf in the inputs propagate; they are not checked.
+ *  - Calls that share a workspace must be ordered on one stream.
+ */
+#ifndef MUON_NS_H
+#define MUON_NS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MUON_API __attribute__((visibility("default")))
+#else
+#define MUON_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MUON_OK = 0,
+    MUON_ERR_ARG = 1,          /* null pointer, negative count, bad enum, bad scalar */
+    MUON_ERR_SHAPE = 2,        /* a dimension <= 0 or above MUON_MAX_DIM */
+    MUON_ERR_ALIGN = 3,        /* workspace not 256-byte aligned, or a tensor not aligned to its element size */
+    MUON_ERR_WORKSPACE = 4,    /* ws_bytes too small for even one matrix of a bucket */
+    MUON_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed (message has the CUDA error) */
+    MUON_ERR_TIMEOUT = 6,      /* a kernel's bounded wait ran out (reported by muon_device_status) */
+    MUON_ERR_UNSUPPORTED = 7   /* e.g. no sm_103a device for the tensor-core path */
+} muon_status;
+
+typedef enum {
+    MUON_BF16 = 0,   /* grad, W (and X/out of muon_ns_batched) are bfloat16; momentum is fp32 */
+    MUON_FP32 = 1    /* all tensors fp32; NS computed with fp32 arithmetic */
+} muon_dtype;
+
+typedef enum {
+    MUON_SCHED_AUTO = 0,     /* cheapest schedule that meets the dtype's accuracy (see below) */
+    MUON_SCHED_GRAM_X3 = 1,  /* Gram space; symmetric products with split-bf16 operands (hi*hi + hi*lo + lo*hi) */
+    MUON_SCHED_GRAM_X1 = 2,  /* Gram space; plain bf16 operands (fast mode, larger error) */
+    MUON_SCHED_ORIG = 3      /* original space; bf16 operands, fp32 carry of X */
+} muon_sched;
+
+#define MUON_MAX_DIM 65536   /* largest accepted m or n */
+#define MUON_MAX_STEPS 100   /* largest accepted number of NS steps */
+#define MUON_WS_ALIGN 256    /* required alignment of the workspace pointer */
+
+/*
+ * muon_ns_batched -- NS orthogonalisation of B same-shape matrices.
+ *   X      [B, m, n] contiguous, dtype dt (device, read only).
+ *   B      number of matrices (0 is a no-op).
+ *   m, n   shape of each matrix.
+ *   steps  NS iterations T (0 returns X0, the normalised input).
+ *   coeffs host array {a, b, c}; NULL selects the quintic (3.4445, -4.7750, 2.0315).
+ *   out    [B, m, n] contiguous, dtype dt (device, written; must not overlap X
+ *          or the workspace).  out[i] = O_i as defined above.
+ *   dt, sc dtype and schedule.
+ *   ws, ws_bytes  workspace (device, 256-byte aligned) and its size.  If it
+ *          is smaller than muon_workspace_bytes() for this problem, the batch
+ *          is processed in smaller chunks; below one matrix it is an error.
+ *   stream cudaStream_t.
+ */
+MUON_API muon_status muon_ns_batched(const void* X, int B, int m, int n, int steps,
+                            const float* coeffs, void* out, muon_dtype dt,
+                            muon_sched sc, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * muon_step -- one owner-side Muon step over `count` matrices of any shapes.
+ *   W      host array of `count` device pointers to weights [m_i, n_i], dtype
+ *          dt, updated in place: W <- W - lr * O.
+ *   grad   host array of device pointers to gradients [m_i, n_i], dtype dt (read only).
+ *   mom    host array of device pointers to fp32 momentum [m_i, n_i], updated
+ *          in place: M <- beta*M + G.
+ *   shapes host int64 array {m_0, n_0, m_1, n_1, ...}.
+ *   Matrices are grouped by (short side, long side); each group is run as one
+ *   batch (wider groups are split to fit the workspace).  W, grad and mom of
+ *   different matrices must not overlap.
+ *   The remaining arguments are as for muon_ns_batched.
+ */
+MUON_API muon_status muon_step(void* const* W, const void* const* grad, float* const* mom,
+                      const int64_t* shapes, int count, float beta, float lr, int steps,
+                      const float* coeffs, muon_dtype dt, muon_sched sc,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * muon_workspace_bytes -- workspace that lets every shape group of the given
+ * matrices run as one batch (capped at 256 matrices per batch) with schedule
+ * `sc` (AUTO resolved per group as the library would).  Returns 0 on bad
+ * arguments (see muon_last_error).
+ */
+MUON_API size_t muon_workspace_bytes(const int64_t* shapes, int count, int steps,
+                            muon_dtype dt, muon_sched sc);
+
+/*
+ * muon_resolve_schedule -- the schedule AUTO picks for one s x l group
+ * (s <= l) with `steps` iterations.  Host only.
+ */
+MUON_API muon_sched muon_resolve_schedule(int64_t m, int64_t n, int steps, muon_dtype dt, muon_sched sc);
+
+/*
+ * muon_bucket_plan -- the grouping muon_step uses, for inspection.  Fills
+ * order[count] with matrix indices (groups by increasing (short, long) key,
+ * members in input order) and group_start[count+1] with the offsets of each
+ * group in `order`; returns the number of groups, or -1 on bad arguments.
+ * Host only, no GPU needed.
+ */
+MUON_API int muon_bucket_plan(const int64_t* shapes, int count, int* order, int* group_start);
+
+/*
+ * muon_device_status -- synchronise `stream`, then read and clear the status
+ * word of workspace `ws`.  Returns MUON_ERR_TIMEOUT if a kernel gave up on a
+ * bounded wait since the last check, MUON_ERR_CUDA on a CUDA error, else MUON_OK.
+ */
+MUON_API muon_status muon_device_status(void* ws, void* stream);
+
+/*
+ * muon_debug_bounded_wait -- failure-detection self-test: launches one block
+ * that waits on an on-chip barrier nobody arrives at, with a bound of
+ * `max_cycles` SM cycles, records MUON_ERR_TIMEOUT in the workspace status
+ * word and returns.  Used by the tests to check that a timed-out wait is
+ * reported and leaves the context usable.
+ */
+MUON_API muon_status muon_debug_bounded_wait(void* ws, long long max_cycles, void* stream);
+
+/*
+ * muon_debug_gemm -- test hook exposing one batched GEMM kernel on its own.
+ *   out[b] (fp32, [M, N] row-major, ld = N) = A[b] * op(B[b]) with
+ *   A [M, K] row-major and B either [N, K] row-major (b_mn = 0, out = A B^T)
+ *   or [K, N] row-major (b_mn = 1, out = A B).  Batch strides are M*K, N*K
+ *   (or K*N) and M*N elements.  dt = MUON_BF16 runs the tcgen05 tensor-core
+ *   kernel (split = 1: A, B; split = 3: A = A + A_lo, B = B + B_lo with the
+ *   three-product split; A_lo/B_lo ignored for split 1); dt = MUON_FP32 runs
+ *   the FFMA kernel (A, B fp32).  sym = 1 (M == N) computes only the lower
+ *   triangle and mirrors it.  Sizes: bf16 needs M % 128, N % 256, K % 64 == 0;
+ *   fp32 needs M, N % 128 and K % 16 == 0.  Synchronous error checking only;
+ *   the kernel is enqueued on `stream`.
+ */
+MUON_API muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, const void* B_lo, int batch,
+                                     int M, int N, int K, int split, int b_mn, int sym, muon_dtype dt,
+                                     float* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Launch profiling (process-wide, not thread safe; off by default).
+ * muon_profile_enable(1) clears the record list and starts recording a pair of
+ * CUDA events around every kernel the library enqueues (on the caller's
+ * stream); muon_profile_enable(0) stops.  muon_profile_get(i, ...) waits for
+ * record i and returns its kernel kind ("pack", "tc_syrk", "tc_sym",
+ * "tc_rect", ...), elapsed milliseconds, and the launch's algorithmic flops and
+ * HBM bytes (symmetric products counted once).
+ */
+MUON_API void muon_profile_enable(int on);
+MUON_API int muon_profile_count(void);
+MUON_API muon_status muon_profile_get(int i, const char** kind, float* ms, double* flops, double* bytes);
+
+/* Thread-local message of the last failed call on this thread ("" if none). */
+MUON_API const char* muon_last_error(void);
+
+/* Library version string. */
+MUON_API const char* muon_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_NS_H */

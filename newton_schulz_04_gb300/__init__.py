@@ -1,0 +1,10 @@
+"""Owner-side Muon update for one GB300 (sm_103a): momentum accumulate,
+Newton-Schulz orthogonalisation in Gram or original space on tcgen05 tensor
+cores, and the scaled apply, behind the C ABI in include/muon_ns.h.
+
+Importing the package does not load the CUDA library; the first call does.
+"""
+from .binding import (  # noqa: F401
+    MuonError, MuonUpdater, bucket_plan, debug_bounded_wait, debug_gemm, device_status, library_path, load, muon_step,
+    new_workspace, ns_batched, profile_enable, profile_records, resolve_schedule, workspace_bytes,
+)

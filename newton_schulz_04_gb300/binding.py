@@ -1,0 +1,258 @@
+"""ctypes binding of libmuon_ns.so (argument marshalling only).
+
+Every step of the update runs in the library's CUDA kernels.  PyTorch is used
+here only to own device memory (the workspace, outputs) and to name the CUDA
+stream.  There is no fallback: if the library is missing or the device is not
+an sm_103 GPU the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+import torch
+
+from . import build as _build
+
+OK, ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = range(8)
+STATUS_NAMES = ["OK", "ERR_ARG", "ERR_SHAPE", "ERR_ALIGN", "ERR_WORKSPACE", "ERR_CUDA", "ERR_TIMEOUT",
+                "ERR_UNSUPPORTED"]
+BF16, FP32 = 0, 1
+SCHED = {"auto": 0, "gram_x3": 1, "gram_x1": 2, "orig": 3}
+SCHED_NAMES = {v: k for k, v in SCHED.items()}
+WS_ALIGN = 256
+
+_lib = None
+
+
+class MuonError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        self.status = status
+        super().__init__(f"{STATUS_NAMES[status] if 0 <= status < 8 else status}: {msg}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load the in-tree shared library (optionally building it first)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"{path} is missing: run newton_schulz_04_gb300.build.build() first")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    vp, sz, i32, i64, f32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    fptr = ctypes.POINTER(ctypes.c_float)
+    lib.muon_ns_batched.argtypes = [vp, i32, i32, i32, i32, fptr, vp, i32, i32, vp, sz, vp]
+    lib.muon_ns_batched.restype = i32
+    lib.muon_step.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64), i32,
+                              f32, f32, i32, fptr, i32, i32, vp, sz, vp]
+    lib.muon_step.restype = i32
+    lib.muon_workspace_bytes.argtypes = [ctypes.POINTER(i64), i32, i32, i32, i32]
+    lib.muon_workspace_bytes.restype = sz
+    lib.muon_resolve_schedule.argtypes = [i64, i64, i32, i32, i32]
+    lib.muon_resolve_schedule.restype = i32
+    lib.muon_bucket_plan.argtypes = [ctypes.POINTER(i64), i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.muon_bucket_plan.restype = i32
+    lib.muon_device_status.argtypes = [vp, vp]
+    lib.muon_device_status.restype = i32
+    lib.muon_debug_bounded_wait.argtypes = [vp, ctypes.c_longlong, vp]
+    lib.muon_debug_bounded_wait.restype = i32
+    lib.muon_debug_gemm.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp]
+    lib.muon_debug_gemm.restype = i32
+    lib.muon_profile_enable.argtypes = [i32]
+    lib.muon_profile_enable.restype = None
+    lib.muon_profile_count.argtypes = []
+    lib.muon_profile_count.restype = i32
+    lib.muon_profile_get.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float),
+                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+    lib.muon_profile_get.restype = i32
+    lib.muon_last_error.argtypes = []
+    lib.muon_last_error.restype = ctypes.c_char_p
+    lib.muon_version.argtypes = []
+    lib.muon_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != OK:
+        raise MuonError(status, load().muon_last_error().decode())
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return BF16
+    if dt == torch.float32:
+        return FP32
+    raise TypeError(f"unsupported dtype {dt}: bfloat16 or float32")
+
+
+def _shapes_arr(shapes):
+    flat = [int(v) for mn in shapes for v in mn]
+    return (ctypes.c_int64 * max(len(flat), 1))(*flat)
+
+
+def _coeffs(coeffs):
+    if coeffs is None:
+        return None
+    return (ctypes.c_float * 3)(*[float(c) for c in coeffs])
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def workspace_bytes(shapes, steps=5, dtype=torch.bfloat16, schedule="auto") -> int:
+    lib = load()
+    n = lib.muon_workspace_bytes(_shapes_arr(shapes), len(shapes), int(steps), _dtype_code(dtype), SCHED[schedule])
+    if n == 0:
+        raise MuonError(ERR_ARG, lib.muon_last_error().decode())
+    return int(n)
+
+
+def resolve_schedule(m, n, steps=5, dtype=torch.bfloat16, schedule="auto") -> str:
+    return SCHED_NAMES[load().muon_resolve_schedule(int(m), int(n), int(steps), _dtype_code(dtype),
+                                                    SCHED[schedule])]
+
+
+def bucket_plan(shapes):
+    """(order, group_start) exactly as the library groups the matrices."""
+    lib = load()
+    n = len(shapes)
+    order = (ctypes.c_int * max(n, 1))()
+    start = (ctypes.c_int * (n + 1))()
+    g = lib.muon_bucket_plan(_shapes_arr(shapes), n, order, start)
+    if g < 0:
+        raise MuonError(ERR_ARG, "bad shapes")
+    return list(order[:n]), list(start[:g + 1])
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """Caller-owned workspace (uint8, 256-byte aligned, status word zeroed)."""
+    ws = torch.empty(int(nbytes) + WS_ALIGN, dtype=torch.uint8, device=device or "cuda")
+    off = (-ws.data_ptr()) % WS_ALIGN
+    ws = ws[off:off + int(nbytes)]
+    ws[:16].zero_()
+    return ws
+
+
+def ns_batched(X: torch.Tensor, steps: int = 5, coeffs=None, schedule: str = "auto", out=None,
+               workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """O_i = NS(X_i) for a [B, m, n] bf16/fp32 CUDA tensor (C-ABI muon_ns_batched)."""
+    lib = load()
+    if X.dim() != 3 or not X.is_cuda or not X.is_contiguous():
+        raise ValueError("X must be a contiguous [B, m, n] CUDA tensor")
+    B, m, n = X.shape
+    dt = _dtype_code(X.dtype)
+    if out is None:
+        out = torch.empty_like(X)
+    if workspace is None:
+        workspace = new_workspace(workspace_bytes([(m, n)] * max(B, 1), steps, X.dtype, schedule), X.device)
+    st = lib.muon_ns_batched(ctypes.c_void_p(X.data_ptr()), B, m, n, int(steps), _coeffs(coeffs),
+                             ctypes.c_void_p(out.data_ptr()), dt, SCHED[schedule],
+                             ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                             ctypes.c_void_p(_stream_ptr(stream)))
+    _check(st)
+    return out
+
+
+def muon_step(weights: Sequence[torch.Tensor], grads: Sequence[torch.Tensor], moms: Sequence[torch.Tensor],
+              beta: float = 0.95, lr: float = 0.02, steps: int = 5, coeffs=None, schedule: str = "auto",
+              workspace: torch.Tensor | None = None, stream=None) -> None:
+    """In place: mom <- beta mom + grad; W <- W - lr NS(mom) (C-ABI muon_step)."""
+    lib = load()
+    count = len(weights)
+    if not (len(grads) == count == len(moms)):
+        raise ValueError("weights, grads and moms must have the same length")
+    if count == 0:
+        return
+    dtype = weights[0].dtype
+    for w, g, mo in zip(weights, grads, moms):
+        if w.dim() != 2 or w.shape != g.shape or w.shape != mo.shape:
+            raise ValueError("each weight, grad and momentum must be 2-D of one shape")
+        if w.dtype != dtype or g.dtype != dtype or mo.dtype != torch.float32:
+            raise TypeError("weights and grads share one dtype; momentum is float32")
+        if not (w.is_contiguous() and g.is_contiguous() and mo.is_contiguous()):
+            raise ValueError("tensors must be contiguous")
+    shapes = [tuple(w.shape) for w in weights]
+    if workspace is None:
+        workspace = new_workspace(workspace_bytes(shapes, steps, dtype, schedule), weights[0].device)
+    P = ctypes.c_void_p * count
+    st = lib.muon_step(P(*[w.data_ptr() for w in weights]), P(*[g.data_ptr() for g in grads]),
+                       P(*[m.data_ptr() for m in moms]), _shapes_arr(shapes), count, float(beta), float(lr),
+                       int(steps), _coeffs(coeffs), _dtype_code(dtype), SCHED[schedule],
+                       ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                       ctypes.c_void_p(_stream_ptr(stream)))
+    _check(st)
+
+
+def device_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise and read/clear the workspace status word (OK or ERR_TIMEOUT)."""
+    return load().muon_device_status(ctypes.c_void_p(workspace.data_ptr()), ctypes.c_void_p(_stream_ptr(stream)))
+
+
+def debug_bounded_wait(workspace: torch.Tensor, max_cycles: int, stream=None) -> None:
+    _check(load().muon_debug_bounded_wait(ctypes.c_void_p(workspace.data_ptr()), int(max_cycles),
+                                          ctypes.c_void_p(_stream_ptr(stream))))
+
+
+def debug_gemm(A, B, A_lo=None, B_lo=None, split=1, b_mn=False, sym=False, workspace=None, stream=None):
+    """Test hook: fp32 out[b] = A[b] @ (B[b] if b_mn else B[b]^T) through one library kernel."""
+    lib = load()
+    batch, M, K = A.shape
+    N = B.shape[2] if b_mn else B.shape[1]
+    out = torch.zeros(batch, M, N, dtype=torch.float32, device=A.device)
+    if workspace is None:
+        workspace = new_workspace(4096, A.device)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    _check(lib.muon_debug_gemm(ptr(A), ptr(A_lo), ptr(B), ptr(B_lo), batch, M, N, K, split, int(b_mn), int(sym),
+                               _dtype_code(A.dtype), ptr(out), ptr(workspace), workspace.numel(),
+                               ctypes.c_void_p(_stream_ptr(stream))))
+    return out
+
+
+def profile_enable(on: bool = True) -> None:
+    """Start (clearing old records) or stop per-launch CUDA-event timing."""
+    load().muon_profile_enable(1 if on else 0)
+
+
+def profile_records():
+    """[(kind, ms, flops, bytes)] for every launch recorded since profile_enable(True)."""
+    lib = load()
+    out = []
+    for i in range(lib.muon_profile_count()):
+        k, ms, fl, by = ctypes.c_char_p(), ctypes.c_float(), ctypes.c_double(), ctypes.c_double()
+        _check(lib.muon_profile_get(i, ctypes.byref(k), ctypes.byref(ms), ctypes.byref(fl), ctypes.byref(by)))
+        out.append((k.value.decode(), ms.value, fl.value, by.value))
+    return out
+
+
+class MuonUpdater:
+    """Owner-side Muon step over a fixed list of 2-D parameters.
+
+    Holds the fp32 momentum buffers and one caller-side workspace sized for the
+    parameter shapes; `step(grads)` calls the C-ABI once.
+    """
+
+    def __init__(self, params: Sequence[torch.Tensor], beta=0.95, lr=0.02, steps=5, coeffs=None,
+                 schedule="auto", workspace_limit: int | None = None):
+        self.params = list(params)
+        self.beta, self.lr, self.steps, self.coeffs, self.schedule = beta, lr, steps, coeffs, schedule
+        self.moms = [torch.zeros(p.shape, dtype=torch.float32, device=p.device) for p in self.params]
+        need = workspace_bytes([tuple(p.shape) for p in self.params], steps, self.params[0].dtype, schedule)
+        if workspace_limit is not None:
+            need = min(need, int(workspace_limit))
+        self.workspace = new_workspace(need, self.params[0].device)
+
+    def step(self, grads: Sequence[torch.Tensor], stream=None):
+        muon_step(self.params, grads, self.moms, self.beta, self.lr, self.steps, self.coeffs, self.schedule,
+                  self.workspace, stream)

@@ -1,0 +1,117 @@
+// common.cuh -- types shared by the kernels and the host engine: the epilogue
+// description every GEMM kernel finishes with, the packing arguments, and the
+// per-element epilogue arithmetic.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+
+namespace muon {
+
+constexpr int kMaxBatch = 256;     // matrices per launch (pointer tables travel as kernel parameters)
+constexpr int kStatusTimeout = 1;  // bit set in the workspace status word on a bounded-wait timeout
+
+typedef __nv_bfloat16 bf16;
+
+enum FinalMode : int { FINAL_NONE = 0, FINAL_STORE = 1, FINAL_APPLY = 2 };
+
+// How a GEMM turns its fp32 accumulator into outputs.  For output element (r, c)
+// of matrix b (r, c in the packed, short-side-first orientation):
+//
+//   v = sc_b * (c_acc * acc + c_res * R[b][r][c]) + (r == c && r < rows_valid ? c_id : 0)
+//   sc_b = 1, inv_norm[b] or inv_norm[b]^2 (scale_pow = 0, 1, 2)
+//
+// and then either stores v into packed buffers (fp32 `Of`, bf16 `Oh`, and the
+// bf16 residual `Ol` = bf16(v - float(Oh)), so that Oh + Ol carries ~16
+// significant bits), or, in a final mode, writes v (FINAL_STORE) or applies
+// W <- W - lr * v (FINAL_APPLY) to the caller's un-packed matrix dst[b].
+// With `sym` set only elements with r >= c are produced, and each one with
+// r > c is also written at (c, r): the output is symmetric by construction.
+struct EpiParams {
+  const float* inv_norm;  // [B] 1 / (||X||_F + eps)
+  int scale_pow;
+  float c_acc, c_res, c_id;
+  const float* R;  // packed fp32 residual or nullptr
+  float* Of;       // packed fp32 output or nullptr
+  bf16* Oh;        // packed bf16 output or nullptr
+  bf16* Ol;        // packed bf16 low part or nullptr
+  long long ld;    // leading dimension (elements) of R / Of / Oh / Ol
+  long long bs;    // batch stride (elements) of R / Of / Oh / Ol
+  int sym;
+  int rows_valid;  // true short side s (padding rows are >= s)
+  int cols_valid;  // true long side (or s for square outputs)
+  // final-mode fields
+  int final_mode;
+  int dst_fp32;  // 1: dst is fp32, 0: bf16
+  float lr;
+  void* dst[kMaxBatch];
+  unsigned char tr[kMaxBatch];  // 1: dst[b] is [cols_valid, rows_valid] (the packed matrix transposed)
+};
+
+__device__ __forceinline__ float epi_scale(const EpiParams& e, int b) {
+  if (e.scale_pow == 0) return 1.f;
+  const float iv = e.inv_norm[b];
+  return e.scale_pow == 2 ? iv * iv : iv;
+}
+
+// Final write of one element: packed (p, q) -> caller's matrix.
+__device__ __forceinline__ void epi_final_elem(const EpiParams& e, int b, int p, int q, float v) {
+  if (p >= e.rows_valid || q >= e.cols_valid) return;
+  const long long idx =
+      e.tr[b] ? (long long)q * e.rows_valid + p : (long long)p * e.cols_valid + q;
+  if (e.dst_fp32) {
+    float* d = static_cast<float*>(e.dst[b]) + idx;
+    if (e.final_mode == FINAL_APPLY) *d = *d - e.lr * v;
+    else *d = v;
+  } else {
+    bf16* d = static_cast<bf16*>(e.dst[b]) + idx;
+    if (e.final_mode == FINAL_APPLY) *d = __float2bfloat16_rn(__bfloat162float(*d) - e.lr * v);
+    else *d = __float2bfloat16_rn(v);
+  }
+}
+
+// Store of one element into the packed outputs (no symmetry handling).
+__device__ __forceinline__ void epi_store_elem(const EpiParams& e, long long off, float v) {
+  if (e.Of) e.Of[off] = v;
+  if (e.Oh) {
+    const bf16 h = __float2bfloat16_rn(v);
+    e.Oh[off] = h;
+    if (e.Ol) e.Ol[off] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+}
+
+// Full scalar epilogue for one accumulator element (used by the SIMT kernels
+// and by tensor-core tiles on the diagonal or at ragged edges).
+__device__ __forceinline__ void epi_elem(const EpiParams& e, int b, int r, int c, float acc, float sc) {
+  if (e.sym && c > r) return;
+  float v = e.c_acc * acc;
+  if (e.R) v += e.c_res * e.R[(long long)b * e.bs + (long long)r * e.ld + c];
+  v *= sc;
+  if (r == c && r < e.rows_valid) v += e.c_id;
+  if (e.final_mode != FINAL_NONE) {
+    epi_final_elem(e, b, r, c, v);
+    return;
+  }
+  const long long base = (long long)b * e.bs;
+  epi_store_elem(e, base + (long long)r * e.ld + c, v);
+  if (e.sym && r > c) epi_store_elem(e, base + (long long)c * e.ld + r, v);
+}
+
+// Arguments of the momentum / pack / norm kernel.
+struct PackArgs {
+  int m, n;          // caller's shape of every matrix in this launch
+  int sp, lp;        // padded packed shape (short side first)
+  int has_mom;       // 1: M = beta*mom + src, written back to mom; 0: M = src
+  int src_fp32;      // source dtype: 1 fp32, 0 bf16
+  float beta;
+  float* Xf;         // packed fp32 copy of M (or nullptr)
+  bf16* Xh;          // packed bf16(M) (or nullptr)
+  bf16* Xl;          // packed bf16(M - float(Xh)) (or nullptr)
+  long long bs;      // batch stride of the packed buffers (elements)
+  float* partial;    // [B][tiles] partial sums of squares
+  int tiles;         // tiles per matrix
+  const void* src[kMaxBatch];
+  float* mom[kMaxBatch];
+  unsigned char tr[kMaxBatch];
+};
+
+}  // namespace muon

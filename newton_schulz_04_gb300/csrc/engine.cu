@@ -1,0 +1,850 @@
+// engine.cu -- host engine and C ABI of the owner-side Muon update.
+//
+// Per call: validate every argument (no launch before that), group the matrices
+// by (short side, long side) (DMuon technical summary, §2.2: same-shape matrices
+// run the Gram recurrence jointly), carve the caller's workspace, and enqueue one
+// schedule per group on the caller's stream:
+//
+//   ORIG     original space, bf16 tensor-core products, fp32 carry of X:
+//            A = X X^T (SYRK), B = b A + c A^2, X <- a X + B X
+//   GRAM_X3  Gram space with split-bf16 operands (hi*hi + hi*lo + lo*hi):
+//            G0 = X0 X0^T; P_k = a I + b G_k + c G_k^2; Q <- P_k Q;
+//            G_{k+1} = P_k (P_k G_k); O = Q X0
+//   GRAM_X1  the same recurrence with plain bf16 operands
+//   fp32     the ORIG or Gram recurrence with fp32 FFMA products
+//
+// Why these: the Gram recurrence squares the condition number, so plain bf16
+// products in Gram space exceed a 2e-2 relative error on ill-conditioned
+// inputs; split operands restore it at three products per product.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/muon_ns.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace muon {
+
+static thread_local std::string g_last_error;
+
+static muon_status fail(muon_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+// ------------------------------------------------------------------ profiling
+// Optional per-launch CUDA-event timing on the caller's stream (off by default).
+struct ProfRec {
+  const char* kind;
+  cudaEvent_t a, b;
+  double flops;  // algorithmic flops of the launch (symmetric products counted once)
+  double bytes;  // algorithmic HBM bytes of the launch
+};
+static bool g_prof_on = false;
+static std::vector<ProfRec> g_prof;
+static std::vector<cudaEvent_t> g_event_pool;
+static size_t g_event_next = 0;
+
+static cudaEvent_t prof_event() {
+  if (g_event_next == g_event_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_event_pool.push_back(e);
+  }
+  return g_event_pool[g_event_next++];
+}
+
+struct ProfScope {
+  bool on;
+  cudaStream_t st;
+  size_t idx;
+  ProfScope(const char* kind, double flops, double bytes, cudaStream_t s) : on(g_prof_on), st(s), idx(0) {
+    if (!on) return;
+    ProfRec r{kind, prof_event(), prof_event(), flops, bytes};
+    if (!r.a || !r.b) {
+      on = false;
+      return;
+    }
+    cudaEventRecord(r.a, st);
+    idx = g_prof.size();
+    g_prof.push_back(r);
+  }
+  ~ProfScope() {
+    if (on) cudaEventRecord(g_prof[idx].b, st);
+  }
+};
+
+static const float kQuintic[3] = {3.4445f, -4.7750f, 2.0315f};
+static const float kEps = 1e-7f;
+
+static inline long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+
+// One matrix of a call, in the caller's layout.
+struct Mat {
+  const void* src;  // gradient (step) or X (ns only)
+  float* mom;       // momentum or nullptr
+  void* dst;        // W (apply) or out (store)
+  int m, n;
+};
+
+// ------------------------------------------------------------------ bucketing
+// Groups by (short, long) key in increasing key order; members keep input order.
+static int bucket_plan(const std::vector<std::pair<long long, long long>>& shapes, std::vector<int>& order,
+                       std::vector<int>& start) {
+  const int count = static_cast<int>(shapes.size());
+  order.resize(count);
+  for (int i = 0; i < count; ++i) order[i] = i;
+  auto key = [&](int i) {
+    const long long a = shapes[i].first, b = shapes[i].second;
+    return std::make_pair(std::min(a, b), std::max(a, b));
+  };
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return key(x) < key(y); });
+  start.clear();
+  for (int t = 0; t < count; ++t)
+    if (t == 0 || key(order[t]) != key(order[t - 1])) start.push_back(t);
+  const int groups = static_cast<int>(start.size());
+  start.push_back(count);
+  return groups;
+}
+
+// ------------------------------------------------------------------ schedules
+static muon_sched resolve(long long s, long long l, int steps, muon_dtype dt, muon_sched sc) {
+  if (dt == MUON_FP32) {
+    if (sc == MUON_SCHED_ORIG) return MUON_SCHED_ORIG;
+    if (sc == MUON_SCHED_AUTO) {
+      // fp32 Gram costs 3 s^2 l + (4T - 3) s^3 vs T (3 s^2 l + s^3): never more, equal when square.
+      return (l > s && steps > 0) ? MUON_SCHED_GRAM_X3 : MUON_SCHED_ORIG;
+    }
+    return steps > 0 ? MUON_SCHED_GRAM_X3 : MUON_SCHED_ORIG;  // both Gram modes run in fp32 here
+  }
+  if (steps == 0) return MUON_SCHED_ORIG;  // only the packed fp32 copy is needed
+  if (sc != MUON_SCHED_AUTO) return sc;
+  // Tensor-core work (symmetric products counted once):
+  //   ORIG     T (3 s^2 l + s^3)
+  //   GRAM_X3  3 s^2 l (SYRK, split) + 3 (4T - 3) s^3 + 6 s^2 l (Q X0, split)
+  const double S = static_cast<double>(s), L = static_cast<double>(l), T = steps;
+  const double orig = T * (3 * S * S * L + S * S * S);
+  const double x3 = 9 * S * S * L + 3 * (4 * T - 3) * S * S * S;
+  return x3 < orig ? MUON_SCHED_GRAM_X3 : MUON_SCHED_ORIG;
+}
+
+// Bump allocator over the workspace; with base == nullptr it only measures.
+struct Carve {
+  char* base;
+  size_t off;
+  void* take(size_t bytes) {
+    off = static_cast<size_t>(round_up(static_cast<long long>(off), 1024));
+    void* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+constexpr size_t kHeader = 1024;  // status word + reserved
+
+struct Buffers {
+  float* inv_norm = nullptr;
+  float* partial = nullptr;
+  // packed X
+  float* Xf = nullptr;
+  float* Xf2 = nullptr;
+  bf16* Xb[2] = {nullptr, nullptr};
+  bf16* Xl = nullptr;
+  // s x s
+  float* Gf = nullptr;
+  bf16* Gh = nullptr;
+  bf16* Gl = nullptr;
+  bf16* Bh = nullptr;
+  bf16* Ph[2] = {nullptr, nullptr};
+  bf16* Pl[2] = {nullptr, nullptr};
+  bf16* Qh[2] = {nullptr, nullptr};
+  bf16* Ql[2] = {nullptr, nullptr};
+  bf16* Hh = nullptr;
+  bf16* Hl = nullptr;
+  float* Pf[2] = {nullptr, nullptr};
+  float* Qf[2] = {nullptr, nullptr};
+  float* Hf = nullptr;
+  float* Af = nullptr;
+  float* Bf = nullptr;
+};
+
+static size_t carve_buffers(char* base, int Bc, long long sp, long long lp, int tiles, muon_dtype dt,
+                            muon_sched sc, Buffers& bf) {
+  Carve c{base, kHeader};
+  const size_t nx = static_cast<size_t>(Bc) * sp * lp;
+  const size_t ns = static_cast<size_t>(Bc) * sp * sp;
+  bf.inv_norm = static_cast<float*>(c.take(sizeof(float) * Bc));
+  bf.partial = static_cast<float*>(c.take(sizeof(float) * Bc * static_cast<size_t>(tiles)));
+  if (dt == MUON_FP32) {
+    bf.Xf = static_cast<float*>(c.take(4 * nx));
+    if (sc == MUON_SCHED_ORIG) {
+      bf.Xf2 = static_cast<float*>(c.take(4 * nx));
+      bf.Af = static_cast<float*>(c.take(4 * ns));
+      bf.Bf = static_cast<float*>(c.take(4 * ns));
+    } else {
+      bf.Gf = static_cast<float*>(c.take(4 * ns));
+      for (int q = 0; q < 2; ++q) bf.Pf[q] = static_cast<float*>(c.take(4 * ns));
+      for (int q = 0; q < 2; ++q) bf.Qf[q] = static_cast<float*>(c.take(4 * ns));
+      bf.Hf = static_cast<float*>(c.take(4 * ns));
+    }
+    return c.off;
+  }
+  if (sc == MUON_SCHED_ORIG) {
+    bf.Xf = static_cast<float*>(c.take(4 * nx));
+    bf.Xb[0] = static_cast<bf16*>(c.take(2 * nx));
+    bf.Xb[1] = static_cast<bf16*>(c.take(2 * nx));
+    bf.Gf = static_cast<float*>(c.take(4 * ns));
+    bf.Gh = static_cast<bf16*>(c.take(2 * ns));
+    bf.Bh = static_cast<bf16*>(c.take(2 * ns));
+    return c.off;
+  }
+  const bool x3 = (sc == MUON_SCHED_GRAM_X3);
+  bf.Xb[0] = static_cast<bf16*>(c.take(2 * nx));
+  if (x3) bf.Xl = static_cast<bf16*>(c.take(2 * nx));
+  bf.Gf = static_cast<float*>(c.take(4 * ns));
+  bf.Gh = static_cast<bf16*>(c.take(2 * ns));
+  if (x3) bf.Gl = static_cast<bf16*>(c.take(2 * ns));
+  for (int q = 0; q < 2; ++q) {
+    bf.Ph[q] = static_cast<bf16*>(c.take(2 * ns));
+    if (x3) bf.Pl[q] = static_cast<bf16*>(c.take(2 * ns));
+    bf.Qh[q] = static_cast<bf16*>(c.take(2 * ns));
+    if (x3) bf.Ql[q] = static_cast<bf16*>(c.take(2 * ns));
+  }
+  bf.Hh = static_cast<bf16*>(c.take(2 * ns));
+  if (x3) bf.Hl = static_cast<bf16*>(c.take(2 * ns));
+  return c.off;
+}
+
+struct Group {
+  long long s, l, sp, lp;
+  int tiles;  // pack tiles per matrix
+  muon_sched sc;
+};
+
+static Group make_group(long long m, long long n, int steps, muon_dtype dt, muon_sched sc) {
+  Group g;
+  g.s = std::min(m, n);
+  g.l = std::max(m, n);
+  g.sp = round_up(g.s, 256);
+  g.lp = round_up(g.l, 256);
+  g.tiles = static_cast<int>((g.sp / 64) * (g.lp / 64));
+  g.sc = resolve(g.s, g.l, steps, dt, sc);
+  return g;
+}
+
+static size_t group_bytes(const Group& g, int Bc, muon_dtype dt) {
+  Buffers bf;
+  return carve_buffers(nullptr, Bc, g.sp, g.lp, g.tiles, dt, g.sc, bf);
+}
+
+// Largest batch width that fits in ws_bytes (0 if none).
+static int fit_batch(const Group& g, int want, muon_dtype dt, size_t ws_bytes) {
+  want = std::min(want, kMaxBatch);
+  if (want <= 0) return 0;
+  if (group_bytes(g, want, dt) <= ws_bytes) return want;
+  const size_t one = group_bytes(g, 1, dt);
+  if (one > ws_bytes) return 0;
+  const size_t per = group_bytes(g, 2, dt) - one;
+  int bc = static_cast<int>(std::min<size_t>(want, 1 + (ws_bytes - one) / std::max<size_t>(per, 1)));
+  while (bc > 1 && group_bytes(g, bc, dt) > ws_bytes) --bc;
+  return bc;
+}
+
+// ------------------------------------------------------------------ device info
+static int device_sms(int* major, int* minor, muon_status* st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    *st = fail(MUON_ERR_CUDA, "no CUDA device available");
+    return 0;
+  }
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(minor, cudaDevAttrComputeCapabilityMinor, dev);
+  *st = MUON_OK;
+  return sms;
+}
+
+// ------------------------------------------------------------------ one group
+struct Ctx {
+  cudaStream_t st;
+  int sms;
+  int* status;
+  muon_dtype dt;
+  int steps;
+  float a, b, c;
+  float beta, lr;
+  bool apply;   // W <- W - lr O (else out = O)
+  bool has_mom;
+};
+
+#define CK(expr)                                                                                  \
+  do {                                                                                            \
+    cudaError_t e_ = (expr);                                                                      \
+    if (e_ != cudaSuccess)                                                                        \
+      return fail(MUON_ERR_CUDA, "%s failed: %s%s%s", #expr, cudaGetErrorString(e_), why ? ": " : "", \
+                  why ? why : "");                                                                \
+  } while (0)
+
+static EpiParams epi_packed(const Group& g, const Buffers& bf, int scale_pow, float c_acc, float c_res, float c_id,
+                            const float* R, float* Of, bf16* Oh, bf16* Ol, long long ld, long long bs) {
+  EpiParams e;
+  memset(&e, 0, sizeof(e));
+  e.inv_norm = bf.inv_norm;
+  e.scale_pow = scale_pow;
+  e.c_acc = c_acc;
+  e.c_res = c_res;
+  e.c_id = c_id;
+  e.R = R;
+  e.Of = Of;
+  e.Oh = Oh;
+  e.Ol = Ol;
+  e.ld = ld;
+  e.bs = bs;
+  e.rows_valid = static_cast<int>(g.s);
+  e.cols_valid = static_cast<int>(g.s);
+  e.final_mode = FINAL_NONE;
+  return e;
+}
+
+static void epi_set_final(EpiParams& e, const Ctx& cx, const Group& g, const Mat* mats, int Bc) {
+  e.Of = nullptr;
+  e.Oh = nullptr;
+  e.Ol = nullptr;
+  e.final_mode = cx.apply ? FINAL_APPLY : FINAL_STORE;
+  e.dst_fp32 = cx.dt == MUON_FP32 ? 1 : 0;
+  e.lr = cx.lr;
+  e.rows_valid = static_cast<int>(g.s);
+  e.cols_valid = static_cast<int>(g.l);
+  for (int q = 0; q < Bc; ++q) {
+    e.dst[q] = mats[q].dst;
+    e.tr[q] = mats[q].m > mats[q].n ? 1 : 0;
+  }
+}
+
+static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int Bc, char* ws) {
+  const char* why = nullptr;
+  Buffers bf;
+  carve_buffers(ws, Bc, g.sp, g.lp, g.tiles, cx.dt, g.sc, bf);
+  const long long sp = g.sp, lp = g.lp;
+  const long long bsx = sp * lp, bss = sp * sp;
+  const bool fp32 = cx.dt == MUON_FP32;
+  const bool x3 = g.sc == MUON_SCHED_GRAM_X3;
+
+  // ---- momentum + pack + norm
+  PackArgs pa;
+  memset(&pa, 0, sizeof(pa));
+  pa.m = mats[0].m;
+  pa.n = mats[0].n;
+  pa.sp = static_cast<int>(sp);
+  pa.lp = static_cast<int>(lp);
+  pa.has_mom = cx.has_mom ? 1 : 0;
+  pa.src_fp32 = fp32 ? 1 : 0;
+  pa.beta = cx.beta;
+  pa.bs = bsx;
+  pa.partial = bf.partial;
+  pa.tiles = g.tiles;
+  if (fp32 || g.sc == MUON_SCHED_ORIG) pa.Xf = bf.Xf;
+  if (!fp32) pa.Xh = bf.Xb[0];
+  if (!fp32 && x3) pa.Xl = bf.Xl;
+  for (int q = 0; q < Bc; ++q) {
+    // a bucket can mix m x n and n x m members: the pack kernel transposes per member
+    pa.src[q] = mats[q].src;
+    pa.mom[q] = mats[q].mom;
+    pa.tr[q] = mats[q].m > mats[q].n ? 1 : 0;
+  }
+  {
+    // One pack launch covers members stored the same way round (the chunk is
+    // ordered m x n before n x m); a mixed chunk takes two launches.
+    int q = 1;
+    while (q < Bc && mats[q].m == pa.m) ++q;
+    const double el = static_cast<double>(g.s) * g.l;
+    const double esz = fp32 ? 4.0 : 2.0;
+    const double pbytes = el * (esz + (cx.has_mom ? 8.0 : 0.0) + (pa.Xf ? 4.0 : 0.0) + (pa.Xh ? 2.0 : 0.0) +
+                                (pa.Xl ? 2.0 : 0.0));
+    ProfScope ps("pack", 0.0, pbytes * Bc, cx.st);
+    CK(launch_pack(pa, q, cx.st));
+    if (q < Bc) {
+      PackArgs pb = pa;
+      pb.m = mats[q].m;
+      pb.n = mats[q].n;
+      for (int r = q; r < Bc; ++r) {
+        pb.src[r - q] = mats[r].src;
+        pb.mom[r - q] = mats[r].mom;
+        pb.tr[r - q] = pa.tr[r];
+      }
+      if (pb.Xf) pb.Xf += q * bsx;
+      if (pb.Xh) pb.Xh += q * bsx;
+      if (pb.Xl) pb.Xl += q * bsx;
+      pb.partial += static_cast<long long>(q) * g.tiles;
+      CK(launch_pack(pb, Bc - q, cx.st));
+    }
+  }
+  {
+    ProfScope ps("norm_finalize", 0.0, 4.0 * g.tiles * Bc, cx.st);
+    CK(launch_norm_finalize(bf.partial, g.tiles, Bc, kEps, bf.inv_norm, cx.st));
+  }
+
+  if (cx.steps == 0) {
+    EpiParams e = epi_packed(g, bf, 1, 1.f, 0.f, 0.f, nullptr, nullptr, nullptr, nullptr, lp, bsx);
+    epi_set_final(e, cx, g, mats, Bc);
+    ProfScope ps("final_from_packed", 0.0, Bc * static_cast<double>(g.s) * g.l * (fp32 ? 12.0 : 8.0), cx.st);
+    CK(launch_final_from_packed(bf.Xf, lp, bsx, Bc, e, cx.st));
+    return MUON_OK;
+  }
+  const int T = cx.steps;
+  const int S = static_cast<int>(sp), L = static_cast<int>(lp);
+
+  if (fp32) {
+    auto simt = [&](const float* A, long long lda, long long bsa, const float* Bm, long long ldb, long long bsb,
+                    int M, int N, int K, int sym, int b_mn, const EpiParams& e) {
+      SimtGemmDesc d{Bc, M, N, K, sym, b_mn, A, lda, bsa, Bm, ldb, bsb};
+      const double Kt = K == S ? static_cast<double>(g.s) : static_cast<double>(g.l);
+      const double fl = sym ? Bc * static_cast<double>(g.s) * g.s * Kt : 2.0 * Bc * g.s * g.l * Kt;
+      ProfScope ps(sym ? "simt_sym" : "simt_rect", fl, 0.0, cx.st);
+      return launch_simt_gemm(d, e, cx.st);
+    };
+    if (g.sc == MUON_SCHED_ORIG) {
+      float* cur = bf.Xf;
+      float* nxt = bf.Xf2;
+      for (int k = 0; k < T; ++k) {
+        EpiParams e1 = epi_packed(g, bf, k == 0 ? 2 : 0, 1.f, 0.f, 0.f, nullptr, bf.Af, nullptr, nullptr, sp, bss);
+        CK(simt(cur, lp, bsx, cur, lp, bsx, S, S, L, 1, 0, e1));
+        EpiParams e2 = epi_packed(g, bf, 0, cx.c, cx.b, 0.f, bf.Af, bf.Bf, nullptr, nullptr, sp, bss);
+        CK(simt(bf.Af, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, e2));
+        EpiParams e3 = epi_packed(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, cur, nxt, nullptr, nullptr, lp, bsx);
+        e3.cols_valid = static_cast<int>(g.l);
+        if (k == T - 1) epi_set_final(e3, cx, g, mats, Bc);
+        CK(simt(bf.Bf, sp, bss, cur, lp, bsx, S, L, S, 0, 1, e3));
+        std::swap(cur, nxt);
+      }
+      return MUON_OK;
+    }
+    // fp32 Gram
+    EpiParams e0 = epi_packed(g, bf, 2, 1.f, 0.f, 0.f, nullptr, bf.Gf, nullptr, nullptr, sp, bss);
+    CK(simt(bf.Xf, lp, bsx, bf.Xf, lp, bsx, S, S, L, 1, 0, e0));
+    const float* Q = nullptr;
+    int qi = 0;
+    for (int k = 0; k < T; ++k) {
+      float* P = bf.Pf[k & 1];
+      EpiParams ep = epi_packed(g, bf, 0, cx.c, cx.b, cx.a, bf.Gf, P, nullptr, nullptr, sp, bss);
+      CK(simt(bf.Gf, sp, bss, bf.Gf, sp, bss, S, S, S, 1, 0, ep));
+      if (k == 0) {
+        Q = P;
+      } else {
+        float* Qn = bf.Qf[qi];
+        qi ^= 1;
+        EpiParams eq = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, Qn, nullptr, nullptr, sp, bss);
+        CK(simt(P, sp, bss, Q, sp, bss, S, S, S, 1, 0, eq));
+        Q = Qn;
+      }
+      if (k + 1 < T) {
+        EpiParams eh = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Hf, nullptr, nullptr, sp, bss);
+        CK(simt(P, sp, bss, bf.Gf, sp, bss, S, S, S, 1, 0, eh));
+        EpiParams eg = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Gf, nullptr, nullptr, sp, bss);
+        CK(simt(P, sp, bss, bf.Hf, sp, bss, S, S, S, 1, 0, eg));
+      }
+    }
+    EpiParams ef = epi_packed(g, bf, 1, 1.f, 0.f, 0.f, nullptr, nullptr, nullptr, nullptr, lp, bsx);
+    epi_set_final(ef, cx, g, mats, Bc);
+    CK(simt(Q, sp, bss, bf.Xf, lp, bsx, S, L, S, 0, 1, ef));
+    return MUON_OK;
+  }
+
+  auto tc = [&](int split, int b_mn, int sym, int M, int N, int K, const bf16* Ah, const bf16* Al, long long lda,
+                long long bsa, const bf16* Bh, const bf16* Bl, long long ldb, long long bsb, const EpiParams& e) {
+    TcGemmDesc d;
+    d.B = Bc;
+    d.M = M;
+    d.N = N;
+    d.K = K;
+    d.sym = sym;
+    d.split = split;
+    d.b_mn = b_mn;
+    d.A = TcOperand{Ah, Al, lda, bsa};
+    d.Bop = TcOperand{Bh, Bl, ldb, bsb};
+    const double Kt = K == S ? static_cast<double>(g.s) : static_cast<double>(g.l);
+    const double fl = sym ? Bc * static_cast<double>(g.s) * g.s * Kt : 2.0 * Bc * g.s * g.l * Kt;
+    const char* kind = sym ? (K == S ? (split == 3 ? "tc_sym_x3" : "tc_sym") : (split == 3 ? "tc_syrk_x3" : "tc_syrk"))
+                           : (split == 3 ? "tc_rect_x3" : "tc_rect");
+    ProfScope ps(kind, fl, 0.0, cx.st);
+    return launch_tc_gemm(d, e, cx.status, cx.st, cx.sms, &why);
+  };
+
+  if (g.sc == MUON_SCHED_ORIG) {
+    bf16* cur = bf.Xb[0];
+    bf16* nxt = bf.Xb[1];
+    for (int k = 0; k < T; ++k) {
+      // A = X X^T (k = 0: X = M / s, so scale by inv_norm^2)
+      EpiParams e1 = epi_packed(g, bf, k == 0 ? 2 : 0, 1.f, 0.f, 0.f, nullptr, bf.Gf, bf.Gh, nullptr, sp, bss);
+      CK(tc(1, 0, 1, S, S, L, cur, nullptr, lp, bsx, cur, nullptr, lp, bsx, e1));
+      // B = b A + c A^2
+      EpiParams e2 = epi_packed(g, bf, 0, cx.c, cx.b, 0.f, bf.Gf, nullptr, bf.Bh, nullptr, sp, bss);
+      CK(tc(1, 0, 1, S, S, S, bf.Gh, nullptr, sp, bss, bf.Gh, nullptr, sp, bss, e2));
+      // X <- a X + B X (k = 0: both terms carry 1 / s)
+      EpiParams e3 = epi_packed(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, bf.Xf, bf.Xf, nxt, nullptr, lp, bsx);
+      e3.cols_valid = static_cast<int>(g.l);
+      if (k == T - 1) epi_set_final(e3, cx, g, mats, Bc);
+      CK(tc(1, 1, 0, S, L, S, bf.Bh, nullptr, sp, bss, cur, nullptr, lp, bsx, e3));
+      std::swap(cur, nxt);
+    }
+    return MUON_OK;
+  }
+
+  // Gram space (split 3 or 1)
+  const int sp3 = x3 ? 3 : 1;
+  EpiParams e0 = epi_packed(g, bf, 2, 1.f, 0.f, 0.f, nullptr, bf.Gf, bf.Gh, bf.Gl, sp, bss);
+  CK(tc(sp3, 0, 1, S, S, L, bf.Xb[0], bf.Xl, lp, bsx, bf.Xb[0], bf.Xl, lp, bsx, e0));
+  const bf16* Qh = nullptr;
+  const bf16* Ql = nullptr;
+  int qi = 0;
+  for (int k = 0; k < T; ++k) {
+    bf16* Ph = bf.Ph[k & 1];
+    bf16* Pl = bf.Pl[k & 1];
+    // P = a I + b G + c G^2
+    EpiParams ep = epi_packed(g, bf, 0, cx.c, cx.b, cx.a, bf.Gf, nullptr, Ph, Pl, sp, bss);
+    CK(tc(sp3, 0, 1, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, ep));
+    if (k == 0) {
+      Qh = Ph;
+      Ql = Pl;
+    } else {
+      bf16* Qnh = bf.Qh[qi];
+      bf16* Qnl = bf.Ql[qi];
+      qi ^= 1;
+      EpiParams eq = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, Qnh, Qnl, sp, bss);
+      CK(tc(sp3, 0, 1, S, S, S, Ph, Pl, sp, bss, Qh, Ql, sp, bss, eq));
+      Qh = Qnh;
+      Ql = Qnl;
+    }
+    if (k + 1 < T) {
+      EpiParams eh = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Hh, bf.Hl, sp, bss);
+      CK(tc(sp3, 0, 1, S, S, S, Ph, Pl, sp, bss, bf.Gh, bf.Gl, sp, bss, eh));
+      EpiParams eg = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Gf, bf.Gh, bf.Gl, sp, bss);
+      CK(tc(sp3, 0, 1, S, S, S, Ph, Pl, sp, bss, bf.Hh, bf.Hl, sp, bss, eg));
+    }
+  }
+  // O = Q X0 = Q X / s
+  EpiParams ef = epi_packed(g, bf, 1, 1.f, 0.f, 0.f, nullptr, nullptr, nullptr, nullptr, lp, bsx);
+  epi_set_final(ef, cx, g, mats, Bc);
+  CK(tc(sp3, 1, 0, S, L, S, Qh, Ql, sp, bss, bf.Xb[0], bf.Xl, lp, bsx, ef));
+  return MUON_OK;
+}
+#undef CK
+
+// ------------------------------------------------------------------ validation
+static bool valid_dt(int dt) { return dt == MUON_BF16 || dt == MUON_FP32; }
+static bool valid_sc(int sc) { return sc >= MUON_SCHED_AUTO && sc <= MUON_SCHED_ORIG; }
+
+static muon_status check_common(int steps, const float* coeffs, int dt, int sc, void* ws, size_t ws_bytes) {
+  if (steps < 0 || steps > MUON_MAX_STEPS) return fail(MUON_ERR_ARG, "steps=%d out of [0, %d]", steps, MUON_MAX_STEPS);
+  if (!valid_dt(dt)) return fail(MUON_ERR_ARG, "bad dtype %d", dt);
+  if (!valid_sc(sc)) return fail(MUON_ERR_ARG, "bad schedule %d", sc);
+  if (coeffs && !(std::isfinite(coeffs[0]) && std::isfinite(coeffs[1]) && std::isfinite(coeffs[2])))
+    return fail(MUON_ERR_ARG, "coefficients must be finite");
+  if (!ws) return fail(MUON_ERR_ARG, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % MUON_WS_ALIGN) return fail(MUON_ERR_ALIGN, "workspace not %d-byte aligned", MUON_WS_ALIGN);
+  if (ws_bytes < kHeader) return fail(MUON_ERR_WORKSPACE, "workspace smaller than its %zu-byte header", kHeader);
+  return MUON_OK;
+}
+
+static muon_status run_all(std::vector<Mat>& mats, int steps, const float* coeffs, muon_dtype dt, muon_sched sc,
+                           float beta, float lr, bool apply, bool has_mom, void* ws, size_t ws_bytes,
+                           void* stream) {
+  const int count = static_cast<int>(mats.size());
+  std::vector<std::pair<long long, long long>> shapes(count);
+  for (int i = 0; i < count; ++i) shapes[i] = {mats[i].m, mats[i].n};
+  std::vector<int> order, start;
+  const int groups = bucket_plan(shapes, order, start);
+  // plan every group before launching anything
+  std::vector<Group> gs(groups);
+  std::vector<int> widths(groups);
+  for (int gi = 0; gi < groups; ++gi) {
+    const Mat& m0 = mats[order[start[gi]]];
+    gs[gi] = make_group(m0.m, m0.n, steps, dt, sc);
+    widths[gi] = fit_batch(gs[gi], start[gi + 1] - start[gi], dt, ws_bytes);
+    if (widths[gi] <= 0)
+      return fail(MUON_ERR_WORKSPACE, "workspace of %zu bytes cannot hold one %lldx%lld matrix (needs %zu)", ws_bytes,
+                  gs[gi].s, gs[gi].l, group_bytes(gs[gi], 1, dt));
+  }
+  if (count == 0) return MUON_OK;
+  int major = 0, minor = 0;
+  muon_status dst;
+  const int sms = device_sms(&major, &minor, &dst);
+  if (dst != MUON_OK) return dst;
+  if (major != 10 || minor != 3)
+    return fail(MUON_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300); device is sm_%d%d", major, minor);
+  Ctx cx;
+  cx.st = static_cast<cudaStream_t>(stream);
+  cx.sms = sms;
+  cx.status = static_cast<int*>(ws);
+  cx.dt = dt;
+  cx.steps = steps;
+  const float* cf = coeffs ? coeffs : kQuintic;
+  cx.a = cf[0];
+  cx.b = cf[1];
+  cx.c = cf[2];
+  cx.beta = beta;
+  cx.lr = lr;
+  cx.apply = apply;
+  cx.has_mom = has_mom;
+  std::vector<Mat> chunk;
+  for (int gi = 0; gi < groups; ++gi) {
+    const int n = start[gi + 1] - start[gi];
+    for (int c0 = 0; c0 < n; c0 += widths[gi]) {
+      const int bc = std::min(widths[gi], n - c0);
+      chunk.clear();
+      for (int q = 0; q < bc; ++q) chunk.push_back(mats[order[start[gi] + c0 + q]]);
+      // pack requires equal caller shapes in one launch: order m x n before n x m
+      std::stable_sort(chunk.begin(), chunk.end(), [](const Mat& x, const Mat& y) { return x.m < y.m; });
+      const muon_status r = run_chunk(cx, gs[gi], chunk.data(), bc, static_cast<char*>(ws));
+      if (r != MUON_OK) return r;
+    }
+  }
+  return MUON_OK;
+}
+
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace muon
+
+using namespace muon;
+
+extern "C" {
+
+muon_status muon_ns_batched(const void* X, int B, int m, int n, int steps, const float* coeffs, void* out,
+                            muon_dtype dt, muon_sched sc, void* ws, size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  try {
+    if (B < 0) return fail(MUON_ERR_ARG, "B=%d < 0", B);
+    if (B > 0 && (!X || !out)) return fail(MUON_ERR_ARG, "X or out is NULL");
+    if (m <= 0 || n <= 0 || m > MUON_MAX_DIM || n > MUON_MAX_DIM)
+      return fail(MUON_ERR_SHAPE, "bad shape %dx%d", m, n);
+    muon_status s = check_common(steps, coeffs, dt, sc, ws, ws_bytes);
+    if (s != MUON_OK) return s;
+    const size_t esz = dt == MUON_FP32 ? 4 : 2;
+    if (reinterpret_cast<uintptr_t>(X) % esz || reinterpret_cast<uintptr_t>(out) % esz)
+      return fail(MUON_ERR_ALIGN, "X/out not aligned to the element size");
+    const size_t bytes = static_cast<size_t>(B) * m * n * esz;
+    if (B > 0 && overlaps(X, bytes, out, bytes)) return fail(MUON_ERR_ARG, "out overlaps X");
+    if (B > 0 && overlaps(ws, ws_bytes, out, bytes)) return fail(MUON_ERR_ARG, "out overlaps the workspace");
+    if (B > 0 && overlaps(ws, ws_bytes, X, bytes)) return fail(MUON_ERR_ARG, "X overlaps the workspace");
+    std::vector<Mat> mats(B);
+    for (int i = 0; i < B; ++i) {
+      mats[i].src = static_cast<const char*>(X) + static_cast<size_t>(i) * m * n * esz;
+      mats[i].mom = nullptr;
+      mats[i].dst = static_cast<char*>(out) + static_cast<size_t>(i) * m * n * esz;
+      mats[i].m = m;
+      mats[i].n = n;
+    }
+    return run_all(mats, steps, coeffs, dt, sc, 0.f, 0.f, false, false, ws, ws_bytes, stream);
+  } catch (...) {
+    return fail(MUON_ERR_ARG, "internal exception");
+  }
+}
+
+muon_status muon_step(void* const* W, const void* const* grad, float* const* mom, const int64_t* shapes, int count,
+                      float beta, float lr, int steps, const float* coeffs, muon_dtype dt, muon_sched sc, void* ws,
+                      size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  try {
+    if (count < 0) return fail(MUON_ERR_ARG, "count=%d < 0", count);
+    if (count > 0 && (!W || !grad || !mom || !shapes)) return fail(MUON_ERR_ARG, "a pointer array is NULL");
+    if (!std::isfinite(beta) || !std::isfinite(lr)) return fail(MUON_ERR_ARG, "beta and lr must be finite");
+    muon_status s = check_common(steps, coeffs, dt, sc, ws, ws_bytes);
+    if (s != MUON_OK) return s;
+    const size_t esz = dt == MUON_FP32 ? 4 : 2;
+    std::vector<Mat> mats(count);
+    for (int i = 0; i < count; ++i) {
+      const int64_t m = shapes[2 * i], n = shapes[2 * i + 1];
+      if (m <= 0 || n <= 0 || m > MUON_MAX_DIM || n > MUON_MAX_DIM)
+        return fail(MUON_ERR_SHAPE, "matrix %d has bad shape %lldx%lld", i, (long long)m, (long long)n);
+      if (!W[i] || !grad[i] || !mom[i]) return fail(MUON_ERR_ARG, "matrix %d has a NULL pointer", i);
+      if (reinterpret_cast<uintptr_t>(W[i]) % esz || reinterpret_cast<uintptr_t>(grad[i]) % esz ||
+          reinterpret_cast<uintptr_t>(mom[i]) % 4)
+        return fail(MUON_ERR_ALIGN, "matrix %d: pointer not aligned to its element size", i);
+      const size_t nel = static_cast<size_t>(m) * n;
+      if (overlaps(W[i], nel * esz, mom[i], nel * 4) || overlaps(W[i], nel * esz, grad[i], nel * esz) ||
+          overlaps(grad[i], nel * esz, mom[i], nel * 4))
+        return fail(MUON_ERR_ARG, "matrix %d: W, grad and mom overlap", i);
+      if (overlaps(ws, ws_bytes, W[i], nel * esz) || overlaps(ws, ws_bytes, mom[i], nel * 4))
+        return fail(MUON_ERR_ARG, "matrix %d overlaps the workspace", i);
+      mats[i].src = grad[i];
+      mats[i].mom = mom[i];
+      mats[i].dst = W[i];
+      mats[i].m = static_cast<int>(m);
+      mats[i].n = static_cast<int>(n);
+    }
+    return run_all(mats, steps, coeffs, dt, sc, beta, lr, true, true, ws, ws_bytes, stream);
+  } catch (...) {
+    return fail(MUON_ERR_ARG, "internal exception");
+  }
+}
+
+size_t muon_workspace_bytes(const int64_t* shapes, int count, int steps, muon_dtype dt, muon_sched sc) {
+  g_last_error.clear();
+  if (count < 0 || (count > 0 && !shapes) || !valid_dt(dt) || !valid_sc(sc) || steps < 0 || steps > MUON_MAX_STEPS) {
+    fail(MUON_ERR_ARG, "bad arguments to muon_workspace_bytes");
+    return 0;
+  }
+  std::vector<std::pair<long long, long long>> sh(count);
+  for (int i = 0; i < count; ++i) {
+    if (shapes[2 * i] <= 0 || shapes[2 * i + 1] <= 0 || shapes[2 * i] > MUON_MAX_DIM ||
+        shapes[2 * i + 1] > MUON_MAX_DIM) {
+      fail(MUON_ERR_SHAPE, "matrix %d has a bad shape", i);
+      return 0;
+    }
+    sh[i] = {shapes[2 * i], shapes[2 * i + 1]};
+  }
+  std::vector<int> order, start;
+  const int groups = bucket_plan(sh, order, start);
+  size_t best = kHeader;
+  for (int gi = 0; gi < groups; ++gi) {
+    const auto& s0 = sh[order[start[gi]]];
+    const Group g = make_group(s0.first, s0.second, steps, dt, sc);
+    const int w = std::min(start[gi + 1] - start[gi], kMaxBatch);
+    best = std::max(best, group_bytes(g, w, dt));
+  }
+  return best;
+}
+
+muon_sched muon_resolve_schedule(int64_t m, int64_t n, int steps, muon_dtype dt, muon_sched sc) {
+  return resolve(std::min<long long>(m, n), std::max<long long>(m, n), steps, dt, sc);
+}
+
+int muon_bucket_plan(const int64_t* shapes, int count, int* order, int* group_start) {
+  if (count < 0 || (count > 0 && (!shapes || !order || !group_start))) return -1;
+  std::vector<std::pair<long long, long long>> sh(count);
+  for (int i = 0; i < count; ++i) sh[i] = {shapes[2 * i], shapes[2 * i + 1]};
+  std::vector<int> ord, st;
+  const int groups = bucket_plan(sh, ord, st);
+  for (int i = 0; i < count; ++i) order[i] = ord[i];
+  for (int gi = 0; gi <= groups; ++gi) group_start[gi] = st[gi];
+  return groups;
+}
+
+muon_status muon_device_status(void* ws, void* stream) {
+  g_last_error.clear();
+  if (!ws) return fail(MUON_ERR_ARG, "workspace is NULL");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  int word = 0;
+  e = cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (word) {
+    const int zero = 0;
+    cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (word & kStatusTimeout) return fail(MUON_ERR_TIMEOUT, "a kernel gave up on a bounded wait");
+  }
+  return MUON_OK;
+}
+
+muon_status muon_debug_bounded_wait(void* ws, long long max_cycles, void* stream) {
+  g_last_error.clear();
+  if (!ws) return fail(MUON_ERR_ARG, "workspace is NULL");
+  if (max_cycles <= 0 || max_cycles > 10000000000LL) return fail(MUON_ERR_ARG, "max_cycles out of range");
+  const cudaError_t e = launch_debug_wait(static_cast<int*>(ws), max_cycles, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  return MUON_OK;
+}
+
+muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, const void* B_lo, int batch, int M,
+                            int N, int K, int split, int b_mn, int sym, muon_dtype dt, float* out, void* ws,
+                            size_t ws_bytes, void* stream) {
+  g_last_error.clear();
+  if (!A || !B || !out || !ws || batch <= 0 || batch > kMaxBatch) return fail(MUON_ERR_ARG, "bad pointers or batch");
+  if (ws_bytes < kHeader || reinterpret_cast<uintptr_t>(ws) % MUON_WS_ALIGN)
+    return fail(MUON_ERR_WORKSPACE, "workspace must hold the %zu-byte header", kHeader);
+  if (sym && M != N) return fail(MUON_ERR_SHAPE, "sym needs M == N");
+  if (b_mn != 0 && b_mn != 1) return fail(MUON_ERR_ARG, "b_mn must be 0 or 1");
+  EpiParams e;
+  memset(&e, 0, sizeof(e));
+  e.c_acc = 1.f;
+  e.Of = out;
+  e.ld = N;
+  e.bs = static_cast<long long>(M) * N;
+  e.rows_valid = M;
+  e.cols_valid = N;
+  const long long bsb = static_cast<long long>(N) * K;
+  cudaError_t err;
+  const char* why = nullptr;
+  if (dt == MUON_BF16) {
+    if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 256 || K % 64) return fail(MUON_ERR_SHAPE, "bf16 sizes");
+    if (split != 1 && split != 3) return fail(MUON_ERR_ARG, "split must be 1 or 3");
+    if (split == 3 && (!A_lo || !B_lo)) return fail(MUON_ERR_ARG, "split 3 needs A_lo and B_lo");
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(A_lo) |
+         reinterpret_cast<uintptr_t>(B_lo)) % 16)
+      return fail(MUON_ERR_ALIGN, "bf16 operands must be 16-byte aligned");
+    int major = 0, minor = 0;
+    muon_status ds;
+    const int sms = device_sms(&major, &minor, &ds);
+    if (ds != MUON_OK) return ds;
+    if (major != 10 || minor != 3) return fail(MUON_ERR_UNSUPPORTED, "needs sm_103a");
+    TcGemmDesc d;
+    d.B = batch;
+    d.M = M;
+    d.N = N;
+    d.K = K;
+    d.sym = sym;
+    d.split = split;
+    d.b_mn = b_mn;
+    d.A = TcOperand{static_cast<const bf16*>(A), static_cast<const bf16*>(A_lo), K, static_cast<long long>(M) * K};
+    d.Bop = TcOperand{static_cast<const bf16*>(B), static_cast<const bf16*>(B_lo), b_mn ? N : K, bsb};
+    err = launch_tc_gemm(d, e, static_cast<int*>(ws), static_cast<cudaStream_t>(stream), sms, &why);
+  } else if (dt == MUON_FP32) {
+    if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 16) return fail(MUON_ERR_SHAPE, "fp32 sizes");
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) % 16)
+      return fail(MUON_ERR_ALIGN, "fp32 operands must be 16-byte aligned");
+    SimtGemmDesc d{batch, M, N, K, sym, b_mn, static_cast<const float*>(A), K, static_cast<long long>(M) * K,
+                   static_cast<const float*>(B), b_mn ? N : K, bsb};
+    err = launch_simt_gemm(d, e, static_cast<cudaStream_t>(stream));
+  } else {
+    return fail(MUON_ERR_ARG, "bad dtype");
+  }
+  if (err != cudaSuccess)
+    return fail(MUON_ERR_CUDA, "launch: %s%s%s", cudaGetErrorString(err), why ? ": " : "", why ? why : "");
+  return MUON_OK;
+}
+
+void muon_profile_enable(int on) {
+  g_prof_on = on != 0;
+  g_prof.clear();
+  g_event_next = 0;
+}
+
+int muon_profile_count(void) { return static_cast<int>(g_prof.size()); }
+
+muon_status muon_profile_get(int i, const char** kind, float* ms, double* flops, double* bytes) {
+  g_last_error.clear();
+  if (i < 0 || i >= static_cast<int>(g_prof.size())) return fail(MUON_ERR_ARG, "no record %d", i);
+  const ProfRec& r = g_prof[i];
+  if (cudaEventSynchronize(r.b) != cudaSuccess) return fail(MUON_ERR_CUDA, "event synchronize failed");
+  float t = 0.f;
+  if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return fail(MUON_ERR_CUDA, "elapsed time failed");
+  if (kind) *kind = r.kind;
+  if (ms) *ms = t;
+  if (flops) *flops = r.flops;
+  if (bytes) *bytes = r.bytes;
+  return MUON_OK;
+}
+
+const char* muon_last_error(void) { return g_last_error.c_str(); }
+
+const char* muon_version(void) { return "muon-ns-gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,57 @@
+// kernels.h -- host-side launchers of the library's kernels (internal interface
+// between the engine and the .cu files; not part of the C ABI).
+#pragma once
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace muon {
+
+// A bf16 operand of the tensor-core GEMM: [batch][rows][ld] row-major, with an
+// optional residual part `lo` of the same layout (split operands).
+struct TcOperand {
+  const bf16* hi;
+  const bf16* lo;
+  long long ld;  // row stride (elements)
+  long long bs;  // batch stride (elements)
+};
+
+// C[b] (M x N) = A[b] (M x K, row-major) * op(B[b]):
+//   b_mn = 0: B stored [N][K] (K-major), C = A B^T      (symmetric right operands, SYRK)
+//   b_mn = 1: B stored [K][N] (MN-major), C = A B        (e.g. Q X)
+// sym = 1 computes only the tiles touching the lower triangle (M == N).
+struct TcGemmDesc {
+  int B, M, N, K;  // M % 128 == 0, N % 256 == 0, K % 64 == 0
+  int sym;
+  int split;  // 1 or 3
+  int b_mn;
+  TcOperand A, Bop;
+};
+
+cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* status, cudaStream_t st, int num_sms,
+                           const char** why);
+int tc_tiles(int M, int N, int sym);
+
+// fp32 SIMT GEMM with the same conventions (fp32 operands, 128 x 128 tiles).
+struct SimtGemmDesc {
+  int B, M, N, K;  // multiples of 128 (M, N) and 16 (K)
+  int sym;
+  int b_mn;
+  const float* A;
+  long long lda, bsa;
+  const float* Bm;
+  long long ldb, bsb;
+};
+cudaError_t launch_simt_gemm(const SimtGemmDesc& d, const EpiParams& epi, cudaStream_t st);
+
+// Momentum + pack + partial norms, then per-matrix 1 / (||M||_F + eps).
+cudaError_t launch_pack(const PackArgs& a, int B, cudaStream_t st);
+cudaError_t launch_norm_finalize(const float* partial, int tiles, int B, float eps, float* inv_norm,
+                                 cudaStream_t st);
+// O = Xf * inv_norm written through a final-mode epilogue (zero NS steps).
+cudaError_t launch_final_from_packed(const float* Xf, long long ld, long long bs, int B, const EpiParams& e,
+                                     cudaStream_t st);
+// Failure-detection self test: a bounded wait on a barrier that never completes.
+cudaError_t launch_debug_wait(int* status, long long cycles, cudaStream_t st);
+
+}  // namespace muon

@@ -1,0 +1,127 @@
+"""Unit tests of the library's GEMM kernels through the muon_debug_gemm hook,
+against PyTorch fp32 products of the same operands.  Ordered from the
+smallest single-tile case up, so a layout or descriptor slip shows up in the
+simplest shape that exhibits it."""
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+def _lib():
+    import newton_schulz_04_gb300 as m
+    m.load(build_if_missing=True)
+    return m
+
+
+def _rel(a, b):
+    return (a - b).norm().item() / max(b.norm().item(), 1e-30)
+
+
+def _ref(A, B, b_mn):
+    A = A.float()
+    B = B.float()
+    return A @ B if b_mn else A @ B.transpose(1, 2)
+
+
+def _rand(shape, seed, dtype=torch.bfloat16):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    return torch.randn(*shape, generator=g).to(dtype).cuda()
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (128, 256, 128), (256, 512, 320), (384, 768, 1024)])
+def test_tc_gemm_kmajor_b(M, N, K):
+    m = _lib()
+    A = _rand((2, M, K), 1)
+    B = _rand((2, N, K), 2)
+    out = m.debug_gemm(A, B)
+    torch.cuda.synchronize()
+    # same bf16 operands, fp32 accumulation on both sides: only summation order differs
+    assert _rel(out, _ref(A, B, False)) < 1e-5
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 192), (384, 1024, 512)])
+def test_tc_gemm_mnmajor_b(M, N, K):
+    m = _lib()
+    A = _rand((2, M, K), 3)
+    B = _rand((2, K, N), 4)
+    out = m.debug_gemm(A, B, b_mn=True)
+    torch.cuda.synchronize()
+    assert _rel(out, _ref(A, B, True)) < 1e-5
+
+
+@pytest.mark.parametrize("S,K", [(256, 64), (512, 256), (768, 1024)])
+def test_tc_syrk_lower_and_mirror(S, K):
+    m = _lib()
+    X = _rand((3, S, K), 5)
+    out = m.debug_gemm(X, X, sym=True)
+    torch.cuda.synchronize()
+    ref = _ref(X, X, False)
+    assert _rel(out, ref) < 1e-5
+    assert torch.equal(out, out.transpose(1, 2))
+
+
+def _split(x32):
+    hi = x32.to(torch.bfloat16)
+    lo = (x32 - hi.float()).to(torch.bfloat16)
+    return hi, lo
+
+
+@pytest.mark.parametrize("b_mn", [False, True])
+def test_tc_gemm_split3(b_mn):
+    m = _lib()
+    g = torch.Generator().manual_seed(6)
+    A32 = torch.randn(2, 256, 512, generator=g).cuda()
+    B32 = (torch.randn(2, 512, 512, generator=g) if b_mn else torch.randn(2, 512, 512, generator=g)).cuda()
+    Ah, Al = _split(A32)
+    Bh, Bl = _split(B32)
+    out = m.debug_gemm(Ah, Bh, Al, Bl, split=3, b_mn=b_mn)
+    torch.cuda.synchronize()
+    ref = _ref(A32.double(), B32.double(), b_mn).float()
+    one = _ref(Ah, Bh, b_mn)
+    # three products of ~8-bit operands reach ~16-bit operand accuracy
+    assert _rel(out, ref) < 2e-5
+    assert _rel(one, ref) > 1e-3
+
+
+def test_tc_sym_split3_symmetric_operands():
+    m = _lib()
+    g = torch.Generator().manual_seed(7)
+    X = torch.randn(2, 512, 512, generator=g, dtype=torch.float64)
+    Gs = (X @ X.transpose(1, 2)) / 512
+    Ps = Gs @ Gs - 0.5 * Gs
+    Gh, Gl = _split(Gs.float().cuda())
+    Ph, Pl = _split(Ps.float().cuda())
+    out = m.debug_gemm(Ph, Gh, Pl, Gl, split=3, sym=True)
+    torch.cuda.synchronize()
+    ref = (Ps @ Gs).float().cuda()
+    assert _rel(out, ref) < 2e-5
+    assert torch.equal(out, out.transpose(1, 2))
+
+
+@pytest.mark.parametrize("M,N,K,b_mn,sym", [(128, 128, 16, False, False), (256, 384, 80, True, False),
+                                             (384, 384, 48, False, True)])
+def test_simt_gemm(M, N, K, b_mn, sym):
+    m = _lib()
+    A = _rand((2, M, K), 8, torch.float32)
+    B = _rand((2, K, N) if b_mn else (2, N, K), 9, torch.float32)
+    if sym:
+        B = A
+    out = m.debug_gemm(A, B, b_mn=b_mn, sym=sym)
+    torch.cuda.synchronize()
+    ref = _ref(A.double(), B.double(), b_mn).float()
+    assert _rel(out, ref) < 1e-6
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    m = _lib()
+    ws = m.new_workspace(4096)
+    m.debug_bounded_wait(ws, 2_000_000)  # ~1 ms of SM cycles, nobody arrives
+    assert m.device_status(ws) == 6  # MUON_ERR_TIMEOUT
+    assert m.device_status(ws) == 0  # cleared
+    A = _rand((1, 128, 64), 10)
+    B = _rand((1, 256, 64), 11)
+    out = m.debug_gemm(A, B, workspace=ws)
+    torch.cuda.synchronize()
+    assert _rel(out, _ref(A, B, False)) < 1e-5
+    assert m.device_status(ws) == 0

@@ -1,0 +1,141 @@
+"""Host-side tests of the C ABI: the library loads on a CPU-only host, exports
+every entry point the header declares, validates arguments before touching
+the GPU, and groups matrices exactly like the reference grouping."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from newton_schulz_04_gb300 import build as b
+    b.build()
+    import newton_schulz_04_gb300 as m
+    return m.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "muon_ns.h")).read()
+    return sorted(set(re.findall(r"MUON_API\s+[\w\s\*]*?\b(muon_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    syms = declared_symbols()
+    for s in ["muon_ns_batched", "muon_step", "muon_workspace_bytes", "muon_last_error", "muon_device_status"]:
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+        assert ctypes.cast(getattr(lib, s), ctypes.c_void_p).value
+
+
+def test_bucket_plan_matches_reference_grouping(lib):
+    import newton_schulz_04_gb300 as m
+    g = torch.Generator().manual_seed(0)
+    for trial in range(50):
+        n = int(torch.randint(1, 40, (1,), generator=g))
+        dims = [64, 128, 200, 256]
+        shapes = [(dims[int(torch.randint(0, 4, (1,), generator=g))], dims[int(torch.randint(0, 4, (1,), generator=g))])
+                  for _ in range(n)]
+        order, start = m.bucket_plan(shapes)
+        ref = oracle.bucket_order(shapes)
+        got = [((min(shapes[order[start[k]]]), max(shapes[order[start[k]]])), order[start[k]:start[k + 1]])
+               for k in range(len(start) - 1)]
+        assert got == ref
+
+
+def test_bucket_plan_llama_shapes(lib):
+    import newton_schulz_04_gb300 as m
+    shapes = synth.c3_shapes()
+    order, start = m.bucket_plan(shapes)
+    assert start == [0, 128, 224]
+    assert order[:4] == [0, 1, 2, 3]
+    assert sorted(order) == list(range(len(shapes)))
+
+
+def test_schedule_choice(lib):
+    import newton_schulz_04_gb300 as m
+    # symmetric-aware tensor work: ORIG T(3 s^2 l + s^3) vs split Gram 9 s^2 l + 3 (4T-3) s^3
+    assert m.resolve_schedule(1024, 1024) == "orig"
+    assert m.resolve_schedule(4096, 14336) == "orig"
+    assert m.resolve_schedule(1024, 8192) == "gram_x3"
+    assert m.resolve_schedule(16384, 1024) == "gram_x3"
+    assert m.resolve_schedule(1024, 8192, steps=0) == "orig"
+    assert m.resolve_schedule(1024, 8192, schedule="gram_x1") == "gram_x1"
+    assert m.resolve_schedule(128, 256, dtype=torch.float32) == "gram_x3"
+    assert m.resolve_schedule(128, 128, dtype=torch.float32) == "orig"
+
+
+def test_workspace_sizes(lib):
+    import newton_schulz_04_gb300 as m
+    one = m.workspace_bytes([(1024, 1024)])
+    many = m.workspace_bytes([(1024, 1024)] * 16)
+    assert many > one
+    # ORIG bf16 per matrix: fp32 X + 2 bf16 X + fp32 A + bf16 A + bf16 B
+    assert many >= 16 * 1024 * 1024 * (4 + 4 + 4 + 2 + 2)
+    assert m.workspace_bytes([(1024, 1024)] * 300) == m.workspace_bytes([(1024, 1024)] * 256)
+
+
+def _ns_call(lib, X=1, B=1, m=8, n=8, steps=5, out=2, dt=0, sc=0, ws=256, wsb=1 << 20, coeffs=None):
+    return lib.muon_ns_batched(ctypes.c_void_p(X), B, m, n, steps, coeffs, ctypes.c_void_p(out), dt, sc,
+                               ctypes.c_void_p(ws), wsb, None)
+
+
+def test_argument_errors_before_any_launch(lib):
+    E = {"arg": 1, "shape": 2, "align": 3, "ws": 4}
+    big = 1 << 40
+    assert _ns_call(lib, X=0, out=big) == E["arg"]
+    assert _ns_call(lib, B=-1) == E["arg"]
+    assert _ns_call(lib, X=big, out=2 * big, m=0) == E["shape"]
+    assert _ns_call(lib, X=big, out=2 * big, n=70000) == E["shape"]
+    assert _ns_call(lib, X=big, out=2 * big, steps=-1) == E["arg"]
+    assert _ns_call(lib, X=big, out=2 * big, steps=1000) == E["arg"]
+    assert _ns_call(lib, X=big, out=2 * big, dt=7) == E["arg"]
+    assert _ns_call(lib, X=big, out=2 * big, sc=9) == E["arg"]
+    assert _ns_call(lib, X=big, out=2 * big, ws=0) == E["arg"]
+    assert _ns_call(lib, X=big, out=2 * big, ws=big + 8 * 1024 * 1024 + 3) == E["align"]
+    assert _ns_call(lib, X=big + 1, out=2 * big) == E["align"]
+    assert _ns_call(lib, X=big, out=big + 64) == E["arg"]  # overlap
+    nan = (ctypes.c_float * 3)(float("nan"), 0.0, 0.0)
+    assert _ns_call(lib, X=big, out=2 * big, coeffs=nan) == E["arg"]
+    # workspace too small for one 4096 x 4096 matrix
+    assert _ns_call(lib, X=big, out=2 * big, m=4096, n=4096, ws=4 * big, wsb=1 << 20) == E["ws"]
+    assert "workspace" in lib.muon_last_error().decode()
+
+
+def test_step_argument_errors(lib):
+    P = ctypes.c_void_p * 2
+    shapes = (ctypes.c_int64 * 4)(8, 8, 8, 8)
+    big = 1 << 40
+    W = P(big, big + (1 << 20))
+    G = P(2 * big, 2 * big + (1 << 20))
+    Mm = P(3 * big, 3 * big + (1 << 20))
+    ws = ctypes.c_void_p(4 * big)
+    if not torch.cuda.is_available():
+        # Every argument is valid (the pointers are fake), so this call gets as far
+        # as the first CUDA call, which fails cleanly on a host without a GPU.  It
+        # is never made where a GPU exists: there it would launch on fake pointers.
+        st = lib.muon_step(W, G, Mm, shapes, 2, 0.95, 0.02, 5, None, 0, 0, ws, 1 << 26, None)
+        assert st == 5
+    bad = P(big, 0)
+    assert lib.muon_step(bad, G, Mm, shapes, 2, 0.95, 0.02, 5, None, 0, 0, ws, 1 << 20, None) == 1
+    assert lib.muon_step(W, G, Mm, shapes, -1, 0.95, 0.02, 5, None, 0, 0, ws, 1 << 20, None) == 1
+    assert lib.muon_step(W, G, Mm, shapes, 2, float("inf"), 0.02, 5, None, 0, 0, ws, 1 << 20, None) == 1
+    Wo = P(3 * big, big + (1 << 20))  # W[0] aliases mom[0]
+    assert lib.muon_step(Wo, G, Mm, shapes, 2, 0.95, 0.02, 5, None, 0, 0, ws, 1 << 20, None) == 1
+    shp_bad = (ctypes.c_int64 * 4)(8, -8, 8, 8)
+    assert lib.muon_step(W, G, Mm, shp_bad, 2, 0.95, 0.02, 5, None, 0, 0, ws, 1 << 20, None) == 2
+
+
+def test_empty_batch_is_a_noop(lib):
+    assert _ns_call(lib, X=1 << 40, B=0, out=1 << 41, ws=1 << 42) == 0
