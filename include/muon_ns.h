@@ -75,7 +75,7 @@ typedef enum {
     MUON_SCHED_AUTO = 0,     /* cheapest schedule that meets the dtype's accuracy (see below) */
     MUON_SCHED_GRAM_X3 = 1,  /* Gram space; symmetric products with split-bf16 operands (hi*hi + hi*lo + lo*hi) */
     MUON_SCHED_GRAM_X1 = 2,  /* Gram space; plain bf16 operands (fast mode, larger error) */
-    MUON_SCHED_ORIG = 3      /* original space; bf16 operands, fp32 carry of X */
+    MUON_SCHED_ORIG = 3      /* original space; fp32 carry of X, split-bf16 A in A*A and B in B*X */
 } muon_sched;
 
 #define MUON_MAX_DIM 65536   /* largest accepted m or n */
@@ -165,8 +165,9 @@ MUON_API muon_status muon_debug_bounded_wait(void* ws, long long max_cycles, voi
  *   A [M, K] row-major and B either [N, K] row-major (b_mn = 0, out = A B^T)
  *   or [K, N] row-major (b_mn = 1, out = A B).  Batch strides are M*K, N*K
  *   (or K*N) and M*N elements.  dt = MUON_BF16 runs the tcgen05 tensor-core
- *   kernel (split = 1: A, B; split = 3: A = A + A_lo, B = B + B_lo with the
- *   three-product split; A_lo/B_lo ignored for split 1); dt = MUON_FP32 runs
+ *   kernel (split = 1: A, B; split = 2: (A + A_lo) B, supported with
+ *   b_mn = 1 only; split = 3: A = A + A_lo, B = B + B_lo with the
+ *   three-product split; unused lo parts are ignored); dt = MUON_FP32 runs
  *   the FFMA kernel (A, B fp32).  sym = 1 (M == N) computes only the lower
  *   triangle and mirrors it.  Sizes: bf16 needs M % 128, N % 256, K % 64 == 0;
  *   fp32 needs M, N % 128 and K % 16 == 0.  Synchronous error checking only;

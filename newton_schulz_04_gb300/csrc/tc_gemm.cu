@@ -16,7 +16,7 @@
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, fused scalar epilogue
 //               (EpiParams), global stores
 //
-// Operand modes (template SPLIT): 1: A*B; 3: Ah*Bh + Ah*Bl + Al*Bh where
+// Operand modes (template SPLIT): 1: A*B; 2: Ah*B + Al*B; 3: Ah*Bh + Ah*Bl + Al*Bh where
 // X = Xh + Xl is a value split into a bf16 head and a bf16 residual (about 16
 // significant bits per operand, fp32 accumulation).  B is read K-major
 // ([N, K] row-major, used for symmetric right operands, whose rows are their
@@ -430,6 +430,7 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* statu
   *why = nullptr;
   if (d.split == 1 && !d.b_mn) return launch_impl<1, false, 128>(d, epi, status, st, num_sms, why);
   if (d.split == 1 && d.b_mn) return launch_impl<1, true, 128>(d, epi, status, st, num_sms, why);
+  if (d.split == 2 && d.b_mn) return launch_impl<2, true, 64>(d, epi, status, st, num_sms, why);
   if (d.split == 3 && !d.b_mn) return launch_impl<3, false, 64>(d, epi, status, st, num_sms, why);
   if (d.split == 3 && d.b_mn) return launch_impl<3, true, 64>(d, epi, status, st, num_sms, why);
   *why = "unsupported operand split";

@@ -84,6 +84,19 @@ def test_tc_gemm_split3(b_mn):
     assert _rel(one, ref) > 1e-3
 
 
+def test_tc_gemm_split2_mnmajor():
+    m = _lib()
+    g = torch.Generator().manual_seed(12)
+    A32 = torch.randn(2, 256, 512, generator=g).cuda()
+    B = torch.randn(2, 512, 768, generator=g).to(torch.bfloat16).cuda()
+    Ah, Al = _split(A32)
+    out = m.debug_gemm(Ah, B, Al, None, split=2, b_mn=True)
+    torch.cuda.synchronize()
+    ref = (A32.double() @ B.double()).float()
+    assert _rel(out, ref) < 2e-5
+    assert _rel(_ref(Ah, B, True), ref) > 1e-3
+
+
 def test_tc_sym_split3_symmetric_operands():
     m = _lib()
     g = torch.Generator().manual_seed(7)

@@ -17,6 +17,8 @@ pytestmark = pytest.mark.gpu
 
 TOL_BF16 = 2e-2
 TOL_FP32 = 1e-4
+# The C ABI takes beta as fp32; the oracle is given that same value (widened).
+BETA32 = float(np.float32(0.95))
 
 
 def _m():
@@ -127,18 +129,42 @@ def _check_step(shapes, dtype=torch.bfloat16, seed=0, sched="auto", steps=5, mom
     m.muon_step(W, G, M, beta=0.95, lr=0.02, steps=steps, schedule=sched, workspace=ws)
     torch.cuda.synchronize()
     for i in range(len(shapes)):
-        Wn, Mn, O = oracle.muon_update(Ws[i], Gs[i], Ms[i], 0.95, 0.02, steps)
+        Wn, Mn, O = oracle.muon_update(Ws[i], Gs[i], Ms[i], BETA32, 0.02, steps)
         Mg = M[i].cpu().double().numpy()
         # fp32 momentum within one ulp of the fp64 value
         ulp = np.spacing(np.abs(Mn).astype(np.float32)).astype(np.float64)
         assert np.all(np.abs(Mg - Mn) <= ulp), i
         Wg = W[i].cpu().double().numpy()
-        if dtype == torch.bfloat16:
-            ref = oracle.bf16_round(Wn)
-            assert np.all(np.abs(Wg - ref) <= bf16_ulp(ref)), i
-        else:
-            O_gpu = (Ws[i].double().numpy() - Wg) / 0.02
-            assert rel(O_gpu, O) < 10 * TOL_FP32, i
+        W0 = Ws[i].double().numpy()
+        # W_gpu = round(W0 - lr O_gpu): the implied O differs from O_gpu by at most
+        # half a unit of W's last place per element, divided by lr.
+        q = np.linalg.norm((bf16_ulp(Wg) if dtype == torch.bfloat16 else np.spacing(np.abs(Wg).astype(np.float32)))
+                           / 2) / (0.02 * np.linalg.norm(O))
+        tol = (TOL_BF16 if dtype == torch.bfloat16 else TOL_FP32) + 1.01 * q
+        assert rel((W0 - Wg) / 0.02, O) < tol, (i, rel((W0 - Wg) / 0.02, O), tol)
+
+
+def test_apply_and_momentum_exact_at_zero_steps():
+    """With zero NS steps O = M / (||M||_F + eps) is known to fp32 accuracy, so
+    the bf16 weight must be within one bf16 ulp of RNE(W0 - lr O) and the fp32
+    momentum within one fp32 ulp of beta*M0 + G."""
+    m = _m()
+    shapes = [(256, 512), (512, 256), (200, 328)]
+    Ws = [synth.random_matrix(a, b, seed=2000 + i, std=0.02).to(torch.bfloat16) for i, (a, b) in enumerate(shapes)]
+    Gs = [synth.random_matrix(a, b, seed=2100 + i).to(torch.bfloat16) for i, (a, b) in enumerate(shapes)]
+    Ms = [synth.random_matrix(a, b, seed=2200 + i) for i, (a, b) in enumerate(shapes)]
+    W = [w.clone().cuda() for w in Ws]
+    G = [g.clone().cuda() for g in Gs]
+    M = [x.clone().cuda() for x in Ms]
+    lr = 0.5  # large, so O is visible above W's rounding
+    m.muon_step(W, G, M, beta=0.95, lr=lr, steps=0)
+    torch.cuda.synchronize()
+    for i in range(len(shapes)):
+        Wn, Mn, O = oracle.muon_update(Ws[i], Gs[i], Ms[i], BETA32, lr, 0)
+        ulp = np.spacing(np.abs(Mn).astype(np.float32)).astype(np.float64)
+        assert np.all(np.abs(M[i].cpu().double().numpy() - Mn) <= ulp), i
+        ref = oracle.bf16_round(Wn)
+        assert np.all(np.abs(W[i].cpu().double().numpy() - ref) <= bf16_ulp(ref)), i
 
 
 def test_muon_step_mixed_shapes_and_orientations():
@@ -213,9 +239,11 @@ def test_c2_full_size_sampled():
     torch.cuda.synchronize()
     for i in [0, 13]:
         Wn, Mn, O = oracle.muon_update(w.weights[i], w.grads[i], np.zeros((1024, 1024)), w.beta, w.lr, 5)
-        ref = oracle.bf16_round(Wn)
         Wg = W[i].cpu().double().numpy()
-        assert np.all(np.abs(Wg - ref) <= bf16_ulp(ref))
+        W0 = w.weights[i].double().numpy()
+        q = np.linalg.norm(bf16_ulp(Wg) / 2) / (w.lr * np.linalg.norm(O))
+        assert rel((W0 - Wg) / w.lr, O) < TOL_BF16 + 1.01 * q
+        assert np.array_equal(M[i].cpu().double().numpy(), Mn)
     # O itself at full size through muon_ns_batched
     X = torch.stack(G[:4])
     O = m.ns_batched(X, steps=5)
