@@ -161,21 +161,21 @@ MUON_API muon_status muon_debug_bounded_wait(void* ws, long long max_cycles, voi
 
 /*
  * muon_debug_gemm -- test hook exposing one batched GEMM kernel on its own.
- *   out[b] (fp32, [M, N] row-major, ld = N) = A[b] * op(B[b]) with
- *   A [M, K] row-major and B either [N, K] row-major (b_mn = 0, out = A B^T)
- *   or [K, N] row-major (b_mn = 1, out = A B).  Batch strides are M*K, N*K
- *   (or K*N) and M*N elements.  dt = MUON_BF16 runs the tcgen05 tensor-core
- *   kernel (split = 1: A, B; split = 2: (A + A_lo) B, supported with
- *   b_mn = 1 only; split = 3: A = A + A_lo, B = B + B_lo with the
- *   three-product split; unused lo parts are ignored); dt = MUON_FP32 runs
- *   the FFMA kernel (A, B fp32).  sym = 1 (M == N) computes only the lower
- *   triangle and mirrors it.  Sizes: bf16 needs M % 128, N % 256, K % 64 == 0;
- *   fp32 needs M, N % 128 and K % 16 == 0.  Synchronous error checking only;
- *   the kernel is enqueued on `stream`.
+ *   C[b] = A[b] * op(B[b]) with A [M, K] row-major and B either [N, K]
+ *   row-major (b_mn = 0, C = A B^T) or [K, N] row-major (b_mn = 1, C = A B).
+ *   Batch strides are M*K, N*K (or K*N) and M*N elements.
+ *   dt = MUON_BF16 runs the tcgen05 tensor-core kernel: split = 1 uses A, B;
+ *   split = 2 uses (A + A_lo) B (b_mn = 1 only); split = 3 uses
+ *   A B + A B_lo + A_lo B.  C is returned as a bf16 pair: out = bf16(C) and,
+ *   if out_lo is not NULL, out_lo = bf16(C - out) ([batch, M, N] each).
+ *   dt = MUON_FP32 runs the FFMA kernel on fp32 A, B and writes fp32 C to out.
+ *   sym = 1 (M == N) computes only the lower triangle and mirrors it.
+ *   Sizes: bf16 needs M % 128, N % 256, K % 64 == 0; fp32 needs M, N % 128 and
+ *   K % 16 == 0.  The kernel is enqueued on `stream`.
  */
 MUON_API muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, const void* B_lo, int batch,
                                      int M, int N, int K, int split, int b_mn, int sym, muon_dtype dt,
-                                     float* out, void* ws, size_t ws_bytes, void* stream);
+                                     void* out, void* out_lo, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Launch profiling (process-wide, not thread safe; off by default).

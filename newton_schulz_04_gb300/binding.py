@@ -64,7 +64,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.muon_device_status.restype = i32
     lib.muon_debug_bounded_wait.argtypes = [vp, ctypes.c_longlong, vp]
     lib.muon_debug_bounded_wait.restype = i32
-    lib.muon_debug_gemm.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, sz, vp]
+    lib.muon_debug_gemm.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, sz, vp]
     lib.muon_debug_gemm.restype = i32
     lib.muon_profile_enable.argtypes = [i32]
     lib.muon_profile_enable.restype = None
@@ -206,18 +206,26 @@ def debug_bounded_wait(workspace: torch.Tensor, max_cycles: int, stream=None) ->
 
 
 def debug_gemm(A, B, A_lo=None, B_lo=None, split=1, b_mn=False, sym=False, workspace=None, stream=None):
-    """Test hook: fp32 out[b] = A[b] @ (B[b] if b_mn else B[b]^T) through one library kernel."""
+    """Test hook: out[b] = A[b] @ (B[b] if b_mn else B[b]^T) through one library kernel.
+
+    bf16 operands run the tensor-core kernel and return the fp32 sum of the
+    bf16 head/residual pair it writes; fp32 operands run the FFMA kernel."""
     lib = load()
     batch, M, K = A.shape
     N = B.shape[2] if b_mn else B.shape[1]
-    out = torch.zeros(batch, M, N, dtype=torch.float32, device=A.device)
     if workspace is None:
         workspace = new_workspace(4096, A.device)
     ptr = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    if A.dtype == torch.float32:
+        out = torch.zeros(batch, M, N, dtype=torch.float32, device=A.device)
+        lo = None
+    else:
+        out = torch.zeros(batch, M, N, dtype=torch.bfloat16, device=A.device)
+        lo = torch.zeros_like(out)
     _check(lib.muon_debug_gemm(ptr(A), ptr(A_lo), ptr(B), ptr(B_lo), batch, M, N, K, split, int(b_mn), int(sym),
-                               _dtype_code(A.dtype), ptr(out), ptr(workspace), workspace.numel(),
+                               _dtype_code(A.dtype), ptr(out), ptr(lo), ptr(workspace), workspace.numel(),
                                ctypes.c_void_p(_stream_ptr(stream))))
-    return out
+    return out if lo is None else out.float() + lo.float()
 
 
 def profile_enable(on: bool = True) -> None:

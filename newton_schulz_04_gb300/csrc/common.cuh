@@ -20,25 +20,29 @@ enum FinalMode : int { FINAL_NONE = 0, FINAL_STORE = 1, FINAL_APPLY = 2 };
 //   v = sc_b * (c_acc * acc + c_res * R[b][r][c]) + (r == c && r < rows_valid ? c_id : 0)
 //   sc_b = 1, inv_norm[b] or inv_norm[b]^2 (scale_pow = 0, 1, 2)
 //
-// and then either stores v into packed buffers (fp32 `Of`, bf16 `Oh`, and the
-// bf16 residual `Ol` = bf16(v - float(Oh)), so that Oh + Ol carries ~16
-// significant bits), or, in a final mode, writes v (FINAL_STORE) or applies
-// W <- W - lr * v (FINAL_APPLY) to the caller's un-packed matrix dst[b].
-// With `sym` set only elements with r >= c are produced, and each one with
-// r > c is also written at (c, r): the output is symmetric by construction.
+// R is either fp32 (`R`, CUDA-core path) or a bf16 pair (`Rh` + `Rl`,
+// tensor-core path).  v is then stored into packed buffers -- fp32 `Of`
+// (CUDA-core path) or the bf16 pair `Oh` = bf16(v), `Ol` = bf16(v - Oh), which
+// carries ~16 significant bits (tensor-core path) -- or, in a final mode,
+// written (FINAL_STORE) or applied as W <- W - lr * v (FINAL_APPLY) to the
+// caller's un-packed matrix dst[b].  With `sym` set only the lower triangle is
+// computed and every stored element is also stored at its mirror position, so
+// the output is symmetric by construction.
 struct EpiParams {
   const float* inv_norm;  // [B] 1 / (||X||_F + eps)
   int scale_pow;
   float c_acc, c_res, c_id;
-  const float* R;  // packed fp32 residual or nullptr
-  float* Of;       // packed fp32 output or nullptr
-  bf16* Oh;        // packed bf16 output or nullptr
-  bf16* Ol;        // packed bf16 low part or nullptr
-  long long ld;    // leading dimension (elements) of R / Of / Oh / Ol
-  long long bs;    // batch stride (elements) of R / Of / Oh / Ol
+  const float* R;   // packed fp32 residual or nullptr (CUDA-core path)
+  float* Of;        // packed fp32 output or nullptr (CUDA-core path)
+  const bf16* Rh;   // packed bf16 residual pair or nullptr (tensor-core path)
+  const bf16* Rl;
+  bf16* Oh;         // packed bf16 output pair (tensor-core path; written through TMA maps)
+  bf16* Ol;         // may be nullptr when only the head is needed
+  long long ld;     // leading dimension (elements) of the packed residual / outputs
+  long long bs;     // batch stride (elements)
   int sym;
-  int rows_valid;  // true short side s (padding rows are >= s)
-  int cols_valid;  // true long side (or s for square outputs)
+  int rows_valid;   // true short side s (padding rows are >= s)
+  int cols_valid;   // true long side (or s for square outputs)
   // final-mode fields
   int final_mode;
   int dst_fp32;  // 1: dst is fp32, 0: bf16
@@ -69,18 +73,7 @@ __device__ __forceinline__ void epi_final_elem(const EpiParams& e, int b, int p,
   }
 }
 
-// Store of one element into the packed outputs (no symmetry handling).
-__device__ __forceinline__ void epi_store_elem(const EpiParams& e, long long off, float v) {
-  if (e.Of) e.Of[off] = v;
-  if (e.Oh) {
-    const bf16 h = __float2bfloat16_rn(v);
-    e.Oh[off] = h;
-    if (e.Ol) e.Ol[off] = __float2bfloat16_rn(v - __bfloat162float(h));
-  }
-}
-
-// Full scalar epilogue for one accumulator element (used by the SIMT kernels
-// and by tensor-core tiles on the diagonal or at ragged edges).
+// Full scalar epilogue of one fp32 accumulator element (CUDA-core path).
 __device__ __forceinline__ void epi_elem(const EpiParams& e, int b, int r, int c, float acc, float sc) {
   if (e.sym && c > r) return;
   float v = e.c_acc * acc;
@@ -92,8 +85,8 @@ __device__ __forceinline__ void epi_elem(const EpiParams& e, int b, int r, int c
     return;
   }
   const long long base = (long long)b * e.bs;
-  epi_store_elem(e, base + (long long)r * e.ld + c, v);
-  if (e.sym && r > c) epi_store_elem(e, base + (long long)c * e.ld + r, v);
+  e.Of[base + (long long)r * e.ld + c] = v;
+  if (e.sym && r > c) e.Of[base + (long long)c * e.ld + r] = v;
 }
 
 // Arguments of the momentum / pack / norm kernel.

@@ -26,7 +26,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/muon_ns.h"
+#include "muon_ns.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -88,6 +88,8 @@ struct ProfScope {
 
 static const float kQuintic[3] = {3.4445f, -4.7750f, 2.0315f};
 static const float kEps = 1e-7f;
+// ORIG: number of final NS steps whose A*A and B*X products use split operands.
+static const int kSplitSteps = 3;
 
 static inline long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 
@@ -132,10 +134,12 @@ static muon_sched resolve(long long s, long long l, int steps, muon_dtype dt, mu
   if (steps == 0) return MUON_SCHED_ORIG;  // only the packed fp32 copy is needed
   if (sc != MUON_SCHED_AUTO) return sc;
   // Tensor-core work (symmetric products counted once):
-  //   ORIG     T (5 s^2 l + 3 s^3): SYRK s^2 l, split A*A 3 s^3, split B*X 4 s^2 l
+  //   ORIG     per plain step 3 s^2 l + s^3, per split step 5 s^2 l + 3 s^3
+  //            (SYRK s^2 l, A*A s^3 or 3 s^3, B*X 2 s^2 l or 4 s^2 l)
   //   GRAM_X3  3 s^2 l (SYRK, split) + 3 (4T - 3) s^3 + 6 s^2 l (Q X0, split)
   const double S = static_cast<double>(s), L = static_cast<double>(l), T = steps;
-  const double orig = T * (5 * S * S * L + 3 * S * S * S);
+  const double ns = std::min<double>(T, kSplitSteps);
+  const double orig = (T - ns) * (3 * S * S * L + S * S * S) + ns * (5 * S * S * L + 3 * S * S * S);
   const double x3 = 9 * S * S * L + 3 * (4 * T - 3) * S * S * S;
   return x3 < orig ? MUON_SCHED_GRAM_X3 : MUON_SCHED_ORIG;
 }
@@ -161,6 +165,7 @@ struct Buffers {
   float* Xf = nullptr;
   float* Xf2 = nullptr;
   bf16* Xb[2] = {nullptr, nullptr};
+  bf16* Xlo[2] = {nullptr, nullptr};
   bf16* Xl = nullptr;
   // s x s
   float* Gf = nullptr;
@@ -182,14 +187,15 @@ struct Buffers {
 };
 
 static size_t carve_buffers(char* base, int Bc, long long sp, long long lp, int tiles, muon_dtype dt,
-                            muon_sched sc, Buffers& bf) {
+                            muon_sched sc, int steps, Buffers& bf) {
   Carve c{base, kHeader};
   const size_t nx = static_cast<size_t>(Bc) * sp * lp;
   const size_t ns = static_cast<size_t>(Bc) * sp * sp;
   bf.inv_norm = static_cast<float*>(c.take(sizeof(float) * Bc));
   bf.partial = static_cast<float*>(c.take(sizeof(float) * Bc * static_cast<size_t>(tiles)));
-  if (dt == MUON_FP32) {
+  if (dt == MUON_FP32 || steps == 0) {
     bf.Xf = static_cast<float*>(c.take(4 * nx));
+    if (steps == 0) return c.off;
     if (sc == MUON_SCHED_ORIG) {
       bf.Xf2 = static_cast<float*>(c.take(4 * nx));
       bf.Af = static_cast<float*>(c.take(4 * ns));
@@ -203,10 +209,11 @@ static size_t carve_buffers(char* base, int Bc, long long sp, long long lp, int 
     return c.off;
   }
   if (sc == MUON_SCHED_ORIG) {
-    bf.Xf = static_cast<float*>(c.take(4 * nx));
-    bf.Xb[0] = static_cast<bf16*>(c.take(2 * nx));
-    bf.Xb[1] = static_cast<bf16*>(c.take(2 * nx));
-    bf.Gf = static_cast<float*>(c.take(4 * ns));
+    // X carried as a bf16 pair (head + residual, ~16 significant bits), ping-ponged
+    for (int q = 0; q < 2; ++q) {
+      bf.Xb[q] = static_cast<bf16*>(c.take(2 * nx));
+      bf.Xlo[q] = static_cast<bf16*>(c.take(2 * nx));
+    }
     bf.Gh = static_cast<bf16*>(c.take(2 * ns));
     bf.Gl = static_cast<bf16*>(c.take(2 * ns));
     bf.Bh = static_cast<bf16*>(c.take(2 * ns));
@@ -216,9 +223,8 @@ static size_t carve_buffers(char* base, int Bc, long long sp, long long lp, int 
   const bool x3 = (sc == MUON_SCHED_GRAM_X3);
   bf.Xb[0] = static_cast<bf16*>(c.take(2 * nx));
   if (x3) bf.Xl = static_cast<bf16*>(c.take(2 * nx));
-  bf.Gf = static_cast<float*>(c.take(4 * ns));
   bf.Gh = static_cast<bf16*>(c.take(2 * ns));
-  if (x3) bf.Gl = static_cast<bf16*>(c.take(2 * ns));
+  bf.Gl = static_cast<bf16*>(c.take(2 * ns));  // kept in both modes: G = Gh + Gl feeds the P epilogue
   for (int q = 0; q < 2; ++q) {
     bf.Ph[q] = static_cast<bf16*>(c.take(2 * ns));
     if (x3) bf.Pl[q] = static_cast<bf16*>(c.take(2 * ns));
@@ -234,6 +240,7 @@ struct Group {
   long long s, l, sp, lp;
   int tiles;  // pack tiles per matrix
   muon_sched sc;
+  int steps;
 };
 
 static Group make_group(long long m, long long n, int steps, muon_dtype dt, muon_sched sc) {
@@ -244,12 +251,13 @@ static Group make_group(long long m, long long n, int steps, muon_dtype dt, muon
   g.lp = round_up(g.l, 256);
   g.tiles = static_cast<int>((g.sp / 64) * (g.lp / 64));
   g.sc = resolve(g.s, g.l, steps, dt, sc);
+  g.steps = steps;
   return g;
 }
 
 static size_t group_bytes(const Group& g, int Bc, muon_dtype dt) {
   Buffers bf;
-  return carve_buffers(nullptr, Bc, g.sp, g.lp, g.tiles, dt, g.sc, bf);
+  return carve_buffers(nullptr, Bc, g.sp, g.lp, g.tiles, dt, g.sc, g.steps, bf);
 }
 
 // Largest batch width that fits in ws_bytes (0 if none).
@@ -302,8 +310,9 @@ struct Ctx {
                   why ? why : "");                                                                \
   } while (0)
 
+// fp32 (CUDA-core) epilogue: residual R and output Of.
 static EpiParams epi_packed(const Group& g, const Buffers& bf, int scale_pow, float c_acc, float c_res, float c_id,
-                            const float* R, float* Of, bf16* Oh, bf16* Ol, long long ld, long long bs) {
+                            const float* R, float* Of, long long ld, long long bs) {
   EpiParams e;
   memset(&e, 0, sizeof(e));
   e.inv_norm = bf.inv_norm;
@@ -313,13 +322,22 @@ static EpiParams epi_packed(const Group& g, const Buffers& bf, int scale_pow, fl
   e.c_id = c_id;
   e.R = R;
   e.Of = Of;
-  e.Oh = Oh;
-  e.Ol = Ol;
   e.ld = ld;
   e.bs = bs;
   e.rows_valid = static_cast<int>(g.s);
   e.cols_valid = static_cast<int>(g.s);
   e.final_mode = FINAL_NONE;
+  return e;
+}
+
+// bf16-pair (tensor-core) epilogue: residual Rh + Rl and outputs Oh (+ Ol).
+static EpiParams epi_pair(const Group& g, const Buffers& bf, int scale_pow, float c_acc, float c_res, float c_id,
+                          const bf16* Rh, const bf16* Rl, bf16* Oh, bf16* Ol, long long ld, long long bs) {
+  EpiParams e = epi_packed(g, bf, scale_pow, c_acc, c_res, c_id, nullptr, nullptr, ld, bs);
+  e.Rh = Rh;
+  e.Rl = Rl;
+  e.Oh = Oh;
+  e.Ol = Ol;
   return e;
 }
 
@@ -341,7 +359,7 @@ static void epi_set_final(EpiParams& e, const Ctx& cx, const Group& g, const Mat
 static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int Bc, char* ws) {
   const char* why = nullptr;
   Buffers bf;
-  carve_buffers(ws, Bc, g.sp, g.lp, g.tiles, cx.dt, g.sc, bf);
+  carve_buffers(ws, Bc, g.sp, g.lp, g.tiles, cx.dt, g.sc, cx.steps, bf);
   const long long sp = g.sp, lp = g.lp;
   const long long bsx = sp * lp, bss = sp * sp;
   const bool fp32 = cx.dt == MUON_FP32;
@@ -360,9 +378,11 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   pa.bs = bsx;
   pa.partial = bf.partial;
   pa.tiles = g.tiles;
-  if (fp32 || g.sc == MUON_SCHED_ORIG) pa.Xf = bf.Xf;
-  if (!fp32) pa.Xh = bf.Xb[0];
-  if (!fp32 && x3) pa.Xl = bf.Xl;
+  pa.Xf = bf.Xf;  // fp32 path, or zero steps
+  if (!fp32 && cx.steps > 0) {
+    pa.Xh = bf.Xb[0];
+    pa.Xl = g.sc == MUON_SCHED_ORIG ? bf.Xlo[0] : (x3 ? bf.Xl : nullptr);
+  }
   for (int q = 0; q < Bc; ++q) {
     // a bucket can mix m x n and n x m members: the pack kernel transposes per member
     pa.src[q] = mats[q].src;
@@ -402,7 +422,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   }
 
   if (cx.steps == 0) {
-    EpiParams e = epi_packed(g, bf, 1, 1.f, 0.f, 0.f, nullptr, nullptr, nullptr, nullptr, lp, bsx);
+    EpiParams e = epi_packed(g, bf, 1, 1.f, 0.f, 0.f, nullptr, nullptr, lp, bsx);
     epi_set_final(e, cx, g, mats, Bc);
     ProfScope ps("final_from_packed", 0.0, Bc * static_cast<double>(g.s) * g.l * (fp32 ? 12.0 : 8.0), cx.st);
     CK(launch_final_from_packed(bf.Xf, lp, bsx, Bc, e, cx.st));
@@ -424,11 +444,11 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
       float* cur = bf.Xf;
       float* nxt = bf.Xf2;
       for (int k = 0; k < T; ++k) {
-        EpiParams e1 = epi_packed(g, bf, k == 0 ? 2 : 0, 1.f, 0.f, 0.f, nullptr, bf.Af, nullptr, nullptr, sp, bss);
+        EpiParams e1 = epi_packed(g, bf, k == 0 ? 2 : 0, 1.f, 0.f, 0.f, nullptr, bf.Af, sp, bss);
         CK(simt(cur, lp, bsx, cur, lp, bsx, S, S, L, 1, 0, e1));
-        EpiParams e2 = epi_packed(g, bf, 0, cx.c, cx.b, 0.f, bf.Af, bf.Bf, nullptr, nullptr, sp, bss);
+        EpiParams e2 = epi_packed(g, bf, 0, cx.c, cx.b, 0.f, bf.Af, bf.Bf, sp, bss);
         CK(simt(bf.Af, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, e2));
-        EpiParams e3 = epi_packed(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, cur, nxt, nullptr, nullptr, lp, bsx);
+        EpiParams e3 = epi_packed(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, cur, nxt, lp, bsx);
         e3.cols_valid = static_cast<int>(g.l);
         if (k == T - 1) epi_set_final(e3, cx, g, mats, Bc);
         CK(simt(bf.Bf, sp, bss, cur, lp, bsx, S, L, S, 0, 1, e3));
@@ -437,31 +457,31 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
       return MUON_OK;
     }
     // fp32 Gram
-    EpiParams e0 = epi_packed(g, bf, 2, 1.f, 0.f, 0.f, nullptr, bf.Gf, nullptr, nullptr, sp, bss);
+    EpiParams e0 = epi_packed(g, bf, 2, 1.f, 0.f, 0.f, nullptr, bf.Gf, sp, bss);
     CK(simt(bf.Xf, lp, bsx, bf.Xf, lp, bsx, S, S, L, 1, 0, e0));
     const float* Q = nullptr;
     int qi = 0;
     for (int k = 0; k < T; ++k) {
       float* P = bf.Pf[k & 1];
-      EpiParams ep = epi_packed(g, bf, 0, cx.c, cx.b, cx.a, bf.Gf, P, nullptr, nullptr, sp, bss);
+      EpiParams ep = epi_packed(g, bf, 0, cx.c, cx.b, cx.a, bf.Gf, P, sp, bss);
       CK(simt(bf.Gf, sp, bss, bf.Gf, sp, bss, S, S, S, 1, 0, ep));
       if (k == 0) {
         Q = P;
       } else {
         float* Qn = bf.Qf[qi];
         qi ^= 1;
-        EpiParams eq = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, Qn, nullptr, nullptr, sp, bss);
+        EpiParams eq = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, Qn, sp, bss);
         CK(simt(P, sp, bss, Q, sp, bss, S, S, S, 1, 0, eq));
         Q = Qn;
       }
       if (k + 1 < T) {
-        EpiParams eh = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Hf, nullptr, nullptr, sp, bss);
+        EpiParams eh = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Hf, sp, bss);
         CK(simt(P, sp, bss, bf.Gf, sp, bss, S, S, S, 1, 0, eh));
-        EpiParams eg = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Gf, nullptr, nullptr, sp, bss);
+        EpiParams eg = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Gf, sp, bss);
         CK(simt(P, sp, bss, bf.Hf, sp, bss, S, S, S, 1, 0, eg));
       }
     }
-    EpiParams ef = epi_packed(g, bf, 1, 1.f, 0.f, 0.f, nullptr, nullptr, nullptr, nullptr, lp, bsx);
+    EpiParams ef = epi_packed(g, bf, 1, 1.f, 0.f, 0.f, nullptr, nullptr, lp, bsx);
     epi_set_final(ef, cx, g, mats, Bc);
     CK(simt(Q, sp, bss, bf.Xf, lp, bsx, S, L, S, 0, 1, ef));
     return MUON_OK;
@@ -491,30 +511,35 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
 
   if (g.sc == MUON_SCHED_ORIG) {
     // Operand splits measured against the fp64 oracle: plain bf16 products miss
-    // a 2e-2 relative error on Gaussian inputs of aspect >= 1:2; splitting A in
-    // A*A (an s^3 product) and B in B*X keeps it below ~1e-2.
-    bf16* cur = bf.Xb[0];
-    bf16* nxt = bf.Xb[1];
+    // a 2e-2 relative error on Gaussian inputs of aspect >= 1:2, mostly through
+    // the rounding of the last steps (where sigma ~ 1 and the b, c terms are
+    // large); splitting A in A*A and B in B*X during the last kSplitSteps steps
+    // brings the error to that of splitting every step (~1e-2 at worst).
+    int cur = 0;
     for (int k = 0; k < T; ++k) {
-      // A = X X^T (k = 0: X = M / s, so scale by inv_norm^2); keep fp32 and hi/lo
-      EpiParams e1 = epi_packed(g, bf, k == 0 ? 2 : 0, 1.f, 0.f, 0.f, nullptr, bf.Gf, bf.Gh, bf.Gl, sp, bss);
-      CK(tc(1, 0, 1, S, S, L, cur, nullptr, lp, bsx, cur, nullptr, lp, bsx, e1));
-      // B = b A + c A^2 (split operands)
-      EpiParams e2 = epi_packed(g, bf, 0, cx.c, cx.b, 0.f, bf.Gf, nullptr, bf.Bh, bf.Bl, sp, bss);
-      CK(tc(3, 0, 1, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, e2));
-      // X <- a X + (Bh + Bl) X (k = 0: both terms carry 1 / s)
-      EpiParams e3 = epi_packed(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, bf.Xf, bf.Xf, nxt, nullptr, lp, bsx);
+      const bool split = k >= T - kSplitSteps;
+      const int nxt = cur ^ 1;
+      // A = X X^T (k = 0: X = M / s, so scale by inv_norm^2)
+      EpiParams e1 = epi_pair(g, bf, k == 0 ? 2 : 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, bf.Gl, sp, bss);
+      CK(tc(1, 0, 1, S, S, L, bf.Xb[cur], nullptr, lp, bsx, bf.Xb[cur], nullptr, lp, bsx, e1));
+      // B = b A + c A^2 with A = Ah + Al in the epilogue
+      EpiParams e2 =
+          epi_pair(g, bf, 0, cx.c, cx.b, 0.f, bf.Gh, bf.Gl, bf.Bh, split ? bf.Bl : nullptr, sp, bss);
+      CK(tc(split ? 3 : 1, 0, 1, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, e2));
+      // X <- a X + B X (k = 0: both terms carry 1 / s); X kept as a bf16 pair
+      EpiParams e3 = epi_pair(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, bf.Xb[cur], bf.Xlo[cur], bf.Xb[nxt],
+                              bf.Xlo[nxt], lp, bsx);
       e3.cols_valid = static_cast<int>(g.l);
       if (k == T - 1) epi_set_final(e3, cx, g, mats, Bc);
-      CK(tc(2, 1, 0, S, L, S, bf.Bh, bf.Bl, sp, bss, cur, nullptr, lp, bsx, e3));
-      std::swap(cur, nxt);
+      CK(tc(split ? 2 : 1, 1, 0, S, L, S, bf.Bh, bf.Bl, sp, bss, bf.Xb[cur], nullptr, lp, bsx, e3));
+      cur = nxt;
     }
     return MUON_OK;
   }
 
   // Gram space (split 3 or 1)
   const int sp3 = x3 ? 3 : 1;
-  EpiParams e0 = epi_packed(g, bf, 2, 1.f, 0.f, 0.f, nullptr, bf.Gf, bf.Gh, bf.Gl, sp, bss);
+  EpiParams e0 = epi_pair(g, bf, 2, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, bf.Gl, sp, bss);
   CK(tc(sp3, 0, 1, S, S, L, bf.Xb[0], bf.Xl, lp, bsx, bf.Xb[0], bf.Xl, lp, bsx, e0));
   const bf16* Qh = nullptr;
   const bf16* Ql = nullptr;
@@ -523,7 +548,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     bf16* Ph = bf.Ph[k & 1];
     bf16* Pl = bf.Pl[k & 1];
     // P = a I + b G + c G^2
-    EpiParams ep = epi_packed(g, bf, 0, cx.c, cx.b, cx.a, bf.Gf, nullptr, Ph, Pl, sp, bss);
+    EpiParams ep = epi_pair(g, bf, 0, cx.c, cx.b, cx.a, bf.Gh, bf.Gl, Ph, Pl, sp, bss);
     CK(tc(sp3, 0, 1, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, ep));
     if (k == 0) {
       Qh = Ph;
@@ -532,20 +557,20 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
       bf16* Qnh = bf.Qh[qi];
       bf16* Qnl = bf.Ql[qi];
       qi ^= 1;
-      EpiParams eq = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, Qnh, Qnl, sp, bss);
+      EpiParams eq = epi_pair(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, Qnh, Qnl, sp, bss);
       CK(tc(sp3, 0, 1, S, S, S, Ph, Pl, sp, bss, Qh, Ql, sp, bss, eq));
       Qh = Qnh;
       Ql = Qnl;
     }
     if (k + 1 < T) {
-      EpiParams eh = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Hh, bf.Hl, sp, bss);
+      EpiParams eh = epi_pair(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Hh, bf.Hl, sp, bss);
       CK(tc(sp3, 0, 1, S, S, S, Ph, Pl, sp, bss, bf.Gh, bf.Gl, sp, bss, eh));
-      EpiParams eg = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Gf, bf.Gh, bf.Gl, sp, bss);
+      EpiParams eg = epi_pair(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, bf.Gl, sp, bss);
       CK(tc(sp3, 0, 1, S, S, S, Ph, Pl, sp, bss, bf.Hh, bf.Hl, sp, bss, eg));
     }
   }
   // O = Q X0 = Q X / s
-  EpiParams ef = epi_packed(g, bf, 1, 1.f, 0.f, 0.f, nullptr, nullptr, nullptr, nullptr, lp, bsx);
+  EpiParams ef = epi_pair(g, bf, 1, 1.f, 0.f, 0.f, nullptr, nullptr, nullptr, nullptr, lp, bsx);
   epi_set_final(ef, cx, g, mats, Bc);
   CK(tc(sp3, 1, 0, S, L, S, Qh, Ql, sp, bss, bf.Xb[0], bf.Xl, lp, bsx, ef));
   return MUON_OK;
@@ -772,8 +797,8 @@ muon_status muon_debug_bounded_wait(void* ws, long long max_cycles, void* stream
 }
 
 muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, const void* B_lo, int batch, int M,
-                            int N, int K, int split, int b_mn, int sym, muon_dtype dt, float* out, void* ws,
-                            size_t ws_bytes, void* stream) {
+                            int N, int K, int split, int b_mn, int sym, muon_dtype dt, void* out, void* out_lo,
+                            void* ws, size_t ws_bytes, void* stream) {
   g_last_error.clear();
   if (!A || !B || !out || !ws || batch <= 0 || batch > kMaxBatch) return fail(MUON_ERR_ARG, "bad pointers or batch");
   if (ws_bytes < kHeader || reinterpret_cast<uintptr_t>(ws) % MUON_WS_ALIGN)
@@ -783,7 +808,12 @@ muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, cons
   EpiParams e;
   memset(&e, 0, sizeof(e));
   e.c_acc = 1.f;
-  e.Of = out;
+  if (dt == MUON_FP32) {
+    e.Of = static_cast<float*>(out);
+  } else {
+    e.Oh = static_cast<bf16*>(out);
+    e.Ol = static_cast<bf16*>(out_lo);
+  }
   e.ld = N;
   e.bs = static_cast<long long>(M) * N;
   e.rows_valid = M;

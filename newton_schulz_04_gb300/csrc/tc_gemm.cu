@@ -41,15 +41,22 @@ struct TcCfg {
   static constexpr int NA = (SPLIT >= 2) ? 2 : 1;
   static constexpr int NB = (SPLIT == 3) ? 2 : 1;
   static constexpr int STAGE = NA * A_TILE + NB * B_TILE;
-  static constexpr int STAGES_RAW = (196 * 1024) / STAGE;
+  // Epilogue staging: per epilogue warp, NBUF sets of four 32 x 32 bf16 boxes
+  // (head, residual, and their mirrors), 2 KB each.
+  static constexpr int NBUF = 2;
+  static constexpr int BOX = 32 * 32 * 2;
+  static constexpr int STG_WARP = NBUF * 4 * BOX;
+  static constexpr int STG = 4 * STG_WARP;
+  static constexpr int STAGES_RAW = (224 * 1024 - STG) / STAGE;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = STAGES * STAGE + BAR_BYTES + 1024;
+  static constexpr int SMEM = STAGES * STAGE + STG + BAR_BYTES + 1024;
   static constexpr uint32_t SWZ = (SWB == 128) ? 2u : 4u;  // descriptor swizzle code
   static constexpr int MN_ATOM = SWB / 2;                  // MN elements per swizzle row (MN-major)
   static constexpr int MN_BOX_BYTES = BK * SWB;            // one [BK x MN_ATOM] box
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static_assert(STAGES >= 2, "need at least two stages");
+  static_assert(STAGES >= 3, "need at least three stages");
+  static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(BAR_BYTES >= (2 * STAGES + 5) * 8 + 8, "barrier area too small");
 };
 
@@ -94,76 +101,78 @@ __device__ __forceinline__ void decode_tile(const TcArgs& a, int t, int& b, int&
   }
 }
 
-// Epilogue of 32 consecutive accumulator columns of one row.
-__device__ __forceinline__ void epi_row32(const EpiParams& e, int b, int r, int c0, float (&v)[32], float sc) {
-  if (e.final_mode != FINAL_NONE || (e.sym && !(c0 + 31 < r))) {
+// Byte offset inside a [32 rows x 64 B] box stored with the 64-byte TMA swizzle
+// (16-byte chunk index XOR-ed with bits 7..8 of the row address).
+__device__ __forceinline__ uint32_t sw64(int row, int byte) {
+  return static_cast<uint32_t>(row * 64 + ((((byte >> 4) ^ (row >> 1)) & 3) << 4) + (byte & 15));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+}
+
+// Stage one thread's 32 values (row `row` of a 32 x 32 box) as bf16 head and residual.
+__device__ __forceinline__ void stage_rows(uint8_t* box_h, uint8_t* box_l, int row, const float (&v)[32]) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) epi_elem(e, b, r, c0 + j, v[j], sc);
-    return;
-  }
-  const long long base = static_cast<long long>(b) * e.bs;
-  const long long roff = base + static_cast<long long>(r) * e.ld + c0;
-  if (e.R) {
-    const float4* R4 = reinterpret_cast<const float4*>(e.R + roff);
+  for (int q = 0; q < 4; ++q) {
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 x = R4[q];
-      v[4 * q + 0] = sc * (e.c_acc * v[4 * q + 0] + e.c_res * x.x);
-      v[4 * q + 1] = sc * (e.c_acc * v[4 * q + 1] + e.c_res * x.y);
-      v[4 * q + 2] = sc * (e.c_acc * v[4 * q + 2] + e.c_res * x.z);
-      v[4 * q + 3] = sc * (e.c_acc * v[4 * q + 3] + e.c_res * x.w);
+    for (int t = 0; t < 4; ++t) {
+      const float a = v[8 * q + 2 * t], b = v[8 * q + 2 * t + 1];
+      h[t] = pack_bf16x2(a, b);
+      if (box_l) {
+        const float ra = a - __bfloat162float(__float2bfloat16_rn(a));
+        const float rb = b - __bfloat162float(__float2bfloat16_rn(b));
+        l[t] = pack_bf16x2(ra, rb);
+      }
     }
-  } else {
-    const float f = sc * e.c_acc;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] *= f;
-  }
-  if (e.Of) {
-    float4* O4 = reinterpret_cast<float4*>(e.Of + roff);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) O4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-  }
-  if (e.Oh) {
-    uint32_t hw[16], lw[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const bf16 h0 = __float2bfloat16_rn(v[2 * q]);
-      const bf16 h1 = __float2bfloat16_rn(v[2 * q + 1]);
-      hw[q] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
-              (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
-      const bf16 l0 = __float2bfloat16_rn(v[2 * q] - __bfloat162float(h0));
-      const bf16 l1 = __float2bfloat16_rn(v[2 * q + 1] - __bfloat162float(h1));
-      lw[q] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
-              (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
-    }
-    uint4* H4 = reinterpret_cast<uint4*>(e.Oh + roff);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) H4[q] = make_uint4(hw[4 * q], hw[4 * q + 1], hw[4 * q + 2], hw[4 * q + 3]);
-    if (e.Ol) {
-      uint4* L4 = reinterpret_cast<uint4*>(e.Ol + roff);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) L4[q] = make_uint4(lw[4 * q], lw[4 * q + 1], lw[4 * q + 2], lw[4 * q + 3]);
-    }
-  }
-  if (e.sym) {
-    // Mirror: element (r, c0 + j) also goes to (c0 + j, r); across the warp r is
-    // consecutive, so each of these stores is one coalesced segment.
-#pragma unroll
-    for (int j = 0; j < 32; ++j) epi_store_elem(e, base + static_cast<long long>(c0 + j) * e.ld + r, v[j]);
+    *reinterpret_cast<uint4*>(box_h + sw64(row, q * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
+    if (box_l) *reinterpret_cast<uint4*>(box_l + sw64(row, q * 16)) = make_uint4(l[0], l[1], l[2], l[3]);
   }
 }
+
+// Stage the transpose: thread `col` holds column `col` of the mirrored box.
+__device__ __forceinline__ void stage_cols(uint8_t* box_h, uint8_t* box_l, int col, const float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const bf16 h = __float2bfloat16_rn(v[j]);
+    *reinterpret_cast<bf16*>(box_h + sw64(j, col * 2)) = h;
+    if (box_l) *reinterpret_cast<bf16*>(box_l + sw64(j, col * 2)) = __float2bfloat16_rn(v[j] - __bfloat162float(h));
+  }
+}
+
+// Residual pair R = Rh + Rl for 32 consecutive columns of one row.
+__device__ __forceinline__ void load_residual(const EpiParams& e, long long off, uint4 (&rh)[4], uint4 (&rl)[4]) {
+  const uint4* ph = reinterpret_cast<const uint4*>(e.Rh + off);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) rh[q] = ph[q];
+  if (e.Rl) {
+    const uint4* pl = reinterpret_cast<const uint4*>(e.Rl + off);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) rl[q] = pl[q];
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) rl[q] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 template <int SPLIT, bool BMN, int SWB>
 __global__ void __launch_bounds__(192, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAl,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBl,
+                   const __grid_constant__ CUtensorMap tmOh, const __grid_constant__ CUtensorMap tmOl,
                    const __grid_constant__ TcArgs args) {
   using C = TcCfg<SPLIT, BMN, SWB>;
   extern __shared__ uint8_t smem_raw[];
   // Swizzled tiles must start on a 1024-byte boundary of the shared window.
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* tiles = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+  uint8_t* staging = smem + C::STAGES * C::STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::STG);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;  // [2]
   uint64_t* tempty = tfull + 2;         // [2]
@@ -303,9 +312,16 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
+    // Each warp owns 32 accumulator rows (its TMEM lane quarter).  Per 32-column
+    // chunk: residual prefetch, tcgen05.ld, fused arithmetic, then either the
+    // final write to the caller's matrix or swizzled staging of 32 x 32 bf16
+    // boxes (and their transposes for symmetric outputs) that one lane sends to
+    // global memory with TMA bulk-tensor stores.
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     const EpiParams& e = args.epi;
-    int tcount = 0;
+    uint8_t* stg = staging + (warp - 2) * C::STG_WARP;
+    const bool has_lo = e.Ol != nullptr;
+    int tcount = 0, sbuf = 0;
     for (int t = blockIdx.x; t < args.total; t += gridDim.x, ++tcount) {
       int b, i, j;
       decode_tile(args, t, b, i, j);
@@ -318,22 +334,72 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      const int r = m0 + quarter * 32 + lane;
-      const int warp_row_max = m0 + quarter * 32 + 31;
+      const int r0 = m0 + quarter * 32;
+      const int r = r0 + lane;
       const float sc = epi_scale(e, b);
+      const long long base = static_cast<long long>(b) * e.bs;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + abuf * C::BN;
 #pragma unroll 1
       for (int cc = 0; cc < C::BN / 32; ++cc) {
         const int c0 = n0 + cc * 32;
-        if (args.sym && c0 > warp_row_max) break;  // rest of the tile is above the diagonal
+        if (args.sym && c0 > r0) break;  // the rest of this warp's rows lies above the diagonal
+        uint4 rh[4], rl[4];
+        if (e.Rh) load_residual(e, base + static_cast<long long>(r) * e.ld + c0, rh, rl);
         float v[32];
         __syncwarp();
         tmem_ld_32x32b_x32(tbase + cc * 32, v);
-        epi_row32(e, b, r, c0, v, sc);
+        if (e.Rh) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t hw[4] = {rh[q].x, rh[q].y, rh[q].z, rh[q].w};
+            const uint32_t lw[4] = {rl[q].x, rl[q].y, rl[q].z, rl[q].w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float r0v = bf_lo(hw[u]) + bf_lo(lw[u]);
+              const float r1v = bf_hi(hw[u]) + bf_hi(lw[u]);
+              v[8 * q + 2 * u] = sc * (e.c_acc * v[8 * q + 2 * u] + e.c_res * r0v);
+              v[8 * q + 2 * u + 1] = sc * (e.c_acc * v[8 * q + 2 * u + 1] + e.c_res * r1v);
+            }
+          }
+        } else {
+          const float f = sc * e.c_acc;
+#pragma unroll
+          for (int u = 0; u < 32; ++u) v[u] *= f;
+        }
+        if (e.c_id != 0.f && r >= c0 && r < c0 + 32 && r < e.rows_valid) {
+#pragma unroll
+          for (int u = 0; u < 32; ++u)
+            if (c0 + u == r) v[u] += e.c_id;
+        }
+        if (e.final_mode != FINAL_NONE) {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) epi_final_elem(e, b, r, c0 + u, v[u]);
+          continue;
+        }
+        const bool mirror = args.sym && c0 < r0;  // strictly-lower 32 x 32 block: also store its transpose
+        if (lane == 0) bulk_wait_read<C::NBUF - 1>();  // this staging buffer's previous stores have read it
+        __syncwarp();
+        uint8_t* sb = stg + sbuf * (4 * C::BOX);
+        stage_rows(sb, has_lo ? sb + C::BOX : nullptr, lane, v);
+        if (mirror) stage_cols(sb + 2 * C::BOX, has_lo ? sb + 3 * C::BOX : nullptr, lane, v);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tmOh, sb, c0, r0, b);
+          if (has_lo) tma_store_3d(&tmOl, sb + C::BOX, c0, r0, b);
+          if (mirror) {
+            tma_store_3d(&tmOh, sb + 2 * C::BOX, r0, c0, b);
+            if (has_lo) tma_store_3d(&tmOl, sb + 3 * C::BOX, r0, c0, b);
+          }
+          bulk_commit();
+        }
+        sbuf = (sbuf + 1) % C::NBUF;
       }
       tc_fence_before();
       mbar_arrive(&tempty[abuf]);
     }
+    if (lane == 0) bulk_wait_all();  // stores complete before the CTA retires
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -398,8 +464,22 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
     ok = ok && make_map(&mBl, (C::NB == 2 && d.Bop.lo) ? d.Bop.lo : d.Bop.hi, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs,
                         C::MN_ATOM, C::BK, SWB);
   }
+  // Output maps: 32 x 32 bf16 boxes with the 64-byte swizzle (dummies in final mode).
+  CUtensorMap mOh, mOl;
+  bf16* oh = epi.Oh ? epi.Oh : const_cast<bf16*>(d.A.hi);
+  bf16* ol = epi.Ol ? epi.Ol : oh;
+  const long long old_ = epi.Oh ? epi.ld : d.A.ld;
+  const long long obs = epi.Oh ? epi.bs : d.A.bs;
+  const uint64_t orows = epi.Oh ? static_cast<uint64_t>(d.M) : static_cast<uint64_t>(d.M);
+  const uint64_t ocols = epi.Oh ? static_cast<uint64_t>(epi.ld) : static_cast<uint64_t>(d.K);
+  ok = ok && make_map(&mOh, oh, ocols, orows, d.B, old_, obs, 32, 32, 64);
+  ok = ok && make_map(&mOl, ol, ocols, orows, d.B, old_, obs, 32, 32, 64);
   if (!ok) {
     *why = "cuTensorMapEncodeTiled failed";
+    return cudaErrorInvalidValue;
+  }
+  if (epi.final_mode == FINAL_NONE && !epi.Oh) {
+    *why = "tensor-core epilogue needs a bf16 output pair";
     return cudaErrorInvalidValue;
   }
   TcArgs a;
@@ -421,7 +501,7 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
   a.epi.sym = d.sym;
   const int grid = a.total < num_sms ? a.total : num_sms;
   if (grid <= 0) return cudaSuccess;
-  tc_gemm_kernel<SPLIT, BMN, SWB><<<grid, 192, C::SMEM, st>>>(mA, mAl, mB, mBl, a);
+  tc_gemm_kernel<SPLIT, BMN, SWB><<<grid, 192, C::SMEM, st>>>(mA, mAl, mB, mBl, mOh, mOl, a);
   return cudaGetLastError();
 }
 

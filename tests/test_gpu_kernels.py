@@ -36,8 +36,9 @@ def test_tc_gemm_kmajor_b(M, N, K):
     B = _rand((2, N, K), 2)
     out = m.debug_gemm(A, B)
     torch.cuda.synchronize()
-    # same bf16 operands, fp32 accumulation on both sides: only summation order differs
-    assert _rel(out, _ref(A, B, False)) < 1e-5
+    # same bf16 operands, fp32 accumulation on both sides: only summation order
+    # and the 16-bit output pair (2^-17 relative per element) differ
+    assert _rel(out, _ref(A, B, False)) < 2e-5
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 192), (384, 1024, 512)])
@@ -47,7 +48,7 @@ def test_tc_gemm_mnmajor_b(M, N, K):
     B = _rand((2, K, N), 4)
     out = m.debug_gemm(A, B, b_mn=True)
     torch.cuda.synchronize()
-    assert _rel(out, _ref(A, B, True)) < 1e-5
+    assert _rel(out, _ref(A, B, True)) < 2e-5
 
 
 @pytest.mark.parametrize("S,K", [(256, 64), (512, 256), (768, 1024)])
@@ -57,7 +58,7 @@ def test_tc_syrk_lower_and_mirror(S, K):
     out = m.debug_gemm(X, X, sym=True)
     torch.cuda.synchronize()
     ref = _ref(X, X, False)
-    assert _rel(out, ref) < 1e-5
+    assert _rel(out, ref) < 2e-5
     assert torch.equal(out, out.transpose(1, 2))
 
 
@@ -80,7 +81,7 @@ def test_tc_gemm_split3(b_mn):
     ref = _ref(A32.double(), B32.double(), b_mn).float()
     one = _ref(Ah, Bh, b_mn)
     # three products of ~8-bit operands reach ~16-bit operand accuracy
-    assert _rel(out, ref) < 2e-5
+    assert _rel(out, ref) < 4e-5
     assert _rel(one, ref) > 1e-3
 
 
@@ -93,7 +94,7 @@ def test_tc_gemm_split2_mnmajor():
     out = m.debug_gemm(Ah, B, Al, None, split=2, b_mn=True)
     torch.cuda.synchronize()
     ref = (A32.double() @ B.double()).float()
-    assert _rel(out, ref) < 2e-5
+    assert _rel(out, ref) < 4e-5
     assert _rel(_ref(Ah, B, True), ref) > 1e-3
 
 
@@ -108,7 +109,7 @@ def test_tc_sym_split3_symmetric_operands():
     out = m.debug_gemm(Ph, Gh, Pl, Gl, split=3, sym=True)
     torch.cuda.synchronize()
     ref = (Ps @ Gs).float().cuda()
-    assert _rel(out, ref) < 2e-5
+    assert _rel(out, ref) < 4e-5
     assert torch.equal(out, out.transpose(1, 2))
 
 
@@ -136,5 +137,5 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     B = _rand((1, 256, 64), 11)
     out = m.debug_gemm(A, B, workspace=ws)
     torch.cuda.synchronize()
-    assert _rel(out, _ref(A, B, False)) < 1e-5
+    assert _rel(out, _ref(A, B, False)) < 2e-5
     assert m.device_status(ws) == 0
