@@ -41,11 +41,14 @@ struct TcCfg {
   static constexpr int NA = (SPLIT >= 2) ? 2 : 1;
   static constexpr int NB = (SPLIT == 3) ? 2 : 1;
   static constexpr int STAGE = NA * A_TILE + NB * B_TILE;
-  // Epilogue staging: per epilogue warp, NBUF sets of four 32 x 32 bf16 boxes
-  // (head, residual, and their mirrors), 2 KB each.
-  static constexpr int NBUF = 2;
+  // Epilogue staging per epilogue warp: NBUF sets of four 32 x 32 bf16 output
+  // boxes (head, residual part, and their mirrors) and two sets of two input
+  // boxes for the prefetched residual pair R = Rh + Rl; 2 KB per box.
   static constexpr int BOX = 32 * 32 * 2;
-  static constexpr int STG_WARP = NBUF * 4 * BOX;
+  static constexpr int NBUF = STAGE >= 48 * 1024 ? 1 : 2;
+  static constexpr int OUT_WARP = NBUF * 4 * BOX;
+  static constexpr int RIN_WARP = 2 * 2 * BOX;
+  static constexpr int STG_WARP = OUT_WARP + RIN_WARP;
   static constexpr int STG = 4 * STG_WARP;
   static constexpr int STAGES_RAW = (224 * 1024 - STG) / STAGE;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
@@ -57,7 +60,7 @@ struct TcCfg {
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static_assert(STAGES >= 3, "need at least three stages");
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(BAR_BYTES >= (2 * STAGES + 5) * 8 + 8, "barrier area too small");
+  static_assert(BAR_BYTES >= (2 * STAGES + 5 + 8) * 8 + 8, "barrier area too small");
 };
 
 struct TcArgs {
@@ -112,48 +115,48 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
 }
 
-// Stage one thread's 32 values (row `row` of a 32 x 32 box) as bf16 head and residual.
-__device__ __forceinline__ void stage_rows(uint8_t* box_h, uint8_t* box_l, int row, const float (&v)[32]) {
+// Split 32 values into packed bf16x2 words: head hw = bf16(v), residual lw = bf16(v - head).
+__device__ __forceinline__ void split_words(const float (&v)[32], uint32_t (&hw)[16], uint32_t (&lw)[16]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t h[4], l[4];
+  for (int k = 0; k < 16; ++k) {
+    const float a = v[2 * k], b = v[2 * k + 1];
+    const bf16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
+    hw[k] = static_cast<uint32_t>(__bfloat16_as_ushort(ha)) | (static_cast<uint32_t>(__bfloat16_as_ushort(hb)) << 16);
+    lw[k] = pack_bf16x2(a - __bfloat162float(ha), b - __bfloat162float(hb));
+  }
+}
+
+// Row `row` of a 32 x 32 box from 16 packed words.
+__device__ __forceinline__ void stage_row(uint8_t* box, int row, const uint32_t (&w)[16]) {
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const float a = v[8 * q + 2 * t], b = v[8 * q + 2 * t + 1];
-      h[t] = pack_bf16x2(a, b);
-      if (box_l) {
-        const float ra = a - __bfloat162float(__float2bfloat16_rn(a));
-        const float rb = b - __bfloat162float(__float2bfloat16_rn(b));
-        l[t] = pack_bf16x2(ra, rb);
-      }
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(box + sw64(row, q * 16)) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+}
+
+// Transposed box: lane t holds row t of the block; the box gets column t.  Lane
+// pairs (2u, 2u+1) swap one packed word per step, so each step writes rows 2u
+// (even lanes) and 2u + 1 (odd lanes) with 32-bit stores into opposite bank halves.
+__device__ __forceinline__ void stage_col(uint8_t* box, int lane, const uint32_t (&w)[16]) {
+  const bool odd = lane & 1;
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, w[u], 1);
+    const uint32_t word = odd ? __byte_perm(y, w[u], 0x7632) : __byte_perm(w[u], y, 0x5410);
+    const int row = 2 * u + (odd ? 1 : 0);
+    const int col = lane & ~1;
+    *reinterpret_cast<uint32_t*>(box + sw64(row, col * 2)) = word;
+  }
+}
+
+// Make a staged diagonal block exactly symmetric: copy the strictly lower
+// triangle onto the upper one (lane t writes row t).
+__device__ __forceinline__ void symmetrize_box(uint8_t* box, int lane) {
+#pragma unroll 4
+  for (int j = 1; j < 32; ++j) {
+    if (j > lane) {
+      const uint16_t x = *reinterpret_cast<const uint16_t*>(box + sw64(j, lane * 2));
+      *reinterpret_cast<uint16_t*>(box + sw64(lane, j * 2)) = x;
     }
-    *reinterpret_cast<uint4*>(box_h + sw64(row, q * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
-    if (box_l) *reinterpret_cast<uint4*>(box_l + sw64(row, q * 16)) = make_uint4(l[0], l[1], l[2], l[3]);
-  }
-}
-
-// Stage the transpose: thread `col` holds column `col` of the mirrored box.
-__device__ __forceinline__ void stage_cols(uint8_t* box_h, uint8_t* box_l, int col, const float (&v)[32]) {
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const bf16 h = __float2bfloat16_rn(v[j]);
-    *reinterpret_cast<bf16*>(box_h + sw64(j, col * 2)) = h;
-    if (box_l) *reinterpret_cast<bf16*>(box_l + sw64(j, col * 2)) = __float2bfloat16_rn(v[j] - __bfloat162float(h));
-  }
-}
-
-// Residual pair R = Rh + Rl for 32 consecutive columns of one row.
-__device__ __forceinline__ void load_residual(const EpiParams& e, long long off, uint4 (&rh)[4], uint4 (&rl)[4]) {
-  const uint4* ph = reinterpret_cast<const uint4*>(e.Rh + off);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) rh[q] = ph[q];
-  if (e.Rl) {
-    const uint4* pl = reinterpret_cast<const uint4*>(e.Rl + off);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) rl[q] = pl[q];
-  } else {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) rl[q] = make_uint4(0, 0, 0, 0);
   }
 }
 
@@ -165,6 +168,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAl,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBl,
                    const __grid_constant__ CUtensorMap tmOh, const __grid_constant__ CUtensorMap tmOl,
+                   const __grid_constant__ CUtensorMap tmRh, const __grid_constant__ CUtensorMap tmRl,
                    const __grid_constant__ TcArgs args) {
   using C = TcCfg<SPLIT, BMN, SWB>;
   extern __shared__ uint8_t smem_raw[];
@@ -177,7 +181,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tfull = empty + C::STAGES;  // [2]
   uint64_t* tempty = tfull + 2;         // [2]
   uint64_t* drain = tempty + 2;         // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* rbar = drain + 1;           // [4 warps][2] residual-box barriers
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -193,6 +198,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&tempty[a], 128);
     }
     mbar_init(drain, 1);
+    for (int q = 0; q < 8; ++q) mbar_init(&rbar[q], 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -318,14 +324,41 @@ __global__ void __launch_bounds__(192, 1)
     // boxes (and their transposes for symmetric outputs) that one lane sends to
     // global memory with TMA bulk-tensor stores.
     const int quarter = warp & 3;  // TMEM lanes this warp may read
+    const int ew = warp - 2;
     const EpiParams& e = args.epi;
-    uint8_t* stg = staging + (warp - 2) * C::STG_WARP;
+    uint8_t* stg = staging + ew * C::STG_WARP;
+    uint8_t* rin = stg + C::OUT_WARP;
+    uint64_t* rb = rbar + 2 * ew;
     const bool has_lo = e.Ol != nullptr;
+    const bool has_r = e.Rh != nullptr;
+    const bool has_rl = e.Rl != nullptr;
+    const uint32_t rbytes = has_rl ? 2 * C::BOX : C::BOX;
     int tcount = 0, sbuf = 0;
+    // Residual boxes go through a two-deep ring per warp; r_issued / r_used
+    // count the boxes requested / consumed (warp-uniform, lane 0 issues).
+    int r_issued = 0, r_used = 0;
+    auto issue_r = [&](int c0, int r0, int b) {
+      const int buf = r_issued & 1;
+      if (lane == 0) {
+        uint8_t* dst = rin + buf * 2 * C::BOX;
+        mbar_arrive_expect_tx(&rb[buf], rbytes);
+        tma_load_3d(&tmRh, &rb[buf], dst, c0, r0, b);
+        if (has_rl) tma_load_3d(&tmRl, &rb[buf], dst + C::BOX, c0, r0, b);
+      }
+      ++r_issued;
+    };
     for (int t = blockIdx.x; t < args.total; t += gridDim.x, ++tcount) {
       int b, i, j;
       decode_tile(args, t, b, i, j);
       const int m0 = i * C::BM, n0 = j * C::BN;
+      const int r0 = m0 + quarter * 32;
+      const int r = r0 + lane;
+      // chunks of 32 columns this warp handles (symmetric: up to its diagonal block)
+      const int nch = args.sym ? min(C::BN / 32, ((r0 - n0) >> 5) + 1) : C::BN / 32;
+      const int rbase = r_issued;
+      if (has_r) {
+        for (int q = 0; q < 2 && q < nch; ++q) issue_r(n0 + 32 * q, r0, b);
+      }
       const int abuf = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       if (*abort_flag || !mbar_wait(&tfull[abuf], aph)) {
@@ -334,32 +367,42 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      const int r0 = m0 + quarter * 32;
-      const int r = r0 + lane;
       const float sc = epi_scale(e, b);
-      const long long base = static_cast<long long>(b) * e.bs;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + abuf * C::BN;
+      bool ok = true;
 #pragma unroll 1
-      for (int cc = 0; cc < C::BN / 32; ++cc) {
+      for (int cc = 0; cc < nch; ++cc) {
         const int c0 = n0 + cc * 32;
-        if (args.sym && c0 > r0) break;  // the rest of this warp's rows lies above the diagonal
-        uint4 rh[4], rl[4];
-        if (e.Rh) load_residual(e, base + static_cast<long long>(r) * e.ld + c0, rh, rl);
+        uint32_t rhw[16], rlw[16];
+        if (has_r) {
+          const int idx = rbase + cc;
+          if (!mbar_wait(&rb[idx & 1], (idx >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* src = rin + (idx & 1) * 2 * C::BOX;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 h = *reinterpret_cast<const uint4*>(src + sw64(lane, q * 16));
+            rhw[4 * q] = h.x, rhw[4 * q + 1] = h.y, rhw[4 * q + 2] = h.z, rhw[4 * q + 3] = h.w;
+            uint4 l = make_uint4(0, 0, 0, 0);
+            if (has_rl) l = *reinterpret_cast<const uint4*>(src + C::BOX + sw64(lane, q * 16));
+            rlw[4 * q] = l.x, rlw[4 * q + 1] = l.y, rlw[4 * q + 2] = l.z, rlw[4 * q + 3] = l.w;
+          }
+          r_used = idx + 1;
+          __syncwarp();
+          if (cc + 2 < nch) issue_r(c0 + 64, r0, b);  // the buffer just read is free again
+        }
         float v[32];
         __syncwarp();
         tmem_ld_32x32b_x32(tbase + cc * 32, v);
-        if (e.Rh) {
+        if (has_r) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t hw[4] = {rh[q].x, rh[q].y, rh[q].z, rh[q].w};
-            const uint32_t lw[4] = {rl[q].x, rl[q].y, rl[q].z, rl[q].w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float r0v = bf_lo(hw[u]) + bf_lo(lw[u]);
-              const float r1v = bf_hi(hw[u]) + bf_hi(lw[u]);
-              v[8 * q + 2 * u] = sc * (e.c_acc * v[8 * q + 2 * u] + e.c_res * r0v);
-              v[8 * q + 2 * u + 1] = sc * (e.c_acc * v[8 * q + 2 * u + 1] + e.c_res * r1v);
-            }
+          for (int u = 0; u < 16; ++u) {
+            const float x0 = bf_lo(rhw[u]) + bf_lo(rlw[u]);
+            const float x1 = bf_hi(rhw[u]) + bf_hi(rlw[u]);
+            v[2 * u] = sc * (e.c_acc * v[2 * u] + e.c_res * x0);
+            v[2 * u + 1] = sc * (e.c_acc * v[2 * u + 1] + e.c_res * x1);
           }
         } else {
           const float f = sc * e.c_acc;
@@ -376,12 +419,24 @@ __global__ void __launch_bounds__(192, 1)
           for (int u = 0; u < 32; ++u) epi_final_elem(e, b, r, c0 + u, v[u]);
           continue;
         }
-        const bool mirror = args.sym && c0 < r0;  // strictly-lower 32 x 32 block: also store its transpose
+        const bool diag = args.sym && c0 == r0;
+        const bool mirror = args.sym && c0 < r0;  // strictly-lower block: also store its transpose
+        uint32_t hw[16], lw[16];
+        split_words(v, hw, lw);
         if (lane == 0) bulk_wait_read<C::NBUF - 1>();  // this staging buffer's previous stores have read it
         __syncwarp();
         uint8_t* sb = stg + sbuf * (4 * C::BOX);
-        stage_rows(sb, has_lo ? sb + C::BOX : nullptr, lane, v);
-        if (mirror) stage_cols(sb + 2 * C::BOX, has_lo ? sb + 3 * C::BOX : nullptr, lane, v);
+        stage_row(sb, lane, hw);
+        if (has_lo) stage_row(sb + C::BOX, lane, lw);
+        if (mirror) {
+          stage_col(sb + 2 * C::BOX, lane, hw);
+          if (has_lo) stage_col(sb + 3 * C::BOX, lane, lw);
+        }
+        if (diag) {
+          __syncwarp();
+          symmetrize_box(sb, lane);
+          if (has_lo) symmetrize_box(sb + C::BOX, lane);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -395,10 +450,19 @@ __global__ void __launch_bounds__(192, 1)
         }
         sbuf = (sbuf + 1) % C::NBUF;
       }
+      if (!ok) {
+        if (lane == 0) atomicOr(args.status, kStatusTimeout);
+        *abort_flag = 1;
+        break;
+      }
       tc_fence_before();
       mbar_arrive(&tempty[abuf]);
     }
-    if (lane == 0) bulk_wait_all();  // stores complete before the CTA retires
+    if (lane == 0) {
+      // residual boxes still in flight land before the CTA can retire
+      for (int idx = r_used; idx < r_issued; ++idx) mbar_wait(&rb[idx & 1], (idx >> 1) & 1);
+      bulk_wait_all();  // stores complete before the CTA retires
+    }
     __syncwarp();
   }
 
@@ -474,6 +538,15 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
   const uint64_t ocols = epi.Oh ? static_cast<uint64_t>(epi.ld) : static_cast<uint64_t>(d.K);
   ok = ok && make_map(&mOh, oh, ocols, orows, d.B, old_, obs, 32, 32, 64);
   ok = ok && make_map(&mOl, ol, ocols, orows, d.B, old_, obs, 32, 32, 64);
+  // Residual maps (same box and swizzle as the outputs; dummies without a residual).
+  CUtensorMap mRh, mRl;
+  const bf16* rh = epi.Rh ? epi.Rh : oh;
+  const bf16* rl = epi.Rl ? epi.Rl : rh;
+  const long long rld = epi.Rh ? epi.ld : old_;
+  const long long rbs = epi.Rh ? epi.bs : obs;
+  const uint64_t rcols = epi.Rh ? static_cast<uint64_t>(epi.ld) : ocols;
+  ok = ok && make_map(&mRh, rh, rcols, orows, d.B, rld, rbs, 32, 32, 64);
+  ok = ok && make_map(&mRl, rl, rcols, orows, d.B, rld, rbs, 32, 32, 64);
   if (!ok) {
     *why = "cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
@@ -501,7 +574,7 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
   a.epi.sym = d.sym;
   const int grid = a.total < num_sms ? a.total : num_sms;
   if (grid <= 0) return cudaSuccess;
-  tc_gemm_kernel<SPLIT, BMN, SWB><<<grid, 192, C::SMEM, st>>>(mA, mAl, mB, mBl, mOh, mOl, a);
+  tc_gemm_kernel<SPLIT, BMN, SWB><<<grid, 192, C::SMEM, st>>>(mA, mAl, mB, mBl, mOh, mOl, mRh, mRl, a);
   return cudaGetLastError();
 }
 
