@@ -4,23 +4,28 @@
 // batch of same-shape matrices (DMuon technical summary, §2.2: same-shape
 // matrices are batched so small problems still fill the GPU).  For symmetric
 // outputs (the Gram matrix G = X X^T and every product of the commuting
-// polynomials of G) only tiles that touch the lower triangle are computed; the
-// epilogue writes each lower element and its mirror (same section: the
-// symmetric products compute only the lower triangle).
+// polynomials of G) only tiles that touch the lower triangle are computed and
+// the epilogue also stores each block's transpose (same section: the symmetric
+// products compute only the lower triangle).
 //
 // Warp roles (192 threads):
 //   warp 0      TMA producer: fills a ring of shared-memory stages (mbarrier full/empty)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer; accumulators are
 //               double-buffered in TMEM (2 x 256 fp32 columns) so the epilogue of
 //               one tile overlaps the main loop of the next
-//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, fused scalar epilogue
-//               (EpiParams), global stores
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, fused arithmetic
+//               (EpiParams), then 32 x 32 bf16 boxes staged in shared memory and
+//               written with TMA bulk-tensor stores
 //
-// Operand modes (template SPLIT): 1: A*B; 2: Ah*B + Al*B; 3: Ah*Bh + Ah*Bl + Al*Bh where
-// X = Xh + Xl is a value split into a bf16 head and a bf16 residual (about 16
-// significant bits per operand, fp32 accumulation).  B is read K-major
-// ([N, K] row-major, used for symmetric right operands, whose rows are their
-// columns) or MN-major ([K, N] row-major, e.g. X in Q X).
+// Split operands.  A value X carried as a bf16 head Xh and a bf16 residual Xl
+// (X ~ Xh + Xl to ~16 significant bits) is multiplied as a sum of plain bf16
+// products: Ah Bh + Ah Bl + Al Bh (three "K segments", the lo*lo term dropped)
+// or Ah B + Al B (two).  Each segment is an ordinary pass over K with its own
+// pair of tensor maps, all accumulating into the same TMEM tile, so split
+// products run on the same 128-byte-swizzled pipeline as plain ones.
+//
+// B is read K-major ([N, K] row-major: symmetric right operands, whose rows are
+// their columns) or MN-major ([K, N] row-major, e.g. X in B X or Q X).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -31,45 +36,42 @@
 
 namespace muon {
 
-template <int SPLIT, bool BMN, int SWB>
 struct TcCfg {
   static constexpr int BM = 128;
   static constexpr int BN = 256;
-  static constexpr int BK = SWB / 2;  // bf16 elements per swizzled row
+  static constexpr int BK = 64;  // bf16 elements per 128-byte swizzled row
   static constexpr int A_TILE = BM * BK * 2;
   static constexpr int B_TILE = BN * BK * 2;
-  static constexpr int NA = (SPLIT >= 2) ? 2 : 1;
-  static constexpr int NB = (SPLIT == 3) ? 2 : 1;
-  static constexpr int STAGE = NA * A_TILE + NB * B_TILE;
-  // Epilogue staging per epilogue warp: NBUF sets of four 32 x 32 bf16 output
-  // boxes (head, residual part, and their mirrors) and two sets of two input
-  // boxes for the prefetched residual pair R = Rh + Rl; 2 KB per box.
+  static constexpr int STAGE = A_TILE + B_TILE;
+  static constexpr int STAGES = 3;
+  // Epilogue staging per epilogue warp: four 32 x 32 bf16 output boxes (head,
+  // residual part, and their mirrors) and two sets of two input boxes for the
+  // prefetched residual pair R = Rh + Rl; 2 KB per box.
   static constexpr int BOX = 32 * 32 * 2;
-  static constexpr int NBUF = STAGE >= 48 * 1024 ? 1 : 2;
-  static constexpr int OUT_WARP = NBUF * 4 * BOX;
+  static constexpr int OUT_WARP = 4 * BOX;
   static constexpr int RIN_WARP = 2 * 2 * BOX;
   static constexpr int STG_WARP = OUT_WARP + RIN_WARP;
   static constexpr int STG = 4 * STG_WARP;
-  static constexpr int STAGES_RAW = (224 * 1024 - STG) / STAGE;
-  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = STAGES * STAGE + STG + BAR_BYTES + 1024;
-  static constexpr uint32_t SWZ = (SWB == 128) ? 2u : 4u;  // descriptor swizzle code
-  static constexpr int MN_ATOM = SWB / 2;                  // MN elements per swizzle row (MN-major)
-  static constexpr int MN_BOX_BYTES = BK * SWB;            // one [BK x MN_ATOM] box
+  static constexpr uint32_t SWZ = 2u;            // descriptor code for the 128-byte swizzle
+  static constexpr int MN_ATOM = 64;             // MN elements per swizzled row (MN-major)
+  static constexpr int MN_BOX_BYTES = BK * 128;  // one [BK x MN_ATOM] box
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static_assert(STAGES >= 3, "need at least three stages");
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(BAR_BYTES >= (2 * STAGES + 5 + 8) * 8 + 8, "barrier area too small");
 };
 
 struct TcArgs {
-  int M, N, K;  // padded sizes (multiples of 128 / 256 / BK)
-  int sym;      // 1: lower-triangle tiles of a symmetric M x M output
-  int nI, nJ;   // tile grid of one matrix
-  int tpm;      // tiles per matrix
-  int total;    // tiles over the batch
-  int* status;  // workspace status word
+  int M, N, K;    // padded sizes (multiples of 128 / 256 / 64)
+  int sym;        // 1: lower-triangle tiles of a symmetric M x M output
+  int nI, nJ;     // tile grid of one matrix
+  int tpm;        // tiles per matrix
+  int total;      // tiles over the batch
+  int nseg;       // K segments (1 plain, 2 or 3 split)
+  int seg_lo;     // bit 2s: segment s reads A's residual map; bit 2s+1: B's residual map
+  int final_vec;  // final mode may use 16-byte accesses to the caller's rows
+  int* status;    // workspace status word
   EpiParams epi;
 };
 
@@ -110,19 +112,21 @@ __device__ __forceinline__ uint32_t sw64(int row, int byte) {
   return static_cast<uint32_t>(row * 64 + ((((byte >> 4) ^ (row >> 1)) & 3) << 4) + (byte & 15));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // a in the low half
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Split 32 values into packed bf16x2 words: head hw = bf16(v), residual lw = bf16(v - head).
-__device__ __forceinline__ void split_words(const float (&v)[32], uint32_t (&hw)[16], uint32_t (&lw)[16]) {
+__device__ __forceinline__ void split_words(const float (&v)[32], uint32_t (&hw)[16], uint32_t (&lw)[16],
+                                            bool want_lo) {
 #pragma unroll
   for (int k = 0; k < 16; ++k) {
-    const float a = v[2 * k], b = v[2 * k + 1];
-    const bf16 ha = __float2bfloat16_rn(a), hb = __float2bfloat16_rn(b);
-    hw[k] = static_cast<uint32_t>(__bfloat16_as_ushort(ha)) | (static_cast<uint32_t>(__bfloat16_as_ushort(hb)) << 16);
-    lw[k] = pack_bf16x2(a - __bfloat162float(ha), b - __bfloat162float(hb));
+    hw[k] = pack2(v[2 * k], v[2 * k + 1]);
+    if (want_lo) lw[k] = pack2(v[2 * k] - bf_lo(hw[k]), v[2 * k + 1] - bf_hi(hw[k]));
   }
 }
 
@@ -130,7 +134,8 @@ __device__ __forceinline__ void split_words(const float (&v)[32], uint32_t (&hw)
 __device__ __forceinline__ void stage_row(uint8_t* box, int row, const uint32_t (&w)[16]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q)
-    *reinterpret_cast<uint4*>(box + sw64(row, q * 16)) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    *reinterpret_cast<uint4*>(box + sw64(row, q * 16)) =
+        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
 }
 
 // Transposed box: lane t holds row t of the block; the box gets column t.  Lane
@@ -143,8 +148,7 @@ __device__ __forceinline__ void stage_col(uint8_t* box, int lane, const uint32_t
     const uint32_t y = __shfl_xor_sync(0xffffffffu, w[u], 1);
     const uint32_t word = odd ? __byte_perm(y, w[u], 0x7632) : __byte_perm(w[u], y, 0x5410);
     const int row = 2 * u + (odd ? 1 : 0);
-    const int col = lane & ~1;
-    *reinterpret_cast<uint32_t*>(box + sw64(row, col * 2)) = word;
+    *reinterpret_cast<uint32_t*>(box + sw64(row, (lane & ~1) * 2)) = word;
   }
 }
 
@@ -160,17 +164,76 @@ __device__ __forceinline__ void symmetrize_box(uint8_t* box, int lane) {
   }
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// Final write of a full 32 x 32 block to a caller's row-major matrix (not
+// transposed): global memory is read and written a warp-wide few rows at a time
+// through a padded shared-memory box, lane t owning row t in between.
+template <typename T>
+__device__ __forceinline__ void final_block_rows(const EpiParams& e, int b, int r0, int c0, int lane,
+                                                 const float (&v)[32], uint8_t* box) {
+  constexpr int ROWB = 32 * static_cast<int>(sizeof(T));  // bytes of one block row
+  constexpr int STRIDE = ROWB + 16;                        // padded row stride in shared memory
+  constexpr int PIECES = ROWB / 16;                        // 16-byte pieces per row
+  constexpr int ROWS_PER = 32 / PIECES;                    // rows covered by one warp-wide access
+  constexpr int EPP = 16 / static_cast<int>(sizeof(T));    // elements per piece
+  const long long cols = e.cols_valid;
+  T* dst = static_cast<T*>(e.dst[b]);
+  const bool apply = e.final_mode == FINAL_APPLY;
+  if (apply) {
+#pragma unroll
+    for (int it = 0; it < PIECES; ++it) {
+      const int row = it * ROWS_PER + lane / PIECES, pc = lane % PIECES;
+      const uint4 x = *reinterpret_cast<const uint4*>(dst + (r0 + row) * cols + c0 + pc * EPP);
+      *reinterpret_cast<uint4*>(box + row * STRIDE + pc * 16) = x;
+    }
+    __syncwarp();
+  }
+  // lane owns row `lane`
+#pragma unroll
+  for (int pc = 0; pc < PIECES; ++pc) {
+    uint4* p = reinterpret_cast<uint4*>(box + lane * STRIDE + pc * 16);
+    if (sizeof(T) == 2) {
+      uint32_t w[4];
+      if (apply) {
+        const uint4 x = *p;
+        const uint32_t in[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          w[u] = pack2(bf_lo(in[u]) - e.lr * v[pc * 8 + 2 * u], bf_hi(in[u]) - e.lr * v[pc * 8 + 2 * u + 1]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) w[u] = pack2(v[pc * 8 + 2 * u], v[pc * 8 + 2 * u + 1]);
+      }
+      *p = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      float4 y;
+      if (apply) {
+        const float4 x = *reinterpret_cast<const float4*>(p);
+        y = make_float4(x.x - e.lr * v[pc * 4], x.y - e.lr * v[pc * 4 + 1], x.z - e.lr * v[pc * 4 + 2],
+                        x.w - e.lr * v[pc * 4 + 3]);
+      } else {
+        y = make_float4(v[pc * 4], v[pc * 4 + 1], v[pc * 4 + 2], v[pc * 4 + 3]);
+      }
+      *reinterpret_cast<float4*>(p) = y;
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < PIECES; ++it) {
+    const int row = it * ROWS_PER + lane / PIECES, pc = lane % PIECES;
+    *reinterpret_cast<uint4*>(dst + (r0 + row) * cols + c0 + pc * EPP) =
+        *reinterpret_cast<const uint4*>(box + row * STRIDE + pc * 16);
+  }
+  __syncwarp();
+}
 
-template <int SPLIT, bool BMN, int SWB>
+template <bool BMN>
 __global__ void __launch_bounds__(192, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAl,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBl,
                    const __grid_constant__ CUtensorMap tmOh, const __grid_constant__ CUtensorMap tmOl,
                    const __grid_constant__ CUtensorMap tmRh, const __grid_constant__ CUtensorMap tmRl,
                    const __grid_constant__ TcArgs args) {
-  using C = TcCfg<SPLIT, BMN, SWB>;
+  using C = TcCfg;
   extern __shared__ uint8_t smem_raw[];
   // Swizzled tiles must start on a 1024-byte boundary of the shared window.
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -203,8 +266,10 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (C::NA == 2) tma_prefetch_desc(&tmAl);
-    if (C::NB == 2) tma_prefetch_desc(&tmBl);
+    if (args.nseg > 1) {
+      tma_prefetch_desc(&tmAl);
+      tma_prefetch_desc(&tmBl);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -214,7 +279,8 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int nk = args.K / C::BK;
+  const int nk = args.K / C::BK;   // k-blocks per segment
+  const int nkb = nk * args.nseg;  // k-blocks per tile
 
   if (warp == 0) {
     if (lane == 0) {
@@ -225,29 +291,27 @@ __global__ void __launch_bounds__(192, 1)
         int b, i, j;
         decode_tile(args, t, b, i, j);
         const int m0 = i * C::BM, n0 = j * C::BN;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
           if (*abort_flag || !mbar_wait(&empty[s], ph ^ 1)) {
             ok = false;
             break;
           }
+          const int seg = kb / nk;
+          const CUtensorMap* ma = ((args.seg_lo >> (2 * seg)) & 1) ? &tmAl : &tmA;
+          const CUtensorMap* mb = ((args.seg_lo >> (2 * seg + 1)) & 1) ? &tmBl : &tmB;
           uint8_t* st = tiles + s * C::STAGE;
           mbar_arrive_expect_tx(&full[s], C::STAGE);
-          const int k0 = kb * C::BK;
-          tma_load_3d(&tmA, &full[s], st, k0, m0, b);
-          if (C::NA == 2) tma_load_3d(&tmAl, &full[s], st + C::A_TILE, k0, m0, b);
-          uint8_t* sb = st + C::NA * C::A_TILE;
+          const int k0 = (kb - seg * nk) * C::BK;
+          tma_load_3d(ma, &full[s], st, k0, m0, b);
+          uint8_t* sb = st + C::A_TILE;
           if (!BMN) {
-            tma_load_3d(&tmB, &full[s], sb, k0, n0, b);
-            if (C::NB == 2) tma_load_3d(&tmBl, &full[s], sb + C::B_TILE, k0, n0, b);
+            tma_load_3d(mb, &full[s], sb, k0, n0, b);
           } else {
 #pragma unroll
-            for (int q = 0; q < C::BN / C::MN_ATOM; ++q) {
-              tma_load_3d(&tmB, &full[s], sb + q * C::MN_BOX_BYTES, n0 + q * C::MN_ATOM, k0, b);
-              if (C::NB == 2)
-                tma_load_3d(&tmBl, &full[s], sb + C::B_TILE + q * C::MN_BOX_BYTES, n0 + q * C::MN_ATOM, k0, b);
-            }
+            for (int q = 0; q < C::BN / C::MN_ATOM; ++q)
+              tma_load_3d(mb, &full[s], sb + q * C::MN_BOX_BYTES, n0 + q * C::MN_ATOM, k0, b);
           }
         }
       }
@@ -263,7 +327,7 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t idesc = make_idesc_bf16(C::BM, C::BN, BMN);
-      constexpr uint32_t SBO = 8 * SWB;
+      constexpr uint32_t SBO = 8 * 128;
       int it = 0, tcount = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < args.total && ok; t += gridDim.x, ++tcount) {
@@ -275,7 +339,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + abuf * C::BN;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
           if (*abort_flag || !mbar_wait(&full[s], ph)) {
@@ -284,24 +348,13 @@ __global__ void __launch_bounds__(192, 1)
           }
           tc_fence_after();
           const uint32_t a0 = smem_u32(tiles + s * C::STAGE);
-          const uint32_t al = a0 + C::A_TILE;
-          const uint32_t b0 = a0 + C::NA * C::A_TILE;
-          const uint32_t bl = b0 + C::B_TILE;
+          const uint32_t b0 = a0 + C::A_TILE;
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
             const uint64_t ad = make_sdesc(a0 + kk * 32, 16, SBO, C::SWZ);
-            const uint64_t adl = make_sdesc(al + kk * 32, 16, SBO, C::SWZ);
-            const uint64_t bd = BMN ? make_sdesc(b0 + kk * 16 * SWB, C::MN_BOX_BYTES, SBO, C::SWZ)
+            const uint64_t bd = BMN ? make_sdesc(b0 + kk * 16 * 128, C::MN_BOX_BYTES, SBO, C::SWZ)
                                     : make_sdesc(b0 + kk * 32, 16, SBO, C::SWZ);
-            const uint64_t bdl = BMN ? make_sdesc(bl + kk * 16 * SWB, C::MN_BOX_BYTES, SBO, C::SWZ)
-                                     : make_sdesc(bl + kk * 32, 16, SBO, C::SWZ);
-            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-            tc_mma_bf16(d, ad, bd, idesc, acc);
-            if (SPLIT == 2) tc_mma_bf16(d, adl, bd, idesc, 1u);
-            if (SPLIT == 3) {
-              tc_mma_bf16(d, ad, bdl, idesc, 1u);
-              tc_mma_bf16(d, adl, bd, idesc, 1u);
-            }
+            tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[s]);  // stage is free once these MMAs have read it
         }
@@ -319,7 +372,8 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     // Each warp owns 32 accumulator rows (its TMEM lane quarter).  Per 32-column
-    // chunk: residual prefetch, tcgen05.ld, fused arithmetic, then either the
+    // chunk: residual boxes prefetched by TMA, tcgen05.ld of the next chunk
+    // issued before this one is processed, fused arithmetic, then either the
     // final write to the caller's matrix or swizzled staging of 32 x 32 bf16
     // boxes (and their transposes for symmetric outputs) that one lane sends to
     // global memory with TMA bulk-tensor stores.
@@ -333,7 +387,6 @@ __global__ void __launch_bounds__(192, 1)
     const bool has_r = e.Rh != nullptr;
     const bool has_rl = e.Rl != nullptr;
     const uint32_t rbytes = has_rl ? 2 * C::BOX : C::BOX;
-    int tcount = 0, sbuf = 0;
     // Residual boxes go through a two-deep ring per warp; r_issued / r_used
     // count the boxes requested / consumed (warp-uniform, lane 0 issues).
     int r_issued = 0, r_used = 0;
@@ -347,7 +400,9 @@ __global__ void __launch_bounds__(192, 1)
       }
       ++r_issued;
     };
-    for (int t = blockIdx.x; t < args.total; t += gridDim.x, ++tcount) {
+    int tcount = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < args.total && ok; t += gridDim.x, ++tcount) {
       int b, i, j;
       decode_tile(args, t, b, i, j);
       const int m0 = i * C::BM, n0 = j * C::BN;
@@ -362,18 +417,34 @@ __global__ void __launch_bounds__(192, 1)
       const int abuf = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       if (*abort_flag || !mbar_wait(&tfull[abuf], aph)) {
-        if (lane == 0) atomicOr(args.status, kStatusTimeout);
-        *abort_flag = 1;
+        ok = false;
         break;
       }
       tc_fence_after();
       const float sc = epi_scale(e, b);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + abuf * C::BN;
-      bool ok = true;
+      uint32_t acc[2][32];
+      __syncwarp();
+      tmem_ld_32x32b_x32_start(tbase, acc[0]);
 #pragma unroll 1
       for (int cc = 0; cc < nch; ++cc) {
         const int c0 = n0 + cc * 32;
-        uint32_t rhw[16], rlw[16];
+        float v[32];
+        // Wait for chunk cc, then start loading chunk cc + 1 into the other set.
+        if (cc & 1) {
+          tmem_ld_wait(acc[1]);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) v[u] = __uint_as_float(acc[1][u]);
+        } else {
+          tmem_ld_wait(acc[0]);
+#pragma unroll
+          for (int u = 0; u < 32; ++u) v[u] = __uint_as_float(acc[0][u]);
+        }
+        if (cc + 1 < nch) {
+          __syncwarp();
+          if (cc & 1) tmem_ld_32x32b_x32_start(tbase + (cc + 1) * 32, acc[0]);
+          else tmem_ld_32x32b_x32_start(tbase + (cc + 1) * 32, acc[1]);
+        }
         if (has_r) {
           const int idx = rbase + cc;
           if (!mbar_wait(&rb[idx & 1], (idx >> 1) & 1)) {
@@ -381,6 +452,7 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           const uint8_t* src = rin + (idx & 1) * 2 * C::BOX;
+          uint32_t rhw[16], rlw[16];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint4 h = *reinterpret_cast<const uint4*>(src + sw64(lane, q * 16));
@@ -392,11 +464,6 @@ __global__ void __launch_bounds__(192, 1)
           r_used = idx + 1;
           __syncwarp();
           if (cc + 2 < nch) issue_r(c0 + 64, r0, b);  // the buffer just read is free again
-        }
-        float v[32];
-        __syncwarp();
-        tmem_ld_32x32b_x32(tbase + cc * 32, v);
-        if (has_r) {
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
             const float x0 = bf_lo(rhw[u]) + bf_lo(rlw[u]);
@@ -414,18 +481,24 @@ __global__ void __launch_bounds__(192, 1)
           for (int u = 0; u < 32; ++u)
             if (c0 + u == r) v[u] += e.c_id;
         }
+        uint8_t* sb = stg;
         if (e.final_mode != FINAL_NONE) {
+          const bool full_block = r0 + 32 <= e.rows_valid && c0 + 32 <= e.cols_valid;
+          if (!e.tr[b] && args.final_vec && full_block) {
+            if (e.dst_fp32) final_block_rows<float>(e, b, r0, c0, lane, v, sb);
+            else final_block_rows<bf16>(e, b, r0, c0, lane, v, sb);
+          } else {
 #pragma unroll
-          for (int u = 0; u < 32; ++u) epi_final_elem(e, b, r, c0 + u, v[u]);
+            for (int u = 0; u < 32; ++u) epi_final_elem(e, b, r, c0 + u, v[u]);
+          }
           continue;
         }
         const bool diag = args.sym && c0 == r0;
         const bool mirror = args.sym && c0 < r0;  // strictly-lower block: also store its transpose
         uint32_t hw[16], lw[16];
-        split_words(v, hw, lw);
-        if (lane == 0) bulk_wait_read<C::NBUF - 1>();  // this staging buffer's previous stores have read it
+        split_words(v, hw, lw, has_lo);
+        if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have read the staging boxes
         __syncwarp();
-        uint8_t* sb = stg + sbuf * (4 * C::BOX);
         stage_row(sb, lane, hw);
         if (has_lo) stage_row(sb + C::BOX, lane, lw);
         if (mirror) {
@@ -448,15 +521,18 @@ __global__ void __launch_bounds__(192, 1)
           }
           bulk_commit();
         }
-        sbuf = (sbuf + 1) % C::NBUF;
       }
       if (!ok) {
-        if (lane == 0) atomicOr(args.status, kStatusTimeout);
-        *abort_flag = 1;
+        // a TMEM load may still be in flight: complete it before leaving
+        tmem_ld_wait(acc[0]);
         break;
       }
       tc_fence_before();
       mbar_arrive(&tempty[abuf]);
+    }
+    if (!ok) {
+      if (lane == 0) atomicOr(args.status, kStatusTimeout);
+      *abort_flag = 1;
     }
     if (lane == 0) {
       // residual boxes still in flight land before the CTA can retire
@@ -506,52 +582,53 @@ static bool make_map(CUtensorMap* m, const bf16* base, uint64_t inner, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
-template <int SPLIT, bool BMN, int SWB>
+template <bool BMN>
 static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* status, cudaStream_t st,
                                int num_sms, const char** why) {
-  using C = TcCfg<SPLIT, BMN, SWB>;
+  using C = TcCfg;
   {
-    const cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<SPLIT, BMN, SWB>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    const cudaError_t e =
+        cudaFuncSetAttribute(tc_gemm_kernel<BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap mA, mAl, mB, mBl;
-  bool ok = make_map(&mA, d.A.hi, d.K, d.M, d.B, d.A.ld, d.A.bs, C::BK, C::BM, SWB);
-  ok = ok && make_map(&mAl, (C::NA == 2 && d.A.lo) ? d.A.lo : d.A.hi, d.K, d.M, d.B, d.A.ld, d.A.bs, C::BK,
-                      C::BM, SWB);
+  const bf16* alo = d.A.lo ? d.A.lo : d.A.hi;
+  const bf16* blo = d.Bop.lo ? d.Bop.lo : d.Bop.hi;
+  bool ok = make_map(&mA, d.A.hi, d.K, d.M, d.B, d.A.ld, d.A.bs, C::BK, C::BM, 128);
+  ok = ok && make_map(&mAl, alo, d.K, d.M, d.B, d.A.ld, d.A.bs, C::BK, C::BM, 128);
   if (!BMN) {
-    ok = ok && make_map(&mB, d.Bop.hi, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::BK, C::BN, SWB);
-    ok = ok && make_map(&mBl, (C::NB == 2 && d.Bop.lo) ? d.Bop.lo : d.Bop.hi, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs,
-                        C::BK, C::BN, SWB);
+    ok = ok && make_map(&mB, d.Bop.hi, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::BK, C::BN, 128);
+    ok = ok && make_map(&mBl, blo, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::BK, C::BN, 128);
   } else {
-    ok = ok && make_map(&mB, d.Bop.hi, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, SWB);
-    ok = ok && make_map(&mBl, (C::NB == 2 && d.Bop.lo) ? d.Bop.lo : d.Bop.hi, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs,
-                        C::MN_ATOM, C::BK, SWB);
+    ok = ok && make_map(&mB, d.Bop.hi, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
+    ok = ok && make_map(&mBl, blo, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
   }
   // Output maps: 32 x 32 bf16 boxes with the 64-byte swizzle (dummies in final mode).
   CUtensorMap mOh, mOl;
-  bf16* oh = epi.Oh ? epi.Oh : const_cast<bf16*>(d.A.hi);
-  bf16* ol = epi.Ol ? epi.Ol : oh;
-  const long long old_ = epi.Oh ? epi.ld : d.A.ld;
-  const long long obs = epi.Oh ? epi.bs : d.A.bs;
-  const uint64_t orows = epi.Oh ? static_cast<uint64_t>(d.M) : static_cast<uint64_t>(d.M);
-  const uint64_t ocols = epi.Oh ? static_cast<uint64_t>(epi.ld) : static_cast<uint64_t>(d.K);
+  const bool has_out = epi.Oh != nullptr;
+  const bf16* oh = has_out ? epi.Oh : d.A.hi;
+  const bf16* ol = epi.Ol ? epi.Ol : oh;
+  const long long old_ = has_out ? epi.ld : d.A.ld;
+  const long long obs = has_out ? epi.bs : d.A.bs;
+  const uint64_t ocols = has_out ? static_cast<uint64_t>(epi.ld) : static_cast<uint64_t>(d.K);
+  const uint64_t orows = static_cast<uint64_t>(d.M);
   ok = ok && make_map(&mOh, oh, ocols, orows, d.B, old_, obs, 32, 32, 64);
   ok = ok && make_map(&mOl, ol, ocols, orows, d.B, old_, obs, 32, 32, 64);
   // Residual maps (same box and swizzle as the outputs; dummies without a residual).
   CUtensorMap mRh, mRl;
-  const bf16* rh = epi.Rh ? epi.Rh : oh;
+  const bool has_r = epi.Rh != nullptr;
+  const bf16* rh = has_r ? epi.Rh : oh;
   const bf16* rl = epi.Rl ? epi.Rl : rh;
-  const long long rld = epi.Rh ? epi.ld : old_;
-  const long long rbs = epi.Rh ? epi.bs : obs;
-  const uint64_t rcols = epi.Rh ? static_cast<uint64_t>(epi.ld) : ocols;
+  const long long rld = has_r ? epi.ld : old_;
+  const long long rbs = has_r ? epi.bs : obs;
+  const uint64_t rcols = has_r ? static_cast<uint64_t>(epi.ld) : ocols;
   ok = ok && make_map(&mRh, rh, rcols, orows, d.B, rld, rbs, 32, 32, 64);
   ok = ok && make_map(&mRl, rl, rcols, orows, d.B, rld, rbs, 32, 32, 64);
   if (!ok) {
     *why = "cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
   }
-  if (epi.final_mode == FINAL_NONE && !epi.Oh) {
+  if (epi.final_mode == FINAL_NONE && !has_out) {
     *why = "tensor-core epilogue needs a bf16 output pair";
     return cudaErrorInvalidValue;
   }
@@ -569,25 +646,47 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
     a.tpm = a.nI * a.nJ;
   }
   a.total = a.tpm * d.B;
+  // K segments of the split products (bit 2s: A residual, bit 2s+1: B residual)
+  if (d.split == 1) {
+    a.nseg = 1;
+    a.seg_lo = 0;
+  } else if (d.split == 2) {  // Ah B + Al B
+    a.nseg = 2;
+    a.seg_lo = 1 << 2;
+  } else {  // Ah Bh + Ah Bl + Al Bh
+    a.nseg = 3;
+    a.seg_lo = (1 << 3) | (1 << 4);
+  }
   a.status = status;
   a.epi = epi;
   a.epi.sym = d.sym;
+  // 16-byte row accesses to the caller's matrices in final mode need aligned rows
+  a.final_vec = 1;
+  if (epi.final_mode != FINAL_NONE) {
+    const int esz = epi.dst_fp32 ? 4 : 2;
+    if ((static_cast<long long>(epi.cols_valid) * esz) % 16) a.final_vec = 0;
+    for (int q = 0; q < d.B; ++q)
+      if (reinterpret_cast<uintptr_t>(epi.dst[q]) % 16) a.final_vec = 0;
+  }
   const int grid = a.total < num_sms ? a.total : num_sms;
   if (grid <= 0) return cudaSuccess;
-  tc_gemm_kernel<SPLIT, BMN, SWB><<<grid, 192, C::SMEM, st>>>(mA, mAl, mB, mBl, mOh, mOl, mRh, mRl, a);
+  tc_gemm_kernel<BMN><<<grid, 192, C::SMEM, st>>>(mA, mAl, mB, mBl, mOh, mOl, mRh, mRl, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* status, cudaStream_t st, int num_sms,
                            const char** why) {
   *why = nullptr;
-  if (d.split == 1 && !d.b_mn) return launch_impl<1, false, 128>(d, epi, status, st, num_sms, why);
-  if (d.split == 1 && d.b_mn) return launch_impl<1, true, 128>(d, epi, status, st, num_sms, why);
-  if (d.split == 2 && d.b_mn) return launch_impl<2, true, 64>(d, epi, status, st, num_sms, why);
-  if (d.split == 3 && !d.b_mn) return launch_impl<3, false, 64>(d, epi, status, st, num_sms, why);
-  if (d.split == 3 && d.b_mn) return launch_impl<3, true, 64>(d, epi, status, st, num_sms, why);
-  *why = "unsupported operand split";
-  return cudaErrorInvalidValue;
+  if (d.split < 1 || d.split > 3 || (d.split == 2 && !d.b_mn)) {
+    *why = "unsupported operand split";
+    return cudaErrorInvalidValue;
+  }
+  if ((d.split >= 2 && !d.A.lo) || (d.split == 3 && !d.Bop.lo)) {
+    *why = "split products need the residual operands";
+    return cudaErrorInvalidValue;
+  }
+  return d.b_mn ? launch_impl<true>(d, epi, status, st, num_sms, why)
+                : launch_impl<false>(d, epi, status, st, num_sms, why);
 }
 
 int tc_tiles(int M, int N, int sym) {
