@@ -169,7 +169,11 @@ MUON_API muon_status muon_debug_bounded_wait(void* ws, long long max_cycles, voi
  *   A B + A B_lo + A_lo B.  C is returned as a bf16 pair: out = bf16(C) and,
  *   if out_lo is not NULL, out_lo = bf16(C - out) ([batch, M, N] each).
  *   dt = MUON_FP32 runs the FFMA kernel on fp32 A, B and writes fp32 C to out.
- *   sym = 1 (M == N) computes only the lower triangle and mirrors it.
+ *   sym bit 0 (M == N): symmetric output; the bf16 kernel computes the tiles
+ *   touching the lower triangle and stores the output "block-lower" (only the
+ *   256 x 256 blocks on or below the diagonal are written), the fp32 kernel
+ *   writes the full matrix.  sym bits 1 / 2 (bf16 only): A / B is a symmetric
+ *   matrix given in block-lower storage (its upper blocks are never read).
  *   Sizes: bf16 needs M % 128, N % 256, K % 64 == 0; fp32 needs M, N % 128 and
  *   K % 16 == 0.  The kernel is enqueued on `stream`.
  */

@@ -205,11 +205,14 @@ def debug_bounded_wait(workspace: torch.Tensor, max_cycles: int, stream=None) ->
                                           ctypes.c_void_p(_stream_ptr(stream))))
 
 
-def debug_gemm(A, B, A_lo=None, B_lo=None, split=1, b_mn=False, sym=False, workspace=None, stream=None):
+def debug_gemm(A, B, A_lo=None, B_lo=None, split=1, b_mn=False, sym=False, a_sym=False, b_sym=False,
+               workspace=None, stream=None):
     """Test hook: out[b] = A[b] @ (B[b] if b_mn else B[b]^T) through one library kernel.
 
     bf16 operands run the tensor-core kernel and return the fp32 sum of the
-    bf16 head/residual pair it writes; fp32 operands run the FFMA kernel."""
+    bf16 head/residual pair it writes (with sym, only the 256 x 256 blocks on
+    or below the diagonal are written); a_sym / b_sym declare operands given
+    in that block-lower storage.  fp32 operands run the FFMA kernel."""
     lib = load()
     batch, M, K = A.shape
     N = B.shape[2] if b_mn else B.shape[1]
@@ -222,7 +225,8 @@ def debug_gemm(A, B, A_lo=None, B_lo=None, split=1, b_mn=False, sym=False, works
     else:
         out = torch.zeros(batch, M, N, dtype=torch.bfloat16, device=A.device)
         lo = torch.zeros_like(out)
-    _check(lib.muon_debug_gemm(ptr(A), ptr(A_lo), ptr(B), ptr(B_lo), batch, M, N, K, split, int(b_mn), int(sym),
+    flags = int(sym) | (int(a_sym) << 1) | (int(b_sym) << 2)
+    _check(lib.muon_debug_gemm(ptr(A), ptr(A_lo), ptr(B), ptr(B_lo), batch, M, N, K, split, int(b_mn), flags,
                                _dtype_code(A.dtype), ptr(out), ptr(lo), ptr(workspace), workspace.numel(),
                                ctypes.c_void_p(_stream_ptr(stream))))
     return out if lo is None else out.float() + lo.float()

@@ -487,6 +487,8 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     return MUON_OK;
   }
 
+  // sym: bit 0 = symmetric output (lower tiles, block-lower storage); bits 1 / 2 =
+  // A / B is a symmetric operand in that storage.
   auto tc = [&](int split, int b_mn, int sym, int M, int N, int K, const bf16* Ah, const bf16* Al, long long lda,
                 long long bsa, const bf16* Bh, const bf16* Bl, long long ldb, long long bsb, const EpiParams& e) {
     TcGemmDesc d;
@@ -494,17 +496,19 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     d.M = M;
     d.N = N;
     d.K = K;
-    d.sym = sym;
+    d.sym = sym & 1;
+    d.a_sym = (sym >> 1) & 1;
+    d.b_sym = (sym >> 2) & 1;
     d.split = split;
     d.b_mn = b_mn;
     d.A = TcOperand{Ah, Al, lda, bsa};
     d.Bop = TcOperand{Bh, Bl, ldb, bsb};
     const double Kt = K == S ? static_cast<double>(g.s) : static_cast<double>(g.l);
-    const double fl = sym ? Bc * static_cast<double>(g.s) * g.s * Kt : 2.0 * Bc * g.s * g.l * Kt;
+    const double fl = d.sym ? Bc * static_cast<double>(g.s) * g.s * Kt : 2.0 * Bc * g.s * g.l * Kt;
     static const char* const kSym[4] = {"", "tc_sym", "tc_sym_x2", "tc_sym_x3"};
     static const char* const kSyrk[4] = {"", "tc_syrk", "tc_syrk_x2", "tc_syrk_x3"};
     static const char* const kRect[4] = {"", "tc_rect", "tc_rect_x2", "tc_rect_x3"};
-    const char* kind = sym ? (K == S ? kSym[split] : kSyrk[split]) : kRect[split];
+    const char* kind = d.sym ? (K == S ? kSym[split] : kSyrk[split]) : kRect[split];
     ProfScope ps(kind, fl, 0.0, cx.st);
     return launch_tc_gemm(d, e, cx.status, cx.st, cx.sms, &why);
   };
@@ -525,13 +529,13 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
       // B = b A + c A^2 with A = Ah + Al in the epilogue
       EpiParams e2 =
           epi_pair(g, bf, 0, cx.c, cx.b, 0.f, bf.Gh, bf.Gl, bf.Bh, split ? bf.Bl : nullptr, sp, bss);
-      CK(tc(split ? 3 : 1, 0, 1, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, e2));
+      CK(tc(split ? 3 : 1, 0, 7, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, e2));
       // X <- a X + B X (k = 0: both terms carry 1 / s); X kept as a bf16 pair
       EpiParams e3 = epi_pair(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, bf.Xb[cur], bf.Xlo[cur], bf.Xb[nxt],
                               bf.Xlo[nxt], lp, bsx);
       e3.cols_valid = static_cast<int>(g.l);
       if (k == T - 1) epi_set_final(e3, cx, g, mats, Bc);
-      CK(tc(split ? 2 : 1, 1, 0, S, L, S, bf.Bh, bf.Bl, sp, bss, bf.Xb[cur], nullptr, lp, bsx, e3));
+      CK(tc(split ? 2 : 1, 1, 2, S, L, S, bf.Bh, bf.Bl, sp, bss, bf.Xb[cur], nullptr, lp, bsx, e3));
       cur = nxt;
     }
     return MUON_OK;
@@ -549,7 +553,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     bf16* Pl = bf.Pl[k & 1];
     // P = a I + b G + c G^2
     EpiParams ep = epi_pair(g, bf, 0, cx.c, cx.b, cx.a, bf.Gh, bf.Gl, Ph, Pl, sp, bss);
-    CK(tc(sp3, 0, 1, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, ep));
+    CK(tc(sp3, 0, 7, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, ep));
     if (k == 0) {
       Qh = Ph;
       Ql = Pl;
@@ -558,21 +562,21 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
       bf16* Qnl = bf.Ql[qi];
       qi ^= 1;
       EpiParams eq = epi_pair(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, Qnh, Qnl, sp, bss);
-      CK(tc(sp3, 0, 1, S, S, S, Ph, Pl, sp, bss, Qh, Ql, sp, bss, eq));
+      CK(tc(sp3, 0, 7, S, S, S, Ph, Pl, sp, bss, Qh, Ql, sp, bss, eq));
       Qh = Qnh;
       Ql = Qnl;
     }
     if (k + 1 < T) {
       EpiParams eh = epi_pair(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Hh, bf.Hl, sp, bss);
-      CK(tc(sp3, 0, 1, S, S, S, Ph, Pl, sp, bss, bf.Gh, bf.Gl, sp, bss, eh));
+      CK(tc(sp3, 0, 7, S, S, S, Ph, Pl, sp, bss, bf.Gh, bf.Gl, sp, bss, eh));
       EpiParams eg = epi_pair(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, bf.Gl, sp, bss);
-      CK(tc(sp3, 0, 1, S, S, S, Ph, Pl, sp, bss, bf.Hh, bf.Hl, sp, bss, eg));
+      CK(tc(sp3, 0, 7, S, S, S, Ph, Pl, sp, bss, bf.Hh, bf.Hl, sp, bss, eg));
     }
   }
   // O = Q X0 = Q X / s
   EpiParams ef = epi_pair(g, bf, 1, 1.f, 0.f, 0.f, nullptr, nullptr, nullptr, nullptr, lp, bsx);
   epi_set_final(ef, cx, g, mats, Bc);
-  CK(tc(sp3, 1, 0, S, L, S, Qh, Ql, sp, bss, bf.Xb[0], bf.Xl, lp, bsx, ef));
+  CK(tc(sp3, 1, 2, S, L, S, Qh, Ql, sp, bss, bf.Xb[0], bf.Xl, lp, bsx, ef));
   return MUON_OK;
 }
 #undef CK
@@ -803,7 +807,7 @@ muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, cons
   if (!A || !B || !out || !ws || batch <= 0 || batch > kMaxBatch) return fail(MUON_ERR_ARG, "bad pointers or batch");
   if (ws_bytes < kHeader || reinterpret_cast<uintptr_t>(ws) % MUON_WS_ALIGN)
     return fail(MUON_ERR_WORKSPACE, "workspace must hold the %zu-byte header", kHeader);
-  if (sym && M != N) return fail(MUON_ERR_SHAPE, "sym needs M == N");
+  if ((sym & 1) && M != N) return fail(MUON_ERR_SHAPE, "sym needs M == N");
   if (b_mn != 0 && b_mn != 1) return fail(MUON_ERR_ARG, "b_mn must be 0 or 1");
   EpiParams e;
   memset(&e, 0, sizeof(e));
@@ -839,17 +843,20 @@ muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, cons
     d.M = M;
     d.N = N;
     d.K = K;
-    d.sym = sym;
+    d.sym = sym & 1;
+    d.a_sym = (sym >> 1) & 1;
+    d.b_sym = (sym >> 2) & 1;
     d.split = split;
     d.b_mn = b_mn;
     d.A = TcOperand{static_cast<const bf16*>(A), static_cast<const bf16*>(A_lo), K, static_cast<long long>(M) * K};
     d.Bop = TcOperand{static_cast<const bf16*>(B), static_cast<const bf16*>(B_lo), b_mn ? N : K, bsb};
     err = launch_tc_gemm(d, e, static_cast<int*>(ws), static_cast<cudaStream_t>(stream), sms, &why);
+    if (err == cudaErrorInvalidValue && why) return fail(MUON_ERR_ARG, "%s", why);
   } else if (dt == MUON_FP32) {
     if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 16) return fail(MUON_ERR_SHAPE, "fp32 sizes");
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) % 16)
       return fail(MUON_ERR_ALIGN, "fp32 operands must be 16-byte aligned");
-    SimtGemmDesc d{batch, M, N, K, sym, b_mn, static_cast<const float*>(A), K, static_cast<long long>(M) * K,
+    SimtGemmDesc d{batch, M, N, K, sym & 1, b_mn, static_cast<const float*>(A), K, static_cast<long long>(M) * K,
                    static_cast<const float*>(B), b_mn ? N : K, bsb};
     err = launch_simt_gemm(d, e, static_cast<cudaStream_t>(stream));
   } else {

@@ -19,10 +19,13 @@ struct TcOperand {
 // C[b] (M x N) = A[b] (M x K, row-major) * op(B[b]):
 //   b_mn = 0: B stored [N][K] (K-major), C = A B^T      (symmetric right operands, SYRK)
 //   b_mn = 1: B stored [K][N] (MN-major), C = A B        (e.g. Q X)
-// sym = 1 computes only the tiles touching the lower triangle (M == N).
+// sym = 1 computes only the tiles touching the lower triangle (M == N) and
+// stores the output block-lower (256 x 256 blocks on or below the diagonal).
+// a_sym / b_sym mark operands that are symmetric matrices in that storage.
 struct TcGemmDesc {
-  int B, M, N, K;  // M % 128 == 0, N % 256 == 0, K % 64 == 0
+  int B, M, N, K;  // M % 128 == 0, N % 256 == 0, K % 256 == 0
   int sym;
+  int a_sym, b_sym;
   int split;  // 1 or 3
   int b_mn;
   TcOperand A, Bop;

@@ -4,9 +4,15 @@
 // batch of same-shape matrices (DMuon technical summary, §2.2: same-shape
 // matrices are batched so small problems still fill the GPU).  For symmetric
 // outputs (the Gram matrix G = X X^T and every product of the commuting
-// polynomials of G) only tiles that touch the lower triangle are computed and
-// the epilogue also stores each block's transpose (same section: the symmetric
-// products compute only the lower triangle).
+// polynomials of G) only tiles that touch the lower triangle are computed (same
+// section: the symmetric products compute only the lower triangle).
+//
+// Symmetric storage.  A symmetric s x s matrix is stored "block-lower": only
+// its 256 x 256 blocks (I, J) with J <= I are written (diagonal blocks in
+// full).  When such a matrix is an operand, a 64-wide k-block that falls in an
+// upper block is read as the transposed (MN-major) box of the stored lower
+// block and the MMA instruction descriptor switches that operand's major-ness
+// for it; so no mirror is ever written.
 //
 // Warp roles (192 threads):
 //   warp 0      TMA producer: fills a ring of shared-memory stages (mbarrier full/empty)
@@ -44,11 +50,11 @@ struct TcCfg {
   static constexpr int B_TILE = BN * BK * 2;
   static constexpr int STAGE = A_TILE + B_TILE;
   static constexpr int STAGES = 3;
-  // Epilogue staging per epilogue warp: four 32 x 32 bf16 output boxes (head,
-  // residual part, and their mirrors) and two sets of two input boxes for the
+  // Epilogue staging per epilogue warp: two 32 x 32 bf16 output boxes (head and
+  // residual part, double buffered) and two sets of two input boxes for the
   // prefetched residual pair R = Rh + Rl; 2 KB per box.
   static constexpr int BOX = 32 * 32 * 2;
-  static constexpr int OUT_WARP = 4 * BOX;
+  static constexpr int OUT_WARP = 2 * 2 * BOX;
   static constexpr int RIN_WARP = 2 * 2 * BOX;
   static constexpr int STG_WARP = OUT_WARP + RIN_WARP;
   static constexpr int STG = 4 * STG_WARP;
@@ -69,6 +75,8 @@ struct TcArgs {
   int tpm;        // tiles per matrix
   int total;      // tiles over the batch
   int nseg;       // K segments (1 plain, 2 or 3 split)
+  int a_sym;      // A is a symmetric matrix in block-lower storage (upper k-blocks read transposed)
+  int b_sym;      // same for B (K-major kernels only)
   int seg_lo;     // bit 2s: segment s reads A's residual map; bit 2s+1: B's residual map
   int final_vec;  // final mode may use 16-byte accesses to the caller's rows
   int* status;    // workspace status word
@@ -138,32 +146,6 @@ __device__ __forceinline__ void stage_row(uint8_t* box, int row, const uint32_t 
         make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
 }
 
-// Transposed box: lane t holds row t of the block; the box gets column t.  Lane
-// pairs (2u, 2u+1) swap one packed word per step, so each step writes rows 2u
-// (even lanes) and 2u + 1 (odd lanes) with 32-bit stores into opposite bank halves.
-__device__ __forceinline__ void stage_col(uint8_t* box, int lane, const uint32_t (&w)[16]) {
-  const bool odd = lane & 1;
-#pragma unroll
-  for (int u = 0; u < 16; ++u) {
-    const uint32_t y = __shfl_xor_sync(0xffffffffu, w[u], 1);
-    const uint32_t word = odd ? __byte_perm(y, w[u], 0x7632) : __byte_perm(w[u], y, 0x5410);
-    const int row = 2 * u + (odd ? 1 : 0);
-    *reinterpret_cast<uint32_t*>(box + sw64(row, (lane & ~1) * 2)) = word;
-  }
-}
-
-// Make a staged diagonal block exactly symmetric: copy the strictly lower
-// triangle onto the upper one (lane t writes row t).
-__device__ __forceinline__ void symmetrize_box(uint8_t* box, int lane) {
-#pragma unroll 4
-  for (int j = 1; j < 32; ++j) {
-    if (j > lane) {
-      const uint16_t x = *reinterpret_cast<const uint16_t*>(box + sw64(j, lane * 2));
-      *reinterpret_cast<uint16_t*>(box + sw64(lane, j * 2)) = x;
-    }
-  }
-}
-
 // Final write of a full 32 x 32 block to a caller's row-major matrix (not
 // transposed): global memory is read and written a warp-wide few rows at a time
 // through a padded shared-memory box, lane t owning row t in between.
@@ -229,7 +211,9 @@ __device__ __forceinline__ void final_block_rows(const EpiParams& e, int b, int 
 template <bool BMN>
 __global__ void __launch_bounds__(192, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAl,
+                   const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmAtl,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBl,
+                   const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ CUtensorMap tmBtl,
                    const __grid_constant__ CUtensorMap tmOh, const __grid_constant__ CUtensorMap tmOl,
                    const __grid_constant__ CUtensorMap tmRh, const __grid_constant__ CUtensorMap tmRl,
                    const __grid_constant__ TcArgs args) {
@@ -299,16 +283,27 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           const int seg = kb / nk;
-          const CUtensorMap* ma = ((args.seg_lo >> (2 * seg)) & 1) ? &tmAl : &tmA;
-          const CUtensorMap* mb = ((args.seg_lo >> (2 * seg + 1)) & 1) ? &tmBl : &tmB;
+          const int k0 = (kb - seg * nk) * C::BK;
+          const bool alo = (args.seg_lo >> (2 * seg)) & 1;
+          const bool blo = (args.seg_lo >> (2 * seg + 1)) & 1;
+          // k-blocks above the diagonal of a block-lower symmetric operand come
+          // from the stored lower block, read transposed
+          const bool a_up = args.a_sym && (k0 >> 8) > (m0 >> 8);
+          const bool b_up = !BMN && args.b_sym && (k0 >> 8) > (n0 >> 8);
           uint8_t* st = tiles + s * C::STAGE;
           mbar_arrive_expect_tx(&full[s], C::STAGE);
-          const int k0 = (kb - seg * nk) * C::BK;
-          tma_load_3d(ma, &full[s], st, k0, m0, b);
-          uint8_t* sb = st + C::A_TILE;
-          if (!BMN) {
-            tma_load_3d(mb, &full[s], sb, k0, n0, b);
+          if (!a_up) {
+            tma_load_3d(alo ? &tmAl : &tmA, &full[s], st, k0, m0, b);
           } else {
+#pragma unroll
+            for (int q = 0; q < C::BM / C::MN_ATOM; ++q)
+              tma_load_3d(alo ? &tmAtl : &tmAt, &full[s], st + q * C::MN_BOX_BYTES, m0 + q * C::MN_ATOM, k0, b);
+          }
+          uint8_t* sb = st + C::A_TILE;
+          if (!BMN && !b_up) {
+            tma_load_3d(blo ? &tmBl : &tmB, &full[s], sb, k0, n0, b);
+          } else {
+            const CUtensorMap* mb = BMN ? (blo ? &tmBl : &tmB) : (blo ? &tmBtl : &tmBt);
 #pragma unroll
             for (int q = 0; q < C::BN / C::MN_ATOM; ++q)
               tma_load_3d(mb, &full[s], sb + q * C::MN_BOX_BYTES, n0 + q * C::MN_ATOM, k0, b);
@@ -326,11 +321,13 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = make_idesc_bf16(C::BM, C::BN, BMN);
       constexpr uint32_t SBO = 8 * 128;
       int it = 0, tcount = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < args.total && ok; t += gridDim.x, ++tcount) {
+        int b, i, j;
+        decode_tile(args, t, b, i, j);
+        const int m0 = i * C::BM, n0 = j * C::BN;
         const int abuf = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
         if (*abort_flag || !mbar_wait(&tempty[abuf], aph ^ 1)) {
@@ -347,13 +344,18 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           tc_fence_after();
+          const int k0 = (kb % nk) * C::BK;
+          const bool a_mn = args.a_sym && (k0 >> 8) > (m0 >> 8);
+          const bool b_mn = BMN || (args.b_sym && (k0 >> 8) > (n0 >> 8));
+          const uint32_t idesc = make_idesc_bf16(C::BM, C::BN, b_mn) | (a_mn ? (1u << 15) : 0u);
           const uint32_t a0 = smem_u32(tiles + s * C::STAGE);
           const uint32_t b0 = a0 + C::A_TILE;
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
-            const uint64_t ad = make_sdesc(a0 + kk * 32, 16, SBO, C::SWZ);
-            const uint64_t bd = BMN ? make_sdesc(b0 + kk * 16 * 128, C::MN_BOX_BYTES, SBO, C::SWZ)
-                                    : make_sdesc(b0 + kk * 32, 16, SBO, C::SWZ);
+            const uint64_t ad = a_mn ? make_sdesc(a0 + kk * 16 * 128, C::MN_BOX_BYTES, SBO, C::SWZ)
+                                     : make_sdesc(a0 + kk * 32, 16, SBO, C::SWZ);
+            const uint64_t bd = b_mn ? make_sdesc(b0 + kk * 16 * 128, C::MN_BOX_BYTES, SBO, C::SWZ)
+                                     : make_sdesc(b0 + kk * 32, 16, SBO, C::SWZ);
             tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit(&empty[s]);  // stage is free once these MMAs have read it
@@ -408,8 +410,7 @@ __global__ void __launch_bounds__(192, 1)
       const int m0 = i * C::BM, n0 = j * C::BN;
       const int r0 = m0 + quarter * 32;
       const int r = r0 + lane;
-      // chunks of 32 columns this warp handles (symmetric: up to its diagonal block)
-      const int nch = args.sym ? min(C::BN / 32, ((r0 - n0) >> 5) + 1) : C::BN / 32;
+      const int nch = C::BN / 32;  // 32-column chunks of this warp's rows
       const int rbase = r_issued;
       if (has_r) {
         for (int q = 0; q < 2 && q < nch; ++q) issue_r(n0 + 32 * q, r0, b);
@@ -493,32 +494,18 @@ __global__ void __launch_bounds__(192, 1)
           }
           continue;
         }
-        const bool diag = args.sym && c0 == r0;
-        const bool mirror = args.sym && c0 < r0;  // strictly-lower block: also store its transpose
         uint32_t hw[16], lw[16];
         split_words(v, hw, lw, has_lo);
-        if (lane == 0) bulk_wait_read<0>();  // the previous chunk's stores have read the staging boxes
+        sb = stg + (cc & 1) * 2 * C::BOX;  // double-buffered: the stores of chunk cc - 2 used it
+        if (lane == 0) bulk_wait_read<1>();
         __syncwarp();
         stage_row(sb, lane, hw);
         if (has_lo) stage_row(sb + C::BOX, lane, lw);
-        if (mirror) {
-          stage_col(sb + 2 * C::BOX, lane, hw);
-          if (has_lo) stage_col(sb + 3 * C::BOX, lane, lw);
-        }
-        if (diag) {
-          __syncwarp();
-          symmetrize_box(sb, lane);
-          if (has_lo) symmetrize_box(sb + C::BOX, lane);
-        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           tma_store_3d(&tmOh, sb, c0, r0, b);
           if (has_lo) tma_store_3d(&tmOl, sb + C::BOX, c0, r0, b);
-          if (mirror) {
-            tma_store_3d(&tmOh, sb + 2 * C::BOX, r0, c0, b);
-            if (has_lo) tma_store_3d(&tmOl, sb + 3 * C::BOX, r0, c0, b);
-          }
           bulk_commit();
         }
       }
@@ -591,17 +578,24 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
         cudaFuncSetAttribute(tc_gemm_kernel<BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
   }
-  CUtensorMap mA, mAl, mB, mBl;
+  CUtensorMap mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl;
   const bf16* alo = d.A.lo ? d.A.lo : d.A.hi;
   const bf16* blo = d.Bop.lo ? d.Bop.lo : d.Bop.hi;
+  // K-major boxes {64 k, rows}; transposed boxes {64 mn, 64 k} (symmetric operands: K == rows)
   bool ok = make_map(&mA, d.A.hi, d.K, d.M, d.B, d.A.ld, d.A.bs, C::BK, C::BM, 128);
   ok = ok && make_map(&mAl, alo, d.K, d.M, d.B, d.A.ld, d.A.bs, C::BK, C::BM, 128);
+  ok = ok && make_map(&mAt, d.A.hi, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
+  ok = ok && make_map(&mAtl, alo, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
   if (!BMN) {
     ok = ok && make_map(&mB, d.Bop.hi, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::BK, C::BN, 128);
     ok = ok && make_map(&mBl, blo, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::BK, C::BN, 128);
+    ok = ok && make_map(&mBt, d.Bop.hi, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
+    ok = ok && make_map(&mBtl, blo, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
   } else {
     ok = ok && make_map(&mB, d.Bop.hi, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
     ok = ok && make_map(&mBl, blo, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
+    mBt = mB;
+    mBtl = mBl;
   }
   // Output maps: 32 x 32 bf16 boxes with the 64-byte swizzle (dummies in final mode).
   CUtensorMap mOh, mOl;
@@ -657,6 +651,8 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
     a.nseg = 3;
     a.seg_lo = (1 << 3) | (1 << 4);
   }
+  a.a_sym = d.a_sym;
+  a.b_sym = BMN ? 0 : d.b_sym;
   a.status = status;
   a.epi = epi;
   a.epi.sym = d.sym;
@@ -670,7 +666,7 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
   }
   const int grid = a.total < num_sms ? a.total : num_sms;
   if (grid <= 0) return cudaSuccess;
-  tc_gemm_kernel<BMN><<<grid, 192, C::SMEM, st>>>(mA, mAl, mB, mBl, mOh, mOl, mRh, mRl, a);
+  tc_gemm_kernel<BMN><<<grid, 192, C::SMEM, st>>>(mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl, mOh, mOl, mRh, mRl, a);
   return cudaGetLastError();
 }
 
@@ -683,6 +679,10 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* statu
   }
   if ((d.split >= 2 && !d.A.lo) || (d.split == 3 && !d.Bop.lo)) {
     *why = "split products need the residual operands";
+    return cudaErrorInvalidValue;
+  }
+  if ((d.a_sym && d.K != d.M) || (d.b_sym && (d.b_mn || d.K != d.N)) || ((d.a_sym || d.b_sym) && d.K % 256)) {
+    *why = "symmetric operands must be square with K a multiple of 256";
     return cudaErrorInvalidValue;
   }
   return d.b_mn ? launch_impl<true>(d, epi, status, st, num_sms, why)
