@@ -143,10 +143,14 @@ static muon_sched resolve(long long s, long long l, int steps, muon_dtype dt, mu
   const double x3 = 9 * S * S * L + 3 * (4 * T - 3) * S * S * S;
   // Gram space squares the condition number, and the tensor cores' fp32
   // accumulation is measurably coarser than IEEE fp32 (error ~1e-6 of the sum
-  // of |products| per element), so on ill-conditioned inputs the split Gram
-  // recurrence can exceed the 2e-2 target where the original-space schedule
-  // does not.  AUTO therefore takes Gram space only where it saves >= 25 %.
-  return x3 < 0.75 * orig ? MUON_SCHED_GRAM_X3 : MUON_SCHED_ORIG;
+  // of |products| per element, growing with K): on ill-conditioned inputs
+  // (rank-8 + noise) the split Gram recurrence exceeds the 2e-2 target even
+  // at aspect 1:8, where it would save ~30 % of the work, while the
+  // original-space schedule stays near 1e-2.  AUTO therefore runs bf16 in
+  // original space; GRAM_X3 / GRAM_X1 remain available on request.
+  (void)orig;
+  (void)x3;
+  return MUON_SCHED_ORIG;
 }
 
 // Bump allocator over the workspace; with base == nullptr it only measures.

@@ -263,16 +263,16 @@ def test_c2_full_size_sampled():
 
 @pytest.mark.parametrize("n", [8192])
 def test_aspect_sweep_gram_auto(n):
-    """Workload c5 at n = 8192 (AUTO picks split Gram): 2 of the 8 matrices,
-    row 0 scaled by 100 to skew the spectrum."""
+    """Workload c5 at n = 8192: 2 of the 8 matrices, row 0 scaled by 100 to
+    skew the spectrum, through the default schedule and split Gram space."""
     m = _m()
     w = synth.c5(n=n, batch=2)
     X = torch.stack(w.grads).cuda()
-    assert m.resolve_schedule(1024, n) == "gram_x3"
-    O = m.ns_batched(X, steps=5)
-    torch.cuda.synchronize()
-    for i in range(2):
-        assert rel(O[i].float().cpu(), oracle_O(w.grads[i])) < TOL_BF16
+    for sched in ["auto", "gram_x3"]:
+        O = m.ns_batched(X, steps=5, schedule=sched)
+        torch.cuda.synchronize()
+        for i in range(2):
+            assert rel(O[i].float().cpu(), oracle_O(w.grads[i])) < TOL_BF16, sched
 
 
 def test_c3_one_layer_full_size():

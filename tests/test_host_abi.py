@@ -65,17 +65,11 @@ def test_bucket_plan_llama_shapes(lib):
 
 def test_schedule_choice(lib):
     import newton_schulz_04_gb300 as m
-    # symmetric-aware tensor work at T = 5: ORIG with its last three steps split,
-    # 2 (3 s^2 l + s^3) + 3 (5 s^2 l + 3 s^3) = 21 s^2 l + 11 s^3, vs split Gram
-    # 9 s^2 l + 51 s^3; AUTO takes Gram only when it saves >= 25 %, i.e. l > 6.33 s
-    assert m.resolve_schedule(1024, 1024) == "orig"
-    assert m.resolve_schedule(1024, 4096) == "orig"
-    assert m.resolve_schedule(1024, 6144) == "orig"
-    assert m.resolve_schedule(1024, 6656) == "gram_x3"
-    assert m.resolve_schedule(4096, 14336) == "orig"
-    assert m.resolve_schedule(256, 1024) == "orig"
-    assert m.resolve_schedule(1024, 8192) == "gram_x3"
-    assert m.resolve_schedule(16384, 1024) == "gram_x3"
+    # bf16 AUTO runs original space (split Gram misses 2e-2 on ill-conditioned
+    # inputs with the tensor cores' accumulation); fp32 AUTO takes Gram space
+    # whenever l > s, where it never costs more
+    for shp in [(1024, 1024), (1024, 4096), (1024, 8192), (16384, 1024), (4096, 14336), (256, 1024)]:
+        assert m.resolve_schedule(*shp) == "orig"
     assert m.resolve_schedule(1024, 8192, steps=0) == "orig"
     assert m.resolve_schedule(1024, 8192, schedule="gram_x1") == "gram_x1"
     assert m.resolve_schedule(128, 256, dtype=torch.float32) == "gram_x3"
