@@ -194,6 +194,33 @@ MUON_API void muon_profile_enable(int on);
 MUON_API int muon_profile_count(void);
 MUON_API muon_status muon_profile_get(int i, const char** kind, float* ms, double* flops, double* bytes);
 
+/*
+ * muon_ns_batched_static -- muon_ns_batched for callers that cannot allocate
+ * device memory: code running where a cudaMalloc is not allowed or must not
+ * happen (inside a framework that owns every byte of device memory through
+ * its own pool, a latency-critical loop where an allocation would stall the
+ * device, a plug-in that is handed only input and output buffers).  It takes
+ * no workspace: its scratch is one fixed array of muon_static_scratch_bytes()
+ * (64 MiB) compiled into the library, which every GPU that loads the library
+ * holds until the process exits.  The caller still passes X and out
+ * (arguments as for muon_ns_batched).  The pages have no counterpart of this
+ * entry point.
+ *  - Problems whose single matrix needs more scratch than the array holds
+ *    (e.g. a bf16 2048 x 2048 matrix) are rejected with MUON_ERR_WORKSPACE
+ *    before anything is launched; larger batches are processed in chunks.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.  The first
+ *    call on each device looks up the array's device address; make that first
+ *    call before any stream capture.
+ *  - All calls share the one array: calls whose work overlaps on the GPU (two
+ *    streams, two threads without ordering) race and give wrong results.
+ *    Order them on one stream.  Each call resets the array's status word, so
+ *    muon_device_status(scratch) is not available here.
+ */
+MUON_API muon_status muon_ns_batched_static(const void* X, int B, int m, int n, int steps,
+                                            const float* coeffs, void* out, muon_dtype dt,
+                                            muon_sched sc, void* stream);
+MUON_API size_t muon_static_scratch_bytes(void);
+
 /* Thread-local message of the last failed call on this thread ("" if none). */
 MUON_API const char* muon_last_error(void);
 

@@ -6,5 +6,5 @@ Importing the package does not load the CUDA library; the first call does.
 """
 from .binding import (  # noqa: F401
     MuonError, MuonUpdater, bucket_plan, debug_bounded_wait, debug_gemm, device_status, library_path, load, muon_step,
-    new_workspace, ns_batched, profile_enable, profile_records, resolve_schedule, workspace_bytes,
+    new_workspace, ns_batched, ns_batched_static, profile_enable, profile_records, resolve_schedule, workspace_bytes,
 )

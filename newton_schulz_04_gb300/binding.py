@@ -73,6 +73,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.muon_profile_get.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float),
                                      ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
     lib.muon_profile_get.restype = i32
+    lib.muon_ns_batched_static.argtypes = [vp, i32, i32, i32, i32, fptr, vp, i32, i32, vp]
+    lib.muon_ns_batched_static.restype = i32
+    lib.muon_static_scratch_bytes.argtypes = []
+    lib.muon_static_scratch_bytes.restype = sz
     lib.muon_last_error.argtypes = []
     lib.muon_last_error.restype = ctypes.c_char_p
     lib.muon_version.argtypes = []
@@ -162,6 +166,22 @@ def ns_batched(X: torch.Tensor, steps: int = 5, coeffs=None, schedule: str = "au
                              ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                              ctypes.c_void_p(_stream_ptr(stream)))
     _check(st)
+    return out
+
+
+def ns_batched_static(X: torch.Tensor, steps: int = 5, coeffs=None, schedule: str = "auto", out=None,
+                      stream=None) -> torch.Tensor:
+    """As ns_batched, through the entry point that allocates nothing (the
+    library's fixed device scratch; see muon_ns_batched_static)."""
+    lib = load()
+    if X.dim() != 3 or not X.is_cuda or not X.is_contiguous():
+        raise ValueError("X must be a contiguous [B, m, n] CUDA tensor")
+    B, m, n = X.shape
+    if out is None:
+        out = torch.empty_like(X)
+    _check(lib.muon_ns_batched_static(ctypes.c_void_p(X.data_ptr()), B, m, n, int(steps), _coeffs(coeffs),
+                                      ctypes.c_void_p(out.data_ptr()), _dtype_code(X.dtype), SCHED[schedule],
+                                      ctypes.c_void_p(_stream_ptr(stream))))
     return out
 
 

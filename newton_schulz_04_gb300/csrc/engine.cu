@@ -23,6 +23,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -899,6 +900,58 @@ muon_status muon_profile_get(int i, const char** kind, float* ms, double* flops,
   if (bytes) *bytes = r.bytes;
   return MUON_OK;
 }
+
+// ------------------------------------------------------------------ static scratch
+// Device scratch for muon_ns_batched_static: one file-scope array, present on
+// every GPU that loads this library until the process exits.  Host code only
+// sees a host-side stand-in for this symbol, so its device address is looked
+// up once per device (cudaGetSymbolAddress) and passed to the kernels like any
+// caller workspace.
+static constexpr size_t kStaticScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+static constexpr int kMaxDevices = 64;
+static void* g_static_addr[kMaxDevices] = {nullptr};
+static std::mutex g_static_mu;
+
+muon_status muon_ns_batched_static(const void* X, int B, int m, int n, int steps, const float* coeffs, void* out,
+                                   muon_dtype dt, muon_sched sc, void* stream) {
+  g_last_error.clear();
+  if (B < 0) return fail(MUON_ERR_ARG, "B=%d < 0", B);
+  if (B > 0 && (!X || !out)) return fail(MUON_ERR_ARG, "X or out is NULL");
+  if (m <= 0 || n <= 0 || m > MUON_MAX_DIM || n > MUON_MAX_DIM) return fail(MUON_ERR_SHAPE, "bad shape %dx%d", m, n);
+  if (steps < 0 || steps > MUON_MAX_STEPS) return fail(MUON_ERR_ARG, "steps=%d out of [0, %d]", steps, MUON_MAX_STEPS);
+  if (!valid_dt(dt) || !valid_sc(sc)) return fail(MUON_ERR_ARG, "bad dtype or schedule");
+  // Reject problems whose single matrix does not fit the fixed scratch, before any CUDA call.
+  const Group g = make_group(m, n, steps, dt, sc);
+  const size_t need = group_bytes(g, 1, dt);
+  if (need > kStaticScratchBytes)
+    return fail(MUON_ERR_WORKSPACE,
+                "a %dx%d matrix needs %zu bytes of scratch; the static scratch of muon_ns_batched_static holds "
+                "%zu bytes (use muon_ns_batched with a caller workspace)",
+                m, n, need, kStaticScratchBytes);
+  if (B == 0) return MUON_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(MUON_ERR_UNSUPPORTED, "device %d out of range", dev);
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_addr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_static_scratch);
+      if (e != cudaSuccess || !p) return fail(MUON_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+      g_static_addr[dev] = p;
+    }
+    scratch = g_static_addr[dev];
+  }
+  // The status word starts at zero for every call (the array keeps the last call's contents).
+  e = cudaMemsetAsync(scratch, 0, sizeof(int), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
+  return muon_ns_batched(X, B, m, n, steps, coeffs, out, dt, sc, scratch, kStaticScratchBytes, stream);
+}
+
+size_t muon_static_scratch_bytes(void) { return kStaticScratchBytes; }
 
 const char* muon_last_error(void) { return g_last_error.c_str(); }
 
