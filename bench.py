@@ -238,12 +238,12 @@ def run_ours(args, world, rank, local):
     count = len(shapes)
     W = [w.to(dev) for w in work.weights]
     G = [g.to(dev) for g in work.grads]
-    Mo = [torch.zeros(g.shape, dtype=torch.float32, device=dev) for g in G]
     if args.config != "c3":
         cpu_work = work
     else:
         cpu_work = None
-    ws = pkg.new_workspace(pkg.workspace_bytes(shapes, work.steps, work.dtype), dev)
+    upd = pkg.MuonUpdater(W, work.beta, work.lr, work.steps, work.coeffs, "auto", use_graph=not args.no_graph)
+    Mo = upd.moms
     flops_step = work.flop_count()
     in_bytes = sum(g.numel() * g.element_size() for g in G) + sum(m.numel() * 4 for m in Mo) * 2 + \
         sum(w.numel() * w.element_size() for w in W) * 2
@@ -251,83 +251,61 @@ def run_ours(args, world, rank, local):
     st = torch.cuda.current_stream(dev)
 
     def step():
-        pkg.muon_step(W, G, Mo, work.beta, work.lr, work.steps, work.coeffs, "auto", ws, st)
+        upd.step(G)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    assert pkg.device_status(ws) == 0
-    # ---- device-resident timing; per-launch events on the same stream
-    times = []
-    pkg.profile_enable(True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with Clocks(local) as clk:
-        for _ in range(args.steps):
+    def step_eager():
+        pkg.muon_step(W, G, Mo, work.beta, work.lr, work.steps, work.coeffs, "auto", upd.workspace, st)
+
+    def timed(fn, k):
+        out = []
+        for _ in range(k):
             if flush is not None:
                 flush.zero_()  # evict L2 between timed steps (outside the events)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(st)
-            step()
+            fn()
             b.record(st)
-            times.append((a, b))
+            out.append((a, b))
         torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in out]
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert pkg.device_status(upd.workspace) == 0
+    # ---- timed region: device-resident inputs, one replay (or call) per step
     barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        ms = timed(step, args.steps)
+    barrier(world)
+    # ---- a second pass of the same steps, called directly with a CUDA-event
+    # pair around every library launch, gives the per-kernel times (events
+    # between kernels stop launches from overlapping, so this pass is slower)
+    pkg.profile_enable(True)
+    ms_eager = timed(step_eager, args.steps)
     pkg.profile_enable(False)
-    ms = [a.elapsed_time(b) for a, b in times]
     recs = pkg.profile_records()
-    assert pkg.device_status(ws) == 0
+    assert pkg.device_status(upd.workspace) == 0
     t_total = max_over_ranks(sum(ms) / 1e3, world)
     ms_step = 1e3 * t_total / args.steps
     value = world * flops_step * args.steps / t_total / 1e12
-    # dominant kernel kind by time
-    by = {}
-    for k, t, fl, byt in recs:
-        d = by.setdefault(k, [0.0, 0, 0.0, 0.0])
-        d[0] += t
-        d[1] += 1
-        d[2] += fl
-        d[3] += byt
-    dom = max(by, key=lambda k: by[k][0])
-    pk = peaks()
-    tot_launch_ms = sum(v[0] for v in by.values())
-    if dom.startswith("tc") or dom.startswith("simt"):
-        achieved = by[dom][2] / (by[dom][0] / 1e3) / 1e12
-        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
-                "peak_source": pk["source"], "launches": by[dom][1],
-                "avg_launch_ms": by[dom][0] / by[dom][1], "share_of_launch_time": by[dom][0] / tot_launch_ms}
-    else:
-        achieved = by[dom][3] / (by[dom][0] / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"],
-                "launches": by[dom][1], "avg_launch_ms": by[dom][0] / by[dom][1],
-                "share_of_launch_time": by[dom][0] / tot_launch_ms}
-    kernels = {k: {"launches": v[1], "ms_total": v[0], "share": v[0] / tot_launch_ms,
-                   "tflops": (v[2] / (v[0] / 1e3) / 1e12) if v[2] else None,
-                   "gbs": (v[3] / (v[0] / 1e3) / 1e9) if v[3] else None} for k, v in by.items()}
+    value_eager = world * flops_step * args.steps / max_over_ranks(sum(ms_eager) / 1e3, world) / 1e12
     # ---- end to end through the C ABI with host buffers (pinned)
     Gh = [g.to("cpu").pin_memory() for g in G]
     Wh = [torch.empty(w.shape, dtype=w.dtype).pin_memory() for w in W]
     h2d = sum(g.numel() * g.element_size() for g in Gh)
     d2h = sum(w.numel() * w.element_size() for w in Wh)
-    e2e_ms = []
-    for it in range(args.warmup + args.steps):
-        if flush is not None:
-            flush.zero_()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(st)
+    def e2e_step():
         for g, gh in zip(G, Gh):
             g.copy_(gh, non_blocking=True)
         step()
         for w, wh in zip(W, Wh):
             wh.copy_(w, non_blocking=True)
-        b.record(st)
-        torch.cuda.synchronize()
-        if it >= args.warmup:
-            e2e_ms.append(a.elapsed_time(b))
+
+    timed(e2e_step, args.warmup)
+    e2e_ms = timed(e2e_step, args.steps)
     e2e_t = max_over_ranks(sum(e2e_ms) / 1e3, world)
     e2e_val = world * flops_step * args.steps / e2e_t / 1e12
     launches_per_step = len(recs) / args.steps
@@ -341,7 +319,10 @@ def run_ours(args, world, rank, local):
                    else "inputs larger than L2", "parallelism": f"replicas x{world}" if world > 1 else "1 gpu"},
         "matrices_per_s": world * count * args.steps / t_total,
         "pct_of_bf16_peak": 100.0 * value / pk["bf16_tflops"],
+        "value_without_graph": value_eager,
+        "launch_path": "CUDA graph replay of the C-ABI call sequence" if not args.no_graph else "direct C-ABI calls",
         "gpu_launches": int(round(launches_per_step * args.steps)),
+        "roofline_timing": "per-launch CUDA events in a second pass of the same steps",
         "roofline": roof,
         "kernels": kernels,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -367,6 +348,7 @@ def main():
     ap.add_argument("--config", default="c2")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="call the C ABI per step instead of replaying a graph")
     args = ap.parse_args()
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":

@@ -272,11 +272,14 @@ class MuonUpdater:
     """Owner-side Muon step over a fixed list of 2-D parameters.
 
     Holds the fp32 momentum buffers and one caller-side workspace sized for the
-    parameter shapes; `step(grads)` calls the C-ABI once.
+    parameter shapes; `step(grads)` calls the C ABI once.  With
+    `use_graph=True` the first step with a given set of gradient tensors runs
+    eagerly and is captured into a CUDA graph; later steps with the same
+    tensors replay it (one launch of the whole kernel sequence).
     """
 
     def __init__(self, params: Sequence[torch.Tensor], beta=0.95, lr=0.02, steps=5, coeffs=None,
-                 schedule="auto", workspace_limit: int | None = None):
+                 schedule="auto", workspace_limit: int | None = None, use_graph: bool = False):
         self.params = list(params)
         self.beta, self.lr, self.steps, self.coeffs, self.schedule = beta, lr, steps, coeffs, schedule
         self.moms = [torch.zeros(p.shape, dtype=torch.float32, device=p.device) for p in self.params]
@@ -284,7 +287,28 @@ class MuonUpdater:
         if workspace_limit is not None:
             need = min(need, int(workspace_limit))
         self.workspace = new_workspace(need, self.params[0].device)
+        self.use_graph = use_graph
+        self._graph = None
+        self._graph_key = None
 
-    def step(self, grads: Sequence[torch.Tensor], stream=None):
+    def _eager(self, grads, stream=None):
         muon_step(self.params, grads, self.moms, self.beta, self.lr, self.steps, self.coeffs, self.schedule,
                   self.workspace, stream)
+
+    def step(self, grads: Sequence[torch.Tensor], stream=None):
+        if not self.use_graph:
+            self._eager(grads, stream)
+            return
+        key = tuple(g.data_ptr() for g in grads)
+        if self._graph is not None and key == self._graph_key:
+            self._graph.replay()
+            return
+        # this call's update runs eagerly (and sets up per-device state); the same
+        # launch sequence is then captured for the following calls
+        self._eager(grads)
+        torch.cuda.current_stream().synchronize()
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        with torch.cuda.graph(graph, stream=side):
+            self._eager(grads, side)
+        self._graph, self._graph_key = graph, key

@@ -19,6 +19,8 @@ constexpr int PT = 64;  // packed tile edge of the pack kernel
 __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackArgs a) {
   __shared__ float S[PT][PT + 1];
   __shared__ float red[8];
+  pdl_launch_dependents();
+  pdl_wait();
   const int b = blockIdx.y;
   const int tile = blockIdx.x;
   const int nq = a.lp / PT;
@@ -78,15 +80,15 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackA
 
 cudaError_t launch_pack(const PackArgs& a, int B, cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
-  dim3 grid(a.tiles, B);
-  pack_kernel<<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(pack_kernel, dim3(a.tiles, B), dim3(256), 0, st, a);
 }
 
 // inv_norm[b] = 1 / (sqrt(sum of the partials of b) + eps), summed in a fixed order.
 __global__ void __launch_bounds__(256) norm_finalize_kernel(const float* partial, int tiles, float eps,
                                                             float* inv_norm) {
   __shared__ float red[8];
+  pdl_launch_dependents();
+  pdl_wait();
   const int b = blockIdx.x;
   const float* p = partial + static_cast<long long>(b) * tiles;
   float s = 0.f;
@@ -106,8 +108,7 @@ __global__ void __launch_bounds__(256) norm_finalize_kernel(const float* partial
 cudaError_t launch_norm_finalize(const float* partial, int tiles, int B, float eps, float* inv_norm,
                                  cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
-  norm_finalize_kernel<<<B, 256, 0, st>>>(partial, tiles, eps, inv_norm);
-  return cudaGetLastError();
+  return launch_pdl(norm_finalize_kernel, dim3(B), dim3(256), 0, st, partial, tiles, eps, inv_norm);
 }
 
 struct FinalArgs {
@@ -117,6 +118,8 @@ struct FinalArgs {
 };
 
 __global__ void __launch_bounds__(256) final_from_packed_kernel(const __grid_constant__ FinalArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int b = blockIdx.y;
   const EpiParams& e = a.e;
   const long long n = static_cast<long long>(e.rows_valid) * e.cols_valid;
@@ -136,9 +139,7 @@ cudaError_t launch_final_from_packed(const float* Xf, long long ld, long long bs
   long long blocks = (n + 255) / 256;
   if (blocks > 1024) blocks = 1024;
   if (blocks < 1) blocks = 1;
-  dim3 grid(static_cast<unsigned>(blocks), B);
-  final_from_packed_kernel<<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(final_from_packed_kernel, dim3(static_cast<unsigned>(blocks), B), dim3(256), 0, st, a);
 }
 
 // Waits on a barrier that nobody arrives at; gives up after `cycles` and records it.

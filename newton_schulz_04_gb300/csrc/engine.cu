@@ -89,8 +89,20 @@ struct ProfScope {
 
 static const float kQuintic[3] = {3.4445f, -4.7750f, 2.0315f};
 static const float kEps = 1e-7f;
-// ORIG: number of final NS steps whose A*A and B*X products use split operands.
-static const int kSplitSteps = 3;
+// ORIG: number of final NS steps whose A*A (resp. B*X) products use split
+// operands.  The error of plain bf16 products comes from the last steps; an
+// fp32-exact CPU emulation over Gaussian inputs of aspect 1:1 to 1:3 gives a
+// worst relative error of 2.3e-2 with no splits, 1.04e-2 with both splits in
+// the last two steps, 0.97e-2 in the last three, and 1.3e-2 / 2.1e-2 with only
+// A*A / only B*X split.
+#ifndef MUON_SPLIT_A_STEPS
+#define MUON_SPLIT_A_STEPS 2
+#endif
+#ifndef MUON_SPLIT_B_STEPS
+#define MUON_SPLIT_B_STEPS 2
+#endif
+static const int kSplitA = MUON_SPLIT_A_STEPS;
+static const int kSplitB = MUON_SPLIT_B_STEPS;
 
 static inline long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 
@@ -135,12 +147,12 @@ static muon_sched resolve(long long s, long long l, int steps, muon_dtype dt, mu
   if (steps == 0) return MUON_SCHED_ORIG;  // only the packed fp32 copy is needed
   if (sc != MUON_SCHED_AUTO) return sc;
   // Tensor-core work (symmetric products counted once):
-  //   ORIG     per plain step 3 s^2 l + s^3, per split step 5 s^2 l + 3 s^3
-  //            (SYRK s^2 l, A*A s^3 or 3 s^3, B*X 2 s^2 l or 4 s^2 l)
+  //   ORIG     per step 3 s^2 l + s^3 (SYRK s^2 l, A*A s^3, B*X 2 s^2 l), plus
+  //            2 s^3 per split A*A and 2 s^2 l per split B*X
   //   GRAM_X3  3 s^2 l (SYRK, split) + 3 (4T - 3) s^3 + 6 s^2 l (Q X0, split)
   const double S = static_cast<double>(s), L = static_cast<double>(l), T = steps;
-  const double ns = std::min<double>(T, kSplitSteps);
-  const double orig = (T - ns) * (3 * S * S * L + S * S * S) + ns * (5 * S * S * L + 3 * S * S * S);
+  const double na = std::min<double>(T, kSplitA), nb = std::min<double>(T, kSplitB);
+  const double orig = T * (3 * S * S * L + S * S * S) + na * 2 * S * S * S + nb * 2 * S * S * L;
   const double x3 = 9 * S * S * L + 3 * (4 * T - 3) * S * S * S;
   // Gram space squares the condition number, and the tensor cores' fp32
   // accumulation is measurably coarser than IEEE fp32 (error ~1e-6 of the sum
@@ -524,14 +536,13 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   };
 
   if (g.sc == MUON_SCHED_ORIG) {
-    // Operand splits measured against the fp64 oracle: plain bf16 products miss
-    // a 2e-2 relative error on Gaussian inputs of aspect >= 1:2, mostly through
-    // the rounding of the last steps (where sigma ~ 1 and the b, c terms are
-    // large); splitting A in A*A and B in B*X during the last kSplitSteps steps
-    // brings the error to that of splitting every step (~1e-2 at worst).
+    // Operand splits (see kSplitA / kSplitB): plain bf16 products miss a 2e-2
+    // relative error on Gaussian inputs of aspect >= 1:2, mostly through the
+    // rounding of the last steps, where sigma ~ 1 and the b, c terms are large.
     int cur = 0;
     for (int k = 0; k < T; ++k) {
-      const bool split = k >= T - kSplitSteps;
+      const bool split_a = k >= T - kSplitA;
+      const bool split = k >= T - kSplitB;
       const int nxt = cur ^ 1;
       // A = X X^T (k = 0: X = M / s, so scale by inv_norm^2)
       EpiParams e1 = epi_pair(g, bf, k == 0 ? 2 : 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, bf.Gl, sp, bss);
@@ -539,7 +550,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
       // B = b A + c A^2 with A = Ah + Al in the epilogue
       EpiParams e2 =
           epi_pair(g, bf, 0, cx.c, cx.b, 0.f, bf.Gh, bf.Gl, bf.Bh, split ? bf.Bl : nullptr, sp, bss);
-      CK(tc(split ? 3 : 1, 0, 7, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, e2));
+      CK(tc(split_a ? 3 : 1, 0, 7, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, e2));
       // X <- a X + B X (k = 0: both terms carry 1 / s); X kept as a bf16 pair
       EpiParams e3 = epi_pair(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, bf.Xb[cur], bf.Xlo[cur], bf.Xb[nxt],
                               bf.Xlo[nxt], lp, bsx);

@@ -3,9 +3,30 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace muon {
+
+// Launch with programmatic stream serialization, so the kernel's prologue may
+// overlap the tail of the previous kernel on the stream (every library kernel
+// calls pdl_wait() before touching memory).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // A bf16 operand of the tensor-core GEMM: [batch][rows][ld] row-major, with an
 // optional residual part `lo` of the same layout (split operands).

@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace muon {
 
@@ -24,6 +25,8 @@ constexpr int SK = 16;   // k per smem stage
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const __grid_constant__ SimtArgs a) {
   __shared__ __align__(16) float As[2][SK][SB];
   __shared__ __align__(16) float Bs[2][SK][SB];
+  pdl_launch_dependents();
+  pdl_wait();
   const SimtGemmDesc& d = a.d;
   const int b = blockIdx.y;
   const int u = blockIdx.x;
@@ -129,9 +132,7 @@ cudaError_t launch_simt_gemm(const SimtGemmDesc& d, const EpiParams& epi, cudaSt
   a.epi = epi;
   a.epi.sym = d.sym;
   if (d.B <= 0 || a.tpm <= 0) return cudaSuccess;
-  dim3 grid(a.tpm, d.B);
-  simt_gemm_kernel<<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(simt_gemm_kernel, dim3(a.tpm, d.B), dim3(256), 0, st, a);
 }
 
 }  // namespace muon

@@ -36,6 +36,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -262,6 +264,8 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_launch_dependents();
+  pdl_wait();  // inputs are written by the previous kernel on the stream
   const uint32_t tmem_base = *tmem_slot;
   const int nk = args.K / C::BK;   // k-blocks per segment
   const int nkb = nk * args.nseg;  // k-blocks per tile
@@ -569,13 +573,31 @@ static bool make_map(CUtensorMap* m, const bf16* base, uint64_t inner, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
+// The dynamic shared-memory limit is raised once per device and kernel, so a
+// later call (e.g. under stream capture) only enqueues launches.
+template <bool BMN>
+static cudaError_t ensure_smem_attr() {
+  static std::mutex mu;
+  static bool done[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(tc_gemm_kernel<BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg::SMEM);
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
+}
+
 template <bool BMN>
 static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* status, cudaStream_t st,
                                int num_sms, const char** why) {
   using C = TcCfg;
   {
-    const cudaError_t e =
-        cudaFuncSetAttribute(tc_gemm_kernel<BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    const cudaError_t e = ensure_smem_attr<BMN>();
     if (e != cudaSuccess) return e;
   }
   CUtensorMap mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl;
@@ -666,8 +688,8 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
   }
   const int grid = a.total < num_sms ? a.total : num_sms;
   if (grid <= 0) return cudaSuccess;
-  tc_gemm_kernel<BMN><<<grid, 192, C::SMEM, st>>>(mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl, mOh, mOl, mRh, mRl, a);
-  return cudaGetLastError();
+  return launch_pdl(tc_gemm_kernel<BMN>, dim3(grid), dim3(192), C::SMEM, st, mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl,
+                    mOh, mOl, mRh, mRl, a);
 }
 
 cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* status, cudaStream_t st, int num_sms,
