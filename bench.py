@@ -292,6 +292,32 @@ def run_ours(args, world, rank, local):
     ms_step = 1e3 * t_total / args.steps
     value = world * flops_step * args.steps / t_total / 1e12
     value_eager = world * flops_step * args.steps / max_over_ranks(sum(ms_eager) / 1e3, world) / 1e12
+    # dominant kernel kind by time in the profiled pass
+    by = {}
+    for k, t, fl, byt in recs:
+        d = by.setdefault(k, [0.0, 0, 0.0, 0.0])
+        d[0] += t
+        d[1] += 1
+        d[2] += fl
+        d[3] += byt
+    dom = max(by, key=lambda k: by[k][0])
+    pk = peaks()
+    tot_launch_ms = sum(v[0] for v in by.values())
+    if dom.startswith("tc") or dom.startswith("simt"):
+        achieved = by[dom][2] / (by[dom][0] / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": None,
+                "peak_source": pk["source"], "launches": by[dom][1],
+                "avg_launch_ms": by[dom][0] / by[dom][1], "share_of_launch_time": by[dom][0] / tot_launch_ms}
+    else:
+        achieved = by[dom][3] / (by[dom][0] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"],
+                "launches": by[dom][1], "avg_launch_ms": by[dom][0] / by[dom][1],
+                "share_of_launch_time": by[dom][0] / tot_launch_ms}
+    kernels = {k: {"launches": v[1], "ms_total": v[0], "share": v[0] / tot_launch_ms,
+                   "tflops": (v[2] / (v[0] / 1e3) / 1e12) if v[2] else None,
+                   "gbs": (v[3] / (v[0] / 1e3) / 1e9) if v[3] else None} for k, v in by.items()}
     # ---- end to end through the C ABI with host buffers (pinned)
     Gh = [g.to("cpu").pin_memory() for g in G]
     Wh = [torch.empty(w.shape, dtype=w.dtype).pin_memory() for w in W]
