@@ -70,6 +70,8 @@ def make_workload(name: str, device):
         return synth.c2(device)
     if name == "c3":
         return synth.c3(device)
+    if name == "c3_layer":  # one layer of c3 (same shapes), for profiling
+        return synth.c3(device, layers=1)
     if name == "c4":
         return synth.c4(device)
     if name.startswith("c5"):
@@ -83,6 +85,7 @@ WORKLOAD_DESC = {
     "c3": "Llama-style 32 layers d=4096 ffn=14336 (q,k,v,o 4096^2; gate/up 4096x14336; down 14336x4096), "
           "bf16 grads N(0,1e-6), fp32 momentum, 5 NS steps",
     "c4": "512 matrices from {256x1024,512x2048,768x3072}, rank-8 + 1e-4 noise, bf16, 5 NS steps",
+    "c3_layer": "one layer of the d=4096 ffn=14336 model (4 x 4096^2, 2 x 4096x14336, 14336x4096), bf16, 5 NS steps",
 }
 
 
@@ -233,12 +236,12 @@ def run_ours(args, world, rank, local):
     import newton_schulz_04_gb300 as pkg
     pkg.load(build_if_missing=True)
     dev = torch.device("cuda", local)
-    work = make_workload(args.config, dev if args.config == "c3" else "cpu")
+    work = make_workload(args.config, dev if args.config.startswith("c3") else "cpu")
     shapes = work.shapes
     count = len(shapes)
     W = [w.to(dev) for w in work.weights]
     G = [g.to(dev) for g in work.grads]
-    if args.config != "c3":
+    if not args.config.startswith("c3"):
         cpu_work = work
     else:
         cpu_work = None

@@ -195,3 +195,27 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     torch.cuda.synchronize()
     assert _rel(out, _ref(A, B, False)) < 2e-5
     assert m.device_status(ws) == 0
+
+
+def test_tc_accumulation_precision():
+    """Characterises the fp32 accumulation of the tensor-core kernel: exact bf16
+    operands, one 128x256 tile, K from 256 to 16384, against the fp64 product
+    (printed with -s; the bounds hold with margin on GB300)."""
+    m = _lib()
+    g = torch.Generator().manual_seed(0)
+    print("\n| K | rel_fro | rel_vs_q | max err / sum abs | cuBLAS fp32 rel |")
+    for K, bound in [(256, 1e-5), (1024, 1e-5), (4096, 2e-5), (16384, 6e-5)]:
+        A = torch.randn(1, 128, K, generator=g).to(torch.bfloat16)
+        B = torch.randn(1, 256, K, generator=g).to(torch.bfloat16)
+        ref = A.double() @ B.double().transpose(1, 2)
+        out = m.debug_gemm(A.cuda(), B.cuda()).cpu().double()
+        r32 = ref.float()
+        h = r32.to(torch.bfloat16).float()
+        refq = (h + (r32 - h).to(torch.bfloat16).float()).double()
+        rel_fro = ((out - ref).norm() / ref.norm()).item()
+        rel_q = ((out - refq).norm() / ref.norm()).item()
+        sumabs = A.double().abs() @ B.double().abs().transpose(1, 2)
+        mx = ((out - ref).abs() / sumabs).max().item()
+        cub = ((A.cuda().float() @ B.cuda().float().transpose(1, 2)).cpu().double() - ref).norm() / ref.norm()
+        print(f"| {K} | {rel_fro:.3g} | {rel_q:.3g} | {mx:.3g} | {cub.item():.3g} |")
+        assert rel_q < bound
