@@ -51,13 +51,18 @@ struct TcCfg {
   static constexpr int A_TILE = BM * BK * 2;
   static constexpr int B_TILE = BN * BK * 2;
   static constexpr int STAGE = A_TILE + B_TILE;
-  static constexpr int STAGES = 3;
-  // Epilogue staging per epilogue warp: two 32 x 32 bf16 output boxes (head and
-  // residual part, double buffered) and two sets of two input boxes for the
-  // prefetched residual pair R = Rh + Rl; 2 KB per box.
+  // Four operand stages: with three, the MMA issuer waited for operands ~20 %
+  // of the time on 4096-sized products (TMA latency not covered).
+  static constexpr int STAGES = 4;
+  // Epilogue staging per epilogue warp (the epilogue is busy ~12 % of the
+  // time on large products, so one buffer each is enough): one 32 x 32 bf16
+  // output pair (head, residual part) and one input pair for the prefetched
+  // residual R = Rh + Rl; 2 KB per box.
   static constexpr int BOX = 32 * 32 * 2;
-  static constexpr int OUT_WARP = 2 * 2 * BOX;
-  static constexpr int RIN_WARP = 2 * 2 * BOX;
+  static constexpr int OUT_BUFS = 1;
+  static constexpr int RIN_BUFS = 1;
+  static constexpr int OUT_WARP = OUT_BUFS * 2 * BOX;
+  static constexpr int RIN_WARP = RIN_BUFS * 2 * BOX;
   static constexpr int STG_WARP = OUT_WARP + RIN_WARP;
   static constexpr int STG = 4 * STG_WARP;
   static constexpr int BAR_BYTES = 256;
@@ -68,6 +73,8 @@ struct TcCfg {
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(BAR_BYTES >= (2 * STAGES + 5 + 8) * 8 + 8, "barrier area too small");
+  static_assert(OUT_BUFS >= 1 && OUT_BUFS <= 2 && RIN_BUFS >= 1 && RIN_BUFS <= 2, "staging depth");
+  static_assert(OUT_WARP >= 32 * (64 + 16), "final-mode row box must fit the output staging");
 };
 
 struct TcArgs {
@@ -393,11 +400,11 @@ __global__ void __launch_bounds__(192, 1)
     const bool has_r = e.Rh != nullptr;
     const bool has_rl = e.Rl != nullptr;
     const uint32_t rbytes = has_rl ? 2 * C::BOX : C::BOX;
-    // Residual boxes go through a two-deep ring per warp; r_issued / r_used
-    // count the boxes requested / consumed (warp-uniform, lane 0 issues).
+    // Residual boxes go through a ring of RIN_BUFS buffers per warp; r_issued /
+    // r_used count the boxes requested / consumed (warp-uniform, lane 0 issues).
     int r_issued = 0, r_used = 0;
     auto issue_r = [&](int c0, int r0, int b) {
-      const int buf = r_issued & 1;
+      const int buf = r_issued % C::RIN_BUFS;
       if (lane == 0) {
         uint8_t* dst = rin + buf * 2 * C::BOX;
         mbar_arrive_expect_tx(&rb[buf], rbytes);
@@ -417,7 +424,7 @@ __global__ void __launch_bounds__(192, 1)
       const int nch = C::BN / 32;  // 32-column chunks of this warp's rows
       const int rbase = r_issued;
       if (has_r) {
-        for (int q = 0; q < 2 && q < nch; ++q) issue_r(n0 + 32 * q, r0, b);
+        for (int q = 0; q < C::RIN_BUFS && q < nch; ++q) issue_r(n0 + 32 * q, r0, b);
       }
       const int abuf = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
@@ -452,11 +459,11 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (has_r) {
           const int idx = rbase + cc;
-          if (!mbar_wait(&rb[idx & 1], (idx >> 1) & 1)) {
+          if (!mbar_wait(&rb[idx % C::RIN_BUFS], (idx / C::RIN_BUFS) & 1)) {
             ok = false;
             break;
           }
-          const uint8_t* src = rin + (idx & 1) * 2 * C::BOX;
+          const uint8_t* src = rin + (idx % C::RIN_BUFS) * 2 * C::BOX;
           uint32_t rhw[16], rlw[16];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -468,7 +475,7 @@ __global__ void __launch_bounds__(192, 1)
           }
           r_used = idx + 1;
           __syncwarp();
-          if (cc + 2 < nch) issue_r(c0 + 64, r0, b);  // the buffer just read is free again
+          if (cc + C::RIN_BUFS < nch) issue_r(c0 + 32 * C::RIN_BUFS, r0, b);  // the buffer just read is free
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
             const float x0 = bf_lo(rhw[u]) + bf_lo(rlw[u]);
@@ -489,9 +496,8 @@ __global__ void __launch_bounds__(192, 1)
         uint8_t* sb = stg;
         if (e.final_mode != FINAL_NONE) {
           const bool full_block = r0 + 32 <= e.rows_valid && c0 + 32 <= e.cols_valid;
-          if (!e.tr[b] && args.final_vec && full_block) {
-            if (e.dst_fp32) final_block_rows<float>(e, b, r0, c0, lane, v, sb);
-            else final_block_rows<bf16>(e, b, r0, c0, lane, v, sb);
+          if (!e.tr[b] && !e.dst_fp32 && args.final_vec && full_block) {
+            final_block_rows<bf16>(e, b, r0, c0, lane, v, sb);  // padded box: 2560 B of the staging area
           } else {
 #pragma unroll
             for (int u = 0; u < 32; ++u) epi_final_elem(e, b, r, c0 + u, v[u]);
@@ -500,8 +506,8 @@ __global__ void __launch_bounds__(192, 1)
         }
         uint32_t hw[16], lw[16];
         split_words(v, hw, lw, has_lo);
-        sb = stg + (cc & 1) * 2 * C::BOX;  // double-buffered: the stores of chunk cc - 2 used it
-        if (lane == 0) bulk_wait_read<1>();
+        sb = stg + (cc % C::OUT_BUFS) * 2 * C::BOX;
+        if (lane == 0) bulk_wait_read<C::OUT_BUFS - 1>();  // earlier stores from this buffer have read it
         __syncwarp();
         stage_row(sb, lane, hw);
         if (has_lo) stage_row(sb + C::BOX, lane, lw);
@@ -527,7 +533,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (lane == 0) {
       // residual boxes still in flight land before the CTA can retire
-      for (int idx = r_used; idx < r_issued; ++idx) mbar_wait(&rb[idx & 1], (idx >> 1) & 1);
+      for (int idx = r_used; idx < r_issued; ++idx) mbar_wait(&rb[idx % C::RIN_BUFS], (idx / C::RIN_BUFS) & 1);
       bulk_wait_all();  // stores complete before the CTA retires
     }
     __syncwarp();
