@@ -32,11 +32,21 @@
 //
 // B is read K-major ([N, K] row-major: symmetric right operands, whose rows are
 // their columns) or MN-major ([K, N] row-major, e.g. X in B X or Q X).
+//
+// CTA pairs.  CTAs run in clusters of two that compute vertically adjacent
+// tiles (row blocks 2p and 2p + 1, same column block) and therefore need the
+// same B tile: each CTA loads half of it and multicasts it into both CTAs'
+// shared memory, and a stage is released only when both CTAs' MMAs have read
+// it.  This halves the L2 -> SM traffic of B; with one CTA per tile the
+// operand stream (96 B/clock/SM at full MMA rate) exceeds what L2 delivers
+// (about 75 B/clock/SM measured with TMA loads alone).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -81,8 +91,8 @@ struct TcArgs {
   int M, N, K;    // padded sizes (multiples of 128 / 256 / 64)
   int sym;        // 1: lower-triangle tiles of a symmetric M x M output
   int nI, nJ;     // tile grid of one matrix
-  int tpm;        // tiles per matrix
-  int total;      // tiles over the batch
+  int tpm;        // tile pairs per matrix
+  int total;      // tile pairs over the batch
   int nseg;       // K segments (1 plain, 2 or 3 split)
   int a_sym;      // A is a symmetric matrix in block-lower storage (upper k-blocks read transposed)
   int b_sym;      // same for B (K-major kernels only)
@@ -92,33 +102,29 @@ struct TcArgs {
   EpiParams epi;
 };
 
-// Tile t of the batch -> (matrix b, row block i, column block j).
-__device__ __forceinline__ void decode_tile(const TcArgs& a, int t, int& b, int& i, int& j) {
+// Tile pair t of the batch -> (matrix b, row-block pair p, column block j); the
+// CTA of rank r in the cluster computes row block i = 2 p + r.
+__device__ __forceinline__ void decode_pair(const TcArgs& a, int t, int& b, int& p, int& j) {
   b = t / a.tpm;
   const int u = t - b * a.tpm;
   if (a.sym) {
-    // Row block i (128 rows) needs column blocks j (256 cols) with 256 j <= 128 i + 127,
-    // i.e. j <= i / 2.  Rows 2p and 2p+1 hold p+1 tiles each, starting at p (p + 1).
-    int p = static_cast<int>((sqrtf(4.f * static_cast<float>(u) + 1.f) - 1.f) * 0.5f);
-    while (p > 0 && p * (p + 1) > u) --p;
-    while ((p + 1) * (p + 2) <= u) ++p;
-    const int rr = u - p * (p + 1);
-    if (rr <= p) {
-      i = 2 * p;
-      j = rr;
-    } else {
-      i = 2 * p + 1;
-      j = rr - (p + 1);
-    }
+    // Row blocks 2p and 2p+1 (256 rows) need column blocks j <= p: p + 1 pairs,
+    // starting at p (p + 1) / 2.
+    int q = static_cast<int>((sqrtf(8.f * static_cast<float>(u) + 1.f) - 1.f) * 0.5f);
+    while (q > 0 && q * (q + 1) / 2 > u) --q;
+    while ((q + 1) * (q + 2) / 2 <= u) ++q;
+    p = q;
+    j = u - q * (q + 1) / 2;
   } else {
-    // Groups of 8 row blocks walked column by column keep a wave's operands in L2.
-    constexpr int G = 8;
+    // Groups of 4 row-block pairs walked column by column keep a wave's operands in L2.
+    constexpr int G = 4;
+    const int nP = a.nI / 2;
     const int per = G * a.nJ;
     const int g = u / per;
     const int first = g * G;
-    const int gs = min(a.nI - first, G);
+    const int gs = min(nP - first, G);
     const int w = u - g * per;
-    i = first + w % gs;
+    p = first + w % gs;
     j = w / gs;
   }
 }
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], 2);  // released by the MMAs of both CTAs of the pair
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -269,10 +275,13 @@ __global__ void __launch_bounds__(192, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cluster_sync();  // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
   pdl_launch_dependents();
   pdl_wait();  // inputs are written by the previous kernel on the stream
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
   const uint32_t tmem_base = *tmem_slot;
   const int nk = args.K / C::BK;   // k-blocks per segment
   const int nkb = nk * args.nseg;  // k-blocks per tile
@@ -282,10 +291,10 @@ __global__ void __launch_bounds__(192, 1)
       // ------------------------------------------------------------ producer
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < args.total && ok; t += gridDim.x) {
-        int b, i, j;
-        decode_tile(args, t, b, i, j);
-        const int m0 = i * C::BM, n0 = j * C::BN;
+      for (int t = cid; t < args.total && ok; t += ncl) {
+        int b, p, j;
+        decode_pair(args, t, b, p, j);
+        const int m0 = (2 * p + rank) * C::BM, n0 = j * C::BN;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
@@ -310,14 +319,18 @@ __global__ void __launch_bounds__(192, 1)
             for (int q = 0; q < C::BM / C::MN_ATOM; ++q)
               tma_load_3d(alo ? &tmAtl : &tmAt, &full[s], st + q * C::MN_BOX_BYTES, m0 + q * C::MN_ATOM, k0, b);
           }
+          // this CTA's half of the shared B tile, multicast to both CTAs
           uint8_t* sb = st + C::A_TILE;
           if (!BMN && !b_up) {
-            tma_load_3d(blo ? &tmBl : &tmB, &full[s], sb, k0, n0, b);
+            tma_load_3d_mc(blo ? &tmBl : &tmB, &full[s], sb + rank * (C::B_TILE / 2), k0, n0 + rank * (C::BN / 2),
+                           b, 0x3);
           } else {
             const CUtensorMap* mb = BMN ? (blo ? &tmBl : &tmB) : (blo ? &tmBtl : &tmBt);
 #pragma unroll
-            for (int q = 0; q < C::BN / C::MN_ATOM; ++q)
-              tma_load_3d(mb, &full[s], sb + q * C::MN_BOX_BYTES, n0 + q * C::MN_ATOM, k0, b);
+            for (int h = 0; h < C::BN / C::MN_ATOM / 2; ++h) {
+              const int q = rank * (C::BN / C::MN_ATOM / 2) + h;
+              tma_load_3d_mc(mb, &full[s], sb + q * C::MN_BOX_BYTES, n0 + q * C::MN_ATOM, k0, b, 0x3);
+            }
           }
         }
       }
@@ -335,10 +348,10 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t SBO = 8 * 128;
       int it = 0, tcount = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < args.total && ok; t += gridDim.x, ++tcount) {
-        int b, i, j;
-        decode_tile(args, t, b, i, j);
-        const int m0 = i * C::BM, n0 = j * C::BN;
+      for (int t = cid; t < args.total && ok; t += ncl, ++tcount) {
+        int b, p, j;
+        decode_pair(args, t, b, p, j);
+        const int m0 = (2 * p + rank) * C::BM, n0 = j * C::BN;
         const int abuf = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
         if (*abort_flag || !mbar_wait(&tempty[abuf], aph ^ 1)) {
@@ -369,7 +382,7 @@ __global__ void __launch_bounds__(192, 1)
                                      : make_sdesc(b0 + kk * 32, 16, SBO, C::SWZ);
             tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          tc_commit(&empty[s]);  // stage is free once these MMAs have read it
+          tc_commit_mc(&empty[s], 0x3);  // the pair's stage is free once both CTAs' MMAs have read it
         }
         if (!ok) break;
         tc_commit(&tfull[abuf]);  // accumulator ready for the epilogue
@@ -415,10 +428,10 @@ __global__ void __launch_bounds__(192, 1)
     };
     int tcount = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < args.total && ok; t += gridDim.x, ++tcount) {
-      int b, i, j;
-      decode_tile(args, t, b, i, j);
-      const int m0 = i * C::BM, n0 = j * C::BN;
+    for (int t = cid; t < args.total && ok; t += ncl, ++tcount) {
+      int b, p, j;
+      decode_pair(args, t, b, p, j);
+      const int m0 = (2 * p + rank) * C::BM, n0 = j * C::BN;
       const int r0 = m0 + quarter * 32;
       const int r = r0 + lane;
       const int nch = C::BN / 32;  // 32-column chunks of this warp's rows
@@ -540,7 +553,8 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cluster_sync();  // neither CTA leaves while its peer may still write into it
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -579,6 +593,26 @@ static bool make_map(CUtensorMap* m, const bf16* base, uint64_t inner, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
+// Launch `ncl` clusters of two CTAs with programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pair(void (*kernel)(KArgs...), int ncl, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * ncl);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = TcCfg::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // The dynamic shared-memory limit is raised once per device and kernel, so a
 // later call (e.g. under stream capture) only enqueues launches.
 template <bool BMN>
@@ -598,6 +632,37 @@ static cudaError_t ensure_smem_attr() {
   return cudaSuccess;
 }
 
+// Clusters of two that can be resident at once (queried once per device), so
+// the persistent grid never waits for a second wave of clusters.
+template <bool BMN>
+static int max_clusters(int num_sms) {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!cached[dev]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = TcCfg::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BMN>, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = num_sms / 2;
+    }
+    cached[dev] = std::min(n, num_sms / 2);
+  }
+  return cached[dev];
+}
+
 template <bool BMN>
 static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* status, cudaStream_t st,
                                int num_sms, const char** why) {
@@ -615,8 +680,8 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
   ok = ok && make_map(&mAt, d.A.hi, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
   ok = ok && make_map(&mAtl, alo, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
   if (!BMN) {
-    ok = ok && make_map(&mB, d.Bop.hi, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::BK, C::BN, 128);
-    ok = ok && make_map(&mBl, blo, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::BK, C::BN, 128);
+    ok = ok && make_map(&mB, d.Bop.hi, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::BK, C::BN / 2, 128);
+    ok = ok && make_map(&mBl, blo, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::BK, C::BN / 2, 128);
     ok = ok && make_map(&mBt, d.Bop.hi, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
     ok = ok && make_map(&mBtl, blo, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
   } else {
@@ -663,9 +728,9 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
   a.nJ = d.N / C::BN;
   if (d.sym) {
     const int P = a.nI / 2;
-    a.tpm = P * (P + 1);
+    a.tpm = P * (P + 1) / 2;
   } else {
-    a.tpm = a.nI * a.nJ;
+    a.tpm = (a.nI / 2) * a.nJ;
   }
   a.total = a.tpm * d.B;
   // K segments of the split products (bit 2s: A residual, bit 2s+1: B residual)
@@ -692,10 +757,10 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
     for (int q = 0; q < d.B; ++q)
       if (reinterpret_cast<uintptr_t>(epi.dst[q]) % 16) a.final_vec = 0;
   }
-  const int grid = a.total < num_sms ? a.total : num_sms;
-  if (grid <= 0) return cudaSuccess;
-  return launch_pdl(tc_gemm_kernel<BMN>, dim3(grid), dim3(192), C::SMEM, st, mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl,
-                    mOh, mOl, mRh, mRl, a);
+  const int nclusters = std::min(a.total, max_clusters<BMN>(num_sms));
+  if (nclusters <= 0) return a.total > 0 ? cudaErrorLaunchOutOfResources : cudaSuccess;
+  return launch_pair(tc_gemm_kernel<BMN>, nclusters, st, mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl, mOh, mOl, mRh, mRl,
+                     a);
 }
 
 cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* status, cudaStream_t st, int num_sms,
