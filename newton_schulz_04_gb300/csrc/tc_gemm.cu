@@ -770,6 +770,10 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* statu
     *why = "unsupported operand split";
     return cudaErrorInvalidValue;
   }
+  if (d.M % 256 || d.N % 256 || d.K % 64) {
+    *why = "tensor-core GEMM needs M and N multiples of 256 (CTA pairs) and K a multiple of 64";
+    return cudaErrorInvalidValue;
+  }
   if ((d.split >= 2 && !d.A.lo) || (d.split == 3 && !d.Bop.lo)) {
     *why = "split products need the residual operands";
     return cudaErrorInvalidValue;
