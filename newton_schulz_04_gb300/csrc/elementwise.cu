@@ -78,8 +78,127 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackA
   }
 }
 
+// Same tile and outputs as pack_kernel, with 8-element (16/32-byte) accesses:
+// each thread moves 8 consecutive elements of a source row.  Needs n % 8 == 0
+// and 16-byte aligned matrices (the launcher checks).  Matrices stored long
+// side first go through a shared-memory transpose; the others are packed
+// straight from registers.
+template <bool SRC_FP32>
+__global__ void __launch_bounds__(256) pack_vec_kernel(const __grid_constant__ PackArgs a) {
+  __shared__ float S[PT][PT + 1];
+  __shared__ float red[8];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int b = blockIdx.y;
+  const int tile = blockIdx.x;
+  const int nq = a.lp / PT;
+  const int P0 = (tile / nq) * PT, Q0 = (tile % nq) * PT;
+  const bool tr = a.tr[b] != 0;
+  const int i0 = tr ? Q0 : P0, j0 = tr ? P0 : Q0;
+  const int tid = threadIdx.x;
+  const long long base = static_cast<long long>(b) * a.bs;
+  float ss = 0.f;
+  auto store8 = [&](long long off, const float (&x)[8]) {
+    if (a.Xf) {
+      float4* f = reinterpret_cast<float4*>(a.Xf + off);
+      f[0] = make_float4(x[0], x[1], x[2], x[3]);
+      f[1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+    if (a.Xh) {
+      uint32_t h[4], l[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const __nv_bfloat162 hh = __floats2bfloat162_rn(x[2 * u], x[2 * u + 1]);
+        h[u] = *reinterpret_cast<const uint32_t*>(&hh);
+        const __nv_bfloat162 ll = __floats2bfloat162_rn(x[2 * u] - __low2float(hh), x[2 * u + 1] - __high2float(hh));
+        l[u] = *reinterpret_cast<const uint32_t*>(&ll);
+      }
+      *reinterpret_cast<uint4*>(a.Xh + off) = make_uint4(h[0], h[1], h[2], h[3]);
+      if (a.Xl) *reinterpret_cast<uint4*>(a.Xl + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+  };
+#pragma unroll
+  for (int rep = 0; rep < 2; ++rep) {
+    const int c = rep * 256 + tid;
+    const int ri = c >> 3, cj = (c & 7) * 8;
+    const int gi = i0 + ri, gj = j0 + cj;
+    float x[8];
+    if (gi < a.m && gj < a.n) {  // n % 8 == 0: the 8 elements are all inside
+      const long long off = static_cast<long long>(gi) * a.n + gj;
+      float g[8];
+      if (SRC_FP32) {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(a.src[b]) + off);
+        const float4 u0 = p[0], u1 = p[1];
+        g[0] = u0.x, g[1] = u0.y, g[2] = u0.z, g[3] = u0.w, g[4] = u1.x, g[5] = u1.y, g[6] = u1.z, g[7] = u1.w;
+      } else {
+        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(a.src[b]) + off);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          g[2 * k] = __uint_as_float(w[k] << 16);
+          g[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        }
+      }
+      if (a.has_mom) {
+        float4* mp = reinterpret_cast<float4*>(a.mom[b] + off);
+        const float4 m0 = mp[0], m1 = mp[1];
+        const float mo[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = fmaf(a.beta, mo[k], g[k]);
+        mp[0] = make_float4(x[0], x[1], x[2], x[3]);
+        mp[1] = make_float4(x[4], x[5], x[6], x[7]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = g[k];
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[k] = 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ss = fmaf(x[k], x[k], ss);
+    if (!tr) {
+      store8(base + static_cast<long long>(P0 + ri) * a.lp + (Q0 + cj), x);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) S[ri][cj + k] = x[k];
+    }
+  }
+  if (tr) {
+    __syncthreads();
+#pragma unroll
+    for (int rep = 0; rep < 2; ++rep) {
+      const int c = rep * 256 + tid;
+      const int pr = c >> 3, pc = (c & 7) * 8;  // packed row (= source column), packed column group
+      float x[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[k] = S[pc + k][pr];
+      store8(base + static_cast<long long>(P0 + pr) * a.lp + (Q0 + pc), x);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += red[w];
+    a.partial[static_cast<long long>(b) * a.tiles + tile] = t;
+  }
+}
+
 cudaError_t launch_pack(const PackArgs& a, int B, cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
+  bool vec = a.n % 8 == 0;
+  for (int q = 0; q < B && vec; ++q) {
+    if (reinterpret_cast<uintptr_t>(a.src[q]) % 16) vec = false;
+    if (a.has_mom && reinterpret_cast<uintptr_t>(a.mom[q]) % 16) vec = false;
+  }
+  if (vec) {
+    if (a.src_fp32) return launch_pdl(pack_vec_kernel<true>, dim3(a.tiles, B), dim3(256), 0, st, a);
+    return launch_pdl(pack_vec_kernel<false>, dim3(a.tiles, B), dim3(256), 0, st, a);
+  }
   return launch_pdl(pack_kernel, dim3(a.tiles, B), dim3(256), 0, st, a);
 }
 

@@ -33,13 +33,14 @@
 // B is read K-major ([N, K] row-major: symmetric right operands, whose rows are
 // their columns) or MN-major ([K, N] row-major, e.g. X in B X or Q X).
 //
-// CTA pairs.  CTAs run in clusters of two that compute vertically adjacent
-// tiles (row blocks 2p and 2p + 1, same column block) and therefore need the
-// same B tile: each CTA loads half of it and multicasts it into both CTAs'
-// shared memory, and a stage is released only when both CTAs' MMAs have read
-// it.  This halves the L2 -> SM traffic of B; with one CTA per tile the
-// operand stream (96 B/clock/SM at full MMA rate) exceeds what L2 delivers
-// (about 75 B/clock/SM measured with TMA loads alone).
+// CTA pairs (2-SM MMA).  CTAs run in clusters of two that compute one 256 x 256
+// output tile together: row blocks 2p (leader, rank 0) and 2p + 1 (rank 1).
+// Each CTA loads its own 128 rows of A and one half (128 columns) of B into its
+// own shared memory, signalling the leader's stage barrier; the leader issues
+// tcgen05.mma.cta_group::2 (M = 256), which reads A from each CTA and B from
+// both, and leaves each CTA's 128 rows of the accumulator in that CTA's TMEM.
+// Per SM this is 8 KB of operands per 256 x 256 x 16 step instead of 12 KB for a
+// single-CTA 128 x 256 x 16 step, which ran at about half the tensor rate.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -58,12 +59,11 @@ struct TcCfg {
   static constexpr int BM = 128;
   static constexpr int BN = 256;
   static constexpr int BK = 64;  // bf16 elements per 128-byte swizzled row
+  static constexpr int BNH = BN / 2;  // B columns held by each CTA of the pair
   static constexpr int A_TILE = BM * BK * 2;
-  static constexpr int B_TILE = BN * BK * 2;
+  static constexpr int B_TILE = BNH * BK * 2;  // this CTA's half of the B tile
   static constexpr int STAGE = A_TILE + B_TILE;
-  // Four operand stages: with three, the MMA issuer waited for operands ~20 %
-  // of the time on 4096-sized products (TMA latency not covered).
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = 6;
   // Epilogue staging per epilogue warp (the epilogue is busy ~12 % of the
   // time on large products, so one buffer each is enough): one 32 x 32 bf16
   // output pair (head, residual part) and one input pair for the prefetched
@@ -81,6 +81,7 @@ struct TcCfg {
   static constexpr int MN_ATOM = 64;             // MN elements per swizzled row (MN-major)
   static constexpr int MN_BOX_BYTES = BK * 128;  // one [BK x MN_ATOM] box
   static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr uint32_t EPI_ARRIVALS = 8;  // epilogue warps of both CTAs release a TMEM buffer
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(BAR_BYTES >= (2 * STAGES + 5 + 8) * 8 + 8, "barrier area too small");
   static_assert(OUT_BUFS >= 1 && OUT_BUFS <= 2 && RIN_BUFS >= 1 && RIN_BUFS <= 2, "staging depth");
@@ -252,12 +253,12 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 2);  // released by the MMAs of both CTAs of the pair
+      mbar_init(&full[s], 1);   // leader: its arrive + the bytes of both CTAs
+      mbar_init(&empty[s], 1);  // the leader's MMA commit, multicast to both CTAs
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], C::EPI_ARRIVALS);
     }
     mbar_init(drain, 1);
     for (int q = 0; q < 8; ++q) mbar_init(&rbar[q], 1);
@@ -270,9 +271,9 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_desc(&tmBl);
     }
   }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+  if (warp == 1) {  // both CTAs: the pair's TMEM is allocated collectively
+    tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncwarp();
@@ -311,40 +312,42 @@ __global__ void __launch_bounds__(192, 1)
           const bool a_up = args.a_sym && (k0 >> 8) > (m0 >> 8);
           const bool b_up = !BMN && args.b_sym && (k0 >> 8) > (n0 >> 8);
           uint8_t* st = tiles + s * C::STAGE;
-          mbar_arrive_expect_tx(&full[s], C::STAGE);
+          // both CTAs' copies complete on the leader's barrier for this stage
+          const uint32_t fbar = mapa_cluster(&full[s], 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE);
           if (!a_up) {
-            tma_load_3d(alo ? &tmAl : &tmA, &full[s], st, k0, m0, b);
+            tma_load_3d_pair(alo ? &tmAl : &tmA, fbar, st, k0, m0, b);
           } else {
 #pragma unroll
             for (int q = 0; q < C::BM / C::MN_ATOM; ++q)
-              tma_load_3d(alo ? &tmAtl : &tmAt, &full[s], st + q * C::MN_BOX_BYTES, m0 + q * C::MN_ATOM, k0, b);
+              tma_load_3d_pair(alo ? &tmAtl : &tmAt, fbar, st + q * C::MN_BOX_BYTES, m0 + q * C::MN_ATOM, k0, b);
           }
-          // this CTA's half of the shared B tile, multicast to both CTAs
+          // this CTA's half of the B tile: columns n0 + 128 rank .. + 127
           uint8_t* sb = st + C::A_TILE;
+          const int nb0 = n0 + rank * C::BNH;
           if (!BMN && !b_up) {
-            tma_load_3d_mc(blo ? &tmBl : &tmB, &full[s], sb + rank * (C::B_TILE / 2), k0, n0 + rank * (C::BN / 2),
-                           b, 0x3);
+            tma_load_3d_pair(blo ? &tmBl : &tmB, fbar, sb, k0, nb0, b);
           } else {
             const CUtensorMap* mb = BMN ? (blo ? &tmBl : &tmB) : (blo ? &tmBtl : &tmBt);
 #pragma unroll
-            for (int h = 0; h < C::BN / C::MN_ATOM / 2; ++h) {
-              const int q = rank * (C::BN / C::MN_ATOM / 2) + h;
-              tma_load_3d_mc(mb, &full[s], sb + q * C::MN_BOX_BYTES, n0 + q * C::MN_ATOM, k0, b, 0x3);
-            }
+            for (int q = 0; q < C::BNH / C::MN_ATOM; ++q)
+              tma_load_3d_pair(mb, fbar, sb + q * C::MN_BOX_BYTES, nb0 + q * C::MN_ATOM, k0, b);
           }
         }
       }
       if (!ok) {
         atomicOr(args.status, kStatusTimeout);
         *abort_flag = 1;
-        // Let the copies already issued land before the CTA can exit.
-        for (int q = (it > C::STAGES ? it - C::STAGES : 0); q < it; ++q)
-          mbar_wait(&full[q % C::STAGES], (q / C::STAGES) & 1);
+        // Let the copies already issued land before the CTAs can exit (the
+        // leader's barriers count the bytes of both CTAs).
+        if (rank == 0)
+          for (int q = (it > C::STAGES ? it - C::STAGES : 0); q < it; ++q)
+            mbar_wait(&full[q % C::STAGES], (q / C::STAGES) & 1);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------------------------------ MMA issuer (leader)
       constexpr uint32_t SBO = 8 * 128;
       int it = 0, tcount = 0;
       bool ok = true;
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(192, 1)
           const int k0 = (kb % nk) * C::BK;
           const bool a_mn = args.a_sym && (k0 >> 8) > (m0 >> 8);
           const bool b_mn = BMN || (args.b_sym && (k0 >> 8) > (n0 >> 8));
-          const uint32_t idesc = make_idesc_bf16(C::BM, C::BN, b_mn) | (a_mn ? (1u << 15) : 0u);
+          const uint32_t idesc = make_idesc_bf16(2 * C::BM, C::BN, b_mn) | (a_mn ? (1u << 15) : 0u);
           const uint32_t a0 = smem_u32(tiles + s * C::STAGE);
           const uint32_t b0 = a0 + C::A_TILE;
 #pragma unroll
@@ -380,19 +383,19 @@ __global__ void __launch_bounds__(192, 1)
                                      : make_sdesc(a0 + kk * 32, 16, SBO, C::SWZ);
             const uint64_t bd = b_mn ? make_sdesc(b0 + kk * 16 * 128, C::MN_BOX_BYTES, SBO, C::SWZ)
                                      : make_sdesc(b0 + kk * 32, 16, SBO, C::SWZ);
-            tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          tc_commit_mc(&empty[s], 0x3);  // the pair's stage is free once both CTAs' MMAs have read it
+          tc_commit_pair(&empty[s], 0x3);  // both CTAs' stage s is free once these MMAs have read it
         }
         if (!ok) break;
-        tc_commit(&tfull[abuf]);  // accumulator ready for the epilogue
+        tc_commit_pair(&tfull[abuf], 0x3);  // both CTAs' accumulators ready for their epilogues
       }
       if (!ok) {
         atomicOr(args.status, kStatusTimeout);
         *abort_flag = 1;
       }
       // Every MMA issued by this thread completes before TMEM is released.
-      tc_commit(drain);
+      tc_commit_pair(drain, 0x1);
       mbar_wait(drain, 0);
     }
   } else {
@@ -537,8 +540,10 @@ __global__ void __launch_bounds__(192, 1)
         tmem_ld_wait(acc[0]);
         break;
       }
+      // this warp's TMEM rows are read: release the buffer to the leader's MMA issuer
       tc_fence_before();
-      mbar_arrive(&tempty[abuf]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_cluster(&tempty[abuf], 0));
     }
     if (!ok) {
       if (lane == 0) atomicOr(args.status, kStatusTimeout);
@@ -558,7 +563,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
   }
 }
 
