@@ -174,7 +174,7 @@ MUON_API muon_status muon_debug_bounded_wait(void* ws, long long max_cycles, voi
  *   256 x 256 blocks on or below the diagonal are written), the fp32 kernel
  *   writes the full matrix.  sym bits 1 / 2 (bf16 only): A / B is a symmetric
  *   matrix given in block-lower storage (its upper blocks are never read).
- *   Sizes: bf16 needs M % 256, N % 256, K % 64 == 0; fp32 needs M, N % 128 and
+ *   Sizes: bf16 needs M % 256, N % 256, K % 128 == 0; fp32 needs M, N % 128 and
  *   K % 16 == 0.  The kernel is enqueued on `stream`.
  */
 MUON_API muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, const void* B_lo, int batch,

@@ -847,7 +847,7 @@ muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, cons
   cudaError_t err;
   const char* why = nullptr;
   if (dt == MUON_BF16) {
-    if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 256 || K % 64) return fail(MUON_ERR_SHAPE, "bf16 sizes");
+    if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 256 || K % 128) return fail(MUON_ERR_SHAPE, "bf16 sizes");
     if (split < 1 || split > 3) return fail(MUON_ERR_ARG, "split must be 1, 2 or 3");
     if (split >= 2 && !A_lo) return fail(MUON_ERR_ARG, "split 2 and 3 need A_lo");
     if (split == 3 && !B_lo) return fail(MUON_ERR_ARG, "split 3 needs B_lo");

@@ -44,7 +44,7 @@ struct TcOperand {
 // stores the output block-lower (256 x 256 blocks on or below the diagonal).
 // a_sym / b_sym mark operands that are symmetric matrices in that storage.
 struct TcGemmDesc {
-  int B, M, N, K;  // M % 256 == 0, N % 256 == 0, K % 64 == 0 (K % 256 == 0 with symmetric operands)
+  int B, M, N, K;  // M % 256 == 0, N % 256 == 0, K % 128 == 0 (K % 256 == 0 with symmetric operands)
   int sym;
   int a_sym, b_sym;
   int split;  // 1 or 3

@@ -58,12 +58,18 @@ namespace muon {
 struct TcCfg {
   static constexpr int BM = 128;
   static constexpr int BN = 256;
-  static constexpr int BK = 64;  // bf16 elements per 128-byte swizzled row
-  static constexpr int BNH = BN / 2;  // B columns held by each CTA of the pair
+  // A stage covers 128 of K as two 64-element (128-byte) swizzle atoms, i.e.
+  // 8 MMAs per stage barrier: with 64-wide stages the per-stage wait / commit
+  // round trip left the tensor pipe idle ~45 % of the time.
+  static constexpr int KA = 64;           // bf16 elements per 128-byte swizzled row
+  static constexpr int BK = 128;          // K per stage
+  static constexpr int KATOMS = BK / KA;  // K-major swizzle atoms per operand per stage
+  static constexpr int BNH = BN / 2;      // B columns held by each CTA of the pair
+  static constexpr int KATOM_BYTES = 128 * KA * 2;  // one K-major atom of 128 rows
   static constexpr int A_TILE = BM * BK * 2;
   static constexpr int B_TILE = BNH * BK * 2;  // this CTA's half of the B tile
   static constexpr int STAGE = A_TILE + B_TILE;
-  static constexpr int STAGES = 6;
+  static constexpr int STAGES = 3;
   // Epilogue staging per epilogue warp (the epilogue is busy ~12 % of the
   // time on large products, so one buffer each is enough): one 32 x 32 bf16
   // output pair (head, residual part) and one input pair for the prefetched
@@ -79,7 +85,8 @@ struct TcCfg {
   static constexpr int SMEM = STAGES * STAGE + STG + BAR_BYTES + 1024;
   static constexpr uint32_t SWZ = 2u;            // descriptor code for the 128-byte swizzle
   static constexpr int MN_ATOM = 64;             // MN elements per swizzled row (MN-major)
-  static constexpr int MN_BOX_BYTES = BK * 128;  // one [BK x MN_ATOM] box
+  static constexpr int MN_BOX_BYTES = BK * 128;  // one [BK x MN_ATOM] box (MN-major atom)
+  static_assert(BM == 128 && BNH == 128, "K-major atoms hold 128 rows");
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr uint32_t EPI_ARRIVALS = 8;  // epilogue warps of both CTAs release a TMEM buffer
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -316,7 +323,9 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t fbar = mapa_cluster(&full[s], 0);
           if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE);
           if (!a_up) {
-            tma_load_3d_pair(alo ? &tmAl : &tmA, fbar, st, k0, m0, b);
+#pragma unroll
+            for (int g = 0; g < C::KATOMS; ++g)
+              tma_load_3d_pair(alo ? &tmAl : &tmA, fbar, st + g * C::KATOM_BYTES, k0 + g * C::KA, m0, b);
           } else {
 #pragma unroll
             for (int q = 0; q < C::BM / C::MN_ATOM; ++q)
@@ -326,7 +335,9 @@ __global__ void __launch_bounds__(192, 1)
           uint8_t* sb = st + C::A_TILE;
           const int nb0 = n0 + rank * C::BNH;
           if (!BMN && !b_up) {
-            tma_load_3d_pair(blo ? &tmBl : &tmB, fbar, sb, k0, nb0, b);
+#pragma unroll
+            for (int g = 0; g < C::KATOMS; ++g)
+              tma_load_3d_pair(blo ? &tmBl : &tmB, fbar, sb + g * C::KATOM_BYTES, k0 + g * C::KA, nb0, b);
           } else {
             const CUtensorMap* mb = BMN ? (blo ? &tmBl : &tmB) : (blo ? &tmBtl : &tmBt);
 #pragma unroll
@@ -379,10 +390,12 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t b0 = a0 + C::A_TILE;
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
+            // K-major: atom kk / 4, 32 bytes per 16 of K inside it; MN-major: 16 rows of 128 B
+            const uint32_t koff = (kk / 4) * C::KATOM_BYTES + (kk % 4) * 32;
             const uint64_t ad = a_mn ? make_sdesc(a0 + kk * 16 * 128, C::MN_BOX_BYTES, SBO, C::SWZ)
-                                     : make_sdesc(a0 + kk * 32, 16, SBO, C::SWZ);
+                                     : make_sdesc(a0 + koff, 16, SBO, C::SWZ);
             const uint64_t bd = b_mn ? make_sdesc(b0 + kk * 16 * 128, C::MN_BOX_BYTES, SBO, C::SWZ)
-                                     : make_sdesc(b0 + kk * 32, 16, SBO, C::SWZ);
+                                     : make_sdesc(b0 + koff, 16, SBO, C::SWZ);
             tc_mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit_pair(&empty[s], 0x3);  // both CTAs' stage s is free once these MMAs have read it
@@ -680,13 +693,13 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
   const bf16* alo = d.A.lo ? d.A.lo : d.A.hi;
   const bf16* blo = d.Bop.lo ? d.Bop.lo : d.Bop.hi;
   // K-major boxes {64 k, rows}; transposed boxes {64 mn, 64 k} (symmetric operands: K == rows)
-  bool ok = make_map(&mA, d.A.hi, d.K, d.M, d.B, d.A.ld, d.A.bs, C::BK, C::BM, 128);
-  ok = ok && make_map(&mAl, alo, d.K, d.M, d.B, d.A.ld, d.A.bs, C::BK, C::BM, 128);
+  bool ok = make_map(&mA, d.A.hi, d.K, d.M, d.B, d.A.ld, d.A.bs, C::KA, C::BM, 128);
+  ok = ok && make_map(&mAl, alo, d.K, d.M, d.B, d.A.ld, d.A.bs, C::KA, C::BM, 128);
   ok = ok && make_map(&mAt, d.A.hi, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
   ok = ok && make_map(&mAtl, alo, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
   if (!BMN) {
-    ok = ok && make_map(&mB, d.Bop.hi, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::BK, C::BN / 2, 128);
-    ok = ok && make_map(&mBl, blo, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::BK, C::BN / 2, 128);
+    ok = ok && make_map(&mB, d.Bop.hi, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::KA, C::BNH, 128);
+    ok = ok && make_map(&mBl, blo, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::KA, C::BNH, 128);
     ok = ok && make_map(&mBt, d.Bop.hi, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
     ok = ok && make_map(&mBtl, blo, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
   } else {
@@ -775,8 +788,8 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* statu
     *why = "unsupported operand split";
     return cudaErrorInvalidValue;
   }
-  if (d.M % 256 || d.N % 256 || d.K % 64) {
-    *why = "tensor-core GEMM needs M and N multiples of 256 (CTA pairs) and K a multiple of 64";
+  if (d.M % 256 || d.N % 256 || d.K % 128) {
+    *why = "tensor-core GEMM needs M and N multiples of 256 (CTA pairs) and K a multiple of 128";
     return cudaErrorInvalidValue;
   }
   if ((d.split >= 2 && !d.A.lo) || (d.split == 3 && !d.Bop.lo)) {

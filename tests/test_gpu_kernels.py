@@ -29,7 +29,7 @@ def _rand(shape, seed, dtype=torch.bfloat16):
     return torch.randn(*shape, generator=g).to(dtype).cuda()
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (256, 256, 128), (256, 512, 320), (512, 768, 1024)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (256, 256, 256), (256, 512, 384), (512, 768, 1024)])
 def test_tc_gemm_kmajor_b(M, N, K):
     m = _lib()
     A = _rand((2, M, K), 1)
@@ -41,7 +41,7 @@ def test_tc_gemm_kmajor_b(M, N, K):
     assert _rel(out, _ref(A, B, False)) < 2e-5
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (256, 512, 192), (512, 1024, 512)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (256, 512, 256), (512, 1024, 512)])
 def test_tc_gemm_mnmajor_b(M, N, K):
     m = _lib()
     A = _rand((2, M, K), 3)
@@ -57,7 +57,7 @@ def block_lower(S, device="cuda"):
     return r[:, None] >= r[None, :]
 
 
-@pytest.mark.parametrize("S,K", [(256, 64), (512, 256), (768, 1024)])
+@pytest.mark.parametrize("S,K", [(256, 128), (512, 256), (768, 1024)])
 def test_tc_syrk_block_lower(S, K):
     m = _lib()
     X = _rand((3, S, K), 5)
@@ -189,8 +189,8 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     m.debug_bounded_wait(ws, 2_000_000)  # ~1 ms of SM cycles, nobody arrives
     assert m.device_status(ws) == 6  # MUON_ERR_TIMEOUT
     assert m.device_status(ws) == 0  # cleared
-    A = _rand((1, 256, 64), 10)
-    B = _rand((1, 256, 64), 11)
+    A = _rand((1, 256, 128), 10)
+    B = _rand((1, 256, 128), 11)
     out = m.debug_gemm(A, B, workspace=ws)
     torch.cuda.synchronize()
     assert _rel(out, _ref(A, B, False)) < 2e-5
@@ -223,7 +223,7 @@ def test_tc_accumulation_precision():
 
 def test_tc_rejects_shapes_that_do_not_pair():
     m = _lib()
-    A = _rand((1, 128, 64), 12)
-    B = _rand((1, 256, 64), 13)
+    A = _rand((1, 128, 128), 12)
+    B = _rand((1, 256, 128), 13)
     with pytest.raises(m.MuonError):
         m.debug_gemm(A, B)
