@@ -183,6 +183,36 @@ def barrier(world):
         dist.barrier()
 
 
+def sum_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# Configs that are one model's whole set of matrices: with N ranks each matrix
+# is updated by one owner (strong scaling).  The other configs are a batch per
+# rank (weak scaling).
+OWNER_PLACED = ("c3", "c4")
+
+
+def shard(work, rank, world):
+    """This rank's part of the workload and the scaling it implies.  Placement
+    is the library's LPT over its cost model, computed identically on every
+    rank (no communication)."""
+    if world <= 1 or work.name not in OWNER_PLACED:
+        return work, "weak"
+    import dataclasses
+    import newton_schulz_04_gb300 as pkg
+    mine = pkg.owned(work.shapes, rank, world, steps=work.steps, dtype=work.dtype)
+    sub = dataclasses.replace(work, shapes=[work.shapes[i] for i in mine],
+                              grads=[work.grads[i] for i in mine] if work.grads else [],
+                              weights=[work.weights[i] for i in mine] if work.weights else [])
+    return sub, "strong"
+
+
 def max_over_ranks(x, world):
     if world <= 1:
         return x
@@ -260,6 +290,9 @@ def run_ours(args, world, rank, local):
     pkg.load(build_if_missing=True)
     dev = torch.device("cuda", local)
     work = make_workload(args.config, dev if args.config.startswith("c3") else "cpu")
+    work, scaling = shard(work, rank, world)
+    if not work.shapes:
+        raise SystemExit(f"rank {rank} owns no matrix of {args.config} at world size {world}")
     shapes = work.shapes
     count = len(shapes)
     W = [w.to(dev) for w in work.weights]
@@ -271,6 +304,8 @@ def run_ours(args, world, rank, local):
     upd = pkg.MuonUpdater(W, work.beta, work.lr, work.steps, work.coeffs, "auto", use_graph=not args.no_graph)
     Mo = upd.moms
     flops_step = work.flop_count()
+    flops_all = sum_over_ranks(flops_step, world)  # = world x flops_step under weak scaling
+    count_all = sum_over_ranks(count, world)
     in_bytes = sum(g.numel() * g.element_size() for g in G) + sum(m.numel() * 4 for m in Mo) * 2 + \
         sum(w.numel() * w.element_size() for w in W) * 2
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if in_bytes < 4 * L2_BYTES else None
@@ -316,8 +351,8 @@ def run_ours(args, world, rank, local):
     assert pkg.device_status(upd.workspace) == 0
     t_total = max_over_ranks(sum(ms) / 1e3, world)
     ms_step = 1e3 * t_total / args.steps
-    value = world * flops_step * args.steps / t_total / 1e12
-    value_eager = world * flops_step * args.steps / max_over_ranks(sum(ms_eager) / 1e3, world) / 1e12
+    value = flops_all * args.steps / t_total / 1e12
+    value_eager = flops_all * args.steps / max_over_ranks(sum(ms_eager) / 1e3, world) / 1e12
     # dominant kernel kind by time in the profiled pass
     by = {}
     for k, t, fl, byt in recs:
@@ -363,17 +398,20 @@ def run_ours(args, world, rank, local):
     timed(e2e_step, args.warmup)
     e2e_ms = timed(e2e_step, args.steps)
     e2e_t = max_over_ranks(sum(e2e_ms) / 1e3, world)
-    e2e_val = world * flops_step * args.steps / e2e_t / 1e12
+    e2e_val = flops_all * args.steps / e2e_t / 1e12
     launches_per_step = len(recs) / args.steps
     line = {
         "metric": "Muon update TFLOP/s (algorithmic, symmetric Gram count)",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": scaling, "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC.get(args.config, args.config), "name": args.config,
                    "matrices_per_gpu": count, "l2": "flushed between timed steps" if flush is not None
-                   else "inputs larger than L2", "parallelism": f"replicas x{world}" if world > 1 else "1 gpu"},
-        "matrices_per_s": world * count * args.steps / t_total,
+                   else "inputs larger than L2",
+                   "parallelism": "1 gpu" if world == 1 else
+                   (f"owner placement over {world} ranks (LPT), no data-path collective" if scaling == "strong"
+                    else f"one batch per rank x{world}")},
+        "matrices_per_s": count_all * args.steps / t_total,
         "pct_of_bf16_peak": 100.0 * value / pk["bf16_tflops"],
         "value_without_graph": value_eager,
         "launch_path": "CUDA graph replay of the C-ABI call sequence" if not args.no_graph else "direct C-ABI calls",

@@ -81,6 +81,8 @@ typedef enum {
 #define MUON_MAX_DIM 65536   /* largest accepted m or n */
 #define MUON_MAX_STEPS 100   /* largest accepted number of NS steps */
 #define MUON_WS_ALIGN 256    /* required alignment of the workspace pointer */
+#define MUON_PARTITION_EXACT_MAX 24           /* largest count muon_partition solves exactly */
+#define MUON_PARTITION_NODE_BUDGET 4000000LL  /* search nodes before the exact solver stops */
 
 /*
  * muon_ns_batched -- NS orthogonalisation of B same-shape matrices.
@@ -220,6 +222,53 @@ MUON_API muon_status muon_ns_batched_static(const void* X, int B, int m, int n, 
                                             const float* coeffs, void* out, muon_dtype dt,
                                             muon_sched sc, void* stream);
 MUON_API size_t muon_static_scratch_bytes(void);
+
+/*
+ * ---- owner placement (DMuon technical summary, gist.science 2606.27153,
+ * §2.3 "compute-aware load balancing"): every 2-D matrix is updated by exactly
+ * one owner rank, and the owners are chosen so that the largest per-owner cost
+ * (the makespan) is small.  The pages profile each shape's update time at
+ * start-up and minimise the predicted makespan with a MILP, falling back to a
+ * greedy heuristic on large inputs.  Host only, no GPU needed.
+ */
+
+/*
+ * muon_cost_estimate -- predicted device seconds of one matrix's update for
+ * each matrix of `shapes` (count x 2, int64 m, n, row-major), under the
+ * schedule `sc` resolves to at that shape with `steps` iterations and dtype
+ * `dt`.  It counts the launches muon_step issues, with each launch's executed
+ * flops (padded 256-blocks, symmetric outputs on lower blocks, split operands
+ * 2x / 3x) at a nominal kernel rate and its HBM bytes at a nominal bandwidth,
+ * and takes the larger of the two.  A model for placement when no measured
+ * costs are at hand.  Writes seconds[count].
+ * Errors (nothing written): MUON_ERR_ARG for NULL pointers with count > 0,
+ * count < 0, or bad steps, dtype or schedule; MUON_ERR_SHAPE for m or n
+ * outside [1, MUON_MAX_DIM].
+ */
+MUON_API muon_status muon_cost_estimate(const int64_t* shapes, int count, int steps, muon_dtype dt,
+                                        muon_sched sc, double* seconds);
+
+/*
+ * muon_partition -- assign each of `count` matrices, with costs cost[count]
+ * (finite, >= 0, any unit), to one of `world` owners: owner[i] in [0, world).
+ *  - Greedy longest-processing-time (LPT): matrices in decreasing cost
+ *    (equal costs: lower index first), each to the owner with the least total
+ *    so far (equal totals: lower rank).  Makespan <= (4/3 - 1/(3 world)) x the
+ *    optimum (Graham's bound).
+ *  - If 0 < count <= exact_limit (exact_limit <= MUON_PARTITION_EXACT_MAX), a
+ *    depth-first branch and bound seeded with the LPT answer then replaces it
+ *    by an assignment of strictly smaller makespan if one exists.  The search
+ *    stops after MUON_PARTITION_NODE_BUDGET nodes, keeping the best found, so
+ *    the answer is optimal unless the budget ran out, and never worse than LPT.
+ *  - Deterministic in (cost, world, exact_limit): every rank computes the same
+ *    placement with no communication.
+ * load[world] (may be NULL) receives each owner's total cost.
+ * Errors (nothing written): MUON_ERR_ARG for count < 0, world < 1, NULL
+ * cost/owner with count > 0, exact_limit out of range, or a cost that is
+ * negative, NaN or infinite.
+ */
+MUON_API muon_status muon_partition(const double* cost, int count, int world, int exact_limit,
+                                    int32_t* owner, double* load);
 
 /* Thread-local message of the last failed call on this thread ("" if none). */
 MUON_API const char* muon_last_error(void);

@@ -77,6 +77,11 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.muon_ns_batched_static.restype = i32
     lib.muon_static_scratch_bytes.argtypes = []
     lib.muon_static_scratch_bytes.restype = sz
+    lib.muon_cost_estimate.argtypes = [ctypes.POINTER(i64), i32, i32, i32, i32, ctypes.POINTER(ctypes.c_double)]
+    lib.muon_cost_estimate.restype = i32
+    lib.muon_partition.argtypes = [ctypes.POINTER(ctypes.c_double), i32, i32, i32, ctypes.POINTER(i32),
+                                   ctypes.POINTER(ctypes.c_double)]
+    lib.muon_partition.restype = i32
     lib.muon_last_error.argtypes = []
     lib.muon_last_error.restype = ctypes.c_char_p
     lib.muon_version.argtypes = []
@@ -138,6 +143,80 @@ def bucket_plan(shapes):
     if g < 0:
         raise MuonError(ERR_ARG, "bad shapes")
     return list(order[:n]), list(start[:g + 1])
+
+
+def cost_estimate(shapes, steps=5, dtype=torch.bfloat16, schedule="auto") -> list:
+    """Predicted device seconds of each matrix's update (the library's cost model)."""
+    lib = load()
+    n = len(shapes)
+    out = (ctypes.c_double * max(n, 1))()
+    _check(lib.muon_cost_estimate(_shapes_arr(shapes), n, int(steps), _dtype_code(dtype), SCHED[schedule], out))
+    return list(out[:n])
+
+
+PARTITION_EXACT_MAX = 24
+
+
+def partition(costs, world: int, exact_limit: int = 12):
+    """(owner per matrix, total cost per owner): greedy LPT, solved exactly when
+    len(costs) <= exact_limit.  Same answer on every rank for the same costs."""
+    lib = load()
+    n = len(costs)
+    c = (ctypes.c_double * max(n, 1))(*[float(x) for x in costs])
+    owner = (ctypes.c_int32 * max(n, 1))()
+    load_ = (ctypes.c_double * max(int(world), 1))()
+    _check(lib.muon_partition(c, n, int(world), int(exact_limit), owner, load_))
+    return list(owner[:n]), list(load_[:int(world)])
+
+
+def measure_costs(shapes, steps=5, dtype=torch.bfloat16, schedule="auto", repeats=3, cache=None, device=None):
+    """Measured device seconds per matrix, per shape group, for placement.
+
+    Each distinct (short, long) group of `shapes` runs muon_step on synthetic
+    data at its real batch width; the time per call (CUDA events, after one
+    warm-up) divided by the width is that group's per-matrix cost.  `cache`
+    (a dict, e.g. loaded from and saved to JSON by the caller) keeps results
+    keyed by "s,l,dtype,steps,schedule,width" across calls.
+    """
+    dev = device or torch.device("cuda")
+    groups = {}
+    for i, (m, n) in enumerate(shapes):
+        groups.setdefault((min(m, n), max(m, n)), []).append(i)
+    out = [0.0] * len(shapes)
+    gen = torch.Generator(device="cpu").manual_seed(0)
+    for (s_, l_), idx in sorted(groups.items()):
+        key = f"{s_},{l_},{str(dtype).split('.')[-1]},{steps},{schedule},{len(idx)}"
+        if cache is not None and key in cache:
+            per = float(cache[key])
+        else:
+            W = [torch.zeros(s_, l_, dtype=dtype, device=dev) for _ in idx]
+            G = [torch.randn(s_, l_, generator=gen).to(dtype).to(dev) for _ in idx]
+            M = [torch.zeros(s_, l_, dtype=torch.float32, device=dev) for _ in idx]
+            ws = new_workspace(workspace_bytes([(s_, l_)] * len(idx), steps, dtype, schedule), dev)
+            muon_step(W, G, M, 0.0, 0.0, steps, None, schedule, ws)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(repeats):
+                muon_step(W, G, M, 0.0, 0.0, steps, None, schedule, ws)
+            b.record()
+            b.synchronize()
+            per = a.elapsed_time(b) / 1e3 / repeats / len(idx)
+            del W, G, M, ws
+            if cache is not None:
+                cache[key] = per
+        for i in idx:
+            out[i] = per
+    return out
+
+
+def owned(shapes, rank: int, world: int, costs=None, steps=5, dtype=torch.bfloat16, schedule="auto",
+          exact_limit: int = 12):
+    """Indices of the matrices `rank` owns out of `world` owners (model costs
+    unless measured `costs` are given)."""
+    if costs is None:
+        costs = cost_estimate(shapes, steps, dtype, schedule)
+    owner, _ = partition(costs, world, exact_limit)
+    return [i for i, r in enumerate(owner) if r == rank]
 
 
 def new_workspace(nbytes: int, device=None) -> torch.Tensor:

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libmuon_ns.so")
-SOURCES = ["engine.cu", "tc_gemm.cu", "simt_gemm.cu", "elementwise.cu"]
+SOURCES = ["engine.cu", "tc_gemm.cu", "simt_gemm.cu", "elementwise.cu", "planner.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -49,7 +49,7 @@ def build(verbose=False, force=False, extra=()) -> str:
     objs = []
 
     def comp(src):
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *_flags(extra), "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

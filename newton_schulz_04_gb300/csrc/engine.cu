@@ -35,7 +35,7 @@ namespace muon {
 
 static thread_local std::string g_last_error;
 
-static muon_status fail(muon_status s, const char* fmt, ...) {
+muon_status fail(muon_status s, const char* fmt, ...) {
   char buf[512];
   va_list ap;
   va_start(ap, fmt);
@@ -674,6 +674,59 @@ static muon_status run_all(std::vector<Mat>& mats, int steps, const float* coeff
   return MUON_OK;
 }
 
+// ------------------------------------------------------------------ cost model
+// Predicted device seconds of one matrix's update (pack, norm, the NS products
+// and the apply), counted launch by launch as run_chunk issues them: executed
+// flops over the padded 256-blocks (lower blocks only for symmetric outputs,
+// x2 / x3 for split operands) and HBM bytes, each launch taking the larger of
+// flops / rate and bytes / bandwidth.  The rates are nominal figures for this
+// library's kernels on GB300 under the power cap.
+constexpr double kRateTensor = 1.3e15;  // executed bf16 tensor-core flop/s
+constexpr double kRateSimt = 4.0e13;    // fp32 FFMA flop/s
+constexpr double kRateHbm = 6.0e12;     // byte/s
+
+static double estimate_seconds(long long m, long long n, int steps, muon_dtype dt, muon_sched sc) {
+  const Group g = make_group(m, n, steps, dt, sc);
+  const double S = static_cast<double>(g.sp), L = static_cast<double>(g.lp);
+  const double el = static_cast<double>(g.s) * g.l;
+  const bool fp32 = dt == MUON_FP32;
+  const double rate = fp32 ? kRateSimt : kRateTensor;
+  const double nb = S / 256.0, nl = L / 256.0;
+  const double sym_tiles = nb * (nb + 1) / 2, rect_tiles = nb * nl, tile = 2.0 * 256.0 * 256.0;
+  const double ssz = 4.0;  // bytes of a packed element: fp32, or a bf16 pair
+  double t = 0.0;
+  auto launch = [&](double flops, double bytes) { t += std::max(flops / rate, bytes / kRateHbm); };
+  // pack: read grad + momentum, write momentum + packed copy
+  const bool x1 = !fp32 && g.sc == MUON_SCHED_GRAM_X1;
+  launch(0.0, el * ((fp32 ? 4.0 : 2.0) + 8.0 + (steps == 0 ? 4.0 : (x1 ? 2.0 : 4.0))));
+  const double apply = el * 2.0 * (fp32 ? 4.0 : 2.0);  // W read + write
+  if (steps == 0) {
+    launch(0.0, el * 4.0 + apply);
+    return t;
+  }
+  const double sym_out = sym_tiles * 256.0 * 256.0 * ssz;  // a block-lower s x s output
+  if (g.sc == MUON_SCHED_ORIG) {
+    for (int k = 0; k < steps; ++k) {
+      const double fa = (!fp32 && k >= steps - kSplitA) ? 3.0 : 1.0;
+      const double fb = (!fp32 && k >= steps - kSplitB) ? 2.0 : 1.0;
+      launch(sym_tiles * tile * L, S * L * (fp32 ? 4.0 : 2.0) + sym_out);
+      launch(fa * sym_tiles * tile * S, 2.0 * sym_out);
+      const double out = k == steps - 1 ? apply : S * L * ssz;
+      launch(fb * rect_tiles * tile * S, sym_out + S * L * (fp32 ? 8.0 : 6.0) + out);
+    }
+    return t;
+  }
+  const double f3 = (!fp32 && g.sc == MUON_SCHED_GRAM_X3) ? 3.0 : 1.0;
+  launch(f3 * sym_tiles * tile * L, S * L * ssz + sym_out);
+  for (int k = 0; k < steps; ++k) {
+    launch(f3 * sym_tiles * tile * S, 2.0 * sym_out);
+    const int prods = (k > 0 ? 1 : 0) + (k + 1 < steps ? 2 : 0);
+    for (int p = 0; p < prods; ++p) launch(f3 * sym_tiles * tile * S, 3.0 * sym_out);
+  }
+  launch(f3 * rect_tiles * tile * S, sym_out + S * L * ssz + apply);
+  return t;
+}
+
 static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -684,6 +737,23 @@ static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 using namespace muon;
 
 extern "C" {
+
+muon_status muon_cost_estimate(const int64_t* shapes, int count, int steps, muon_dtype dt, muon_sched sc,
+                               double* seconds) {
+  if (count < 0) return fail(MUON_ERR_ARG, "count=%d < 0", count);
+  if (count > 0 && (!shapes || !seconds)) return fail(MUON_ERR_ARG, "shapes and seconds must not be NULL");
+  if (steps < 0 || steps > MUON_MAX_STEPS) return fail(MUON_ERR_ARG, "steps=%d out of [0, %d]", steps, MUON_MAX_STEPS);
+  if (!valid_dt(dt)) return fail(MUON_ERR_ARG, "bad dtype %d", dt);
+  if (!valid_sc(sc)) return fail(MUON_ERR_ARG, "bad schedule %d", sc);
+  for (int i = 0; i < count; ++i) {
+    const int64_t m = shapes[2 * i], n = shapes[2 * i + 1];
+    if (m < 1 || n < 1 || m > MUON_MAX_DIM || n > MUON_MAX_DIM)
+      return fail(MUON_ERR_SHAPE, "matrix %d has shape %lldx%lld", i, static_cast<long long>(m),
+                  static_cast<long long>(n));
+  }
+  for (int i = 0; i < count; ++i) seconds[i] = estimate_seconds(shapes[2 * i], shapes[2 * i + 1], steps, dt, sc);
+  return MUON_OK;
+}
 
 muon_status muon_ns_batched(const void* X, int B, int m, int n, int steps, const float* coeffs, void* out,
                             muon_dtype dt, muon_sched sc, void* ws, size_t ws_bytes, void* stream) {

@@ -74,17 +74,6 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap* m, uint64_t* bar,
       : "memory");
 }
 
-// Same, delivered to the CTAs of `mask` in the cluster at the same shared
-// offset, each signalling its own barrier at `bar`'s offset.
-__device__ __forceinline__ void tma_load_3d_mc(const CUtensorMap* m, uint64_t* bar, void* dst, int x, int y, int z,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(mask)
-      : "memory");
-}
-
 // Pair (2-SM) form: the destination is this CTA's shared memory, completion is
 // counted on `bar_cluster`, a shared::cluster address that may be in the peer CTA.
 __device__ __forceinline__ void tma_load_3d_pair(const CUtensorMap* m, uint32_t bar_cluster, void* dst, int x, int y,
@@ -172,14 +161,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                    smem_u32(bar))
                : "memory");
 }
-// Same, arriving on the barrier at `bar`'s offset in every CTA of `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
 // ---- pair (2-SM) forms: one MMA spans both CTAs of a cluster pair
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
@@ -204,7 +185,9 @@ __device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc
       : "memory");
 }
 // Arrive once on the barrier at `bar`'s offset in every CTA of `mask` when the
-// pair MMAs issued so far by this thread are done.
+// pair MMAs issued so far by this thread are done.  This is how a 2-SM MMA
+// reports completion to both CTAs; it moves no data (the kernels use no
+// multicast TMA loads).
 __device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(

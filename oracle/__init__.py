@@ -9,3 +9,4 @@ from .ns_oracle import (  # noqa: F401
     momentum_update, orient, frob_normalize, ns_original, ns_gram,
     newton_schulz, muon_update, bf16_round, bucket_order,
 )
+from . import partition  # noqa: F401,E402

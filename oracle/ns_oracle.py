@@ -18,7 +18,7 @@ What it computes, step by step, in the order the pages describe it:
   Gram recurrence must reproduce the original-space result exactly (up to
   rounding).
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 * momentum is heavy-ball, M <- beta*M + G (no Nesterov, no dampening);
 * X0 = X / (||X||_F + eps), eps = 1e-7;
