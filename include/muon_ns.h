@@ -68,15 +68,39 @@ typedef enum {
 
 typedef enum {
     MUON_BF16 = 0,   /* grad, W (and X/out of muon_ns_batched) are bfloat16; momentum is fp32 */
-    MUON_FP32 = 1    /* all tensors fp32; NS computed with fp32 arithmetic */
+    MUON_FP32 = 1,   /* all tensors fp32; NS computed with fp32 arithmetic */
+    MUON_FP16 = 2    /* muon_debug_gemm only: fp16 operands and an fp16 output pair */
 } muon_dtype;
 
 typedef enum {
     MUON_SCHED_AUTO = 0,     /* cheapest schedule that meets the dtype's accuracy (see below) */
     MUON_SCHED_GRAM_X3 = 1,  /* Gram space; symmetric products with split-bf16 operands (hi*hi + hi*lo + lo*hi) */
     MUON_SCHED_GRAM_X1 = 2,  /* Gram space; plain bf16 operands (fast mode, larger error) */
-    MUON_SCHED_ORIG = 3      /* original space; fp32 carry of X, split-bf16 A in A*A and B in B*X */
+    MUON_SCHED_ORIG = 3,     /* original space (bf16: step 0 in bf16, later steps on fp16 operands, see below) */
+    MUON_SCHED_ORIG_BF16 = 4 /* original space on bf16 operands only; split A in A*A and B in B*X in the last two steps */
 } muon_sched;
+
+/*
+ * Schedules and precision.  Every tensor-core product accumulates in fp32.
+ *  - bf16, AUTO: ORIG.  fp32, AUTO: Gram space when rows != cols (never more
+ *    work), else ORIG; the fp32 path multiplies with fp32 FFMA.
+ *  - ORIG (bf16).  Step 0 multiplies the packed bf16 copy of M (exact for bf16
+ *    gradients from a zero momentum state) on bf16 operands.  Every later
+ *    product takes fp16 operands (11 significant bits against bf16's 8).
+ *    Between steps X is carried as an fp16 pair, hi + lo / 2^11 (about 22 bits).
+ *    A = X X^T and B = b A + c A^2 are single fp16 values.  fp16's range is safe:
+ *    the Frobenius normalisation gives sigma(X0) <= 1.  When the polynomial
+ *    p(s) = a s + b s^3 + c s^5 maps [0, 1.25] into [-1.25, 1.25], every
+ *    iterate keeps sigma <= 1.25 (the quintic and the cubic (1.5, -0.5, 0)
+ *    do).  Coefficients that fail this check, or whose |b|, |c| could take B
+ *    out of fp16's range, run as ORIG_BF16.
+ *  - ORIG_BF16.  bf16 operands throughout, with X carried as a bf16 pair (about
+ *    16 bits).  A*A and B*X use split operands in the last two steps.
+ *  - GRAM_X3 / GRAM_X1.  The Gram recurrence on bf16 pairs (split products)
+ *    or on plain bf16.  Gram space squares the condition number, so on
+ *    ill-conditioned inputs it misses the 2e-2 target that ORIG meets.
+ * muon_workspace_bytes is the same for ORIG and ORIG_BF16.
+ */
 
 #define MUON_MAX_DIM 65536   /* largest accepted m or n */
 #define MUON_MAX_STEPS 100   /* largest accepted number of NS steps */
@@ -170,13 +194,15 @@ MUON_API muon_status muon_debug_bounded_wait(void* ws, long long max_cycles, voi
  *   split = 2 uses (A + A_lo) B (b_mn = 1 only); split = 3 uses
  *   A B + A B_lo + A_lo B.  C is returned as a bf16 pair: out = bf16(C) and,
  *   if out_lo is not NULL, out_lo = bf16(C - out) ([batch, M, N] each).
+ *   dt = MUON_FP16: the same kernel on fp16 A, B (and A_lo, B_lo); C is
+ *   returned as an fp16 pair, out = fp16(C), out_lo = fp16((C - out) * 2^11).
  *   dt = MUON_FP32 runs the FFMA kernel on fp32 A, B and writes fp32 C to out.
  *   sym bit 0 (M == N): symmetric output; the bf16 kernel computes the tiles
  *   touching the lower triangle and stores the output "block-lower" (only the
  *   256 x 256 blocks on or below the diagonal are written), the fp32 kernel
  *   writes the full matrix.  sym bits 1 / 2 (bf16 only): A / B is a symmetric
  *   matrix given in block-lower storage (its upper blocks are never read).
- *   Sizes: bf16 needs M % 256, N % 256, K % 128 == 0; fp32 needs M, N % 128 and
+ *   Sizes: bf16 / fp16 need M % 256, N % 256, K % 128 == 0; fp32 needs M, N % 128 and
  *   K % 16 == 0.  The kernel is enqueued on `stream`.
  */
 MUON_API muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, const void* B_lo, int batch,

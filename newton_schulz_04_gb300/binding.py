@@ -18,8 +18,9 @@ from . import build as _build
 OK, ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = range(8)
 STATUS_NAMES = ["OK", "ERR_ARG", "ERR_SHAPE", "ERR_ALIGN", "ERR_WORKSPACE", "ERR_CUDA", "ERR_TIMEOUT",
                 "ERR_UNSUPPORTED"]
-BF16, FP32 = 0, 1
-SCHED = {"auto": 0, "gram_x3": 1, "gram_x1": 2, "orig": 3}
+BF16, FP32, FP16 = 0, 1, 2  # FP16: muon_debug_gemm only
+F16_LO_SCALE = 2048.0  # an fp16 pair stores lo = fp16((v - hi) * 2^11)
+SCHED = {"auto": 0, "gram_x3": 1, "gram_x1": 2, "orig": 3, "orig_bf16": 4}
 SCHED_NAMES = {v: k for k, v in SCHED.items()}
 WS_ALIGN = 256
 
@@ -308,10 +309,11 @@ def debug_gemm(A, B, A_lo=None, B_lo=None, split=1, b_mn=False, sym=False, a_sym
                workspace=None, stream=None):
     """Test hook: out[b] = A[b] @ (B[b] if b_mn else B[b]^T) through one library kernel.
 
-    bf16 operands run the tensor-core kernel and return the fp32 sum of the
-    bf16 head/residual pair it writes (with sym, only the 256 x 256 blocks on
-    or below the diagonal are written); a_sym / b_sym declare operands given
-    in that block-lower storage.  fp32 operands run the FFMA kernel."""
+    bf16 (or fp16) operands run the tensor-core kernel and return the fp32
+    value of the bf16 (fp16) head/residual pair it writes (with sym, only the
+    256 x 256 blocks on or below the diagonal are written); a_sym / b_sym
+    declare operands given in that block-lower storage.  fp32 operands run
+    the FFMA kernel."""
     lib = load()
     batch, M, K = A.shape
     N = B.shape[2] if b_mn else B.shape[1]
@@ -322,13 +324,18 @@ def debug_gemm(A, B, A_lo=None, B_lo=None, split=1, b_mn=False, sym=False, a_sym
         out = torch.zeros(batch, M, N, dtype=torch.float32, device=A.device)
         lo = None
     else:
-        out = torch.zeros(batch, M, N, dtype=torch.bfloat16, device=A.device)
+        out = torch.zeros(batch, M, N, dtype=A.dtype, device=A.device)
         lo = torch.zeros_like(out)
     flags = int(sym) | (int(a_sym) << 1) | (int(b_sym) << 2)
+    code = FP16 if A.dtype == torch.float16 else _dtype_code(A.dtype)
     _check(lib.muon_debug_gemm(ptr(A), ptr(A_lo), ptr(B), ptr(B_lo), batch, M, N, K, split, int(b_mn), flags,
-                               _dtype_code(A.dtype), ptr(out), ptr(lo), ptr(workspace), workspace.numel(),
+                               code, ptr(out), ptr(lo), ptr(workspace), workspace.numel(),
                                ctypes.c_void_p(_stream_ptr(stream))))
-    return out if lo is None else out.float() + lo.float()
+    if lo is None:
+        return out
+    if A.dtype == torch.float16:
+        return out.float() + lo.float() / F16_LO_SCALE
+    return out.float() + lo.float()
 
 
 def profile_enable(on: bool = True) -> None:

@@ -4,11 +4,15 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace muon {
 
 constexpr int kMaxBatch = 256;     // matrices per launch (pointer tables travel as kernel parameters)
 constexpr int kStatusTimeout = 1;  // bit set in the workspace status word on a bounded-wait timeout
+// An fp16 pair stores v as hi = fp16(v), lo = fp16((v - hi) * kF16LoScale): the
+// power-of-two scale keeps the residual out of fp16's subnormal range.
+constexpr float kF16LoScale = 2048.f;
 
 typedef __nv_bfloat16 bf16;
 
@@ -20,24 +24,29 @@ enum FinalMode : int { FINAL_NONE = 0, FINAL_STORE = 1, FINAL_APPLY = 2 };
 //   v = sc_b * (c_acc * acc + c_res * R[b][r][c]) + (r == c && r < rows_valid ? c_id : 0)
 //   sc_b = 1, inv_norm[b] or inv_norm[b]^2 (scale_pow = 0, 1, 2)
 //
-// R is either fp32 (`R`, CUDA-core path) or a bf16 pair (`Rh` + `Rl`,
-// tensor-core path).  v is then stored into packed buffers -- fp32 `Of`
-// (CUDA-core path) or the bf16 pair `Oh` = bf16(v), `Ol` = bf16(v - Oh), which
-// carries ~16 significant bits (tensor-core path) -- or, in a final mode,
-// written (FINAL_STORE) or applied as W <- W - lr * v (FINAL_APPLY) to the
-// caller's un-packed matrix dst[b].  With `sym` set only the lower triangle is
-// computed and every stored element is also stored at its mirror position, so
-// the output is symmetric by construction.
+// R is either fp32 (`R`, CUDA-core path) or a 16-bit pair (`Rh` + `Rl`,
+// tensor-core path; `Rl` may be absent).  v is then stored into packed buffers
+// -- fp32 `Of` (CUDA-core path) or the 16-bit pair `Oh`, `Ol` (tensor-core
+// path; `Ol` may be absent) -- or, in a final mode, written (FINAL_STORE) or
+// applied as W <- W - lr * v (FINAL_APPLY) to the caller's un-packed matrix
+// dst[b].  A 16-bit pair is either bf16, hi = bf16(v) and lo = bf16(v - hi)
+// (about 16 significant bits), or fp16, hi = fp16(v) and lo = fp16((v - hi) *
+// kF16LoScale) (about 22 bits); `r_f16` / `o_f16` select fp16 for the residual
+// / the output.  On the CUDA-core path, `sym` computes the lower triangle and
+// mirrors each element; the tensor-core path stores symmetric outputs
+// block-lower.
 struct EpiParams {
   const float* inv_norm;  // [B] 1 / (||X||_F + eps)
   int scale_pow;
   float c_acc, c_res, c_id;
   const float* R;   // packed fp32 residual or nullptr (CUDA-core path)
   float* Of;        // packed fp32 output or nullptr (CUDA-core path)
-  const bf16* Rh;   // packed bf16 residual pair or nullptr (tensor-core path)
-  const bf16* Rl;
-  bf16* Oh;         // packed bf16 output pair (tensor-core path; written through TMA maps)
-  bf16* Ol;         // may be nullptr when only the head is needed
+  const void* Rh;   // packed 16-bit residual pair or nullptr (tensor-core path)
+  const void* Rl;
+  void* Oh;         // packed 16-bit output pair (tensor-core path; written through TMA maps)
+  void* Ol;         // may be nullptr when only the head is needed
+  int r_f16;        // 1: the residual pair is fp16, 0: bf16
+  int o_f16;        // 1: the output pair is fp16, 0: bf16
   long long ld;     // leading dimension (elements) of the packed residual / outputs
   long long bs;     // batch stride (elements)
   int sym;

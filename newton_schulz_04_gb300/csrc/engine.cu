@@ -89,12 +89,14 @@ struct ProfScope {
 
 static const float kQuintic[3] = {3.4445f, -4.7750f, 2.0315f};
 static const float kEps = 1e-7f;
-// ORIG: number of final NS steps whose A*A (resp. B*X) products use split
+// ORIG_BF16: number of final NS steps whose A*A (resp. B*X) products use split
 // operands.  The error of plain bf16 products comes from the last steps; an
 // fp32-exact CPU emulation over Gaussian inputs of aspect 1:1 to 1:3 gives a
 // worst relative error of 2.3e-2 with no splits, 1.04e-2 with both splits in
 // the last two steps, 0.97e-2 in the last three, and 1.3e-2 / 2.1e-2 with only
-// A*A / only B*X split.
+// A*A / only B*X split.  The ORIG schedule's fp16 operands (11 significant
+// bits) need no splits: the same emulation gives at most 1.8e-3 with X carried
+// as an fp16 pair, including rank-8 and row-scaled inputs.
 #ifndef MUON_SPLIT_A_STEPS
 #define MUON_SPLIT_A_STEPS 2
 #endif
@@ -137,7 +139,7 @@ static int bucket_plan(const std::vector<std::pair<long long, long long>>& shape
 // ------------------------------------------------------------------ schedules
 static muon_sched resolve(long long s, long long l, int steps, muon_dtype dt, muon_sched sc) {
   if (dt == MUON_FP32) {
-    if (sc == MUON_SCHED_ORIG) return MUON_SCHED_ORIG;
+    if (sc == MUON_SCHED_ORIG || sc == MUON_SCHED_ORIG_BF16) return MUON_SCHED_ORIG;  // one fp32 form
     if (sc == MUON_SCHED_AUTO) {
       // fp32 Gram costs 3 s^2 l + (4T - 3) s^3 vs T (3 s^2 l + s^3): never more, equal when square.
       return (l > s && steps > 0) ? MUON_SCHED_GRAM_X3 : MUON_SCHED_ORIG;
@@ -164,6 +166,27 @@ static muon_sched resolve(long long s, long long l, int steps, muon_dtype dt, mu
   (void)orig;
   (void)x3;
   return MUON_SCHED_ORIG;
+}
+
+// ORIG on bf16 data multiplies fp16 operands from step 1 on.  That is safe when
+// every iterate keeps its singular values <= 1.25: X0 has sigma <= 1 (Frobenius
+// normalisation), and the singular values of the next X are |p(sigma)|, so it
+// suffices that p(s) = a s + b s^3 + c s^5 maps [0, 1.25] into [-1.25, 1.25].
+// That is checked on a grid, widened by half a grid step times a bound on |p'|.
+// Then |A| <= 1.5625, and B = b A + c A^2 stays far inside fp16's range when
+// 1.5625 |b| + 2.4414 |c| <= 1e4.
+static bool f16_coefficients_safe(float a, float b, float c) {
+  const double A = std::fabs(a), B = std::fabs(b), C = std::fabs(c);
+  if (!(1.5625 * B + 2.44140625 * C <= 1e4)) return false;
+  const double dmax = A + 3.0 * B * 1.5625 + 5.0 * C * 2.44140625;  // |p'(s)| on [0, 1.25]
+  const int n = 5000;
+  const double h = 1.25 / n;
+  double pmax = 0.0;
+  for (int i = 0; i <= n; ++i) {
+    const double x = i * h, x2 = x * x;
+    pmax = std::max(pmax, std::fabs(x * (a + x2 * (b + x2 * c))));
+  }
+  return pmax + 0.5 * h * dmax <= 1.25;
 }
 
 // Bump allocator over the workspace; with base == nullptr it only measures.
@@ -230,8 +253,8 @@ static size_t carve_buffers(char* base, int Bc, long long sp, long long lp, int 
     }
     return c.off;
   }
-  if (sc == MUON_SCHED_ORIG) {
-    // X carried as a bf16 pair (head + residual, ~16 significant bits), ping-ponged
+  if (sc == MUON_SCHED_ORIG || sc == MUON_SCHED_ORIG_BF16) {
+    // X carried as a 16-bit pair (bf16 pair ~16 significant bits, fp16 pair ~22), ping-ponged
     for (int q = 0; q < 2; ++q) {
       bf.Xb[q] = static_cast<bf16*>(c.take(2 * nx));
       bf.Xlo[q] = static_cast<bf16*>(c.take(2 * nx));
@@ -322,6 +345,7 @@ struct Ctx {
   float beta, lr;
   bool apply;   // W <- W - lr O (else out = O)
   bool has_mom;
+  bool f16_ok;  // the coefficients allow ORIG's fp16 operands
 };
 
 #define CK(expr)                                                                                  \
@@ -354,7 +378,7 @@ static EpiParams epi_packed(const Group& g, const Buffers& bf, int scale_pow, fl
 
 // bf16-pair (tensor-core) epilogue: residual Rh + Rl and outputs Oh (+ Ol).
 static EpiParams epi_pair(const Group& g, const Buffers& bf, int scale_pow, float c_acc, float c_res, float c_id,
-                          const bf16* Rh, const bf16* Rl, bf16* Oh, bf16* Ol, long long ld, long long bs) {
+                          const void* Rh, const void* Rl, void* Oh, void* Ol, long long ld, long long bs) {
   EpiParams e = epi_packed(g, bf, scale_pow, c_acc, c_res, c_id, nullptr, nullptr, ld, bs);
   e.Rh = Rh;
   e.Rl = Rl;
@@ -403,7 +427,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   pa.Xf = bf.Xf;  // fp32 path, or zero steps
   if (!fp32 && cx.steps > 0) {
     pa.Xh = bf.Xb[0];
-    pa.Xl = g.sc == MUON_SCHED_ORIG ? bf.Xlo[0] : (x3 ? bf.Xl : nullptr);
+    pa.Xl = (g.sc == MUON_SCHED_ORIG || g.sc == MUON_SCHED_ORIG_BF16) ? bf.Xlo[0] : (x3 ? bf.Xl : nullptr);
   }
   for (int q = 0; q < Bc; ++q) {
     // a bucket can mix m x n and n x m members: the pack kernel transposes per member
@@ -511,8 +535,9 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
 
   // sym: bit 0 = symmetric output (lower tiles, block-lower storage); bits 1 / 2 =
   // A / B is a symmetric operand in that storage.
-  auto tc = [&](int split, int b_mn, int sym, int M, int N, int K, const bf16* Ah, const bf16* Al, long long lda,
-                long long bsa, const bf16* Bh, const bf16* Bl, long long ldb, long long bsb, const EpiParams& e) {
+  auto tc = [&](int split, int b_mn, int sym, int f16, int M, int N, int K, const void* Ah, const void* Al,
+                long long lda, long long bsa, const void* Bh, const void* Bl, long long ldb, long long bsb,
+                const EpiParams& e) {
     TcGemmDesc d;
     d.B = Bc;
     d.M = M;
@@ -523,6 +548,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     d.b_sym = (sym >> 2) & 1;
     d.split = split;
     d.b_mn = b_mn;
+    d.f16 = f16;
     d.A = TcOperand{Ah, Al, lda, bsa};
     d.Bop = TcOperand{Bh, Bl, ldb, bsb};
     const double Kt = K == S ? static_cast<double>(g.s) : static_cast<double>(g.l);
@@ -535,7 +561,39 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     return launch_tc_gemm(d, e, cx.status, cx.st, cx.sms, &why);
   };
 
-  if (g.sc == MUON_SCHED_ORIG) {
+  if (g.sc == MUON_SCHED_ORIG && cx.f16_ok) {
+    // Step 0 multiplies the packed bf16 copy of M (slot 0: hi, plus lo for
+    // the residual); A is stored as fp16, and B in the type of this step's X.
+    // From step 1 on, X lives in the ping-pong slots as an fp16 pair and
+    // every product takes fp16 operands.  Slot 0's bf16 copy is dead after
+    // step 0, so step 1 writes its fp16 X there.
+    int cur = 0;
+    for (int k = 0; k < T; ++k) {
+      const int nxt = cur ^ 1;
+      const int xf = k == 0 ? 0 : 1;  // 1: X (and so B) are fp16 this step
+      // A = X X^T (k = 0: X = M / s, so scale by inv_norm^2), fp16 out
+      EpiParams e1 = epi_pair(g, bf, k == 0 ? 2 : 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, nullptr, sp, bss);
+      e1.o_f16 = 1;
+      CK(tc(1, 0, 1, xf, S, S, L, bf.Xb[cur], nullptr, lp, bsx, bf.Xb[cur], nullptr, lp, bsx, e1));
+      // B = b A + c A^2 on fp16 operands
+      EpiParams e2 = epi_pair(g, bf, 0, cx.c, cx.b, 0.f, bf.Gh, nullptr, bf.Bh, nullptr, sp, bss);
+      e2.r_f16 = 1;
+      e2.o_f16 = xf;
+      CK(tc(1, 0, 7, 1, S, S, S, bf.Gh, nullptr, sp, bss, bf.Gh, nullptr, sp, bss, e2));
+      // X <- a X + B X (k = 0: both terms carry 1 / s), fp16 pair out
+      EpiParams e3 = epi_pair(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, bf.Xb[cur], bf.Xlo[cur], bf.Xb[nxt],
+                              bf.Xlo[nxt], lp, bsx);
+      e3.r_f16 = xf;
+      e3.o_f16 = 1;
+      e3.cols_valid = static_cast<int>(g.l);
+      if (k == T - 1) epi_set_final(e3, cx, g, mats, Bc);
+      CK(tc(1, 1, 2, xf, S, L, S, bf.Bh, nullptr, sp, bss, bf.Xb[cur], nullptr, lp, bsx, e3));
+      cur = nxt;
+    }
+    return MUON_OK;
+  }
+
+  if (g.sc == MUON_SCHED_ORIG || g.sc == MUON_SCHED_ORIG_BF16) {
     // Operand splits (see kSplitA / kSplitB): plain bf16 products miss a 2e-2
     // relative error on Gaussian inputs of aspect >= 1:2, mostly through the
     // rounding of the last steps, where sigma ~ 1 and the b, c terms are large.
@@ -546,17 +604,17 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
       const int nxt = cur ^ 1;
       // A = X X^T (k = 0: X = M / s, so scale by inv_norm^2)
       EpiParams e1 = epi_pair(g, bf, k == 0 ? 2 : 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, bf.Gl, sp, bss);
-      CK(tc(1, 0, 1, S, S, L, bf.Xb[cur], nullptr, lp, bsx, bf.Xb[cur], nullptr, lp, bsx, e1));
+      CK(tc(1, 0, 1, 0, S, S, L, bf.Xb[cur], nullptr, lp, bsx, bf.Xb[cur], nullptr, lp, bsx, e1));
       // B = b A + c A^2 with A = Ah + Al in the epilogue
       EpiParams e2 =
           epi_pair(g, bf, 0, cx.c, cx.b, 0.f, bf.Gh, bf.Gl, bf.Bh, split ? bf.Bl : nullptr, sp, bss);
-      CK(tc(split_a ? 3 : 1, 0, 7, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, e2));
+      CK(tc(split_a ? 3 : 1, 0, 7, 0, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, e2));
       // X <- a X + B X (k = 0: both terms carry 1 / s); X kept as a bf16 pair
       EpiParams e3 = epi_pair(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, bf.Xb[cur], bf.Xlo[cur], bf.Xb[nxt],
                               bf.Xlo[nxt], lp, bsx);
       e3.cols_valid = static_cast<int>(g.l);
       if (k == T - 1) epi_set_final(e3, cx, g, mats, Bc);
-      CK(tc(split ? 2 : 1, 1, 2, S, L, S, bf.Bh, bf.Bl, sp, bss, bf.Xb[cur], nullptr, lp, bsx, e3));
+      CK(tc(split ? 2 : 1, 1, 2, 0, S, L, S, bf.Bh, bf.Bl, sp, bss, bf.Xb[cur], nullptr, lp, bsx, e3));
       cur = nxt;
     }
     return MUON_OK;
@@ -565,7 +623,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   // Gram space (split 3 or 1)
   const int sp3 = x3 ? 3 : 1;
   EpiParams e0 = epi_pair(g, bf, 2, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, bf.Gl, sp, bss);
-  CK(tc(sp3, 0, 1, S, S, L, bf.Xb[0], bf.Xl, lp, bsx, bf.Xb[0], bf.Xl, lp, bsx, e0));
+  CK(tc(sp3, 0, 1, 0, S, S, L, bf.Xb[0], bf.Xl, lp, bsx, bf.Xb[0], bf.Xl, lp, bsx, e0));
   const bf16* Qh = nullptr;
   const bf16* Ql = nullptr;
   int qi = 0;
@@ -574,7 +632,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     bf16* Pl = bf.Pl[k & 1];
     // P = a I + b G + c G^2
     EpiParams ep = epi_pair(g, bf, 0, cx.c, cx.b, cx.a, bf.Gh, bf.Gl, Ph, Pl, sp, bss);
-    CK(tc(sp3, 0, 7, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, ep));
+    CK(tc(sp3, 0, 7, 0, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, ep));
     if (k == 0) {
       Qh = Ph;
       Ql = Pl;
@@ -583,28 +641,28 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
       bf16* Qnl = bf.Ql[qi];
       qi ^= 1;
       EpiParams eq = epi_pair(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, Qnh, Qnl, sp, bss);
-      CK(tc(sp3, 0, 7, S, S, S, Ph, Pl, sp, bss, Qh, Ql, sp, bss, eq));
+      CK(tc(sp3, 0, 7, 0, S, S, S, Ph, Pl, sp, bss, Qh, Ql, sp, bss, eq));
       Qh = Qnh;
       Ql = Qnl;
     }
     if (k + 1 < T) {
       EpiParams eh = epi_pair(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Hh, bf.Hl, sp, bss);
-      CK(tc(sp3, 0, 7, S, S, S, Ph, Pl, sp, bss, bf.Gh, bf.Gl, sp, bss, eh));
+      CK(tc(sp3, 0, 7, 0, S, S, S, Ph, Pl, sp, bss, bf.Gh, bf.Gl, sp, bss, eh));
       EpiParams eg = epi_pair(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, bf.Gl, sp, bss);
-      CK(tc(sp3, 0, 7, S, S, S, Ph, Pl, sp, bss, bf.Hh, bf.Hl, sp, bss, eg));
+      CK(tc(sp3, 0, 7, 0, S, S, S, Ph, Pl, sp, bss, bf.Hh, bf.Hl, sp, bss, eg));
     }
   }
   // O = Q X0 = Q X / s
   EpiParams ef = epi_pair(g, bf, 1, 1.f, 0.f, 0.f, nullptr, nullptr, nullptr, nullptr, lp, bsx);
   epi_set_final(ef, cx, g, mats, Bc);
-  CK(tc(sp3, 1, 2, S, L, S, Qh, Ql, sp, bss, bf.Xb[0], bf.Xl, lp, bsx, ef));
+  CK(tc(sp3, 1, 2, 0, S, L, S, Qh, Ql, sp, bss, bf.Xb[0], bf.Xl, lp, bsx, ef));
   return MUON_OK;
 }
 #undef CK
 
 // ------------------------------------------------------------------ validation
 static bool valid_dt(int dt) { return dt == MUON_BF16 || dt == MUON_FP32; }
-static bool valid_sc(int sc) { return sc >= MUON_SCHED_AUTO && sc <= MUON_SCHED_ORIG; }
+static bool valid_sc(int sc) { return sc >= MUON_SCHED_AUTO && sc <= MUON_SCHED_ORIG_BF16; }
 
 static muon_status check_common(int steps, const float* coeffs, int dt, int sc, void* ws, size_t ws_bytes) {
   if (steps < 0 || steps > MUON_MAX_STEPS) return fail(MUON_ERR_ARG, "steps=%d out of [0, %d]", steps, MUON_MAX_STEPS);
@@ -658,6 +716,7 @@ static muon_status run_all(std::vector<Mat>& mats, int steps, const float* coeff
   cx.lr = lr;
   cx.apply = apply;
   cx.has_mom = has_mom;
+  cx.f16_ok = f16_coefficients_safe(cx.a, cx.b, cx.c);
   std::vector<Mat> chunk;
   for (int gi = 0; gi < groups; ++gi) {
     const int n = start[gi + 1] - start[gi];
@@ -705,14 +764,18 @@ static double estimate_seconds(long long m, long long n, int steps, muon_dtype d
     return t;
   }
   const double sym_out = sym_tiles * 256.0 * 256.0 * ssz;  // a block-lower s x s output
-  if (g.sc == MUON_SCHED_ORIG) {
+  if (g.sc == MUON_SCHED_ORIG || g.sc == MUON_SCHED_ORIG_BF16) {
+    // ORIG on bf16 data: fp16 operands, no splits, A and B single 16-bit values
+    // (the default coefficients pass the fp16 range check)
+    const bool h16 = !fp32 && g.sc == MUON_SCHED_ORIG;
+    const double sym1 = h16 ? sym_out / 2 : sym_out;
     for (int k = 0; k < steps; ++k) {
-      const double fa = (!fp32 && k >= steps - kSplitA) ? 3.0 : 1.0;
-      const double fb = (!fp32 && k >= steps - kSplitB) ? 2.0 : 1.0;
-      launch(sym_tiles * tile * L, S * L * (fp32 ? 4.0 : 2.0) + sym_out);
-      launch(fa * sym_tiles * tile * S, 2.0 * sym_out);
+      const double fa = (!fp32 && !h16 && k >= steps - kSplitA) ? 3.0 : 1.0;
+      const double fb = (!fp32 && !h16 && k >= steps - kSplitB) ? 2.0 : 1.0;
+      launch(sym_tiles * tile * L, S * L * (fp32 ? 4.0 : 2.0) + sym1);
+      launch(fa * sym_tiles * tile * S, 2.0 * sym1);
       const double out = k == steps - 1 ? apply : S * L * ssz;
-      launch(fb * rect_tiles * tile * S, sym_out + S * L * (fp32 ? 8.0 : 6.0) + out);
+      launch(fb * rect_tiles * tile * S, sym1 + S * L * (fp32 ? 8.0 : 6.0) + out);
     }
     return t;
   }
@@ -906,8 +969,9 @@ muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, cons
   if (dt == MUON_FP32) {
     e.Of = static_cast<float*>(out);
   } else {
-    e.Oh = static_cast<bf16*>(out);
-    e.Ol = static_cast<bf16*>(out_lo);
+    e.Oh = out;
+    e.Ol = out_lo;
+    e.o_f16 = dt == MUON_FP16 ? 1 : 0;
   }
   e.ld = N;
   e.bs = static_cast<long long>(M) * N;
@@ -916,14 +980,14 @@ muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, cons
   const long long bsb = static_cast<long long>(N) * K;
   cudaError_t err;
   const char* why = nullptr;
-  if (dt == MUON_BF16) {
-    if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 256 || K % 128) return fail(MUON_ERR_SHAPE, "bf16 sizes");
+  if (dt == MUON_BF16 || dt == MUON_FP16) {
+    if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 256 || K % 128) return fail(MUON_ERR_SHAPE, "16-bit sizes");
     if (split < 1 || split > 3) return fail(MUON_ERR_ARG, "split must be 1, 2 or 3");
     if (split >= 2 && !A_lo) return fail(MUON_ERR_ARG, "split 2 and 3 need A_lo");
     if (split == 3 && !B_lo) return fail(MUON_ERR_ARG, "split 3 needs B_lo");
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(A_lo) |
          reinterpret_cast<uintptr_t>(B_lo)) % 16)
-      return fail(MUON_ERR_ALIGN, "bf16 operands must be 16-byte aligned");
+      return fail(MUON_ERR_ALIGN, "16-bit operands must be 16-byte aligned");
     int major = 0, minor = 0;
     muon_status ds;
     const int sms = device_sms(&major, &minor, &ds);
@@ -939,8 +1003,9 @@ muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, cons
     d.b_sym = (sym >> 2) & 1;
     d.split = split;
     d.b_mn = b_mn;
-    d.A = TcOperand{static_cast<const bf16*>(A), static_cast<const bf16*>(A_lo), K, static_cast<long long>(M) * K};
-    d.Bop = TcOperand{static_cast<const bf16*>(B), static_cast<const bf16*>(B_lo), b_mn ? N : K, bsb};
+    d.f16 = dt == MUON_FP16 ? 1 : 0;
+    d.A = TcOperand{A, A_lo, K, static_cast<long long>(M) * K};
+    d.Bop = TcOperand{B, B_lo, b_mn ? N : K, bsb};
     err = launch_tc_gemm(d, e, static_cast<int*>(ws), static_cast<cudaStream_t>(stream), sms, &why);
     if (err == cudaErrorInvalidValue && why) return fail(MUON_ERR_ARG, "%s", why);
   } else if (dt == MUON_FP32) {

@@ -28,11 +28,12 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// A bf16 operand of the tensor-core GEMM: [batch][rows][ld] row-major, with an
-// optional residual part `lo` of the same layout (split operands).
+// A 16-bit operand of the tensor-core GEMM (bf16, or fp16 with TcGemmDesc::f16):
+// [batch][rows][ld] row-major, with an optional residual part `lo` of the same
+// layout (split operands).
 struct TcOperand {
-  const bf16* hi;
-  const bf16* lo;
+  const void* hi;
+  const void* lo;
   long long ld;  // row stride (elements)
   long long bs;  // batch stride (elements)
 };
@@ -47,8 +48,9 @@ struct TcGemmDesc {
   int B, M, N, K;  // M % 256 == 0, N % 256 == 0, K % 128 == 0 (K % 256 == 0 with symmetric operands)
   int sym;
   int a_sym, b_sym;
-  int split;  // 1 or 3
+  int split;  // 1, 2 or 3
   int b_mn;
+  int f16;    // 1: both operands are fp16, 0: both bf16 (one tcgen05 kind::f16 MMA takes one type)
   TcOperand A, Bop;
 };
 

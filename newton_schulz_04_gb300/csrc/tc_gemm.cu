@@ -1,4 +1,4 @@
-// tc_gemm.cu -- batched bf16 tensor-core GEMM / SYRK for sm_103a (tcgen05 + TMEM + TMA).
+// tc_gemm.cu -- batched bf16 / fp16 tensor-core GEMM / SYRK for sm_103a (tcgen05 + TMEM + TMA).
 //
 // One persistent CTA per SM walks a list of 128 x 256 output tiles spread over a
 // batch of same-shape matrices (DMuon technical summary, §2.2: same-shape
@@ -20,8 +20,9 @@
 //               double-buffered in TMEM (2 x 256 fp32 columns) so the epilogue of
 //               one tile overlaps the main loop of the next
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, fused arithmetic
-//               (EpiParams), then 32 x 32 bf16 boxes staged in shared memory and
-//               written with TMA bulk-tensor stores
+//               (EpiParams), then 32 x 32 boxes of 16-bit values (bf16 or fp16
+//               pairs) staged in shared memory and written with TMA bulk-tensor
+//               stores
 //
 // Split operands.  A value X carried as a bf16 head Xh and a bf16 residual Xl
 // (X ~ Xh + Xl to ~16 significant bits) is multiplied as a sum of plain bf16
@@ -106,6 +107,7 @@ struct TcArgs {
   int b_sym;      // same for B (K-major kernels only)
   int seg_lo;     // bit 2s: segment s reads A's residual map; bit 2s+1: B's residual map
   int final_vec;  // final mode may use 16-byte accesses to the caller's rows
+  int f16;        // operands are fp16 (else bf16)
   int* status;    // workspace status word
   EpiParams epi;
 };
@@ -151,13 +153,33 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Split 32 values into packed bf16x2 words: head hw = bf16(v), residual lw = bf16(v - head).
+__device__ __forceinline__ uint32_t pack2_h(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);  // a in the low half
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unpack2_h(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+// Split 32 values into packed 16-bit pairs: bf16 head hw = bf16(v), residual
+// lw = bf16(v - head); or fp16 head hw = fp16(v), residual lw = fp16((v - head) * kF16LoScale).
 __device__ __forceinline__ void split_words(const float (&v)[32], uint32_t (&hw)[16], uint32_t (&lw)[16],
-                                            bool want_lo) {
+                                            bool want_lo, bool f16) {
+  if (f16) {
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    hw[k] = pack2(v[2 * k], v[2 * k + 1]);
-    if (want_lo) lw[k] = pack2(v[2 * k] - bf_lo(hw[k]), v[2 * k + 1] - bf_hi(hw[k]));
+    for (int k = 0; k < 16; ++k) {
+      hw[k] = pack2_h(v[2 * k], v[2 * k + 1]);
+      if (want_lo) {
+        const float2 h = unpack2_h(hw[k]);
+        lw[k] = pack2_h((v[2 * k] - h.x) * kF16LoScale, (v[2 * k + 1] - h.y) * kF16LoScale);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      hw[k] = pack2(v[2 * k], v[2 * k + 1]);
+      if (want_lo) lw[k] = pack2(v[2 * k] - bf_lo(hw[k]), v[2 * k + 1] - bf_hi(hw[k]));
+    }
   }
 }
 
@@ -385,7 +407,8 @@ __global__ void __launch_bounds__(192, 1)
           const int k0 = (kb % nk) * C::BK;
           const bool a_mn = args.a_sym && (k0 >> 8) > (m0 >> 8);
           const bool b_mn = BMN || (args.b_sym && (k0 >> 8) > (n0 >> 8));
-          const uint32_t idesc = make_idesc_bf16(2 * C::BM, C::BN, b_mn) | (a_mn ? (1u << 15) : 0u);
+          const uint32_t idesc =
+              make_idesc_f16kind(2 * C::BM, C::BN, b_mn, args.f16 == 0) | (a_mn ? (1u << 15) : 0u);
           const uint32_t a0 = smem_u32(tiles + s * C::STAGE);
           const uint32_t b0 = a0 + C::A_TILE;
 #pragma unroll
@@ -505,12 +528,23 @@ __global__ void __launch_bounds__(192, 1)
           r_used = idx + 1;
           __syncwarp();
           if (cc + C::RIN_BUFS < nch) issue_r(c0 + 32 * C::RIN_BUFS, r0, b);  // the buffer just read is free
+          if (e.r_f16) {
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const float x0 = bf_lo(rhw[u]) + bf_lo(rlw[u]);
-            const float x1 = bf_hi(rhw[u]) + bf_hi(rlw[u]);
-            v[2 * u] = sc * (e.c_acc * v[2 * u] + e.c_res * x0);
-            v[2 * u + 1] = sc * (e.c_acc * v[2 * u + 1] + e.c_res * x1);
+            for (int u = 0; u < 16; ++u) {
+              const float2 h = unpack2_h(rhw[u]), l = unpack2_h(rlw[u]);  // rlw = 0 without a residual part
+              const float x0 = h.x + l.x * (1.f / kF16LoScale);
+              const float x1 = h.y + l.y * (1.f / kF16LoScale);
+              v[2 * u] = sc * (e.c_acc * v[2 * u] + e.c_res * x0);
+              v[2 * u + 1] = sc * (e.c_acc * v[2 * u + 1] + e.c_res * x1);
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const float x0 = bf_lo(rhw[u]) + bf_lo(rlw[u]);
+              const float x1 = bf_hi(rhw[u]) + bf_hi(rlw[u]);
+              v[2 * u] = sc * (e.c_acc * v[2 * u] + e.c_res * x0);
+              v[2 * u + 1] = sc * (e.c_acc * v[2 * u + 1] + e.c_res * x1);
+            }
           }
         } else {
           const float f = sc * e.c_acc;
@@ -534,7 +568,7 @@ __global__ void __launch_bounds__(192, 1)
           continue;
         }
         uint32_t hw[16], lw[16];
-        split_words(v, hw, lw, has_lo);
+        split_words(v, hw, lw, has_lo, e.o_f16 != 0);
         sb = stg + (cc % C::OUT_BUFS) * 2 * C::BOX;
         if (lane == 0) bulk_wait_read<C::OUT_BUFS - 1>();  // earlier stores from this buffer have read it
         __syncwarp();
@@ -595,8 +629,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 3-D bf16 map over [B][rows][inner] with box {box_inner, box_rows, 1}.
-static bool make_map(CUtensorMap* m, const bf16* base, uint64_t inner, uint64_t rows, uint64_t batch,
+// 3-D map of 16-bit elements (bf16, or fp16 with f16) over [B][rows][inner]
+// with box {box_inner, box_rows, 1}.
+static bool make_map(CUtensorMap* m, const void* base, bool f16, uint64_t inner, uint64_t rows, uint64_t batch,
                      long long ld, long long bs, uint32_t box_inner, uint32_t box_rows, int swb) {
   auto enc = get_encode();
   if (!enc) return false;
@@ -604,7 +639,8 @@ static bool make_map(CUtensorMap* m, const bf16* base, uint64_t inner, uint64_t 
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(bs) * 2};
   const cuuint32_t box[3] = {box_inner, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<bf16*>(base), dims, strides, box, estr,
+  const CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                         const_cast<void*>(base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE,
                          swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -690,51 +726,54 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
     if (e != cudaSuccess) return e;
   }
   CUtensorMap mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl;
-  const bf16* alo = d.A.lo ? d.A.lo : d.A.hi;
-  const bf16* blo = d.Bop.lo ? d.Bop.lo : d.Bop.hi;
+  const void* alo = d.A.lo ? d.A.lo : d.A.hi;
+  const void* blo = d.Bop.lo ? d.Bop.lo : d.Bop.hi;
+  const bool f = d.f16 != 0;
   // K-major boxes {64 k, rows}; transposed boxes {64 mn, 64 k} (symmetric operands: K == rows)
-  bool ok = make_map(&mA, d.A.hi, d.K, d.M, d.B, d.A.ld, d.A.bs, C::KA, C::BM, 128);
-  ok = ok && make_map(&mAl, alo, d.K, d.M, d.B, d.A.ld, d.A.bs, C::KA, C::BM, 128);
-  ok = ok && make_map(&mAt, d.A.hi, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
-  ok = ok && make_map(&mAtl, alo, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
+  bool ok = make_map(&mA, d.A.hi, f, d.K, d.M, d.B, d.A.ld, d.A.bs, C::KA, C::BM, 128);
+  ok = ok && make_map(&mAl, alo, f, d.K, d.M, d.B, d.A.ld, d.A.bs, C::KA, C::BM, 128);
+  ok = ok && make_map(&mAt, d.A.hi, f, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
+  ok = ok && make_map(&mAtl, alo, f, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
   if (!BMN) {
-    ok = ok && make_map(&mB, d.Bop.hi, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::KA, C::BNH, 128);
-    ok = ok && make_map(&mBl, blo, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::KA, C::BNH, 128);
-    ok = ok && make_map(&mBt, d.Bop.hi, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
-    ok = ok && make_map(&mBtl, blo, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
+    ok = ok && make_map(&mB, d.Bop.hi, f, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::KA, C::BNH, 128);
+    ok = ok && make_map(&mBl, blo, f, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::KA, C::BNH, 128);
+    ok = ok && make_map(&mBt, d.Bop.hi, f, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
+    ok = ok && make_map(&mBtl, blo, f, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
   } else {
-    ok = ok && make_map(&mB, d.Bop.hi, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
-    ok = ok && make_map(&mBl, blo, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
+    ok = ok && make_map(&mB, d.Bop.hi, f, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
+    ok = ok && make_map(&mBl, blo, f, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
     mBt = mB;
     mBtl = mBl;
   }
-  // Output maps: 32 x 32 bf16 boxes with the 64-byte swizzle (dummies in final mode).
+  // Output maps: 32 x 32 boxes of 16-bit values with the 64-byte swizzle (dummies in final mode).
   CUtensorMap mOh, mOl;
   const bool has_out = epi.Oh != nullptr;
-  const bf16* oh = has_out ? epi.Oh : d.A.hi;
-  const bf16* ol = epi.Ol ? epi.Ol : oh;
+  const bool of = has_out ? epi.o_f16 != 0 : f;
+  const void* oh = has_out ? epi.Oh : d.A.hi;
+  const void* ol = epi.Ol ? epi.Ol : oh;
   const long long old_ = has_out ? epi.ld : d.A.ld;
   const long long obs = has_out ? epi.bs : d.A.bs;
   const uint64_t ocols = has_out ? static_cast<uint64_t>(epi.ld) : static_cast<uint64_t>(d.K);
   const uint64_t orows = static_cast<uint64_t>(d.M);
-  ok = ok && make_map(&mOh, oh, ocols, orows, d.B, old_, obs, 32, 32, 64);
-  ok = ok && make_map(&mOl, ol, ocols, orows, d.B, old_, obs, 32, 32, 64);
+  ok = ok && make_map(&mOh, oh, of, ocols, orows, d.B, old_, obs, 32, 32, 64);
+  ok = ok && make_map(&mOl, ol, of, ocols, orows, d.B, old_, obs, 32, 32, 64);
   // Residual maps (same box and swizzle as the outputs; dummies without a residual).
   CUtensorMap mRh, mRl;
   const bool has_r = epi.Rh != nullptr;
-  const bf16* rh = has_r ? epi.Rh : oh;
-  const bf16* rl = epi.Rl ? epi.Rl : rh;
+  const bool rf = has_r ? epi.r_f16 != 0 : of;
+  const void* rh = has_r ? epi.Rh : oh;
+  const void* rl = epi.Rl ? epi.Rl : rh;
   const long long rld = has_r ? epi.ld : old_;
   const long long rbs = has_r ? epi.bs : obs;
   const uint64_t rcols = has_r ? static_cast<uint64_t>(epi.ld) : ocols;
-  ok = ok && make_map(&mRh, rh, rcols, orows, d.B, rld, rbs, 32, 32, 64);
-  ok = ok && make_map(&mRl, rl, rcols, orows, d.B, rld, rbs, 32, 32, 64);
+  ok = ok && make_map(&mRh, rh, rf, rcols, orows, d.B, rld, rbs, 32, 32, 64);
+  ok = ok && make_map(&mRl, rl, rf, rcols, orows, d.B, rld, rbs, 32, 32, 64);
   if (!ok) {
     *why = "cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
   }
   if (epi.final_mode == FINAL_NONE && !has_out) {
-    *why = "tensor-core epilogue needs a bf16 output pair";
+    *why = "tensor-core epilogue needs a 16-bit output pair";
     return cudaErrorInvalidValue;
   }
   TcArgs a;
@@ -764,6 +803,7 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
   }
   a.a_sym = d.a_sym;
   a.b_sym = BMN ? 0 : d.b_sym;
+  a.f16 = d.f16 ? 1 : 0;
   a.status = status;
   a.epi = epi;
   a.epi.sym = d.sym;

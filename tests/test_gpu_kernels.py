@@ -169,6 +169,67 @@ def test_tc_sym_split3_symmetric_operands():
     assert _rel(out[:, mask], ref[:, mask]) < 4e-5
 
 
+# ---- fp16 operands (the original-space schedule's steps after the first)
+
+@pytest.mark.parametrize("b_mn", [False, True])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (512, 768, 1024)])
+def test_tc_gemm_fp16_operands(M, N, K, b_mn):
+    m = _lib()
+    A = _rand((2, M, K), 31, torch.float16)
+    B = _rand((2, K, N) if b_mn else (2, N, K), 32, torch.float16)
+    out = m.debug_gemm(A, B, b_mn=b_mn)
+    torch.cuda.synchronize()
+    ref = _ref(A.double(), B.double(), b_mn).float()
+    # exact fp16 operands, fp32 accumulation, a ~22-bit fp16 output pair
+    assert _rel(out, ref) < 2e-5
+    # the same bits read as bf16 would give a different product: the type is honoured
+    wrong = _ref(A.view(torch.bfloat16).double(), B.view(torch.bfloat16).double(), b_mn).float()
+    assert _rel(wrong, ref) > 0.5
+
+
+def test_tc_fp16_output_pair_residual_is_scaled():
+    # out + lo / 2^11 reconstructs the fp32 accumulator to ~22 bits; the head
+    # alone is only fp16-accurate
+    m = _lib()
+    A = _rand((1, 256, 256), 33, torch.float16)
+    B = _rand((1, 256, 256), 34, torch.float16)
+    ref = _ref(A.double(), B.double(), False).float()
+    lib = m.load()
+    import ctypes
+    out = torch.zeros(1, 256, 256, dtype=torch.float16, device="cuda")
+    lo = torch.zeros_like(out)
+    ws = m.new_workspace(4096)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    st = lib.muon_debug_gemm(p(A), None, p(B), None, 1, 256, 256, 256, 1, 0, 0, 2, p(out), p(lo), p(ws),
+                             ws.numel(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    head = _rel(out.float(), ref)
+    full = _rel(out.float() + lo.float() / 2048.0, ref)
+    assert 1e-4 < head < 1e-3        # fp16 rounding, 2^-12 relative on average
+    assert full < 2e-6
+    # the stored residual is scaled up, so it sits well above fp16's subnormals
+    assert lo.abs().max().item() > 2 ** -14
+
+
+def test_tc_fp16_symmetric_operands_in_block_lower_storage():
+    m = _lib()
+    g = torch.Generator().manual_seed(35)
+    S = 768
+    X = torch.randn(2, S, S, generator=g, dtype=torch.float64)
+    Gs = (X @ X.transpose(1, 2)) / S
+    mask = block_lower(S, "cpu")
+    Gh = Gs.to(torch.float16).cuda()
+    Gst = Gh.clone()
+    Gst[:, ~mask.cuda()] = float("nan")
+    out = m.debug_gemm(Gst, Gst, sym=True, a_sym=True, b_sym=True)
+    torch.cuda.synchronize()
+    ref = _ref(Gh.double(), Gh.double(), False).float()
+    mk = mask.cuda()
+    assert torch.isfinite(out[:, mk]).all()
+    assert _rel(out[:, mk], ref[:, mk]) < 2e-5
+
+
 @pytest.mark.parametrize("M,N,K,b_mn,sym", [(128, 128, 16, False, False), (256, 384, 80, True, False),
                                              (384, 384, 48, False, True)])
 def test_simt_gemm(M, N, K, b_mn, sym):

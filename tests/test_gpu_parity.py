@@ -46,7 +46,7 @@ def oracle_O(x, steps=5, coeffs=oracle.QUINTIC):
 SHAPES_BF16 = [(256, 512), (512, 256), (200, 328), (328, 200), (256, 256), (130, 1000)]
 
 
-@pytest.mark.parametrize("sched", ["orig", "gram_x3"])
+@pytest.mark.parametrize("sched", ["orig", "orig_bf16", "gram_x3"])
 @pytest.mark.parametrize("shape", SHAPES_BF16)
 def test_ns_batched_bf16(sched, shape):
     m = _m()
@@ -67,12 +67,55 @@ def test_ill_conditioned_low_rank_bf16(shape):
     # accumulation precision: its error here is bounded, not held to 2e-2.
     m = _m()
     X = torch.stack([synth.low_rank(*shape, 8, 1e-4, seed=60 + i) for i in range(2)]).to(torch.bfloat16).cuda()
-    for sched, tol in [("auto", TOL_BF16), ("orig", TOL_BF16), ("gram_x3", 0.1)]:
+    for sched, tol in [("auto", TOL_BF16), ("orig", TOL_BF16), ("orig_bf16", TOL_BF16), ("gram_x3", 0.1)]:
         O = m.ns_batched(X, steps=5, schedule=sched)
         torch.cuda.synchronize()
         for i in range(2):
             e = rel(O[i].float().cpu(), oracle_O(X[i]))
             assert e < tol, (sched, shape, i, e)
+
+
+def _inputs_of_every_kind():
+    yield "gaussian 256x768", synth.random_matrix(256, 768, seed=41)
+    yield "gaussian 512x512", synth.random_matrix(512, 512, seed=42)
+    yield "rank-8 768x3072", synth.low_rank(768, 3072, 8, 1e-4, seed=60)
+    x = synth.random_matrix(512, 2048, seed=43)
+    x[0] *= 100
+    yield "row-scaled 512x2048", x
+
+
+def test_orig_fp16_operands_keep_a_wide_margin():
+    """ORIG multiplies fp16 operands after step 0 and carries X as an fp16 pair.
+    A CPU emulation puts its error at <= 1.8e-3 on these inputs.  The bf16 split
+    schedule reaches ~1e-2, so ORIG must stay well inside 2e-2."""
+    m = _m()
+    for name, x in _inputs_of_every_kind():
+        X = x[None].to(torch.bfloat16).cuda()
+        ref = oracle_O(X[0])
+        e16 = rel(m.ns_batched(X, steps=5, schedule="orig")[0].float().cpu(), ref)
+        ebf = rel(m.ns_batched(X, steps=5, schedule="orig_bf16")[0].float().cpu(), ref)
+        assert e16 < 5e-3, (name, e16)
+        assert ebf < TOL_BF16, (name, ebf)
+
+
+def test_coefficients_outside_the_fp16_range_run_the_bf16_schedule():
+    """The quintic scaled by 1.05 peaks at 1.26 on [0, 1.25] (over the fp16
+    check's 1.25) but its iterates stay bounded.  ORIG must then run the
+    bf16 split schedule, bit-identical to ORIG_BF16.  Its steeper slopes
+    amplify bf16 rounding beyond the quintic's (2.7e-2 measured, against
+    about 1e-2 for the quintic), so the bound here is 4e-2."""
+    m = _m()
+    co = tuple(1.05 * c for c in oracle.QUINTIC)
+    X = torch.stack([synth.random_matrix(256, 512, seed=44 + i) for i in range(2)]).to(torch.bfloat16).cuda()
+    a = m.ns_batched(X, steps=5, coeffs=co, schedule="orig")
+    b = m.ns_batched(X, steps=5, coeffs=co, schedule="orig_bf16")
+    q = m.ns_batched(X, steps=5, schedule="orig")
+    qb = m.ns_batched(X, steps=5, schedule="orig_bf16")
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert not torch.equal(q, qb)  # the quintic itself takes the fp16 operands
+    for i in range(2):
+        assert rel(a[i].float().cpu(), oracle_O(X[i], 5, co)) < 4e-2
 
 
 def test_gram_x1_fast_mode_error_is_bounded_and_larger():
@@ -225,7 +268,7 @@ def test_custom_coefficients_cubic():
 def test_determinism_bitwise():
     m = _m()
     X = torch.stack([synth.random_matrix(512, 1024, seed=97 + i) for i in range(3)]).to(torch.bfloat16).cuda()
-    for sched in ["orig", "gram_x3"]:
+    for sched in ["orig", "orig_bf16", "gram_x3"]:
         a = m.ns_batched(X, steps=5, schedule=sched)
         b = m.ns_batched(X, steps=5, schedule=sched)
         torch.cuda.synchronize()

@@ -180,7 +180,7 @@ def test_cost_estimate_properties():
     f32 = m.cost_estimate([(4096, 4096)], dtype=__import__("torch").float32)
     assert f32[0] > 10 * c[0]                # FFMA vs tensor cores
     zero = m.cost_estimate([(4096, 4096)], steps=0)
-    assert zero[0] < c[0] / 20               # pack + apply only (~370 MB of traffic)
+    assert zero[0] < c[0] / 12               # pack + apply only (~370 MB of traffic)
     with pytest.raises(m.MuonError):
         m.cost_estimate([(0, 16)])
     assert m.cost_estimate([]) == []
