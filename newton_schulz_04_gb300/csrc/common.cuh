@@ -21,7 +21,7 @@ enum FinalMode : int { FINAL_NONE = 0, FINAL_STORE = 1, FINAL_APPLY = 2 };
 // How a GEMM turns its fp32 accumulator into outputs.  For output element (r, c)
 // of matrix b (r, c in the packed, short-side-first orientation):
 //
-//   v = sc_b * (c_acc * acc + c_res * R[b][r][c]) + (r == c && r < rows_valid ? c_id : 0)
+//   v = sc_b * (c_acc * acc + c_res * r_scale * R[b][r][c]) + (r == c && r < rows_valid ? c_id : 0)
 //   sc_b = 1, inv_norm[b] or inv_norm[b]^2 (scale_pow = 0, 1, 2)
 //
 // R is either fp32 (`R`, CUDA-core path) or a 16-bit pair (`Rh` + `Rl`,
@@ -46,6 +46,7 @@ struct EpiParams {
   void* Oh;         // packed 16-bit output pair (tensor-core path; written through TMA maps)
   void* Ol;         // may be nullptr when only the head is needed
   int r_f16;        // 1: the residual pair is fp16, 0: bf16
+  float r_scale;    // multiplies the residual (tensor-core path; e.g. 2^-11 when Rh is the scaled low part of an fp16 pair)
   int o_f16;        // 1: the output pair is fp16, 0: bf16
   long long ld;     // leading dimension (elements) of the packed residual / outputs
   long long bs;     // batch stride (elements)

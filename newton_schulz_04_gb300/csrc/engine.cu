@@ -368,6 +368,7 @@ static EpiParams epi_packed(const Group& g, const Buffers& bf, int scale_pow, fl
   e.c_id = c_id;
   e.R = R;
   e.Of = Of;
+  e.r_scale = 1.f;
   e.ld = ld;
   e.bs = bs;
   e.rows_valid = static_cast<int>(g.s);
@@ -562,11 +563,14 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   };
 
   if (g.sc == MUON_SCHED_ORIG && cx.f16_ok) {
-    // Step 0 multiplies the packed bf16 copy of M (slot 0: hi, plus lo for
+    // Step 0 multiplies the packed bf16 copy of M (slot 0: hi, and lo for
     // the residual); A is stored as fp16, and B in the type of this step's X.
     // From step 1 on, X lives in the ping-pong slots as an fp16 pair and
     // every product takes fp16 operands.  Slot 0's bf16 copy is dead after
     // step 0, so step 1 writes its fp16 X there.
+    // The a X term is folded into the product: B' = a I + b A + c A^2, and
+    //   X <- B' X_hi + a X_lo = a X + B X_hi,
+    // so the update reads only the low part of X as its residual.
     int cur = 0;
     for (int k = 0; k < T; ++k) {
       const int nxt = cur ^ 1;
@@ -575,15 +579,16 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
       EpiParams e1 = epi_pair(g, bf, k == 0 ? 2 : 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, nullptr, sp, bss);
       e1.o_f16 = 1;
       CK(tc(1, 0, 1, xf, S, S, L, bf.Xb[cur], nullptr, lp, bsx, bf.Xb[cur], nullptr, lp, bsx, e1));
-      // B = b A + c A^2 on fp16 operands
-      EpiParams e2 = epi_pair(g, bf, 0, cx.c, cx.b, 0.f, bf.Gh, nullptr, bf.Bh, nullptr, sp, bss);
+      // B' = a I + b A + c A^2 on fp16 operands
+      EpiParams e2 = epi_pair(g, bf, 0, cx.c, cx.b, cx.a, bf.Gh, nullptr, bf.Bh, nullptr, sp, bss);
       e2.r_f16 = 1;
       e2.o_f16 = xf;
       CK(tc(1, 0, 7, 1, S, S, S, bf.Gh, nullptr, sp, bss, bf.Gh, nullptr, sp, bss, e2));
-      // X <- a X + B X (k = 0: both terms carry 1 / s), fp16 pair out
-      EpiParams e3 = epi_pair(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, bf.Xb[cur], bf.Xlo[cur], bf.Xb[nxt],
-                              bf.Xlo[nxt], lp, bsx);
+      // X <- B' X_hi + a X_lo (k = 0: both terms carry 1 / s), fp16 pair out
+      EpiParams e3 = epi_pair(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, bf.Xlo[cur], nullptr, bf.Xb[nxt], bf.Xlo[nxt],
+                              lp, bsx);
       e3.r_f16 = xf;
+      e3.r_scale = xf ? 1.f / kF16LoScale : 1.f;  // an fp16 pair's low part is stored scaled by 2^11
       e3.o_f16 = 1;
       e3.cols_valid = static_cast<int>(g.l);
       if (k == T - 1) epi_set_final(e3, cx, g, mats, Bc);
@@ -966,6 +971,7 @@ muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, cons
   EpiParams e;
   memset(&e, 0, sizeof(e));
   e.c_acc = 1.f;
+  e.r_scale = 1.f;
   if (dt == MUON_FP32) {
     e.Of = static_cast<float*>(out);
   } else {

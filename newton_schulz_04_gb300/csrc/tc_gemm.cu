@@ -14,15 +14,19 @@
 // block and the MMA instruction descriptor switches that operand's major-ness
 // for it; so no mirror is ever written.
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      TMA producer: fills a ring of shared-memory stages (mbarrier full/empty)
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer; accumulators are
 //               double-buffered in TMEM (2 x 256 fp32 columns) so the epilogue of
 //               one tile overlaps the main loop of the next
-//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, fused arithmetic
-//               (EpiParams), then 32 x 32 boxes of 16-bit values (bf16 or fp16
-//               pairs) staged in shared memory and written with TMA bulk-tensor
-//               stores
+//   warps 2..9  epilogue, two warps per TMEM lane quarter (warp % 4), each on one
+//               128-column half of the tile: tcgen05.ld, fused arithmetic
+//               (EpiParams) with the residual read from global memory one chunk
+//               ahead, then 32 x 32 blocks of 16-bit values (bf16 or fp16 pairs)
+//               passed through a padded shared-memory box and written with
+//               row-contiguous 16-byte stores.  With one warp per scheduler the
+//               epilogue ran at a fraction of the issue rate and, at K = 1024,
+//               took as long as the main loop
 //
 // Split operands.  A value X carried as a bf16 head Xh and a bf16 residual Xl
 // (X ~ Xh + Xl to ~16 significant bits) is multiplied as a sum of plain bf16
@@ -71,17 +75,14 @@ struct TcCfg {
   static constexpr int B_TILE = BNH * BK * 2;  // this CTA's half of the B tile
   static constexpr int STAGE = A_TILE + B_TILE;
   static constexpr int STAGES = 3;
-  // Epilogue staging per epilogue warp (the epilogue is busy ~12 % of the
-  // time on large products, so one buffer each is enough): one 32 x 32 bf16
-  // output pair (head, residual part) and one input pair for the prefetched
-  // residual R = Rh + Rl; 2 KB per box.
-  static constexpr int BOX = 32 * 32 * 2;
-  static constexpr int OUT_BUFS = 1;
-  static constexpr int RIN_BUFS = 1;
-  static constexpr int OUT_WARP = OUT_BUFS * 2 * BOX;
-  static constexpr int RIN_WARP = RIN_BUFS * 2 * BOX;
-  static constexpr int STG_WARP = OUT_WARP + RIN_WARP;
-  static constexpr int STG = 4 * STG_WARP;
+  // Epilogue: 8 warps, two per TMEM lane quarter, each on EPI_COLS columns.
+  // Each warp stages its outputs through one padded 32-row box (32 rows of
+  // 64 B at an 80-byte stride), which it writes and reads back itself.
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_COLS = BN / 2;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int ROWBOX = 32 * (64 + 16);
+  static constexpr int STG = EPI_WARPS * ROWBOX;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = STAGES * STAGE + STG + BAR_BYTES + 1024;
   static constexpr uint32_t SWZ = 2u;            // descriptor code for the 128-byte swizzle
@@ -89,11 +90,10 @@ struct TcCfg {
   static constexpr int MN_BOX_BYTES = BK * 128;  // one [BK x MN_ATOM] box (MN-major atom)
   static_assert(BM == 128 && BNH == 128, "K-major atoms hold 128 rows");
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr uint32_t EPI_ARRIVALS = 8;  // epilogue warps of both CTAs release a TMEM buffer
+  static constexpr uint32_t EPI_ARRIVALS = 2 * EPI_WARPS;  // epilogue warps of both CTAs release a TMEM buffer
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(BAR_BYTES >= (2 * STAGES + 5 + 8) * 8 + 8, "barrier area too small");
-  static_assert(OUT_BUFS >= 1 && OUT_BUFS <= 2 && RIN_BUFS >= 1 && RIN_BUFS <= 2, "staging depth");
-  static_assert(OUT_WARP >= 32 * (64 + 16), "final-mode row box must fit the output staging");
+  static_assert(BAR_BYTES >= (2 * STAGES + 5) * 8 + 8, "barrier area too small");
+  static_assert(EPI_WARPS == 8 && EPI_COLS % 32 == 0, "two epilogue warps per TMEM lane quarter");
 };
 
 struct TcArgs {
@@ -183,12 +183,25 @@ __device__ __forceinline__ void split_words(const float (&v)[32], uint32_t (&hw)
   }
 }
 
-// Row `row` of a 32 x 32 box from 16 packed words.
-__device__ __forceinline__ void stage_row(uint8_t* box, int row, const uint32_t (&w)[16]) {
+// Store a 32 x 32 block of 16-bit values to dst (row stride ld elements): lane
+// t holds row t as 16 packed words.  The rows go through the warp's padded
+// box (80-byte stride: a phase of 8 lanes writing 16 bytes each hits 32
+// distinct banks), then each warp-wide 16-byte store covers 8 whole 64-byte
+// row segments.
+__device__ __forceinline__ void store_block16(uint16_t* dst, long long ld, int lane, const uint32_t (&w)[16],
+                                              uint8_t* box) {
+  constexpr int STRIDE = 64 + 16;
 #pragma unroll
   for (int q = 0; q < 4; ++q)
-    *reinterpret_cast<uint4*>(box + sw64(row, q * 16)) =
+    *reinterpret_cast<uint4*>(box + lane * STRIDE + q * 16) =
         make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int row = it * 8 + (lane >> 2), pc = lane & 3;
+    *reinterpret_cast<uint4*>(dst + row * ld + pc * 8) = *reinterpret_cast<const uint4*>(box + row * STRIDE + pc * 16);
+  }
+  __syncwarp();
 }
 
 // Final write of a full 32 x 32 block to a caller's row-major matrix (not
@@ -254,13 +267,11 @@ __device__ __forceinline__ void final_block_rows(const EpiParams& e, int b, int 
 }
 
 template <bool BMN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(TcCfg::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAl,
                    const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmAtl,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBl,
                    const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ CUtensorMap tmBtl,
-                   const __grid_constant__ CUtensorMap tmOh, const __grid_constant__ CUtensorMap tmOl,
-                   const __grid_constant__ CUtensorMap tmRh, const __grid_constant__ CUtensorMap tmRl,
                    const __grid_constant__ TcArgs args) {
   using C = TcCfg;
   extern __shared__ uint8_t smem_raw[];
@@ -273,8 +284,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tfull = empty + C::STAGES;  // [2]
   uint64_t* tempty = tfull + 2;         // [2]
   uint64_t* drain = tempty + 2;         // [1]
-  uint64_t* rbar = drain + 1;           // [4 warps][2] residual-box barriers
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -290,7 +300,6 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&tempty[a], C::EPI_ARRIVALS);
     }
     mbar_init(drain, 1);
-    for (int q = 0; q < 8; ++q) mbar_init(&rbar[q], 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -436,47 +445,44 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    // Each warp owns 32 accumulator rows (its TMEM lane quarter).  Per 32-column
-    // chunk: residual boxes prefetched by TMA, tcgen05.ld of the next chunk
-    // issued before this one is processed, fused arithmetic, then either the
-    // final write to the caller's matrix or swizzled staging of 32 x 32 bf16
-    // boxes (and their transposes for symmetric outputs) that one lane sends to
-    // global memory with TMA bulk-tensor stores.
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     const int ew = warp - 2;
+    const int half = ew >> 2;      // which EPI_COLS columns of the tile
     const EpiParams& e = args.epi;
-    uint8_t* stg = staging + ew * C::STG_WARP;
-    uint8_t* rin = stg + C::OUT_WARP;
-    uint64_t* rb = rbar + 2 * ew;
+    uint8_t* box = staging + ew * C::ROWBOX;
     const bool has_lo = e.Ol != nullptr;
     const bool has_r = e.Rh != nullptr;
     const bool has_rl = e.Rl != nullptr;
-    const uint32_t rbytes = has_rl ? 2 * C::BOX : C::BOX;
-    // Residual boxes go through a ring of RIN_BUFS buffers per warp; r_issued /
-    // r_used count the boxes requested / consumed (warp-uniform, lane 0 issues).
-    int r_issued = 0, r_used = 0;
-    auto issue_r = [&](int c0, int r0, int b) {
-      const int buf = r_issued % C::RIN_BUFS;
-      if (lane == 0) {
-        uint8_t* dst = rin + buf * 2 * C::BOX;
-        mbar_arrive_expect_tx(&rb[buf], rbytes);
-        tma_load_3d(&tmRh, &rb[buf], dst, c0, r0, b);
-        if (has_rl) tma_load_3d(&tmRl, &rb[buf], dst + C::BOX, c0, r0, b);
-      }
-      ++r_issued;
-    };
+    constexpr int NCH = C::EPI_COLS / 32;  // 32-column chunks per warp and tile
+    const uint4 zero4 = make_uint4(0, 0, 0, 0);
     int tcount = 0;
     bool ok = true;
     for (int t = cid; t < args.total && ok; t += ncl, ++tcount) {
       int b, p, j;
       decode_pair(args, t, b, p, j);
-      const int m0 = (2 * p + rank) * C::BM, n0 = j * C::BN;
+      const int m0 = (2 * p + rank) * C::BM;
       const int r0 = m0 + quarter * 32;
       const int r = r0 + lane;
-      const int nch = C::BN / 32;  // 32-column chunks of this warp's rows
-      const int rbase = r_issued;
-      if (has_r) {
-        for (int q = 0; q < C::RIN_BUFS && q < nch; ++q) issue_r(n0 + 32 * q, r0, b);
+      const int cb = j * C::BN + half * C::EPI_COLS;
+      // lane `lane` reads its own row of the residual pair, 32 columns per chunk
+      const long long roff = static_cast<long long>(b) * e.bs + static_cast<long long>(r) * e.ld + cb;
+      const uint16_t* rh = has_r ? static_cast<const uint16_t*>(e.Rh) + roff : nullptr;
+      const uint16_t* rl = has_rl ? static_cast<const uint16_t*>(e.Rl) + roff : nullptr;
+      // While the main loop runs, pull this lane's residual row (and, in the
+      // final apply, its row of the caller's W) into L2.
+      if (has_r) bulk_prefetch_l2(rh, C::EPI_COLS * 2);
+      if (has_rl) bulk_prefetch_l2(rl, C::EPI_COLS * 2);
+      if (e.final_mode == FINAL_APPLY && !e.tr[b] && args.final_vec && r < e.rows_valid &&
+          cb + C::EPI_COLS <= e.cols_valid) {
+        const int esz = e.dst_fp32 ? 4 : 2;
+        bulk_prefetch_l2(static_cast<const uint8_t*>(e.dst[b]) + (static_cast<long long>(r) * e.cols_valid + cb) * esz,
+                         C::EPI_COLS * esz);
+      }
+      uint4 nh[4], nl[4];  // residual words of the next chunk
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        nh[q] = has_r ? __ldg(reinterpret_cast<const uint4*>(rh + q * 8)) : zero4;
+        nl[q] = has_rl ? __ldg(reinterpret_cast<const uint4*>(rl + q * 8)) : zero4;
       }
       const int abuf = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
@@ -486,106 +492,67 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_after();
       const float sc = epi_scale(e, b);
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + abuf * C::BN;
-      uint32_t acc[2][32];
-      __syncwarp();
-      tmem_ld_32x32b_x32_start(tbase, acc[0]);
-#pragma unroll 1
-      for (int cc = 0; cc < nch; ++cc) {
-        const int c0 = n0 + cc * 32;
+      const float ka = sc * e.c_acc, kr = sc * e.c_res * e.r_scale;
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + abuf * C::BN + half * C::EPI_COLS;
+#pragma unroll
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int c0 = cb + cc * 32;
+        __syncwarp();
         float v[32];
-        // Wait for chunk cc, then start loading chunk cc + 1 into the other set.
-        if (cc & 1) {
-          tmem_ld_wait(acc[1]);
+        tmem_ld_32x32b_x32(tbase + cc * 32, v);
+        uint32_t rhw[16], rlw[16];
 #pragma unroll
-          for (int u = 0; u < 32; ++u) v[u] = __uint_as_float(acc[1][u]);
-        } else {
-          tmem_ld_wait(acc[0]);
-#pragma unroll
-          for (int u = 0; u < 32; ++u) v[u] = __uint_as_float(acc[0][u]);
+        for (int q = 0; q < 4; ++q) {
+          rhw[4 * q] = nh[q].x, rhw[4 * q + 1] = nh[q].y, rhw[4 * q + 2] = nh[q].z, rhw[4 * q + 3] = nh[q].w;
+          rlw[4 * q] = nl[q].x, rlw[4 * q + 1] = nl[q].y, rlw[4 * q + 2] = nl[q].z, rlw[4 * q + 3] = nl[q].w;
         }
-        if (cc + 1 < nch) {
-          __syncwarp();
-          if (cc & 1) tmem_ld_32x32b_x32_start(tbase + (cc + 1) * 32, acc[0]);
-          else tmem_ld_32x32b_x32_start(tbase + (cc + 1) * 32, acc[1]);
-        }
-        if (has_r) {
-          const int idx = rbase + cc;
-          if (!mbar_wait(&rb[idx % C::RIN_BUFS], (idx / C::RIN_BUFS) & 1)) {
-            ok = false;
-            break;
-          }
-          const uint8_t* src = rin + (idx % C::RIN_BUFS) * 2 * C::BOX;
-          uint32_t rhw[16], rlw[16];
+        if (cc + 1 < NCH) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint4 h = *reinterpret_cast<const uint4*>(src + sw64(lane, q * 16));
-            rhw[4 * q] = h.x, rhw[4 * q + 1] = h.y, rhw[4 * q + 2] = h.z, rhw[4 * q + 3] = h.w;
-            uint4 l = make_uint4(0, 0, 0, 0);
-            if (has_rl) l = *reinterpret_cast<const uint4*>(src + C::BOX + sw64(lane, q * 16));
-            rlw[4 * q] = l.x, rlw[4 * q + 1] = l.y, rlw[4 * q + 2] = l.z, rlw[4 * q + 3] = l.w;
+            nh[q] = has_r ? __ldg(reinterpret_cast<const uint4*>(rh + (cc + 1) * 32 + q * 8)) : zero4;
+            nl[q] = has_rl ? __ldg(reinterpret_cast<const uint4*>(rl + (cc + 1) * 32 + q * 8)) : zero4;
           }
-          r_used = idx + 1;
-          __syncwarp();
-          if (cc + C::RIN_BUFS < nch) issue_r(c0 + 32 * C::RIN_BUFS, r0, b);  // the buffer just read is free
+        }
+        if (has_r) {
           if (e.r_f16) {
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
               const float2 h = unpack2_h(rhw[u]), l = unpack2_h(rlw[u]);  // rlw = 0 without a residual part
-              const float x0 = h.x + l.x * (1.f / kF16LoScale);
-              const float x1 = h.y + l.y * (1.f / kF16LoScale);
-              v[2 * u] = sc * (e.c_acc * v[2 * u] + e.c_res * x0);
-              v[2 * u + 1] = sc * (e.c_acc * v[2 * u + 1] + e.c_res * x1);
+              v[2 * u] = ka * v[2 * u] + kr * (h.x + l.x * (1.f / kF16LoScale));
+              v[2 * u + 1] = ka * v[2 * u + 1] + kr * (h.y + l.y * (1.f / kF16LoScale));
             }
           } else {
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-              const float x0 = bf_lo(rhw[u]) + bf_lo(rlw[u]);
-              const float x1 = bf_hi(rhw[u]) + bf_hi(rlw[u]);
-              v[2 * u] = sc * (e.c_acc * v[2 * u] + e.c_res * x0);
-              v[2 * u + 1] = sc * (e.c_acc * v[2 * u + 1] + e.c_res * x1);
+              v[2 * u] = ka * v[2 * u] + kr * (bf_lo(rhw[u]) + bf_lo(rlw[u]));
+              v[2 * u + 1] = ka * v[2 * u + 1] + kr * (bf_hi(rhw[u]) + bf_hi(rlw[u]));
             }
           }
         } else {
-          const float f = sc * e.c_acc;
 #pragma unroll
-          for (int u = 0; u < 32; ++u) v[u] *= f;
+          for (int u = 0; u < 32; ++u) v[u] *= ka;
         }
         if (e.c_id != 0.f && r >= c0 && r < c0 + 32 && r < e.rows_valid) {
 #pragma unroll
           for (int u = 0; u < 32; ++u)
             if (c0 + u == r) v[u] += e.c_id;
         }
-        uint8_t* sb = stg;
         if (e.final_mode != FINAL_NONE) {
           const bool full_block = r0 + 32 <= e.rows_valid && c0 + 32 <= e.cols_valid;
           if (!e.tr[b] && !e.dst_fp32 && args.final_vec && full_block) {
-            final_block_rows<bf16>(e, b, r0, c0, lane, v, sb);  // padded box: 2560 B of the staging area
+            final_block_rows<bf16>(e, b, r0, c0, lane, v, box);
           } else {
 #pragma unroll
             for (int u = 0; u < 32; ++u) epi_final_elem(e, b, r, c0 + u, v[u]);
           }
-          continue;
+        } else {
+          uint32_t hw[16], lw[16];
+          split_words(v, hw, lw, has_lo, e.o_f16 != 0);
+          const long long off = static_cast<long long>(b) * e.bs + static_cast<long long>(r0) * e.ld + c0;
+          store_block16(static_cast<uint16_t*>(e.Oh) + off, e.ld, lane, hw, box);
+          if (has_lo) store_block16(static_cast<uint16_t*>(e.Ol) + off, e.ld, lane, lw, box);
         }
-        uint32_t hw[16], lw[16];
-        split_words(v, hw, lw, has_lo, e.o_f16 != 0);
-        sb = stg + (cc % C::OUT_BUFS) * 2 * C::BOX;
-        if (lane == 0) bulk_wait_read<C::OUT_BUFS - 1>();  // earlier stores from this buffer have read it
-        __syncwarp();
-        stage_row(sb, lane, hw);
-        if (has_lo) stage_row(sb + C::BOX, lane, lw);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(&tmOh, sb, c0, r0, b);
-          if (has_lo) tma_store_3d(&tmOl, sb + C::BOX, c0, r0, b);
-          bulk_commit();
-        }
-      }
-      if (!ok) {
-        // a TMEM load may still be in flight: complete it before leaving
-        tmem_ld_wait(acc[0]);
-        break;
       }
       // this warp's TMEM rows are read: release the buffer to the leader's MMA issuer
       tc_fence_before();
@@ -595,11 +562,6 @@ __global__ void __launch_bounds__(192, 1)
     if (!ok) {
       if (lane == 0) atomicOr(args.status, kStatusTimeout);
       *abort_flag = 1;
-    }
-    if (lane == 0) {
-      // residual boxes still in flight land before the CTA can retire
-      for (int idx = r_used; idx < r_issued; ++idx) mbar_wait(&rb[idx % C::RIN_BUFS], (idx / C::RIN_BUFS) & 1);
-      bulk_wait_all();  // stores complete before the CTA retires
     }
     __syncwarp();
   }
@@ -652,7 +614,7 @@ template <typename... KArgs, typename... Args>
 static cudaError_t launch_pair(void (*kernel)(KArgs...), int ncl, cudaStream_t st, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * ncl);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(TcCfg::THREADS);
   cfg.dynamicSmemBytes = TcCfg::SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -698,7 +660,7 @@ static int max_clusters(int num_sms) {
   if (!cached[dev]) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms);
-    cfg.blockDim = dim3(192);
+    cfg.blockDim = dim3(TcCfg::THREADS);
     cfg.dynamicSmemBytes = TcCfg::SMEM;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -745,35 +707,21 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
     mBt = mB;
     mBtl = mBl;
   }
-  // Output maps: 32 x 32 boxes of 16-bit values with the 64-byte swizzle (dummies in final mode).
-  CUtensorMap mOh, mOl;
   const bool has_out = epi.Oh != nullptr;
-  const bool of = has_out ? epi.o_f16 != 0 : f;
-  const void* oh = has_out ? epi.Oh : d.A.hi;
-  const void* ol = epi.Ol ? epi.Ol : oh;
-  const long long old_ = has_out ? epi.ld : d.A.ld;
-  const long long obs = has_out ? epi.bs : d.A.bs;
-  const uint64_t ocols = has_out ? static_cast<uint64_t>(epi.ld) : static_cast<uint64_t>(d.K);
-  const uint64_t orows = static_cast<uint64_t>(d.M);
-  ok = ok && make_map(&mOh, oh, of, ocols, orows, d.B, old_, obs, 32, 32, 64);
-  ok = ok && make_map(&mOl, ol, of, ocols, orows, d.B, old_, obs, 32, 32, 64);
-  // Residual maps (same box and swizzle as the outputs; dummies without a residual).
-  CUtensorMap mRh, mRl;
-  const bool has_r = epi.Rh != nullptr;
-  const bool rf = has_r ? epi.r_f16 != 0 : of;
-  const void* rh = has_r ? epi.Rh : oh;
-  const void* rl = epi.Rl ? epi.Rl : rh;
-  const long long rld = has_r ? epi.ld : old_;
-  const long long rbs = has_r ? epi.bs : obs;
-  const uint64_t rcols = has_r ? static_cast<uint64_t>(epi.ld) : ocols;
-  ok = ok && make_map(&mRh, rh, rf, rcols, orows, d.B, rld, rbs, 32, 32, 64);
-  ok = ok && make_map(&mRl, rl, rf, rcols, orows, d.B, rld, rbs, 32, 32, 64);
   if (!ok) {
     *why = "cuTensorMapEncodeTiled failed";
     return cudaErrorInvalidValue;
   }
   if (epi.final_mode == FINAL_NONE && !has_out) {
     *why = "tensor-core epilogue needs a 16-bit output pair";
+    return cudaErrorInvalidValue;
+  }
+  // packed outputs and residuals are accessed with 16-byte row accesses
+  if ((has_out || epi.Rh) && ((reinterpret_cast<uintptr_t>(epi.Oh) | reinterpret_cast<uintptr_t>(epi.Ol) |
+                               reinterpret_cast<uintptr_t>(epi.Rh) | reinterpret_cast<uintptr_t>(epi.Rl)) %
+                                  16 ||
+                              epi.ld % 8 || epi.bs % 8)) {
+    *why = "tensor-core outputs and residuals need 16-byte aligned rows";
     return cudaErrorInvalidValue;
   }
   TcArgs a;
@@ -817,7 +765,7 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
   }
   const int nclusters = std::min(a.total, max_clusters<BMN>(num_sms));
   if (nclusters <= 0) return a.total > 0 ? cudaErrorLaunchOutOfResources : cudaSuccess;
-  return launch_pair(tc_gemm_kernel<BMN>, nclusters, st, mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl, mOh, mOl, mRh, mRl,
+  return launch_pair(tc_gemm_kernel<BMN>, nclusters, st, mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl,
                      a);
 }
 
