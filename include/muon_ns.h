@@ -250,6 +250,39 @@ MUON_API muon_status muon_ns_batched_static(const void* X, int B, int m, int n, 
 MUON_API size_t muon_static_scratch_bytes(void);
 
 /*
+ * muon_adamw_tail -- one AdamW step over the non-matrix "tail" of a model
+ * (MatrixFSDP technical summary, gist.science 2607.05895, "Metodologia" §1:
+ * 1-D vectors and other non-matrix tensors are packed into a tail that a
+ * separate owner updates with standard AdamW).  For every element of tensor i:
+ *
+ *   p <- p * (1 - lr * weight_decay)                 decoupled weight decay
+ *   m <- beta1 m + (1 - beta1) g
+ *   v <- beta2 v + (1 - beta2) g^2
+ *   p <- p - lr / (1 - beta1^step) * m / (sqrt(v) / sqrt(1 - beta2^step) + eps)
+ *
+ *   params, grads  host arrays of `count` device pointers, dtype dt (bf16 or
+ *                  fp32; params updated in place, grads read only), any shape,
+ *                  numel[i] contiguous elements each.
+ *   exp_avg, exp_avg_sq  host arrays of device pointers to fp32 moments
+ *                  (numel[i] each), updated in place; zero before step 1.
+ *   numel  host int64 array; 0 is allowed.
+ *   step   1 for the first step (bias corrections use it).
+ * Arithmetic is fp32; bf16 parameters are rounded once, to nearest even.
+ * All tensors go through one launch per 512 of them.  Tensors must not
+ * overlap.  16-byte aligned tensors use vector accesses; others take a
+ * scalar path.
+ * Errors (nothing launched): MUON_ERR_ARG for count < 0, NULL arrays or NULL
+ * pointers of non-empty tensors, step < 1, non-finite lr / eps / weight_decay,
+ * eps < 0 or betas outside [0, 1), a bad dtype; MUON_ERR_SHAPE for a negative
+ * numel; MUON_ERR_ALIGN for a pointer not aligned to its element size;
+ * MUON_ERR_UNSUPPORTED without an sm_103 device.
+ */
+MUON_API muon_status muon_adamw_tail(void* const* params, const void* const* grads, float* const* exp_avg,
+                                     float* const* exp_avg_sq, const int64_t* numel, int count, float lr,
+                                     float beta1, float beta2, float eps, float weight_decay, int step,
+                                     muon_dtype dt, void* stream);
+
+/*
  * ---- owner placement (DMuon technical summary, gist.science 2606.27153,
  * §2.3 "compute-aware load balancing"): every 2-D matrix is updated by exactly
  * one owner rank, and the owners are chosen so that the largest per-owner cost

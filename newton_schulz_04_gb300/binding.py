@@ -78,6 +78,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.muon_ns_batched_static.restype = i32
     lib.muon_static_scratch_bytes.argtypes = []
     lib.muon_static_scratch_bytes.restype = sz
+    lib.muon_adamw_tail.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                    ctypes.POINTER(i64), i32, f32, f32, f32, f32, f32, i32, i32, vp]
+    lib.muon_adamw_tail.restype = i32
     lib.muon_cost_estimate.argtypes = [ctypes.POINTER(i64), i32, i32, i32, i32, ctypes.POINTER(ctypes.c_double)]
     lib.muon_cost_estimate.restype = i32
     lib.muon_partition.argtypes = [ctypes.POINTER(ctypes.c_double), i32, i32, i32, ctypes.POINTER(i32),
@@ -144,6 +147,72 @@ def bucket_plan(shapes):
     if g < 0:
         raise MuonError(ERR_ARG, "bad shapes")
     return list(order[:n]), list(start[:g + 1])
+
+
+def adamw_tail(params, grads, exp_avgs, exp_avg_sqs, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01,
+               step=1, stream=None) -> None:
+    """In place: one AdamW step over a list of tensors of any shape (C-ABI
+    muon_adamw_tail).  params / grads share one dtype (bfloat16 or float32);
+    the moments are float32 tensors of the same sizes."""
+    lib = load()
+    count = len(params)
+    if not (len(grads) == count == len(exp_avgs) == len(exp_avg_sqs)):
+        raise ValueError("params, grads and both moment lists must have the same length")
+    if count == 0:
+        return
+    dtype = params[0].dtype
+    for p, g, m, v in zip(params, grads, exp_avgs, exp_avg_sqs):
+        if p.dtype != dtype or g.dtype != dtype or m.dtype != torch.float32 or v.dtype != torch.float32:
+            raise TypeError("params and grads share one dtype; moments are float32")
+        if not (p.numel() == g.numel() == m.numel() == v.numel()):
+            raise ValueError("each param, grad and moment must have the same number of elements")
+        if not (p.is_contiguous() and g.is_contiguous() and m.is_contiguous() and v.is_contiguous()):
+            raise ValueError("tensors must be contiguous")
+    P = ctypes.c_void_p * count
+    n = (ctypes.c_int64 * count)(*[p.numel() for p in params])
+    _check(lib.muon_adamw_tail(P(*[p.data_ptr() for p in params]), P(*[g.data_ptr() for g in grads]),
+                               P(*[m.data_ptr() for m in exp_avgs]), P(*[v.data_ptr() for v in exp_avg_sqs]), n,
+                               count, float(lr), float(betas[0]), float(betas[1]), float(eps), float(weight_decay),
+                               int(step), _dtype_code(dtype), ctypes.c_void_p(_stream_ptr(stream))))
+
+
+class AdamwTail:
+    """AdamW over a fixed list of tensors (the non-matrix tail), with the
+    pointer tables built once and the step count kept here; `step()` is one
+    C-ABI call (one launch per 512 tensors)."""
+
+    def __init__(self, params, grads, exp_avgs, exp_avg_sqs, lr=1e-3, betas=(0.9, 0.999), eps=1e-8,
+                 weight_decay=0.01):
+        lib = load()
+        self._lib = lib
+        self.count = len(params)
+        if not (len(grads) == self.count == len(exp_avgs) == len(exp_avg_sqs)):
+            raise ValueError("params, grads and both moment lists must have the same length")
+        dtype = params[0].dtype if self.count else torch.float32
+        for p, g, m, v in zip(params, grads, exp_avgs, exp_avg_sqs):
+            if p.dtype != dtype or g.dtype != dtype or m.dtype != torch.float32 or v.dtype != torch.float32:
+                raise TypeError("params and grads share one dtype; moments are float32")
+            if not (p.numel() == g.numel() == m.numel() == v.numel()):
+                raise ValueError("each param, grad and moment must have the same number of elements")
+            if not (p.is_contiguous() and g.is_contiguous() and m.is_contiguous() and v.is_contiguous()):
+                raise ValueError("tensors must be contiguous")
+        self._keep = (list(params), list(grads), list(exp_avgs), list(exp_avg_sqs))
+        P = ctypes.c_void_p * max(self.count, 1)
+        self._p = P(*[t.data_ptr() for t in params])
+        self._g = P(*[t.data_ptr() for t in grads])
+        self._m = P(*[t.data_ptr() for t in exp_avgs])
+        self._v = P(*[t.data_ptr() for t in exp_avg_sqs])
+        self._n = (ctypes.c_int64 * max(self.count, 1))(*[t.numel() for t in params])
+        self._dt = _dtype_code(dtype) if self.count else FP32
+        self.lr, self.betas, self.eps, self.weight_decay = lr, betas, eps, weight_decay
+        self.t = 0
+
+    def step(self, stream=None) -> None:
+        self.t += 1
+        _check(self._lib.muon_adamw_tail(self._p, self._g, self._m, self._v, self._n, self.count, float(self.lr),
+                                         float(self.betas[0]), float(self.betas[1]), float(self.eps),
+                                         float(self.weight_decay), self.t, self._dt,
+                                         ctypes.c_void_p(_stream_ptr(stream))))
 
 
 def cost_estimate(shapes, steps=5, dtype=torch.bfloat16, schedule="auto") -> list:

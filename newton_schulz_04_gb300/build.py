@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libmuon_ns.so")
-SOURCES = ["engine.cu", "tc_gemm.cu", "simt_gemm.cu", "elementwise.cu", "planner.cpp"]
+SOURCES = ["engine.cu", "tc_gemm.cu", "simt_gemm.cu", "elementwise.cu", "adamw.cu", "planner.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -806,6 +806,75 @@ using namespace muon;
 
 extern "C" {
 
+muon_status muon_adamw_tail(void* const* params, const void* const* grads, float* const* exp_avg,
+                            float* const* exp_avg_sq, const int64_t* numel, int count, float lr, float beta1,
+                            float beta2, float eps, float weight_decay, int step, muon_dtype dt, void* stream) {
+  g_last_error.clear();
+  if (count < 0) return fail(MUON_ERR_ARG, "count=%d < 0", count);
+  if (count == 0) return MUON_OK;
+  if (!params || !grads || !exp_avg || !exp_avg_sq || !numel) return fail(MUON_ERR_ARG, "NULL array");
+  if (!valid_dt(dt)) return fail(MUON_ERR_ARG, "bad dtype %d", dt);
+  if (step < 1) return fail(MUON_ERR_ARG, "step=%d: steps count from 1", step);
+  if (!(std::isfinite(lr) && std::isfinite(eps) && std::isfinite(weight_decay) && beta1 >= 0.f && beta1 < 1.f &&
+        beta2 >= 0.f && beta2 < 1.f && eps >= 0.f))
+    return fail(MUON_ERR_ARG, "need finite lr, eps >= 0, weight_decay and betas in [0, 1)");
+  const size_t esz = dt == MUON_FP32 ? 4 : 2;
+  long long total = 0;
+  for (int i = 0; i < count; ++i) {
+    if (numel[i] < 0) return fail(MUON_ERR_SHAPE, "numel[%d] < 0", i);
+    if (numel[i] > 0 && (!params[i] || !grads[i] || !exp_avg[i] || !exp_avg_sq[i]))
+      return fail(MUON_ERR_ARG, "tensor %d has a NULL pointer", i);
+    if ((reinterpret_cast<uintptr_t>(params[i]) | reinterpret_cast<uintptr_t>(grads[i])) % esz ||
+        (reinterpret_cast<uintptr_t>(exp_avg[i]) | reinterpret_cast<uintptr_t>(exp_avg_sq[i])) % 4)
+      return fail(MUON_ERR_ALIGN, "tensor %d is not aligned to its element size", i);
+    total += numel[i];
+  }
+  if (total == 0) return MUON_OK;
+  int major = 0, minor = 0;
+  muon_status dst;
+  const int sms = device_sms(&major, &minor, &dst);
+  if (dst != MUON_OK) return dst;
+  if (major != 10 || minor != 3)
+    return fail(MUON_ERR_UNSUPPORTED, "this library is built for sm_103a (GB300); device is sm_%d%d", major, minor);
+  static_assert(sizeof(AdamwArgs) < 32000, "AdamW arguments must fit the kernel parameter space");
+  AdamwArgs a;
+  memset(&a, 0, sizeof(a));
+  a.decay = static_cast<float>(1.0 - static_cast<double>(lr) * weight_decay);
+  a.beta1 = beta1;
+  a.beta2 = beta2;
+  a.eps = eps;
+  const double bc1 = 1.0 - std::pow(static_cast<double>(beta1), step);
+  const double bc2 = 1.0 - std::pow(static_cast<double>(beta2), step);
+  a.step_size = static_cast<float>(lr / bc1);
+  a.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+  const char* why = nullptr;
+  for (int c0 = 0; c0 < count; c0 += kMaxTail) {
+    const int n = std::min(kMaxTail, count - c0);
+    a.count = n;
+    long long gs = 0;
+    for (int i = 0; i < n; ++i) {
+      const int k = c0 + i;
+      a.gstart[i] = gs;
+      gs += (numel[k] + 7) / 8;
+      a.numel[i] = numel[k];
+      a.p[i] = params[k];
+      a.g[i] = grads[k];
+      a.m[i] = exp_avg[k];
+      a.v[i] = exp_avg_sq[k];
+      a.vec_ok[i] = ((reinterpret_cast<uintptr_t>(params[k]) | reinterpret_cast<uintptr_t>(grads[k]) |
+                      reinterpret_cast<uintptr_t>(exp_avg[k]) | reinterpret_cast<uintptr_t>(exp_avg_sq[k])) % 16) == 0;
+    }
+    a.gstart[n] = gs;
+    ProfScope ps("adamw_tail", 0.0, static_cast<double>(gs) * 8.0 * (dt == MUON_FP32 ? 28.0 : 22.0),
+                 static_cast<cudaStream_t>(stream));
+    const cudaError_t e = launch_adamw_tail(a, dt == MUON_BF16, sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+      return fail(MUON_ERR_CUDA, "launch_adamw_tail failed: %s%s%s", cudaGetErrorString(e), why ? ": " : "",
+                  why ? why : "");
+  }
+  return MUON_OK;
+}
+
 muon_status muon_cost_estimate(const int64_t* shapes, int count, int steps, muon_dtype dt, muon_sched sc,
                                double* seconds) {
   if (count < 0) return fail(MUON_ERR_ARG, "count=%d < 0", count);

@@ -77,6 +77,26 @@ cudaError_t launch_norm_finalize(const float* partial, int tiles, int B, float e
 // O = Xf * inv_norm written through a final-mode epilogue (zero NS steps).
 cudaError_t launch_final_from_packed(const float* Xf, long long ld, long long bs, int B, const EpiParams& e,
                                      cudaStream_t st);
+// Fused AdamW over a list of tensors (the non-matrix tail).
+// Tensors per launch: the argument block (49 bytes per tensor) stays inside
+// the 32 KB kernel-parameter limit.
+constexpr int kMaxTail = 512;
+struct AdamwArgs {
+  int count;
+  float decay;         // 1 - lr * weight_decay
+  float beta1, beta2, eps;
+  float step_size;     // lr / (1 - beta1^step)
+  float inv_sqrt_bc2;  // 1 / sqrt(1 - beta2^step)
+  long long gstart[kMaxTail + 1];  // first 8-element group of each tensor; gstart[count] = all groups
+  long long numel[kMaxTail];
+  void* p[kMaxTail];
+  const void* g[kMaxTail];
+  float* m[kMaxTail];
+  float* v[kMaxTail];
+  unsigned char vec_ok[kMaxTail];  // 1: the tensor's four arrays are 16-byte aligned
+};
+cudaError_t launch_adamw_tail(const AdamwArgs& a, bool bf16_params, int num_sms, cudaStream_t st);
+
 // Failure-detection self test: a bounded wait on a barrier that never completes.
 cudaError_t launch_debug_wait(int* status, long long cycles, cudaStream_t st);
 

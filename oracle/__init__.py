@@ -10,3 +10,4 @@ from .ns_oracle import (  # noqa: F401
     newton_schulz, muon_update, bf16_round, bucket_order,
 )
 from . import partition  # noqa: F401,E402
+from . import adamw  # noqa: F401,E402
