@@ -36,6 +36,12 @@ import synth  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# fp32 FFMA peak from unit counts: 152 SMs x 128 FP32 lanes x 2 flops per FMA x SM clock
+FP32_LANES = 152 * 128
+
+
+def fp32_alu_peak_tflops(sm_mhz):
+    return FP32_LANES * 2 * sm_mhz * 1e6 / 1e12
 
 
 def peaks():
@@ -98,6 +104,11 @@ def make_workload(name: str, device):
         return synth.c3(device, layers=1)
     if name == "c4":
         return synth.c4(device)
+    if name == "c1":
+        return synth.c1()
+    if name.startswith("c5f32"):
+        n = int(name.split("_n")[1]) if "_n" in name else 4096
+        return synth.c5(device, n=n, dtype=torch.float32)
     if name.startswith("c5"):
         n = int(name.split("_n")[1]) if "_n" in name else 4096
         return synth.c5(device, n=n)
@@ -109,6 +120,7 @@ WORKLOAD_DESC = {
     "c3": "Llama-style 32 layers d=4096 ffn=14336 (q,k,v,o 4096^2; gate/up 4096x14336; down 14336x4096), "
           "bf16 grads N(0,1e-6), fp32 momentum, 5 NS steps",
     "c4": "512 matrices from {256x1024,512x2048,768x3072}, rank-8 + 1e-4 noise, bf16, 5 NS steps",
+    "c1": "single 128x256 fp32 matrix N(0,1) seed 0, 5 NS steps, beta 0.95, lr 0.02",
     "c3_layer": "one layer of the d=4096 ffn=14336 model (4 x 4096^2, 2 x 4096x14336, 14336x4096), bf16, 5 NS steps",
 }
 
@@ -394,7 +406,16 @@ def run_ours(args, world, rank, local):
     tc_peak = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
     traffic = recorded_traffic(args.config, dom)
     tot_launch_ms = sum(v[0] for v in by.values())
-    if dom.startswith("tc") or dom.startswith("simt"):
+    if dom.startswith("simt"):
+        achieved = by[dom][2] / (by[dom][0] / 1e3) / 1e12
+        mhz = clocks.get("sm_mhz") or 2070.0
+        alu_peak = fp32_alu_peak_tflops(mhz)
+        roof = {"bound": "alu", "kernel": dom, "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                "frac": achieved / alu_peak, "traffic": traffic,
+                "peak_source": f"152 SMs x 128 FP32 lanes x 2 flops x {mhz:.0f} MHz (sampled median, else max)",
+                "launches": by[dom][1], "avg_launch_ms": by[dom][0] / by[dom][1],
+                "share_of_launch_time": by[dom][0] / tot_launch_ms}
+    elif dom.startswith("tc"):
         achieved = by[dom][2] / (by[dom][0] / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": tc_peak,
                 "unit": "TFLOP/s", "frac": achieved / tc_peak, "traffic": traffic,
@@ -430,7 +451,11 @@ def run_ours(args, world, rank, local):
         "metric": "Muon update TFLOP/s (algorithmic, symmetric Gram count)",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": scaling, "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
+        "dtype": "fp32" if work.dtype == torch.float32 else "bf16+fp16",
+        "operands": ("fp32 FFMA on the CUDA cores" if work.dtype == torch.float32 else
+                     "bf16 in and out; NS products on bf16 (step 0) and fp16 (later steps) tensor-core operands, "
+                     "fp32 accumulation"),
+        "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC.get(args.config, args.config), "name": args.config,
                    "matrices_per_gpu": count, "l2": "flushed between timed steps" if flush is not None
                    else "inputs larger than L2",

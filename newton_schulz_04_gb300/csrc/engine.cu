@@ -206,6 +206,7 @@ constexpr size_t kHeader = 1024;  // status word + reserved
 struct Buffers {
   float* inv_norm = nullptr;
   float* partial = nullptr;
+  int* done = nullptr;  // per-matrix completion counters chaining consecutive tensor-core launches
   // packed X
   float* Xf = nullptr;
   float* Xf2 = nullptr;
@@ -238,6 +239,7 @@ static size_t carve_buffers(char* base, int Bc, long long sp, long long lp, int 
   const size_t ns = static_cast<size_t>(Bc) * sp * sp;
   bf.inv_norm = static_cast<float*>(c.take(sizeof(float) * Bc));
   bf.partial = static_cast<float*>(c.take(sizeof(float) * Bc * static_cast<size_t>(tiles)));
+  bf.done = static_cast<int*>(c.take(sizeof(int) * Bc));
   if (dt == MUON_FP32 || steps == 0) {
     bf.Xf = static_cast<float*>(c.take(4 * nx));
     if (steps == 0) return c.off;
@@ -407,6 +409,8 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   const char* why = nullptr;
   Buffers bf;
   carve_buffers(ws, Bc, g.sp, g.lp, g.tiles, cx.dt, g.sc, cx.steps, bf);
+  // stream-ordered: runs after everything before this chunk, before its pack
+  CK(cudaMemsetAsync(bf.done, 0, sizeof(int) * Bc, cx.st));
   const long long sp = g.sp, lp = g.lp;
   const long long bsx = sp * lp, bss = sp * sp;
   const bool fp32 = cx.dt == MUON_FP32;
@@ -534,6 +538,15 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     return MUON_OK;
   }
 
+  // Consecutive tensor-core launches are chained per matrix: each adds to
+  // done[b] as it finishes matrix b's tiles, and every launch after the first
+  // starts matrix b as soon as done[b] reaches the total of all launches
+  // before it, rather than waiting for the whole previous grid.  By induction
+  // every earlier launch has then finished matrix b, so all read-after-write
+  // and write-after-read hazards on b's buffers are covered.  (The counters
+  // are zeroed at the top of the chunk.)
+  int tc_launches = 0;
+  int tc_cum = 0;
   // sym: bit 0 = symmetric output (lower tiles, block-lower storage); bits 1 / 2 =
   // A / B is a symmetric operand in that storage.
   auto tc = [&](int split, int b_mn, int sym, int f16, int M, int N, int K, const void* Ah, const void* Al,
@@ -558,8 +571,14 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     static const char* const kSyrk[4] = {"", "tc_syrk", "tc_syrk_x2", "tc_syrk_x3"};
     static const char* const kRect[4] = {"", "tc_rect", "tc_rect_x2", "tc_rect_x3"};
     const char* kind = d.sym ? (K == S ? kSym[split] : kSyrk[split]) : kRect[split];
+    d.done = bf.done;
+    d.flag_wait = tc_launches > 0 ? 1 : 0;
+    d.wait_target = tc_cum;
     ProfScope ps(kind, fl, 0.0, cx.st);
-    return launch_tc_gemm(d, e, cx.status, cx.st, cx.sms, &why);
+    const cudaError_t err = launch_tc_gemm(d, e, cx.status, cx.st, cx.sms, &why);
+    tc_cum += tc_signals_per_matrix(M, N, d.sym);
+    ++tc_launches;
+    return err;
   };
 
   if (g.sc == MUON_SCHED_ORIG && cx.f16_ok) {

@@ -52,7 +52,15 @@ struct TcGemmDesc {
   int b_mn;
   int f16;    // 1: both operands are fp16, 0: both bf16 (one tcgen05 kind::f16 MMA takes one type)
   TcOperand A, Bop;
+  // Per-matrix chaining with the previous launch on the stream (optional):
+  // every launch adds tc_signals_per_matrix() to done[b] per matrix; with
+  // flag_wait a launch starts matrix b once done[b] >= wait_target, instead of
+  // waiting for the whole previous grid.
+  int* done = nullptr;
+  int wait_target = 0;
+  int flag_wait = 0;
 };
+int tc_signals_per_matrix(int M, int N, int sym);
 
 cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* status, cudaStream_t st, int num_sms,
                            const char** why);

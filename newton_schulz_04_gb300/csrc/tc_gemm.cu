@@ -109,6 +109,14 @@ struct TcArgs {
   int final_vec;  // final mode may use 16-byte accesses to the caller's rows
   int f16;        // operands are fp16 (else bf16)
   int* status;    // workspace status word
+  // Per-matrix completion counters (or nullptr).  Every epilogue warp adds 1
+  // to done[b] once its part of a tile of matrix b is stored.  With
+  // flag_wait, a tile of matrix b starts once done[b] >= wait_target (the
+  // previous launch has finished that matrix) instead of waiting for the
+  // whole previous grid.
+  int* done;
+  int wait_target;
+  int flag_wait;
   EpiParams epi;
 };
 
@@ -318,7 +326,9 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
   cluster_sync();  // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
   pdl_launch_dependents();
-  pdl_wait();  // inputs are written by the previous kernel on the stream
+  // Inputs are written by earlier kernels on the stream: wait for the whole
+  // previous grid, or, chained per matrix, for that matrix's counter below.
+  if (!args.flag_wait) pdl_wait();
   const int rank = static_cast<int>(cluster_ctarank());
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
   const uint32_t tmem_base = *tmem_slot;
@@ -330,10 +340,19 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       // ------------------------------------------------------------ producer
       int it = 0;
       bool ok = true;
+      int ready_b = -1;  // last matrix whose inputs are known to be complete
       for (int t = cid; t < args.total && ok; t += ncl) {
         int b, p, j;
         decode_pair(args, t, b, p, j);
         const int m0 = (2 * p + rank) * C::BM, n0 = j * C::BN;
+        if (args.flag_wait && b != ready_b) {
+          if (!wait_counter(&args.done[b], args.wait_target)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();  // the TMA loads below read what that matrix's writers stored
+          ready_b = b;
+        }
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
@@ -464,10 +483,18 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       const int r0 = m0 + quarter * 32;
       const int r = r0 + lane;
       const int cb = j * C::BN + half * C::EPI_COLS;
-      // lane `lane` reads its own row of the residual pair, 32 columns per chunk
+      // lane `lane` reads its own row of the residual pair, 32 columns per chunk,
+      // through L2 (the previous launch may still be writing other matrices)
       const long long roff = static_cast<long long>(b) * e.bs + static_cast<long long>(r) * e.ld + cb;
       const uint16_t* rh = has_r ? static_cast<const uint16_t*>(e.Rh) + roff : nullptr;
       const uint16_t* rl = has_rl ? static_cast<const uint16_t*>(e.Rl) + roff : nullptr;
+      if (args.flag_wait && has_r) {
+        // the residual may be the previous launch's output: acquire its
+        // counter before the first residual load below
+        if (lane == 0 && !wait_counter(&args.done[b], args.wait_target)) ok = false;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
       // While the main loop runs, pull this lane's residual row (and, in the
       // final apply, its row of the caller's W) into L2.
       if (has_r) bulk_prefetch_l2(rh, C::EPI_COLS * 2);
@@ -481,8 +508,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       uint4 nh[4], nl[4];  // residual words of the next chunk
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        nh[q] = has_r ? __ldg(reinterpret_cast<const uint4*>(rh + q * 8)) : zero4;
-        nl[q] = has_rl ? __ldg(reinterpret_cast<const uint4*>(rl + q * 8)) : zero4;
+        nh[q] = has_r ? __ldcg(reinterpret_cast<const uint4*>(rh + q * 8)) : zero4;
+        nl[q] = has_rl ? __ldcg(reinterpret_cast<const uint4*>(rl + q * 8)) : zero4;
       }
       const int abuf = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
@@ -510,8 +537,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
         if (cc + 1 < NCH) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            nh[q] = has_r ? __ldg(reinterpret_cast<const uint4*>(rh + (cc + 1) * 32 + q * 8)) : zero4;
-            nl[q] = has_rl ? __ldg(reinterpret_cast<const uint4*>(rl + (cc + 1) * 32 + q * 8)) : zero4;
+            nh[q] = has_r ? __ldcg(reinterpret_cast<const uint4*>(rh + (cc + 1) * 32 + q * 8)) : zero4;
+            nl[q] = has_rl ? __ldcg(reinterpret_cast<const uint4*>(rl + (cc + 1) * 32 + q * 8)) : zero4;
           }
         }
         if (has_r) {
@@ -558,6 +585,14 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_cluster(&tempty[abuf], 0));
+      if (args.done) {
+        // this warp's part of the tile is stored: publish it for the next
+        // launch, whose TMA (async proxy) and L2 loads read it
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) red_release_gpu_add(&args.done[b], 1);
+      }
     }
     if (!ok) {
       if (lane == 0) atomicOr(args.status, kStatusTimeout);
@@ -752,6 +787,9 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
   a.a_sym = d.a_sym;
   a.b_sym = BMN ? 0 : d.b_sym;
   a.f16 = d.f16 ? 1 : 0;
+  a.done = d.done;
+  a.wait_target = d.wait_target;
+  a.flag_wait = d.done && d.flag_wait ? 1 : 0;
   a.status = status;
   a.epi = epi;
   a.epi.sym = d.sym;
@@ -790,6 +828,11 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* statu
   }
   return d.b_mn ? launch_impl<true>(d, epi, status, st, num_sms, why)
                 : launch_impl<false>(d, epi, status, st, num_sms, why);
+}
+
+int tc_signals_per_matrix(int M, int N, int sym) {
+  const int P = M / 256;
+  return static_cast<int>(TcCfg::EPI_ARRIVALS) * (sym ? P * (P + 1) / 2 : P * (N / 256));
 }
 
 int tc_tiles(int M, int N, int sym) {
