@@ -183,10 +183,12 @@ def clock_window(local, step, timed, k, world, pad_s=0.3):
     def pad():
         torch.cuda.synchronize()
         t0 = time.perf_counter()
+        n = 1  # grow the batch of steps between clock checks, so long steps pad by one or two steps
         while time.perf_counter() - t0 < pad_s:
-            for _ in range(8):
+            for _ in range(n):
                 step()
             torch.cuda.synchronize()
+            n = min(2 * n, 64)
     t0 = time.perf_counter()
     with Clocks(local) as clk:
         pad()

@@ -483,8 +483,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       const int r0 = m0 + quarter * 32;
       const int r = r0 + lane;
       const int cb = j * C::BN + half * C::EPI_COLS;
-      // lane `lane` reads its own row of the residual pair, 32 columns per chunk,
-      // through L2 (the previous launch may still be writing other matrices)
+      // lane `lane` reads its own row of the residual pair, 32 columns per chunk
       const long long roff = static_cast<long long>(b) * e.bs + static_cast<long long>(r) * e.ld + cb;
       const uint16_t* rh = has_r ? static_cast<const uint16_t*>(e.Rh) + roff : nullptr;
       const uint16_t* rl = has_rl ? static_cast<const uint16_t*>(e.Rl) + roff : nullptr;
@@ -505,11 +504,17 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
         bulk_prefetch_l2(static_cast<const uint8_t*>(e.dst[b]) + (static_cast<long long>(r) * e.cols_valid + cb) * esz,
                          C::EPI_COLS * esz);
       }
+      // Residual loads: through the read-only cache, unless the previous launch
+      // may still be writing other matrices (chained), then from L2.
+      const bool coherent = args.flag_wait != 0;
+      auto ld16 = [&](const uint16_t* q) {
+        return coherent ? __ldcg(reinterpret_cast<const uint4*>(q)) : __ldg(reinterpret_cast<const uint4*>(q));
+      };
       uint4 nh[4], nl[4];  // residual words of the next chunk
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        nh[q] = has_r ? __ldcg(reinterpret_cast<const uint4*>(rh + q * 8)) : zero4;
-        nl[q] = has_rl ? __ldcg(reinterpret_cast<const uint4*>(rl + q * 8)) : zero4;
+        nh[q] = has_r ? ld16(rh + q * 8) : zero4;
+        nl[q] = has_rl ? ld16(rl + q * 8) : zero4;
       }
       const int abuf = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
@@ -537,8 +542,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
         if (cc + 1 < NCH) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            nh[q] = has_r ? __ldcg(reinterpret_cast<const uint4*>(rh + (cc + 1) * 32 + q * 8)) : zero4;
-            nl[q] = has_rl ? __ldcg(reinterpret_cast<const uint4*>(rl + (cc + 1) * 32 + q * 8)) : zero4;
+            nh[q] = has_r ? ld16(rh + (cc + 1) * 32 + q * 8) : zero4;
+            nl[q] = has_rl ? ld16(rl + (cc + 1) * 32 + q * 8) : zero4;
           }
         }
         if (has_r) {
