@@ -202,11 +202,15 @@ struct Carve {
 };
 
 constexpr size_t kHeader = 1024;  // status word + reserved
+constexpr size_t kDebugTileCtr = 512;  // header offset of muon_debug_gemm's tile counter
+// tensor-core launches in one chunk: at most 3 per NS step (ORIG) or 5 (Gram) plus 2
+constexpr int kMaxTcLaunches = 5 * MUON_MAX_STEPS + 8;
 
 struct Buffers {
   float* inv_norm = nullptr;
   float* partial = nullptr;
   int* done = nullptr;  // per-matrix completion counters chaining consecutive tensor-core launches
+  int* tile_ctr = nullptr;  // one tile-scheduler counter per tensor-core launch of the chunk
   // packed X
   float* Xf = nullptr;
   float* Xf2 = nullptr;
@@ -240,6 +244,7 @@ static size_t carve_buffers(char* base, int Bc, long long sp, long long lp, int 
   bf.inv_norm = static_cast<float*>(c.take(sizeof(float) * Bc));
   bf.partial = static_cast<float*>(c.take(sizeof(float) * Bc * static_cast<size_t>(tiles)));
   bf.done = static_cast<int*>(c.take(sizeof(int) * Bc));
+  bf.tile_ctr = static_cast<int*>(c.take(sizeof(int) * kMaxTcLaunches));
   if (dt == MUON_FP32 || steps == 0) {
     bf.Xf = static_cast<float*>(c.take(4 * nx));
     if (steps == 0) return c.off;
@@ -418,6 +423,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   const bool chain = cx.dt == MUON_BF16 && pairs_rect <= 4LL * (cx.sms / 2);
   // stream-ordered: runs after everything before this chunk, before its pack
   if (chain) CK(cudaMemsetAsync(bf.done, 0, sizeof(int) * Bc, cx.st));
+  if (cx.dt == MUON_BF16 && cx.steps > 0) CK(cudaMemsetAsync(bf.tile_ctr, 0, sizeof(int) * kMaxTcLaunches, cx.st));
   const long long sp = g.sp, lp = g.lp;
   const long long bsx = sp * lp, bss = sp * sp;
   const bool fp32 = cx.dt == MUON_FP32;
@@ -580,6 +586,8 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     const char* kind = d.sym ? (K == S ? kSym[split] : kSyrk[split]) : kRect[split];
     d.done = chain ? bf.done : nullptr;
     d.flag_wait = tc_launches > 0 ? 1 : 0;
+    if (tc_launches >= kMaxTcLaunches) return cudaErrorInvalidValue;
+    d.tile_ctr = bf.tile_ctr + tc_launches;
     d.wait_target = tc_cum;
     ProfScope ps(kind, fl, 0.0, cx.st);
     const cudaError_t err = launch_tc_gemm(d, e, cx.status, cx.st, cx.sms, &why);
@@ -1107,6 +1115,9 @@ muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, cons
     d.f16 = dt == MUON_FP16 ? 1 : 0;
     d.A = TcOperand{A, A_lo, K, static_cast<long long>(M) * K};
     d.Bop = TcOperand{B, B_lo, b_mn ? N : K, bsb};
+    d.tile_ctr = reinterpret_cast<int*>(static_cast<char*>(ws) + kDebugTileCtr);
+    if (cudaMemsetAsync(d.tile_ctr, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return fail(MUON_ERR_CUDA, "memset of the tile counter failed");
     err = launch_tc_gemm(d, e, static_cast<int*>(ws), static_cast<cudaStream_t>(stream), sms, &why);
     if (err == cudaErrorInvalidValue && why) return fail(MUON_ERR_ARG, "%s", why);
   } else if (dt == MUON_FP32) {

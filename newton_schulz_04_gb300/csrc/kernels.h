@@ -59,6 +59,10 @@ struct TcGemmDesc {
   int* done = nullptr;
   int wait_target = 0;
   int flag_wait = 0;
+  // Tile scheduler: one int in global memory, zero before the launch; the
+  // CTA pairs take tiles from it in order (atomicAdd), so clusters that start
+  // early (while the previous launch drains) take more of them.
+  int* tile_ctr = nullptr;
 };
 int tc_signals_per_matrix(int M, int N, int sym);
 

@@ -91,8 +91,14 @@ struct TcCfg {
   static_assert(BM == 128 && BNH == 128, "K-major atoms hold 128 rows");
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr uint32_t EPI_ARRIVALS = 2 * EPI_WARPS;  // epilogue warps of both CTAs release a TMEM buffer
+  // Tile queue: the leader's producer fetches tile indices from a counter in
+  // global memory and publishes them to both CTAs; QD slots deep.  A slot is
+  // free again once the peer producer, the MMA issuer and the epilogue warps
+  // of both CTAs have read it.
+  static constexpr int QD = 4;
+  static constexpr uint32_t Q_ARRIVALS = 2 + 2 * EPI_WARPS;
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(BAR_BYTES >= (2 * STAGES + 5) * 8 + 8, "barrier area too small");
+  static_assert(BAR_BYTES >= (2 * STAGES + 5 + 2 * QD) * 8 + 4 * QD + 8, "barrier area too small");
   static_assert(EPI_WARPS == 8 && EPI_COLS % 32 == 0, "two epilogue warps per TMEM lane quarter");
 };
 
@@ -117,6 +123,7 @@ struct TcArgs {
   int* done;
   int wait_target;
   int flag_wait;
+  int* tile_ctr;  // zeroed before the launch; tiles are taken in order by atomicAdd
   EpiParams epi;
 };
 
@@ -292,7 +299,10 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
   uint64_t* tfull = empty + C::STAGES;  // [2]
   uint64_t* tempty = tfull + 2;         // [2]
   uint64_t* drain = tempty + 2;         // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* qfull = drain + 1;          // [QD] tile index published
+  uint64_t* qempty = qfull + C::QD;     // [QD] (leader) slot read by every consumer
+  volatile int* tq = reinterpret_cast<volatile int*>(qempty + C::QD);  // [QD] tile indices (-1: no more)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(tq) + C::QD);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -308,6 +318,10 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       mbar_init(&tempty[a], C::EPI_ARRIVALS);
     }
     mbar_init(drain, 1);
+    for (int q = 0; q < C::QD; ++q) {
+      mbar_init(&qfull[q], 1);
+      mbar_init(&qempty[q], C::Q_ARRIVALS);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -330,8 +344,15 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
   // previous grid, or, chained per matrix, for that matrix's counter below.
   if (!args.flag_wait) pdl_wait();
   const int rank = static_cast<int>(cluster_ctarank());
-  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
   const uint32_t tmem_base = *tmem_slot;
+  // Tile k of this cluster's sequence (every role reads the same sequence):
+  // returns the tile index, -1 at the end, -2 on a timeout.
+  auto take_tile = [&](int k) -> int {
+    const int slot = k % C::QD;
+    if (*abort_flag || !mbar_wait_cluster(&qfull[slot], (k / C::QD) & 1)) return -2;
+    return tq[slot];
+  };
+  auto release_tile = [&](int k) { mbar_arrive_cluster(mapa_cluster(&qempty[k % C::QD], 0)); };
   const int nk = args.K / C::BK;   // k-blocks per segment
   const int nkb = nk * args.nseg;  // k-blocks per tile
 
@@ -341,7 +362,31 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       int it = 0;
       bool ok = true;
       int ready_b = -1;  // last matrix whose inputs are known to be complete
-      for (int t = cid; t < args.total && ok; t += ncl) {
+      for (int k = 0; ok; ++k) {
+        int t;
+        if (rank == 0) {
+          // fetch the next tile and publish it to both CTAs of the pair
+          const int slot = k % C::QD;
+          if (*abort_flag || !mbar_wait(&qempty[slot], ((k / C::QD) & 1) ^ 1)) {
+            ok = false;
+            t = -1;
+          } else {
+            t = atomicAdd(args.tile_ctr, 1);
+            if (t >= args.total) t = -1;
+          }
+          tq[slot] = t;
+          st_shared_cluster(mapa_cluster(const_cast<int*>(&tq[slot]), 1), t);
+          mbar_arrive_cluster(mapa_cluster(&qfull[slot], 0));
+          mbar_arrive_cluster(mapa_cluster(&qfull[slot], 1));
+        } else {
+          t = take_tile(k);
+          if (t == -2) {
+            ok = false;
+            break;
+          }
+          release_tile(k);
+        }
+        if (t < 0) break;
         int b, p, j;
         decode_pair(args, t, b, p, j);
         const int m0 = (2 * p + rank) * C::BM, n0 = j * C::BN;
@@ -412,7 +457,14 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       constexpr uint32_t SBO = 8 * 128;
       int it = 0, tcount = 0;
       bool ok = true;
-      for (int t = cid; t < args.total && ok; t += ncl, ++tcount) {
+      for (int k = 0; ok; ++k, ++tcount) {
+        const int t = take_tile(k);
+        if (t == -2) {
+          ok = false;
+          break;
+        }
+        release_tile(k);
+        if (t < 0) break;
         int b, p, j;
         decode_pair(args, t, b, p, j);
         const int m0 = (2 * p + rank) * C::BM, n0 = j * C::BN;
@@ -476,7 +528,17 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
     const uint4 zero4 = make_uint4(0, 0, 0, 0);
     int tcount = 0;
     bool ok = true;
-    for (int t = cid; t < args.total && ok; t += ncl, ++tcount) {
+    for (int k = 0; ok; ++k, ++tcount) {
+      int t = 0;
+      if (lane == 0) t = take_tile(k);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (t == -2) {
+        ok = false;
+        break;
+      }
+      __syncwarp();
+      if (lane == 0) release_tile(k);
+      if (t < 0) break;
       int b, p, j;
       decode_pair(args, t, b, p, j);
       const int m0 = (2 * p + rank) * C::BM;
@@ -795,6 +857,7 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
   a.done = d.done;
   a.wait_target = d.wait_target;
   a.flag_wait = d.done && d.flag_wait ? 1 : 0;
+  a.tile_ctr = d.tile_ctr;
   a.status = status;
   a.epi = epi;
   a.epi.sym = d.sym;
@@ -817,6 +880,10 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* statu
   *why = nullptr;
   if (d.split < 1 || d.split > 3 || (d.split == 2 && !d.b_mn)) {
     *why = "unsupported operand split";
+    return cudaErrorInvalidValue;
+  }
+  if (!d.tile_ctr) {
+    *why = "tensor-core GEMM needs a zeroed tile counter";
     return cudaErrorInvalidValue;
   }
   if (d.M % 256 || d.N % 256 || d.K % 128) {
