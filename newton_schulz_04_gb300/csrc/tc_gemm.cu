@@ -572,12 +572,35 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       auto ld16 = [&](const uint16_t* q) {
         return coherent ? __ldcg(reinterpret_cast<const uint4*>(q)) : __ldg(reinterpret_cast<const uint4*>(q));
       };
-      uint4 nh[4], nl[4];  // residual words of the next chunk
+      // Each chunk of the residual (32 rows x 64 B per part) is read
+      // coalesced: load `it` of lane `lane` is row it * 8 + lane / 4, 16 bytes
+      // at column (lane % 4) * 8; the rows are turned back into one row per
+      // lane through the warp's box when the chunk is used.
+      const long long rrow0 = static_cast<long long>(b) * e.bs + static_cast<long long>(r0) * e.ld + cb;
+      const long long cpiece = static_cast<long long>(lane >> 2) * e.ld + (lane & 3) * 8;
+      const uint16_t* rh0 = has_r ? static_cast<const uint16_t*>(e.Rh) + rrow0 + cpiece : nullptr;
+      const uint16_t* rl0 = has_rl ? static_cast<const uint16_t*>(e.Rl) + rrow0 + cpiece : nullptr;
+      const long long rows8 = 8 * e.ld;
+      uint4 nh[4], nl[4];  // this lane's coalesced pieces of the next chunk
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        nh[q] = has_r ? ld16(rh + q * 8) : zero4;
-        nl[q] = has_rl ? ld16(rl + q * 8) : zero4;
+        nh[q] = has_r ? ld16(rh0 + q * rows8) : zero4;
+        nl[q] = has_rl ? ld16(rl0 + q * rows8) : zero4;
       }
+      // coalesced pieces -> this lane's row (32 values as 16 words)
+      auto to_rows = [&](const uint4 (&piece)[4], uint32_t (&w)[16]) {
+        constexpr int STRIDE = 64 + 16;
+#pragma unroll
+        for (int it = 0; it < 4; ++it)
+          *reinterpret_cast<uint4*>(box + (it * 8 + (lane >> 2)) * STRIDE + (lane & 3) * 16) = piece[it];
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 x = *reinterpret_cast<const uint4*>(box + lane * STRIDE + q * 16);
+          w[4 * q] = x.x, w[4 * q + 1] = x.y, w[4 * q + 2] = x.z, w[4 * q + 3] = x.w;
+        }
+        __syncwarp();
+      };
       const int abuf = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1;
       if (*abort_flag || !mbar_wait(&tfull[abuf], aph)) {
@@ -596,16 +619,18 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
         float v[32];
         tmem_ld_32x32b_x32(tbase + cc * 32, v);
         uint32_t rhw[16], rlw[16];
+        if (has_r) to_rows(nh, rhw);
+        if (has_rl) {
+          to_rows(nl, rlw);
+        } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          rhw[4 * q] = nh[q].x, rhw[4 * q + 1] = nh[q].y, rhw[4 * q + 2] = nh[q].z, rhw[4 * q + 3] = nh[q].w;
-          rlw[4 * q] = nl[q].x, rlw[4 * q + 1] = nl[q].y, rlw[4 * q + 2] = nl[q].z, rlw[4 * q + 3] = nl[q].w;
+          for (int u = 0; u < 16; ++u) rlw[u] = 0u;
         }
         if (cc + 1 < NCH) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            nh[q] = has_r ? ld16(rh + (cc + 1) * 32 + q * 8) : zero4;
-            nl[q] = has_rl ? ld16(rl + (cc + 1) * 32 + q * 8) : zero4;
+            nh[q] = has_r ? ld16(rh0 + q * rows8 + (cc + 1) * 32) : zero4;
+            nl[q] = has_rl ? ld16(rl0 + q * rows8 + (cc + 1) * 32) : zero4;
           }
         }
         if (has_r) {
