@@ -362,22 +362,37 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       int it = 0;
       bool ok = true;
       int ready_b = -1;  // last matrix whose inputs are known to be complete
+      // Leader: fetch tiles from the counter and publish them to both CTAs,
+      // one tile ahead of its own loads so the fetch's round trip overlaps them.
+      int pub = 0;         // tiles published so far (the last may be the -1 end mark)
+      bool ended = false;  // the end mark is published
+      auto publish_next = [&]() -> bool {
+        const int slot = pub % C::QD;
+        bool live = !*abort_flag && mbar_wait(&qempty[slot], ((pub / C::QD) & 1) ^ 1);
+        int t = -1;
+        if (live) {
+          t = atomicAdd(args.tile_ctr, 1);
+          if (t >= args.total) t = -1;
+        }
+        tq[slot] = t;
+        st_shared_cluster(mapa_cluster(const_cast<int*>(&tq[slot]), 1), t);
+        mbar_arrive_cluster(mapa_cluster(&qfull[slot], 0));
+        mbar_arrive_cluster(mapa_cluster(&qfull[slot], 1));
+        ++pub;
+        ended = t < 0;
+        return live;
+      };
       for (int k = 0; ok; ++k) {
         int t;
         if (rank == 0) {
-          // fetch the next tile and publish it to both CTAs of the pair
-          const int slot = k % C::QD;
-          if (*abort_flag || !mbar_wait(&qempty[slot], ((k / C::QD) & 1) ^ 1)) {
-            ok = false;
-            t = -1;
-          } else {
-            t = atomicAdd(args.tile_ctr, 1);
-            if (t >= args.total) t = -1;
+          while (!ended && pub <= k + 1) {
+            if (!publish_next()) {
+              ok = false;
+              break;
+            }
           }
-          tq[slot] = t;
-          st_shared_cluster(mapa_cluster(const_cast<int*>(&tq[slot]), 1), t);
-          mbar_arrive_cluster(mapa_cluster(&qfull[slot], 0));
-          mbar_arrive_cluster(mapa_cluster(&qfull[slot], 1));
+          if (!ok) break;
+          t = tq[k % C::QD];  // published above (this thread wrote it)
         } else {
           t = take_tile(k);
           if (t == -2) {
