@@ -362,18 +362,16 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       int it = 0;
       bool ok = true;
       int ready_b = -1;  // last matrix whose inputs are known to be complete
-      // Leader: fetch tiles from the counter and publish them to both CTAs,
-      // one tile ahead of its own loads so the fetch's round trip overlaps them.
+      // Leader: take tiles from the counter and publish them to both CTAs.
+      // Tile k + 1 is fetched when tile k starts (the atomic's result is
+      // only read after tile k's loads are issued, so its round trip overlaps
+      // them) and published once those loads are out.
       int pub = 0;         // tiles published so far (the last may be the -1 end mark)
       bool ended = false;  // the end mark is published
-      auto publish_next = [&]() -> bool {
+      auto publish = [&](int t) -> bool {
         const int slot = pub % C::QD;
-        bool live = !*abort_flag && mbar_wait(&qempty[slot], ((pub / C::QD) & 1) ^ 1);
-        int t = -1;
-        if (live) {
-          t = atomicAdd(args.tile_ctr, 1);
-          if (t >= args.total) t = -1;
-        }
+        const bool live = !*abort_flag && mbar_wait(&qempty[slot], ((pub / C::QD) & 1) ^ 1);
+        if (!live || t >= args.total) t = -1;
         tq[slot] = t;
         st_shared_cluster(mapa_cluster(const_cast<int*>(&tq[slot]), 1), t);
         mbar_arrive_cluster(mapa_cluster(&qfull[slot], 0));
@@ -382,17 +380,13 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
         ended = t < 0;
         return live;
       };
+      if (rank == 0 && !publish(atomicAdd(args.tile_ctr, 1))) ok = false;
       for (int k = 0; ok; ++k) {
         int t;
+        int fetched = -1;  // the next tile (leader), in flight during this tile's loads
         if (rank == 0) {
-          while (!ended && pub <= k + 1) {
-            if (!publish_next()) {
-              ok = false;
-              break;
-            }
-          }
-          if (!ok) break;
-          t = tq[k % C::QD];  // published above (this thread wrote it)
+          t = tq[k % C::QD];  // this thread published it
+          if (t >= 0 && !ended) fetched = atomicAdd(args.tile_ctr, 1);
         } else {
           t = take_tile(k);
           if (t == -2) {
@@ -455,6 +449,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
               tma_load_3d_pair(mb, fbar, sb + q * C::MN_BOX_BYTES, nb0 + q * C::MN_ATOM, k0, b);
           }
         }
+        if (rank == 0 && ok && !ended && !publish(fetched)) ok = false;
       }
       if (!ok) {
         atomicOr(args.status, kStatusTimeout);
