@@ -75,13 +75,16 @@ struct TcCfg {
   static constexpr int B_TILE = BNH * BK * 2;  // this CTA's half of the B tile
   static constexpr int STAGE = A_TILE + B_TILE;
   static constexpr int STAGES = 3;
-  // Epilogue: 8 warps, two per TMEM lane quarter, each on EPI_COLS columns.
-  // Each warp stages its outputs through one padded 32-row box (32 rows of
-  // 64 B at an 80-byte stride), which it writes and reads back itself.
-  static constexpr int EPI_WARPS = 8;
-  static constexpr int EPI_COLS = BN / 2;
+  // Epilogue: WPQ warps per TMEM lane quarter; warp q of a quarter takes the
+  // chunks q, q + WPQ, ... of CH columns of its 32 rows.  Each warp stages
+  // its outputs through one padded 32-row box (rows of 2 CH bytes, 16 bytes
+  // of padding), which it writes and reads back itself.
+  static constexpr int CH = 32;
+  static constexpr int WPQ = 2;
+  static constexpr int EPI_WARPS = 4 * WPQ;
+  static constexpr int NCHT = BN / CH;  // chunks per tile row
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr int ROWBOX = 32 * (64 + 16);
+  static constexpr int ROWBOX = 32 * (2 * CH + 16);
   static constexpr int STG = EPI_WARPS * ROWBOX;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = STAGES * STAGE + STG + BAR_BYTES + 1024;
@@ -99,7 +102,7 @@ struct TcCfg {
   static constexpr uint32_t Q_ARRIVALS = 2 + 2 * EPI_WARPS;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(BAR_BYTES >= (2 * STAGES + 5 + 2 * QD) * 8 + 4 * QD + 8, "barrier area too small");
-  static_assert(EPI_WARPS == 8 && EPI_COLS % 32 == 0, "two epilogue warps per TMEM lane quarter");
+  static_assert((CH == 16 || CH == 32) && WPQ >= 1 && NCHT >= WPQ, "epilogue chunking");
 };
 
 struct TcArgs {
@@ -168,6 +171,10 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// One chunk of 32 accumulator rows (this warp's lane quarter) from TMEM.
+__device__ __forceinline__ void tmem_ld_rows(uint32_t taddr, float (&v)[32]) { tmem_ld_32x32b_x32(taddr, v); }
+__device__ __forceinline__ void tmem_ld_rows(uint32_t taddr, float (&v)[16]) { tmem_ld_32x32b_x16(taddr, v); }
+
 __device__ __forceinline__ uint32_t pack2_h(float a, float b) {
   const __half2 h = __floats2half2_rn(a, b);  // a in the low half
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -178,11 +185,12 @@ __device__ __forceinline__ float2 unpack2_h(uint32_t w) {
 
 // Split 32 values into packed 16-bit pairs: bf16 head hw = bf16(v), residual
 // lw = bf16(v - head); or fp16 head hw = fp16(v), residual lw = fp16((v - head) * kF16LoScale).
-__device__ __forceinline__ void split_words(const float (&v)[32], uint32_t (&hw)[16], uint32_t (&lw)[16],
+template <int N>
+__device__ __forceinline__ void split_words(const float (&v)[N], uint32_t (&hw)[N / 2], uint32_t (&lw)[N / 2],
                                             bool want_lo, bool f16) {
   if (f16) {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < N / 2; ++k) {
       hw[k] = pack2_h(v[2 * k], v[2 * k + 1]);
       if (want_lo) {
         const float2 h = unpack2_h(hw[k]);
@@ -191,41 +199,42 @@ __device__ __forceinline__ void split_words(const float (&v)[32], uint32_t (&hw)
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < N / 2; ++k) {
       hw[k] = pack2(v[2 * k], v[2 * k + 1]);
       if (want_lo) lw[k] = pack2(v[2 * k] - bf_lo(hw[k]), v[2 * k + 1] - bf_hi(hw[k]));
     }
   }
 }
 
-// Store a 32 x 32 block of 16-bit values to dst (row stride ld elements): lane
-// t holds row t as 16 packed words.  The rows go through the warp's padded
-// box (80-byte stride: a phase of 8 lanes writing 16 bytes each hits 32
-// distinct banks), then each warp-wide 16-byte store covers 8 whole 64-byte
-// row segments.
-__device__ __forceinline__ void store_block16(uint16_t* dst, long long ld, int lane, const uint32_t (&w)[16],
+// Store a 32 x CH block of 16-bit values to dst (row stride ld elements):
+// lane t holds row t as CH / 2 packed words.  The rows go through the warp's
+// padded box (row stride 2 CH + 16 bytes: the 16-byte accesses of a phase of
+// 8 lanes hit distinct banks), then each warp-wide 16-byte store covers whole
+// row segments of 2 CH bytes.
+template <int CH>
+__device__ __forceinline__ void store_block16(uint16_t* dst, long long ld, int lane, const uint32_t (&w)[CH / 2],
                                               uint8_t* box) {
-  constexpr int STRIDE = 64 + 16;
+  constexpr int STRIDE = 2 * CH + 16, P = 2 * CH / 16, RPI = 32 / P;
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
+  for (int q = 0; q < P; ++q)
     *reinterpret_cast<uint4*>(box + lane * STRIDE + q * 16) =
         make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
   __syncwarp();
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int row = it * 8 + (lane >> 2), pc = lane & 3;
+  for (int it = 0; it < P; ++it) {
+    const int row = it * RPI + lane / P, pc = lane % P;
     *reinterpret_cast<uint4*>(dst + row * ld + pc * 8) = *reinterpret_cast<const uint4*>(box + row * STRIDE + pc * 16);
   }
   __syncwarp();
 }
 
-// Final write of a full 32 x 32 block to a caller's row-major matrix (not
+// Final write of a full 32 x CH block to a caller's row-major matrix (not
 // transposed): global memory is read and written a warp-wide few rows at a time
 // through a padded shared-memory box, lane t owning row t in between.
-template <typename T>
+template <typename T, int CH>
 __device__ __forceinline__ void final_block_rows(const EpiParams& e, int b, int r0, int c0, int lane,
-                                                 const float (&v)[32], uint8_t* box) {
-  constexpr int ROWB = 32 * static_cast<int>(sizeof(T));  // bytes of one block row
+                                                 const float (&v)[CH], uint8_t* box) {
+  constexpr int ROWB = CH * static_cast<int>(sizeof(T));  // bytes of one block row
   constexpr int STRIDE = ROWB + 16;                        // padded row stride in shared memory
   constexpr int PIECES = ROWB / 16;                        // 16-byte pieces per row
   constexpr int ROWS_PER = 32 / PIECES;                    // rows covered by one warp-wide access
@@ -526,15 +535,17 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    const int quarter = warp & 3;  // TMEM lanes this warp may read
+    constexpr int CH = C::CH;
+    constexpr int P = 2 * CH / 16;  // 16-byte pieces per row of a chunk
+    constexpr int RPI = 32 / P;     // rows covered by one warp-wide coalesced access
+    const int quarter = warp & 3;   // TMEM lanes this warp may read
     const int ew = warp - 2;
-    const int half = ew >> 2;      // which EPI_COLS columns of the tile
+    const int jq = ew >> 2;         // this warp's index among the WPQ warps of its quarter
     const EpiParams& e = args.epi;
     uint8_t* box = staging + ew * C::ROWBOX;
     const bool has_lo = e.Ol != nullptr;
     const bool has_r = e.Rh != nullptr;
     const bool has_rl = e.Rl != nullptr;
-    constexpr int NCH = C::EPI_COLS / 32;  // 32-column chunks per warp and tile
     const uint4 zero4 = make_uint4(0, 0, 0, 0);
     int tcount = 0;
     bool ok = true;
@@ -554,11 +565,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       const int m0 = (2 * p + rank) * C::BM;
       const int r0 = m0 + quarter * 32;
       const int r = r0 + lane;
-      const int cb = j * C::BN + half * C::EPI_COLS;
-      // lane `lane` reads its own row of the residual pair, 32 columns per chunk
-      const long long roff = static_cast<long long>(b) * e.bs + static_cast<long long>(r) * e.ld + cb;
-      const uint16_t* rh = has_r ? static_cast<const uint16_t*>(e.Rh) + roff : nullptr;
-      const uint16_t* rl = has_rl ? static_cast<const uint16_t*>(e.Rl) + roff : nullptr;
+      const int cb = j * C::BN;  // first column of the tile
       if (args.flag_wait && has_r) {
         // the residual may be the previous launch's output: acquire its
         // counter before the first residual load below
@@ -566,15 +573,19 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
       }
-      // While the main loop runs, pull this lane's residual row (and, in the
-      // final apply, its row of the caller's W) into L2.
-      if (has_r) bulk_prefetch_l2(rh, C::EPI_COLS * 2);
-      if (has_rl) bulk_prefetch_l2(rl, C::EPI_COLS * 2);
-      if (e.final_mode == FINAL_APPLY && !e.tr[b] && args.final_vec && r < e.rows_valid &&
-          cb + C::EPI_COLS <= e.cols_valid) {
-        const int esz = e.dst_fp32 ? 4 : 2;
-        bulk_prefetch_l2(static_cast<const uint8_t*>(e.dst[b]) + (static_cast<long long>(r) * e.cols_valid + cb) * esz,
-                         C::EPI_COLS * esz);
+      // While the main loop runs, pull this lane's rows of the residual (and,
+      // in the final apply, of the caller's W) into L2 (one warp per quarter).
+      const long long roff = static_cast<long long>(b) * e.bs + static_cast<long long>(r) * e.ld + cb;
+      if (jq == 0) {
+        if (has_r) bulk_prefetch_l2(static_cast<const uint16_t*>(e.Rh) + roff, C::BN * 2);
+        if (has_rl) bulk_prefetch_l2(static_cast<const uint16_t*>(e.Rl) + roff, C::BN * 2);
+        if (e.final_mode == FINAL_APPLY && !e.tr[b] && args.final_vec && r < e.rows_valid &&
+            cb + C::BN <= e.cols_valid) {
+          const int esz = e.dst_fp32 ? 4 : 2;
+          bulk_prefetch_l2(
+              static_cast<const uint8_t*>(e.dst[b]) + (static_cast<long long>(r) * e.cols_valid + cb) * esz,
+              C::BN * esz);
+        }
       }
       // Residual loads: through the read-only cache, unless the previous launch
       // may still be writing other matrices (chained), then from L2.
@@ -582,30 +593,30 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       auto ld16 = [&](const uint16_t* q) {
         return coherent ? __ldcg(reinterpret_cast<const uint4*>(q)) : __ldg(reinterpret_cast<const uint4*>(q));
       };
-      // Each chunk of the residual (32 rows x 64 B per part) is read
-      // coalesced: load `it` of lane `lane` is row it * 8 + lane / 4, 16 bytes
-      // at column (lane % 4) * 8; the rows are turned back into one row per
-      // lane through the warp's box when the chunk is used.
+      // Each chunk of the residual (32 rows x 2 CH bytes per part) is read
+      // coalesced: load `it` of lane `lane` is row it * RPI + lane / P, 16
+      // bytes at column (lane % P) * 8; the rows are turned back into one row
+      // per lane through the warp's box when the chunk is used.
       const long long rrow0 = static_cast<long long>(b) * e.bs + static_cast<long long>(r0) * e.ld + cb;
-      const long long cpiece = static_cast<long long>(lane >> 2) * e.ld + (lane & 3) * 8;
+      const long long cpiece = static_cast<long long>(lane / P) * e.ld + (lane % P) * 8;
       const uint16_t* rh0 = has_r ? static_cast<const uint16_t*>(e.Rh) + rrow0 + cpiece : nullptr;
       const uint16_t* rl0 = has_rl ? static_cast<const uint16_t*>(e.Rl) + rrow0 + cpiece : nullptr;
-      const long long rows8 = 8 * e.ld;
-      uint4 nh[4], nl[4];  // this lane's coalesced pieces of the next chunk
+      const long long rows_it = static_cast<long long>(RPI) * e.ld;
+      uint4 nh[P], nl[P];  // this lane's coalesced pieces of the next chunk
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        nh[q] = has_r ? ld16(rh0 + q * rows8) : zero4;
-        nl[q] = has_rl ? ld16(rl0 + q * rows8) : zero4;
+      for (int q = 0; q < P; ++q) {
+        nh[q] = has_r ? ld16(rh0 + q * rows_it + jq * CH) : zero4;
+        nl[q] = has_rl ? ld16(rl0 + q * rows_it + jq * CH) : zero4;
       }
-      // coalesced pieces -> this lane's row (32 values as 16 words)
-      auto to_rows = [&](const uint4 (&piece)[4], uint32_t (&w)[16]) {
-        constexpr int STRIDE = 64 + 16;
+      // coalesced pieces -> this lane's row (CH values as CH / 2 words)
+      auto to_rows = [&](const uint4 (&piece)[P], uint32_t (&w)[CH / 2]) {
+        constexpr int STRIDE = 2 * CH + 16;
 #pragma unroll
-        for (int it = 0; it < 4; ++it)
-          *reinterpret_cast<uint4*>(box + (it * 8 + (lane >> 2)) * STRIDE + (lane & 3) * 16) = piece[it];
+        for (int it = 0; it < P; ++it)
+          *reinterpret_cast<uint4*>(box + (it * RPI + lane / P) * STRIDE + (lane % P) * 16) = piece[it];
         __syncwarp();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < P; ++q) {
           const uint4 x = *reinterpret_cast<const uint4*>(box + lane * STRIDE + q * 16);
           w[4 * q] = x.x, w[4 * q + 1] = x.y, w[4 * q + 2] = x.z, w[4 * q + 3] = x.w;
         }
@@ -620,67 +631,69 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       tc_fence_after();
       const float sc = epi_scale(e, b);
       const float ka = sc * e.c_acc, kr = sc * e.c_res * e.r_scale;
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + abuf * C::BN + half * C::EPI_COLS;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + abuf * C::BN;
+      constexpr int MAXIT = (C::NCHT + C::WPQ - 1) / C::WPQ;  // chunks of the busiest warp of a quarter
 #pragma unroll
-      for (int cc = 0; cc < NCH; ++cc) {
-        const int c0 = cb + cc * 32;
+      for (int i = 0; i < MAXIT; ++i) {
+        const int cc = jq + i * C::WPQ;
+        if (cc >= C::NCHT) break;
+        const int c0 = cb + cc * CH;
         __syncwarp();
-        float v[32];
-        tmem_ld_32x32b_x32(tbase + cc * 32, v);
-        uint32_t rhw[16], rlw[16];
+        float v[CH];
+        tmem_ld_rows(tbase + cc * CH, v);
+        uint32_t rhw[CH / 2], rlw[CH / 2];
         if (has_r) to_rows(nh, rhw);
         if (has_rl) {
           to_rows(nl, rlw);
         } else {
 #pragma unroll
-          for (int u = 0; u < 16; ++u) rlw[u] = 0u;
+          for (int u = 0; u < CH / 2; ++u) rlw[u] = 0u;
         }
-        if (cc + 1 < NCH) {
+        if (cc + C::WPQ < C::NCHT) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            nh[q] = has_r ? ld16(rh0 + q * rows8 + (cc + 1) * 32) : zero4;
-            nl[q] = has_rl ? ld16(rl0 + q * rows8 + (cc + 1) * 32) : zero4;
+          for (int q = 0; q < P; ++q) {
+            nh[q] = has_r ? ld16(rh0 + q * rows_it + (cc + C::WPQ) * CH) : zero4;
+            nl[q] = has_rl ? ld16(rl0 + q * rows_it + (cc + C::WPQ) * CH) : zero4;
           }
         }
         if (has_r) {
           if (e.r_f16) {
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < CH / 2; ++u) {
               const float2 h = unpack2_h(rhw[u]), l = unpack2_h(rlw[u]);  // rlw = 0 without a residual part
               v[2 * u] = ka * v[2 * u] + kr * (h.x + l.x * (1.f / kF16LoScale));
               v[2 * u + 1] = ka * v[2 * u + 1] + kr * (h.y + l.y * (1.f / kF16LoScale));
             }
           } else {
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < CH / 2; ++u) {
               v[2 * u] = ka * v[2 * u] + kr * (bf_lo(rhw[u]) + bf_lo(rlw[u]));
               v[2 * u + 1] = ka * v[2 * u + 1] + kr * (bf_hi(rhw[u]) + bf_hi(rlw[u]));
             }
           }
-        } else {
+        } else if (ka != 1.f) {
 #pragma unroll
-          for (int u = 0; u < 32; ++u) v[u] *= ka;
+          for (int u = 0; u < CH; ++u) v[u] *= ka;
         }
-        if (e.c_id != 0.f && r >= c0 && r < c0 + 32 && r < e.rows_valid) {
+        if (e.c_id != 0.f && r >= c0 && r < c0 + CH && r < e.rows_valid) {
 #pragma unroll
-          for (int u = 0; u < 32; ++u)
+          for (int u = 0; u < CH; ++u)
             if (c0 + u == r) v[u] += e.c_id;
         }
         if (e.final_mode != FINAL_NONE) {
-          const bool full_block = r0 + 32 <= e.rows_valid && c0 + 32 <= e.cols_valid;
+          const bool full_block = r0 + 32 <= e.rows_valid && c0 + CH <= e.cols_valid;
           if (!e.tr[b] && !e.dst_fp32 && args.final_vec && full_block) {
-            final_block_rows<bf16>(e, b, r0, c0, lane, v, box);
+            final_block_rows<bf16, CH>(e, b, r0, c0, lane, v, box);
           } else {
 #pragma unroll
-            for (int u = 0; u < 32; ++u) epi_final_elem(e, b, r, c0 + u, v[u]);
+            for (int u = 0; u < CH; ++u) epi_final_elem(e, b, r, c0 + u, v[u]);
           }
         } else {
-          uint32_t hw[16], lw[16];
-          split_words(v, hw, lw, has_lo, e.o_f16 != 0);
+          uint32_t hw[CH / 2], lw[CH / 2];
+          split_words<CH>(v, hw, lw, has_lo, e.o_f16 != 0);
           const long long off = static_cast<long long>(b) * e.bs + static_cast<long long>(r0) * e.ld + c0;
-          store_block16(static_cast<uint16_t*>(e.Oh) + off, e.ld, lane, hw, box);
-          if (has_lo) store_block16(static_cast<uint16_t*>(e.Ol) + off, e.ld, lane, lw, box);
+          store_block16<CH>(static_cast<uint16_t*>(e.Oh) + off, e.ld, lane, hw, box);
+          if (has_lo) store_block16<CH>(static_cast<uint16_t*>(e.Ol) + off, e.ld, lane, lw, box);
         }
       }
       // this warp's TMEM rows are read: release the buffer to the leader's MMA issuer
