@@ -157,11 +157,6 @@ __device__ __forceinline__ void decode_pair(const TcArgs& a, int t, int& b, int&
   }
 }
 
-// Byte offset inside a [32 rows x 64 B] box stored with the 64-byte TMA swizzle
-// (16-byte chunk index XOR-ed with bits 7..8 of the row address).
-__device__ __forceinline__ uint32_t sw64(int row, int byte) {
-  return static_cast<uint32_t>(row * 64 + ((((byte >> 4) ^ (row >> 1)) & 3) << 4) + (byte & 15));
-}
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -518,7 +513,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
                                      : make_sdesc(a0 + koff, 16, SBO, C::SWZ);
             const uint64_t bd = b_mn ? make_sdesc(b0 + kk * 16 * 128, C::MN_BOX_BYTES, SBO, C::SWZ)
                                      : make_sdesc(b0 + koff, 16, SBO, C::SWZ);
-            tc_mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit_pair(&empty[s], 0x3);  // both CTAs' stage s is free once these MMAs have read it
         }
