@@ -1,11 +1,18 @@
 // tc_gemm.cu -- batched bf16 / fp16 tensor-core GEMM / SYRK for sm_103a (tcgen05 + TMEM + TMA).
 //
-// One persistent CTA per SM walks a list of 128 x 256 output tiles spread over a
+// A persistent grid of CTA pairs works through the 256 x 256 output tiles of a
 // batch of same-shape matrices (DMuon technical summary, §2.2: same-shape
 // matrices are batched so small problems still fill the GPU).  For symmetric
 // outputs (the Gram matrix G = X X^T and every product of the commuting
 // polynomials of G) only tiles that touch the lower triangle are computed (same
 // section: the symmetric products compute only the lower triangle).
+//
+// Tile scheduling.  Each pair's leader takes tile indices in order from a
+// counter in global memory (atomicAdd) and publishes them to both CTAs through
+// a small shared-memory queue, so pairs that start early -- e.g. while the
+// previous launch on the stream drains -- take more tiles.  Optionally a launch
+// is chained to the previous one per matrix (TcArgs::done): it starts matrix b
+// once the previous launch's epilogues have published all of b's tiles.
 //
 // Symmetric storage.  A symmetric s x s matrix is stored "block-lower": only
 // its 256 x 256 blocks (I, J) with J <= I are written (diagonal blocks in
@@ -19,14 +26,15 @@
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer; accumulators are
 //               double-buffered in TMEM (2 x 256 fp32 columns) so the epilogue of
 //               one tile overlaps the main loop of the next
-//   warps 2..9  epilogue, two warps per TMEM lane quarter (warp % 4), each on one
-//               128-column half of the tile: tcgen05.ld, fused arithmetic
-//               (EpiParams) with the residual read from global memory one chunk
-//               ahead, then 32 x 32 blocks of 16-bit values (bf16 or fp16 pairs)
-//               passed through a padded shared-memory box and written with
-//               row-contiguous 16-byte stores.  With one warp per scheduler the
-//               epilogue ran at a fraction of the issue rate and, at K = 1024,
-//               took as long as the main loop
+//   warps 2..9  epilogue, WPQ = 2 warps per TMEM lane quarter (warp % 4), each
+//               taking every other CH = 32-column chunk of its 32 rows:
+//               tcgen05.ld, fused arithmetic (EpiParams) with the residual read
+//               coalesced from global memory one chunk ahead, then 32 x 32
+//               blocks of 16-bit values (bf16 or fp16 pairs) passed through a
+//               padded shared-memory box and written with row-contiguous
+//               16-byte stores.  With one warp per scheduler the epilogue ran
+//               at a fraction of the issue rate and, at K = 1024, took as long
+//               as the main loop
 //
 // Split operands.  A value X carried as a bf16 head Xh and a bf16 residual Xl
 // (X ~ Xh + Xl to ~16 significant bits) is multiplied as a sum of plain bf16
