@@ -430,11 +430,13 @@ class MuonUpdater:
     parameter shapes; `step(grads)` calls the C ABI once.  With
     `use_graph=True` the first step with a given set of gradient tensors runs
     eagerly and is captured into a CUDA graph; later steps with the same
-    tensors replay it (one launch of the whole kernel sequence).
+    tensors replay it (one launch of the whole kernel sequence).  Graphs are
+    kept for up to `max_graphs` sets of gradient tensors (e.g. two buffers
+    that alternate while the next step's gradients are copied in).
     """
 
     def __init__(self, params: Sequence[torch.Tensor], beta=0.95, lr=0.02, steps=5, coeffs=None,
-                 schedule="auto", workspace_limit: int | None = None, use_graph: bool = False):
+                 schedule="auto", workspace_limit: int | None = None, use_graph: bool = False, max_graphs: int = 4):
         self.params = list(params)
         self.beta, self.lr, self.steps, self.coeffs, self.schedule = beta, lr, steps, coeffs, schedule
         self.moms = [torch.zeros(p.shape, dtype=torch.float32, device=p.device) for p in self.params]
@@ -443,8 +445,8 @@ class MuonUpdater:
             need = min(need, int(workspace_limit))
         self.workspace = new_workspace(need, self.params[0].device)
         self.use_graph = use_graph
-        self._graph = None
-        self._graph_key = None
+        self.max_graphs = max_graphs
+        self._graphs = {}  # tuple of gradient data pointers -> CUDAGraph
 
     def _eager(self, grads, stream=None):
         muon_step(self.params, grads, self.moms, self.beta, self.lr, self.steps, self.coeffs, self.schedule,
@@ -455,8 +457,9 @@ class MuonUpdater:
             self._eager(grads, stream)
             return
         key = tuple(g.data_ptr() for g in grads)
-        if self._graph is not None and key == self._graph_key:
-            self._graph.replay()
+        graph = self._graphs.get(key)
+        if graph is not None:
+            graph.replay()
             return
         # this call's update runs eagerly (and sets up per-device state); the same
         # launch sequence is then captured for the following calls
@@ -466,4 +469,6 @@ class MuonUpdater:
         side = torch.cuda.Stream()
         with torch.cuda.graph(graph, stream=side):
             self._eager(grads, side)
-        self._graph, self._graph_key = graph, key
+        if len(self._graphs) >= self.max_graphs:
+            self._graphs.pop(next(iter(self._graphs)))
+        self._graphs[key] = graph

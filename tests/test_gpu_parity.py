@@ -377,3 +377,28 @@ def test_c5_aspect_sweep_fp32(n):
         torch.cuda.synchronize()
         for i in range(2):
             assert rel(O[i].cpu(), oracle_O(w.grads[i], steps)) < TOL_FP32, (n, steps, i)
+
+
+def test_updater_graphs_for_alternating_gradient_buffers():
+    """MuonUpdater keeps one CUDA graph per set of gradient tensors, so two
+    buffers used in turn (the next step's gradients copied in while this step
+    runs) replay their own graphs.  Four steps must equal four direct calls
+    bit for bit, including the momentum."""
+    m = _m()
+    shapes = [(256, 512), (512, 256), (256, 768)]
+    W0 = [synth.random_matrix(a, b, seed=600 + i, std=0.02).to(torch.bfloat16) for i, (a, b) in enumerate(shapes)]
+    Gs = [[synth.random_matrix(a, b, seed=700 + 10 * k + i).to(torch.bfloat16).cuda() for i, (a, b) in enumerate(shapes)]
+          for k in range(2)]
+    Wg = [w.clone().cuda() for w in W0]
+    We = [w.clone().cuda() for w in W0]
+    upd = m.MuonUpdater(Wg, 0.95, 0.02, 5, use_graph=True)
+    ref = m.MuonUpdater(We, 0.95, 0.02, 5, use_graph=False)
+    for k in range(4):
+        upd.step(Gs[k % 2])
+        ref.step(Gs[k % 2])
+    torch.cuda.synchronize()
+    assert len(upd._graphs) == 2
+    for a, b in zip(Wg, We):
+        assert torch.equal(a, b)
+    for a, b in zip(upd.moms, ref.moms):
+        assert torch.equal(a, b)
