@@ -402,3 +402,21 @@ def test_updater_graphs_for_alternating_gradient_buffers():
         assert torch.equal(a, b)
     for a, b in zip(upd.moms, ref.moms):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("sched,dtype", [("orig", torch.bfloat16), ("gram_x3", torch.bfloat16),
+                                         ("orig", torch.float32), ("gram_x3", torch.float32)])
+@pytest.mark.parametrize("steps", [1, 2, 3])
+def test_each_product_through_few_steps(sched, dtype, steps):
+    """One step is O = P_0 X_0 with P_0 = a I + b G_0 + c G_0^2 (the SYRK, the
+    polynomial and the projection); two steps add the Q and G updates (Gram)
+    or a second X update (original).  Checking T = 1, 2, 3 against the oracle
+    pins each product's contribution, on a ragged shape (200 x 328)."""
+    m = _m()
+    X = torch.stack([synth.random_matrix(200, 328, seed=810 + i) for i in range(2)]).to(dtype).cuda()
+    O = m.ns_batched(X, steps=steps, schedule=sched)
+    torch.cuda.synchronize()
+    tol = TOL_FP32 if dtype == torch.float32 else TOL_BF16
+    for i in range(2):
+        e = rel(O[i].float().cpu(), oracle_O(X[i], steps))
+        assert e < tol, (sched, dtype, steps, i, e)
