@@ -196,6 +196,11 @@ MUON_API muon_status muon_debug_bounded_wait(void* ws, long long max_cycles, voi
  *   if out_lo is not NULL, out_lo = bf16(C - out) ([batch, M, N] each).
  *   dt = MUON_FP16: the same kernel on fp16 A, B (and A_lo, B_lo); C is
  *   returned as an fp16 pair, out = fp16(C), out_lo = fp16((C - out) * 2^11).
+ *   split = 4 (fp16, b_mn = 1, M == K, sym bit 0 clear): C = A B + B_lo / 2^11,
+ *   the second term run on the tensor cores as a diagonal K segment (the
+ *   form the original-space update takes for the low part of X); the
+ *   diagonal table is written into the workspace after the header, so
+ *   ws_bytes must be at least 1024 + 131072.
  *   dt = MUON_FP32 runs the FFMA kernel on fp32 A, B and writes fp32 C to out.
  *   sym bit 0 (M == N): symmetric output; the bf16 kernel computes the tiles
  *   touching the lower triangle and stores the output "block-lower" (only the

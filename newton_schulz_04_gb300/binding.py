@@ -381,13 +381,14 @@ def debug_gemm(A, B, A_lo=None, B_lo=None, split=1, b_mn=False, sym=False, a_sym
     bf16 (or fp16) operands run the tensor-core kernel and return the fp32
     value of the bf16 (fp16) head/residual pair it writes (with sym, only the
     256 x 256 blocks on or below the diagonal are written); a_sym / b_sym
-    declare operands given in that block-lower storage.  fp32 operands run
-    the FFMA kernel."""
+    declare operands given in that block-lower storage.  split=4 (fp16,
+    b_mn, square A) adds B_lo / 2^11 through the diagonal K segment.  fp32
+    operands run the FFMA kernel."""
     lib = load()
     batch, M, K = A.shape
     N = B.shape[2] if b_mn else B.shape[1]
     if workspace is None:
-        workspace = new_workspace(4096, A.device)
+        workspace = new_workspace(1024 + 131072 if split == 4 else 4096, A.device)
     ptr = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
     if A.dtype == torch.float32:
         out = torch.zeros(batch, M, N, dtype=torch.float32, device=A.device)

@@ -31,8 +31,9 @@ enum FinalMode : int { FINAL_NONE = 0, FINAL_STORE = 1, FINAL_APPLY = 2 };
 // applied as W <- W - lr * v (FINAL_APPLY) to the caller's un-packed matrix
 // dst[b].  A 16-bit pair is either bf16, hi = bf16(v) and lo = bf16(v - hi)
 // (about 16 significant bits), or fp16, hi = fp16(v) and lo = fp16((v - hi) *
-// kF16LoScale) (about 22 bits); `r_f16` / `o_f16` select fp16 for the residual
-// / the output.  On the CUDA-core path, `sym` computes the lower triangle and
+// lo_scale) (about 22 bits; lo_scale is kF16LoScale unless the next product
+// folds a coefficient into the stored low part); `r_f16` / `o_f16` select fp16
+// for the residual / the output.  On the CUDA-core path, `sym` computes the lower triangle and
 // mirrors each element; the tensor-core path stores symmetric outputs
 // block-lower.
 struct EpiParams {
@@ -48,6 +49,7 @@ struct EpiParams {
   int r_f16;        // 1: the residual pair is fp16, 0: bf16
   float r_scale;    // multiplies the residual (tensor-core path; e.g. 2^-11 when Rh is the scaled low part of an fp16 pair)
   int o_f16;        // 1: the output pair is fp16, 0: bf16
+  float lo_scale;   // an fp16 output pair's low part is stored as (v - hi) * lo_scale (normally 2^11)
   long long ld;     // leading dimension (elements) of the packed residual / outputs
   long long bs;     // batch stride (elements)
   int sym;

@@ -202,12 +202,36 @@ cudaError_t launch_pack(const PackArgs& a, int B, cudaStream_t st) {
   return launch_pdl(pack_kernel, dim3(a.tiles, B), dim3(256), 0, st, a);
 }
 
+// D = d I (kDiagDim x kDiagDim 16-bit values, d's bit pattern `bits`) written
+// as 16-byte pieces by `nthreads` threads, thread `t` taking pieces t, t + nthreads, ...
+__device__ __forceinline__ void fill_diag(uint4* D, uint16_t bits, int t, int nthreads) {
+  constexpr int PER_ROW = kDiagDim / 8;
+  for (int i = t; i < kDiagDim * PER_ROW; i += nthreads) {
+    const int r = i / PER_ROW, c0 = (i % PER_ROW) * 8;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (r >= c0 && r < c0 + 8) w[(r - c0) >> 1] = static_cast<uint32_t>(bits) << (16 * ((r - c0) & 1));
+    D[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__global__ void __launch_bounds__(256) fill_diag_kernel(uint4* D, uint16_t bits) {
+  pdl_launch_dependents();
+  pdl_wait();
+  fill_diag(D, bits, blockIdx.x * 256 + threadIdx.x, gridDim.x * 256);
+}
+
+cudaError_t launch_fill_diag(void* D, uint16_t bits, cudaStream_t st) {
+  return launch_pdl(fill_diag_kernel, dim3(8), dim3(256), 0, st, static_cast<uint4*>(D), bits);
+}
+
 // inv_norm[b] = 1 / (sqrt(sum of the partials of b) + eps), summed in a fixed order.
+// With `diag`, the blocks also write the table D = d I of the diagonal segment.
 __global__ void __launch_bounds__(256) norm_finalize_kernel(const float* partial, int tiles, float eps,
-                                                            float* inv_norm) {
+                                                            float* inv_norm, uint4* diag, uint16_t diag_bits) {
   __shared__ float red[8];
   pdl_launch_dependents();
   pdl_wait();
+  if (diag) fill_diag(diag, diag_bits, blockIdx.x * 256 + threadIdx.x, gridDim.x * 256);
   const int b = blockIdx.x;
   const float* p = partial + static_cast<long long>(b) * tiles;
   float s = 0.f;
@@ -224,10 +248,11 @@ __global__ void __launch_bounds__(256) norm_finalize_kernel(const float* partial
   }
 }
 
-cudaError_t launch_norm_finalize(const float* partial, int tiles, int B, float eps, float* inv_norm,
-                                 cudaStream_t st) {
+cudaError_t launch_norm_finalize(const float* partial, int tiles, int B, float eps, float* inv_norm, void* diag,
+                                 uint16_t diag_bits, cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
-  return launch_pdl(norm_finalize_kernel, dim3(B), dim3(256), 0, st, partial, tiles, eps, inv_norm);
+  return launch_pdl(norm_finalize_kernel, dim3(B), dim3(256), 0, st, partial, tiles, eps, inv_norm,
+                    static_cast<uint4*>(diag), diag_bits);
 }
 
 struct FinalArgs {

@@ -234,6 +234,7 @@ struct Buffers {
   float* Hf = nullptr;
   float* Af = nullptr;
   float* Bf = nullptr;
+  void* diag = nullptr;  // D = 2^-11 I (fp16) for the update's diagonal segment (ORIG)
 };
 
 static size_t carve_buffers(char* base, int Bc, long long sp, long long lp, int tiles, muon_dtype dt,
@@ -270,6 +271,7 @@ static size_t carve_buffers(char* base, int Bc, long long sp, long long lp, int 
     bf.Gl = static_cast<bf16*>(c.take(2 * ns));
     bf.Bh = static_cast<bf16*>(c.take(2 * ns));
     bf.Bl = static_cast<bf16*>(c.take(2 * ns));
+    bf.diag = c.take(2 * kDiagDim * kDiagDim);
     return c.off;
   }
   const bool x3 = (sc == MUON_SCHED_GRAM_X3);
@@ -376,6 +378,7 @@ static EpiParams epi_packed(const Group& g, const Buffers& bf, int scale_pow, fl
   e.R = R;
   e.Of = Of;
   e.r_scale = 1.f;
+  e.lo_scale = kF16LoScale;
   e.ld = ld;
   e.bs = bs;
   e.rows_valid = static_cast<int>(g.s);
@@ -410,6 +413,21 @@ static void epi_set_final(EpiParams& e, const Ctx& cx, const Group& g, const Mat
   }
 }
 
+// The ORIG update on fp16 operands, X <- B' X_hi + a X_lo, runs the a X_lo
+// term as a diagonal segment of the product (D = 2^-11 I times the low part,
+// stored as a 2^11 (X - X_hi)) when its K (the padded short side) is at most
+// this: 256 more of K per tile is at most 12.5 % more MMA work there, and it
+// takes the residual out of an epilogue that sets the pace at K ~ 1024.  At
+// larger K the main loop already hides the epilogue.
+constexpr long long kDiagMaxK = 2048;
+
+static uint16_t f16_bits(float x) {
+  const __half h = __float2half_rn(x);
+  uint16_t u;
+  memcpy(&u, &h, sizeof(u));
+  return u;
+}
+
 static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int Bc, char* ws) {
   const char* why = nullptr;
   Buffers bf;
@@ -428,6 +446,8 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   const long long bsx = sp * lp, bss = sp * sp;
   const bool fp32 = cx.dt == MUON_FP32;
   const bool x3 = g.sc == MUON_SCHED_GRAM_X3;
+  const bool h16 = !fp32 && g.sc == MUON_SCHED_ORIG && cx.f16_ok;
+  const bool use_diag = h16 && cx.steps >= 2 && sp <= kDiagMaxK;
 
   // ---- momentum + pack + norm
   PackArgs pa;
@@ -482,7 +502,8 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   }
   {
     ProfScope ps("norm_finalize", 0.0, 4.0 * g.tiles * Bc, cx.st);
-    CK(launch_norm_finalize(bf.partial, g.tiles, Bc, kEps, bf.inv_norm, cx.st));
+    CK(launch_norm_finalize(bf.partial, g.tiles, Bc, kEps, bf.inv_norm, use_diag ? bf.diag : nullptr,
+                            f16_bits(1.f / kF16LoScale), cx.st));
   }
 
   if (cx.steps == 0) {
@@ -564,7 +585,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   // A / B is a symmetric operand in that storage.
   auto tc = [&](int split, int b_mn, int sym, int f16, int M, int N, int K, const void* Ah, const void* Al,
                 long long lda, long long bsa, const void* Bh, const void* Bl, long long ldb, long long bsb,
-                const EpiParams& e) {
+                const EpiParams& e, const void* diag = nullptr) {
     TcGemmDesc d;
     d.B = Bc;
     d.M = M;
@@ -578,6 +599,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     d.f16 = f16;
     d.A = TcOperand{Ah, Al, lda, bsa};
     d.Bop = TcOperand{Bh, Bl, ldb, bsb};
+    d.diag = diag;
     const double Kt = K == S ? static_cast<double>(g.s) : static_cast<double>(g.l);
     const double fl = d.sym ? Bc * static_cast<double>(g.s) * g.s * Kt : 2.0 * Bc * g.s * g.l * Kt;
     static const char* const kSym[4] = {"", "tc_sym", "tc_sym_x2", "tc_sym_x3"};
@@ -596,7 +618,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     return err;
   };
 
-  if (g.sc == MUON_SCHED_ORIG && cx.f16_ok) {
+  if (h16) {
     // Step 0 multiplies the packed bf16 copy of M (slot 0: hi, and lo for
     // the residual); A is stored as fp16, and B in the type of this step's X.
     // From step 1 on, X lives in the ping-pong slots as an fp16 pair and
@@ -604,7 +626,10 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     // step 0, so step 1 writes its fp16 X there.
     // The a X term is folded into the product: B' = a I + b A + c A^2, and
     //   X <- B' X_hi + a X_lo = a X + B X_hi,
-    // so the update reads only the low part of X as its residual.
+    // so the update reads only the low part of X as its residual.  With the
+    // diagonal segment (use_diag) the low part written for the next step is
+    // 2^11 a (X - X_hi), and the next update adds 2^-11 I times it on the
+    // tensor cores instead of reading it in the epilogue.
     int cur = 0;
     for (int k = 0; k < T; ++k) {
       const int nxt = cur ^ 1;
@@ -619,14 +644,17 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
       e2.o_f16 = xf;
       CK(tc(1, 0, 7, 1, S, S, S, bf.Gh, nullptr, sp, bss, bf.Gh, nullptr, sp, bss, e2));
       // X <- B' X_hi + a X_lo (k = 0: both terms carry 1 / s), fp16 pair out
-      EpiParams e3 = epi_pair(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, bf.Xlo[cur], nullptr, bf.Xb[nxt], bf.Xlo[nxt],
-                              lp, bsx);
+      const bool dseg = use_diag && k > 0;
+      EpiParams e3 = epi_pair(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, dseg ? nullptr : bf.Xlo[cur], nullptr,
+                              bf.Xb[nxt], bf.Xlo[nxt], lp, bsx);
       e3.r_f16 = xf;
       e3.r_scale = xf ? 1.f / kF16LoScale : 1.f;  // an fp16 pair's low part is stored scaled by 2^11
       e3.o_f16 = 1;
+      if (use_diag) e3.lo_scale = kF16LoScale * cx.a;
       e3.cols_valid = static_cast<int>(g.l);
       if (k == T - 1) epi_set_final(e3, cx, g, mats, Bc);
-      CK(tc(1, 1, 2, xf, S, L, S, bf.Bh, nullptr, sp, bss, bf.Xb[cur], nullptr, lp, bsx, e3));
+      CK(tc(1, 1, 2, xf, S, L, S, bf.Bh, nullptr, sp, bss, bf.Xb[cur], dseg ? bf.Xlo[cur] : nullptr, lp, bsx, e3,
+            dseg ? bf.diag : nullptr));
       cur = nxt;
     }
     return MUON_OK;
@@ -1075,6 +1103,7 @@ muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, cons
   memset(&e, 0, sizeof(e));
   e.c_acc = 1.f;
   e.r_scale = 1.f;
+  e.lo_scale = kF16LoScale;
   if (dt == MUON_FP32) {
     e.Of = static_cast<float*>(out);
   } else {
@@ -1091,9 +1120,13 @@ muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, cons
   const char* why = nullptr;
   if (dt == MUON_BF16 || dt == MUON_FP16) {
     if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 256 || K % 128) return fail(MUON_ERR_SHAPE, "16-bit sizes");
-    if (split < 1 || split > 3) return fail(MUON_ERR_ARG, "split must be 1, 2 or 3");
-    if (split >= 2 && !A_lo) return fail(MUON_ERR_ARG, "split 2 and 3 need A_lo");
-    if (split == 3 && !B_lo) return fail(MUON_ERR_ARG, "split 3 needs B_lo");
+    if (split < 1 || split > 4) return fail(MUON_ERR_ARG, "split must be 1, 2, 3 or 4");
+    if ((split == 2 || split == 3) && !A_lo) return fail(MUON_ERR_ARG, "split 2 and 3 need A_lo");
+    if (split >= 3 && !B_lo) return fail(MUON_ERR_ARG, "split 3 and 4 need B_lo");
+    if (split == 4 && (dt != MUON_FP16 || !b_mn || M != K || (sym & 1)))
+      return fail(MUON_ERR_ARG, "split 4 needs fp16, b_mn = 1, M == K and a full output");
+    if (split == 4 && ws_bytes < kHeader + 2 * kDiagDim * kDiagDim)
+      return fail(MUON_ERR_WORKSPACE, "split 4 needs a %zu-byte workspace", kHeader + 2 * kDiagDim * kDiagDim);
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(A_lo) |
          reinterpret_cast<uintptr_t>(B_lo)) % 16)
       return fail(MUON_ERR_ALIGN, "16-bit operands must be 16-byte aligned");
@@ -1110,14 +1143,20 @@ muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, cons
     d.sym = sym & 1;
     d.a_sym = (sym >> 1) & 1;
     d.b_sym = (sym >> 2) & 1;
-    d.split = split;
+    d.split = split == 4 ? 1 : split;
     d.b_mn = b_mn;
     d.f16 = dt == MUON_FP16 ? 1 : 0;
-    d.A = TcOperand{A, A_lo, K, static_cast<long long>(M) * K};
+    d.A = TcOperand{A, split == 4 ? nullptr : A_lo, K, static_cast<long long>(M) * K};
     d.Bop = TcOperand{B, B_lo, b_mn ? N : K, bsb};
     d.tile_ctr = reinterpret_cast<int*>(static_cast<char*>(ws) + kDebugTileCtr);
     if (cudaMemsetAsync(d.tile_ctr, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return fail(MUON_ERR_CUDA, "memset of the tile counter failed");
+    if (split == 4) {  // D = 2^-11 I after the header
+      d.diag = static_cast<char*>(ws) + kHeader;
+      if (launch_fill_diag(const_cast<void*>(d.diag), f16_bits(1.f / kF16LoScale),
+                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return fail(MUON_ERR_CUDA, "launch of the diagonal fill failed");
+    }
     err = launch_tc_gemm(d, e, static_cast<int*>(ws), static_cast<cudaStream_t>(stream), sms, &why);
     if (err == cudaErrorInvalidValue && why) return fail(MUON_ERR_ARG, "%s", why);
   } else if (dt == MUON_FP32) {

@@ -63,7 +63,13 @@ struct TcGemmDesc {
   // CTA pairs take tiles from it in order (atomicAdd), so clusters that start
   // early (while the previous launch drains) take more of them.
   int* tile_ctr = nullptr;
+  // Diagonal segment (optional; split 1, b_mn = 1, K == M): a kDiagDim x
+  // kDiagDim row-major matrix D = d I of the operand type.  The product is
+  // then C = A B + d Bop.lo, the second term computed by the tensor cores as
+  // D times the pair's own kDiagDim rows of Bop.lo.
+  const void* diag = nullptr;
 };
+constexpr int kDiagDim = 256;
 int tc_signals_per_matrix(int M, int N, int sym);
 
 cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* status, cudaStream_t st, int num_sms,
@@ -84,8 +90,12 @@ cudaError_t launch_simt_gemm(const SimtGemmDesc& d, const EpiParams& epi, cudaSt
 
 // Momentum + pack + partial norms, then per-matrix 1 / (||M||_F + eps).
 cudaError_t launch_pack(const PackArgs& a, int B, cudaStream_t st);
-cudaError_t launch_norm_finalize(const float* partial, int tiles, int B, float eps, float* inv_norm,
-                                 cudaStream_t st);
+// With `diag` (or nullptr) it also writes the diagonal-segment table D = d I
+// (kDiagDim^2 16-bit values, 16-byte aligned; diag_bits = d's bit pattern).
+cudaError_t launch_norm_finalize(const float* partial, int tiles, int B, float eps, float* inv_norm, void* diag,
+                                 uint16_t diag_bits, cudaStream_t st);
+// D = d I on its own (muon_debug_gemm).
+cudaError_t launch_fill_diag(void* D, uint16_t bits, cudaStream_t st);
 // O = Xf * inv_norm written through a final-mode epilogue (zero NS steps).
 cudaError_t launch_final_from_packed(const float* Xf, long long ld, long long bs, int B, const EpiParams& e,
                                      cudaStream_t st);

@@ -43,6 +43,15 @@
 // pair of tensor maps, all accumulating into the same TMEM tile, so split
 // products run on the same 128-byte-swizzled pipeline as plain ones.
 //
+// Diagonal segment.  For C = A B + d B_lo with A square (K == M), B MN-major
+// and d a scalar, the term d B_lo runs on the tensor cores too: rows 256 p ..
+// 256 p + 255 of d B_lo are D B_lo[256 p .. 256 p + 255, :] with D = d I (256
+// x 256), so a CTA pair appends two 128-deep k-blocks to its tile whose A
+// operand is its 128 rows of D (loaded from a small table) and whose B
+// operand is the pair's own 256 rows of B_lo.  This costs 256 more of K per
+// tile and takes the residual out of the epilogue, which at K ~ 1024 sets the
+// pace (the main loop is short).
+
 // B is read K-major ([N, K] row-major: symmetric right operands, whose rows are
 // their columns) or MN-major ([K, N] row-major, e.g. X in B X or Q X).
 //
@@ -123,6 +132,7 @@ struct TcArgs {
   int a_sym;      // A is a symmetric matrix in block-lower storage (upper k-blocks read transposed)
   int b_sym;      // same for B (K-major kernels only)
   int seg_lo;     // bit 2s: segment s reads A's residual map; bit 2s+1: B's residual map
+  int diag_kb;    // k-blocks of the diagonal segment (0, or 256 / BK: D from tmD times B's residual rows)
   int final_vec;  // final mode may use 16-byte accesses to the caller's rows
   int f16;        // operands are fp16 (else bf16)
   int* status;    // workspace status word
@@ -186,18 +196,18 @@ __device__ __forceinline__ float2 unpack2_h(uint32_t w) {
   return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
-// Split 32 values into packed 16-bit pairs: bf16 head hw = bf16(v), residual
-// lw = bf16(v - head); or fp16 head hw = fp16(v), residual lw = fp16((v - head) * kF16LoScale).
+// Split N values into packed 16-bit pairs: bf16 head hw = bf16(v), residual
+// lw = bf16(v - head); or fp16 head hw = fp16(v), residual lw = fp16((v - head) * lo_scale).
 template <int N>
 __device__ __forceinline__ void split_words(const float (&v)[N], uint32_t (&hw)[N / 2], uint32_t (&lw)[N / 2],
-                                            bool want_lo, bool f16) {
+                                            bool want_lo, bool f16, float lo_scale) {
   if (f16) {
 #pragma unroll
     for (int k = 0; k < N / 2; ++k) {
       hw[k] = pack2_h(v[2 * k], v[2 * k + 1]);
       if (want_lo) {
         const float2 h = unpack2_h(hw[k]);
-        lw[k] = pack2_h((v[2 * k] - h.x) * kF16LoScale, (v[2 * k + 1] - h.y) * kF16LoScale);
+        lw[k] = pack2_h((v[2 * k] - h.x) * lo_scale, (v[2 * k + 1] - h.y) * lo_scale);
       }
     }
   } else {
@@ -299,7 +309,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
                    const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmAtl,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBl,
                    const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ CUtensorMap tmBtl,
-                   const __grid_constant__ TcArgs args) {
+                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ TcArgs args) {
   using C = TcCfg;
   extern __shared__ uint8_t smem_raw[];
   // Swizzled tiles must start on a 1024-byte boundary of the shared window.
@@ -338,10 +348,11 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (args.nseg > 1) {
+    if (args.nseg > 1 || args.diag_kb) {
       tma_prefetch_desc(&tmAl);
       tma_prefetch_desc(&tmBl);
     }
+    if (args.diag_kb) tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {  // both CTAs: the pair's TMEM is allocated collectively
     tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
@@ -366,7 +377,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
   };
   auto release_tile = [&](int k) { mbar_arrive_cluster(mapa_cluster(&qempty[k % C::QD], 0)); };
   const int nk = args.K / C::BK;   // k-blocks per segment
-  const int nkb = nk * args.nseg;  // k-blocks per tile
+  const int nks = nk * args.nseg;  // k-blocks of the segments over K
+  const int nkb = nks + args.diag_kb;  // k-blocks per tile
 
   if (warp == 0) {
     if (lane == 0) {
@@ -426,6 +438,24 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
             ok = false;
             break;
           }
+          uint8_t* st = tiles + s * C::STAGE;
+          // both CTAs' copies complete on the leader's barrier for this stage
+          const uint32_t fbar = mapa_cluster(&full[s], 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE);
+          uint8_t* sb = st + C::A_TILE;
+          const int nb0 = n0 + rank * C::BNH;  // this CTA's half of the B tile: columns nb0 .. nb0 + 127
+          if (BMN && kb >= nks) {
+            // diagonal segment: this CTA's 128 rows of D, and the pair's own
+            // rows of B's residual (256 p + 128 dk ..), MN-major
+            const int dk = (kb - nks) * C::BK;
+#pragma unroll
+            for (int g = 0; g < C::KATOMS; ++g)
+              tma_load_3d_pair(&tmD, fbar, st + g * C::KATOM_BYTES, dk + g * C::KA, rank * C::BM, 0);
+#pragma unroll
+            for (int q = 0; q < C::BNH / C::MN_ATOM; ++q)
+              tma_load_3d_pair(&tmBl, fbar, sb + q * C::MN_BOX_BYTES, nb0 + q * C::MN_ATOM, 2 * p * C::BM + dk, b);
+            continue;
+          }
           const int seg = kb / nk;
           const int k0 = (kb - seg * nk) * C::BK;
           const bool alo = (args.seg_lo >> (2 * seg)) & 1;
@@ -434,10 +464,6 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
           // from the stored lower block, read transposed
           const bool a_up = args.a_sym && (k0 >> 8) > (m0 >> 8);
           const bool b_up = !BMN && args.b_sym && (k0 >> 8) > (n0 >> 8);
-          uint8_t* st = tiles + s * C::STAGE;
-          // both CTAs' copies complete on the leader's barrier for this stage
-          const uint32_t fbar = mapa_cluster(&full[s], 0);
-          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE);
           if (!a_up) {
 #pragma unroll
             for (int g = 0; g < C::KATOMS; ++g)
@@ -447,9 +473,6 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
             for (int q = 0; q < C::BM / C::MN_ATOM; ++q)
               tma_load_3d_pair(alo ? &tmAtl : &tmAt, fbar, st + q * C::MN_BOX_BYTES, m0 + q * C::MN_ATOM, k0, b);
           }
-          // this CTA's half of the B tile: columns n0 + 128 rank .. + 127
-          uint8_t* sb = st + C::A_TILE;
-          const int nb0 = n0 + rank * C::BNH;
           if (!BMN && !b_up) {
 #pragma unroll
             for (int g = 0; g < C::KATOMS; ++g)
@@ -506,9 +529,11 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
             break;
           }
           tc_fence_after();
-          const int k0 = (kb % nk) * C::BK;
-          const bool a_mn = args.a_sym && (k0 >> 8) > (m0 >> 8);
-          const bool b_mn = BMN || (args.b_sym && (k0 >> 8) > (n0 >> 8));
+          // the diagonal segment's A (D) is K-major and its B MN-major
+          const bool dseg = kb >= nks;
+          const int k0 = dseg ? 0 : (kb % nk) * C::BK;
+          const bool a_mn = !dseg && args.a_sym && (k0 >> 8) > (m0 >> 8);
+          const bool b_mn = BMN || (!dseg && args.b_sym && (k0 >> 8) > (n0 >> 8));
           const uint32_t idesc =
               make_idesc_f16kind(2 * C::BM, C::BN, b_mn, args.f16 == 0) | (a_mn ? (1u << 15) : 0u);
           const uint32_t a0 = smem_u32(tiles + s * C::STAGE);
@@ -693,7 +718,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
           }
         } else {
           uint32_t hw[CH / 2], lw[CH / 2];
-          split_words<CH>(v, hw, lw, has_lo, e.o_f16 != 0);
+          split_words<CH>(v, hw, lw, has_lo, e.o_f16 != 0, e.lo_scale);
           const long long off = static_cast<long long>(b) * e.bs + static_cast<long long>(r0) * e.ld + c0;
           store_block16<CH>(static_cast<uint16_t*>(e.Oh) + off, e.ld, lane, hw, box);
           if (has_lo) store_block16<CH>(static_cast<uint16_t*>(e.Ol) + off, e.ld, lane, lw, box);
@@ -860,6 +885,9 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
     mBt = mB;
     mBtl = mBl;
   }
+  // D (the diagonal segment's A): one 256 x 256 matrix, K-major boxes like A's
+  CUtensorMap mD = mA;
+  if (d.diag) ok = ok && make_map(&mD, d.diag, f, kDiagDim, kDiagDim, 1, kDiagDim, kDiagDim * kDiagDim, C::KA, C::BM, 128);
   const bool has_out = epi.Oh != nullptr;
   if (!ok) {
     *why = "cuTensorMapEncodeTiled failed";
@@ -902,6 +930,7 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
     a.nseg = 3;
     a.seg_lo = (1 << 3) | (1 << 4);
   }
+  a.diag_kb = d.diag ? kDiagDim / C::BK : 0;
   a.a_sym = d.a_sym;
   a.b_sym = BMN ? 0 : d.b_sym;
   a.f16 = d.f16 ? 1 : 0;
@@ -922,8 +951,7 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
   }
   const int nclusters = std::min(a.total, max_clusters<BMN>(num_sms));
   if (nclusters <= 0) return a.total > 0 ? cudaErrorLaunchOutOfResources : cudaSuccess;
-  return launch_pair(tc_gemm_kernel<BMN>, nclusters, st, mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl,
-                     a);
+  return launch_pair(tc_gemm_kernel<BMN>, nclusters, st, mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl, mD, a);
 }
 
 cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* status, cudaStream_t st, int num_sms,
@@ -947,6 +975,11 @@ cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* statu
   }
   if ((d.a_sym && d.K != d.M) || (d.b_sym && (d.b_mn || d.K != d.N)) || ((d.a_sym || d.b_sym) && d.K % 256)) {
     *why = "symmetric operands must be square with K a multiple of 256";
+    return cudaErrorInvalidValue;
+  }
+  if (d.diag && (d.split != 1 || !d.b_mn || d.K != d.M || !d.Bop.lo ||
+                 reinterpret_cast<uintptr_t>(d.diag) % 16)) {
+    *why = "a diagonal segment needs split 1, an MN-major B with its residual, K == M and an aligned D";
     return cudaErrorInvalidValue;
   }
   return d.b_mn ? launch_impl<true>(d, epi, status, st, num_sms, why)

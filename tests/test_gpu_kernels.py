@@ -230,6 +230,52 @@ def test_tc_fp16_symmetric_operands_in_block_lower_storage():
     assert _rel(out[:, mk], ref[:, mk]) < 2e-5
 
 
+# ---- diagonal K segment: C = A B + B_lo / 2^11 with the second term on the tensor cores
+
+@pytest.mark.parametrize("M,N,batch,a_sym", [(256, 256, 1, False), (512, 768, 2, False), (1024, 256, 3, True),
+                                             (768, 512, 2, True)])
+def test_tc_diagonal_segment(M, N, batch, a_sym):
+    m = _lib()
+    g = torch.Generator().manual_seed(36 + M + N)
+    if a_sym:
+        X = torch.randn(batch, M, M, generator=g, dtype=torch.float64)
+        A64 = (X + X.transpose(1, 2)) / (2 * M)
+    else:
+        A64 = torch.randn(batch, M, M, generator=g, dtype=torch.float64) / M
+    A = A64.to(torch.float16)
+    B = torch.randn(batch, M, N, generator=g).to(torch.float16)
+    B_lo = torch.randn(batch, M, N, generator=g).to(torch.float16)
+    Ad = A.clone()
+    if a_sym:  # block-lower storage: the upper blocks must never be read
+        Ad[:, ~block_lower(M, "cpu")] = float("nan")
+    out = m.debug_gemm(Ad.cuda(), B.cuda(), B_lo=B_lo.cuda(), split=4, b_mn=True, a_sym=a_sym)
+    torch.cuda.synchronize()
+    prod = A.double() @ B.double()
+    ref = prod + B_lo.double() / 2048.0
+    out = out.cpu()
+    assert torch.isfinite(out).all()
+    # every row block gets its own rows of B_lo (a row offset error is O(1) relative)
+    assert _rel(out, ref.float()) < 2e-5
+    assert _rel(prod.float(), ref.float()) > 1e-3  # the segment's term is well above the tolerance
+
+
+def test_tc_diagonal_segment_rejects_unsupported_forms():
+    m = _lib()
+    A = _rand((1, 256, 256), 37, torch.float16)
+    B = _rand((1, 256, 512), 38, torch.float16)
+    with pytest.raises(m.MuonError):  # needs B's residual
+        m.debug_gemm(A, B, split=4, b_mn=True)
+    with pytest.raises(m.MuonError):  # K-major B
+        m.debug_gemm(A, B.transpose(1, 2).contiguous(), B_lo=B, split=4, b_mn=False)
+    with pytest.raises(m.MuonError):  # bf16 operands
+        m.debug_gemm(A.view(torch.bfloat16), B.view(torch.bfloat16), B_lo=B.view(torch.bfloat16), split=4,
+                     b_mn=True)
+    A2 = _rand((1, 256, 512), 39, torch.float16)  # K != M
+    B2 = _rand((1, 512, 256), 40, torch.float16)
+    with pytest.raises(m.MuonError):
+        m.debug_gemm(A2, B2, B_lo=B2, split=4, b_mn=True)
+
+
 @pytest.mark.parametrize("M,N,K,b_mn,sym", [(128, 128, 16, False, False), (256, 384, 80, True, False),
                                              (384, 384, 48, False, True)])
 def test_simt_gemm(M, N, K, b_mn, sym):
