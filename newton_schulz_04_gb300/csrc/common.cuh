@@ -36,7 +36,11 @@ enum FinalMode : int { FINAL_NONE = 0, FINAL_STORE = 1, FINAL_APPLY = 2 };
 // for the residual / the output.  On the CUDA-core path, `sym` computes the lower triangle and
 // mirrors each element; the tensor-core path stores symmetric outputs
 // block-lower.
-struct EpiParams {
+//
+// EpiCore holds the scalars and buffer pointers, EpiFinal the per-matrix
+// tables of the final modes; a tensor-core launch that runs several products
+// carries one EpiCore per product and a single EpiFinal.
+struct EpiCore {
   const float* inv_norm;  // [B] 1 / (||X||_F + eps)
   int scale_pow;
   float c_acc, c_res, c_id;
@@ -59,27 +63,31 @@ struct EpiParams {
   int final_mode;
   int dst_fp32;  // 1: dst is fp32, 0: bf16
   float lr;
+};
+struct EpiFinal {
   void* dst[kMaxBatch];
   unsigned char tr[kMaxBatch];  // 1: dst[b] is [cols_valid, rows_valid] (the packed matrix transposed)
 };
+struct EpiParams : EpiCore, EpiFinal {};
 
-__device__ __forceinline__ float epi_scale(const EpiParams& e, int b) {
+__device__ __forceinline__ float epi_scale(const EpiCore& e, int b) {
   if (e.scale_pow == 0) return 1.f;
   const float iv = e.inv_norm[b];
   return e.scale_pow == 2 ? iv * iv : iv;
 }
 
 // Final write of one element: packed (p, q) -> caller's matrix.
-__device__ __forceinline__ void epi_final_elem(const EpiParams& e, int b, int p, int q, float v) {
+__device__ __forceinline__ void epi_final_elem(const EpiCore& e, const EpiFinal& f, int b, int p, int q,
+                                               float v) {
   if (p >= e.rows_valid || q >= e.cols_valid) return;
   const long long idx =
-      e.tr[b] ? (long long)q * e.rows_valid + p : (long long)p * e.cols_valid + q;
+      f.tr[b] ? (long long)q * e.rows_valid + p : (long long)p * e.cols_valid + q;
   if (e.dst_fp32) {
-    float* d = static_cast<float*>(e.dst[b]) + idx;
+    float* d = static_cast<float*>(f.dst[b]) + idx;
     if (e.final_mode == FINAL_APPLY) *d = *d - e.lr * v;
     else *d = v;
   } else {
-    bf16* d = static_cast<bf16*>(e.dst[b]) + idx;
+    bf16* d = static_cast<bf16*>(f.dst[b]) + idx;
     if (e.final_mode == FINAL_APPLY) *d = __float2bfloat16_rn(__bfloat162float(*d) - e.lr * v);
     else *d = __float2bfloat16_rn(v);
   }
@@ -93,7 +101,7 @@ __device__ __forceinline__ void epi_elem(const EpiParams& e, int b, int r, int c
   v *= sc;
   if (r == c && r < e.rows_valid) v += e.c_id;
   if (e.final_mode != FINAL_NONE) {
-    epi_final_elem(e, b, r, c, v);
+    epi_final_elem(e, e, b, r, c, v);
     return;
   }
   const long long base = (long long)b * e.bs;

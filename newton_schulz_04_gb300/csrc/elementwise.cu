@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(256) final_from_packed_kernel(const __grid_con
   for (long long t = blockIdx.x * 256LL + threadIdx.x; t < n; t += 256LL * gridDim.x) {
     const int p = static_cast<int>(t / e.cols_valid), q = static_cast<int>(t % e.cols_valid);
     const float v = sc * a.Xf[static_cast<long long>(b) * a.bs + static_cast<long long>(p) * a.ld + q];
-    epi_final_elem(e, b, p, q, v);
+    epi_final_elem(e, e, b, p, q, v);
   }
 }
 

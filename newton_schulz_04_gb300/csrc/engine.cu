@@ -579,7 +579,31 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   // every earlier launch has then finished matrix b, so all read-after-write
   // and write-after-read hazards on b's buffers are covered.  (The counters
   // are zeroed at the top of the chunk.)
-  int tc_launches = 0;
+  // On those short chunks the products also share launches: up to
+  // tc_max_products_per_launch() consecutive products run on one persistent
+  // grid, their tiles in one sequence, so the per-launch fill and drain (the
+  // ramp of a grid, its ragged last wave) is paid once per launch instead of
+  // once per product.
+  const bool program = chain;
+  std::vector<TcGemmDesc> pend_d;
+  std::vector<EpiParams> pend_e;
+  double pend_fl = 0.0;
+  auto flush = [&]() -> cudaError_t {
+    if (pend_d.empty()) return cudaSuccess;
+    std::vector<const EpiParams*> ep;
+    for (const EpiParams& x : pend_e) ep.push_back(&x);
+    cudaError_t err;
+    {
+      ProfScope ps("tc_program", pend_fl, 0.0, cx.st);
+      err = launch_tc_program(pend_d.data(), ep.data(), static_cast<int>(pend_d.size()), cx.status, cx.st,
+                              cx.sms, &why);
+    }
+    pend_d.clear();
+    pend_e.clear();
+    pend_fl = 0.0;
+    return err;
+  };
+  int tc_launches = 0;  // products so far (each has its own tile counter slot)
   int tc_cum = 0;
   // sym: bit 0 = symmetric output (lower tiles, block-lower storage); bits 1 / 2 =
   // A / B is a symmetric operand in that storage.
@@ -611,11 +635,16 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     if (tc_launches >= kMaxTcLaunches) return cudaErrorInvalidValue;
     d.tile_ctr = bf.tile_ctr + tc_launches;
     d.wait_target = tc_cum;
-    ProfScope ps(kind, fl, 0.0, cx.st);
-    const cudaError_t err = launch_tc_gemm(d, e, cx.status, cx.st, cx.sms, &why);
     tc_cum += tc_signals_per_matrix(M, N, d.sym);
     ++tc_launches;
-    return err;
+    if (program) {
+      pend_d.push_back(d);
+      pend_e.push_back(e);
+      pend_fl += fl;
+      return static_cast<int>(pend_d.size()) == tc_max_products_per_launch() ? flush() : cudaSuccess;
+    }
+    ProfScope ps(kind, fl, 0.0, cx.st);
+    return launch_tc_gemm(d, e, cx.status, cx.st, cx.sms, &why);
   };
 
   if (h16) {
@@ -657,6 +686,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
             dseg ? bf.diag : nullptr));
       cur = nxt;
     }
+    CK(flush());
     return MUON_OK;
   }
 
@@ -684,6 +714,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
       CK(tc(split ? 2 : 1, 1, 2, 0, S, L, S, bf.Bh, bf.Bl, sp, bss, bf.Xb[cur], nullptr, lp, bsx, e3));
       cur = nxt;
     }
+    CK(flush());
     return MUON_OK;
   }
 
@@ -723,6 +754,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   EpiParams ef = epi_pair(g, bf, 1, 1.f, 0.f, 0.f, nullptr, nullptr, nullptr, nullptr, lp, bsx);
   epi_set_final(ef, cx, g, mats, Bc);
   CK(tc(sp3, 1, 2, 0, S, L, S, Qh, Ql, sp, bss, bf.Xb[0], bf.Xl, lp, bsx, ef));
+  CK(flush());
   return MUON_OK;
 }
 #undef CK

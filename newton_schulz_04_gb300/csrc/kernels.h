@@ -74,6 +74,14 @@ int tc_signals_per_matrix(int M, int N, int sym);
 
 cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* status, cudaStream_t st, int num_sms,
                            const char** why);
+// Several products in one persistent launch (at most tc_max_products_per_launch()):
+// their tiles run as one sequence, and every product after the first waits per
+// matrix on the shared completion counters (flag_wait set, one `done` array),
+// so the launch overlaps consecutive products without a grid boundary between
+// them.  The tile counter is d[0].tile_ctr; at most one product has a final mode.
+cudaError_t launch_tc_program(const TcGemmDesc* d, const EpiParams* const* epi, int n, int* status,
+                              cudaStream_t st, int num_sms, const char** why);
+int tc_max_products_per_launch();
 int tc_tiles(int M, int N, int sym);
 
 // fp32 SIMT GEMM with the same conventions (fp32 operands, 128 x 128 tiles).

@@ -122,35 +122,55 @@ struct TcCfg {
   static_assert((CH == 16 || CH == 32) && WPQ >= 1 && NCHT >= WPQ, "epilogue chunking");
 };
 
-struct TcArgs {
-  int M, N, K;    // padded sizes (multiples of 128 / 256 / 64)
+// One product of a launch.  A launch runs up to NPH products ("phases") on
+// one persistent grid: their tile pairs form one sequence, phase by phase and
+// within a phase matrix by matrix, which the CTA pairs take in order from
+// tile_ctr.  A tile of a phase with `wait` starts once its matrix's counter
+// shows that every earlier product of that matrix has finished.
+struct TcPhase {
+  CUtensorMap tm[9];  // see TcMap
+  int M, N, K;    // padded sizes (multiples of 256 / 256 / 128)
   int sym;        // 1: lower-triangle tiles of a symmetric M x M output
   int nI, nJ;     // tile grid of one matrix
   int tpm;        // tile pairs per matrix
-  int total;      // tile pairs over the batch
+  int first;      // index of this phase's first tile pair in the launch's sequence
   int nseg;       // K segments (1 plain, 2 or 3 split)
   int a_sym;      // A is a symmetric matrix in block-lower storage (upper k-blocks read transposed)
-  int b_sym;      // same for B (K-major kernels only)
+  int b_sym;      // same for B (K-major B only)
+  int bmn;        // 1: B is MN-major ([K, N] row-major), 0: K-major ([N, K])
   int seg_lo;     // bit 2s: segment s reads A's residual map; bit 2s+1: B's residual map
-  int diag_kb;    // k-blocks of the diagonal segment (0, or 256 / BK: D from tmD times B's residual rows)
+  int diag_kb;    // k-blocks of the diagonal segment (0, or 256 / BK: D times B's residual rows)
   int final_vec;  // final mode may use 16-byte accesses to the caller's rows
   int f16;        // operands are fp16 (else bf16)
+  // With `wait`, a tile of matrix b starts once done[b] >= wait_target
+  // instead of after the whole previous grid (griddepcontrol.wait).
+  int wait;
+  int wait_target;
+  EpiCore epi;
+};
+// Tensor maps of a phase: A's K-major boxes, its residual's, A's transposed
+// (MN-major) boxes and its residual's; the same four for B (for an MN-major B
+// the transposed maps repeat the plain ones); D of the diagonal segment.
+enum TcMap { kMapA = 0, kMapAl, kMapAt, kMapAtl, kMapB, kMapBl, kMapBt, kMapBtl, kMapD };
+
+template <int NPH>
+struct TcProgram {
+  int nph;        // phases in use
+  int total;      // tile pairs over all phases
   int* status;    // workspace status word
   // Per-matrix completion counters (or nullptr).  Every epilogue warp adds 1
-  // to done[b] once its part of a tile of matrix b is stored.  With
-  // flag_wait, a tile of matrix b starts once done[b] >= wait_target (the
-  // previous launch has finished that matrix) instead of waiting for the
-  // whole previous grid.
+  // to done[b] once its part of a tile of matrix b is stored.
   int* done;
-  int wait_target;
-  int flag_wait;
   int* tile_ctr;  // zeroed before the launch; tiles are taken in order by atomicAdd
-  EpiParams epi;
+  EpiFinal fin;   // the final modes' per-matrix tables (one final product per launch)
+  TcPhase ph[NPH];
 };
+constexpr int kMaxPhases = 16;
+static_assert(sizeof(TcProgram<kMaxPhases>) <= 32000, "kernel parameter space");
 
 // Tile pair t of the batch -> (matrix b, row-block pair p, column block j); the
 // CTA of rank r in the cluster computes row block i = 2 p + r.
-__device__ __forceinline__ void decode_pair(const TcArgs& a, int t, int& b, int& p, int& j) {
+__device__ __forceinline__ void decode_pair(const TcPhase& a, int t, int& b, int& p, int& j) {
   b = t / a.tpm;
   const int u = t - b * a.tpm;
   if (a.sym) {
@@ -245,15 +265,15 @@ __device__ __forceinline__ void store_block16(uint16_t* dst, long long ld, int l
 // transposed): global memory is read and written a warp-wide few rows at a time
 // through a padded shared-memory box, lane t owning row t in between.
 template <typename T, int CH>
-__device__ __forceinline__ void final_block_rows(const EpiParams& e, int b, int r0, int c0, int lane,
-                                                 const float (&v)[CH], uint8_t* box) {
+__device__ __forceinline__ void final_block_rows(const EpiCore& e, const EpiFinal& f, int b, int r0, int c0,
+                                                 int lane, const float (&v)[CH], uint8_t* box) {
   constexpr int ROWB = CH * static_cast<int>(sizeof(T));  // bytes of one block row
   constexpr int STRIDE = ROWB + 16;                        // padded row stride in shared memory
   constexpr int PIECES = ROWB / 16;                        // 16-byte pieces per row
   constexpr int ROWS_PER = 32 / PIECES;                    // rows covered by one warp-wide access
   constexpr int EPP = 16 / static_cast<int>(sizeof(T));    // elements per piece
   const long long cols = e.cols_valid;
-  T* dst = static_cast<T*>(e.dst[b]);
+  T* dst = static_cast<T*>(f.dst[b]);
   const bool apply = e.final_mode == FINAL_APPLY;
   if (apply) {
 #pragma unroll
@@ -303,13 +323,8 @@ __device__ __forceinline__ void final_block_rows(const EpiParams& e, int b, int 
   __syncwarp();
 }
 
-template <bool BMN>
-__global__ void __launch_bounds__(TcCfg::THREADS, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAl,
-                   const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmAtl,
-                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBl,
-                   const __grid_constant__ CUtensorMap tmBt, const __grid_constant__ CUtensorMap tmBtl,
-                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ TcArgs args) {
+template <int NPH>
+__global__ void __launch_bounds__(TcCfg::THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcProgram<NPH> prog) {
   using C = TcCfg;
   extern __shared__ uint8_t smem_raw[];
   // Swizzled tiles must start on a 1024-byte boundary of the shared window.
@@ -346,13 +361,16 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
     }
     *abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    if (args.nseg > 1 || args.diag_kb) {
-      tma_prefetch_desc(&tmAl);
-      tma_prefetch_desc(&tmBl);
+    for (int pi = 0; pi < prog.nph; ++pi) {
+      const TcPhase& phs = prog.ph[pi];
+      tma_prefetch_desc(&phs.tm[kMapA]);
+      tma_prefetch_desc(&phs.tm[kMapB]);
+      if (phs.nseg > 1 || phs.diag_kb) {
+        tma_prefetch_desc(&phs.tm[kMapAl]);
+        tma_prefetch_desc(&phs.tm[kMapBl]);
+      }
+      if (phs.diag_kb) tma_prefetch_desc(&phs.tm[kMapD]);
     }
-    if (args.diag_kb) tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {  // both CTAs: the pair's TMEM is allocated collectively
     tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
@@ -365,7 +383,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
   pdl_launch_dependents();
   // Inputs are written by earlier kernels on the stream: wait for the whole
   // previous grid, or, chained per matrix, for that matrix's counter below.
-  if (!args.flag_wait) pdl_wait();
+  if (!prog.ph[0].wait) pdl_wait();
   const int rank = static_cast<int>(cluster_ctarank());
   const uint32_t tmem_base = *tmem_slot;
   // Tile k of this cluster's sequence (every role reads the same sequence):
@@ -376,16 +394,20 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
     return tq[slot];
   };
   auto release_tile = [&](int k) { mbar_arrive_cluster(mapa_cluster(&qempty[k % C::QD], 0)); };
-  const int nk = args.K / C::BK;   // k-blocks per segment
-  const int nks = nk * args.nseg;  // k-blocks of the segments over K
-  const int nkb = nks + args.diag_kb;  // k-blocks per tile
+  // phase of tile pair t of the sequence
+  auto phase_of = [&](int t) -> int {
+    int pi = 0;
+    if (NPH > 1)
+      while (pi + 1 < prog.nph && t >= prog.ph[pi + 1].first) ++pi;
+    return pi;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
       int it = 0;
       bool ok = true;
-      int ready_b = -1;  // last matrix whose inputs are known to be complete
+      int ready_b = -1, ready_pi = -1;  // last (phase, matrix) whose inputs are known to be complete
       // Leader: take tiles from the counter and publish them to both CTAs.
       // Tile k + 1 is fetched when tile k starts (the atomic's result is
       // only read after tile k's loads are issued, so its round trip overlaps
@@ -395,7 +417,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       auto publish = [&](int t) -> bool {
         const int slot = pub % C::QD;
         const bool live = !*abort_flag && mbar_wait(&qempty[slot], ((pub / C::QD) & 1) ^ 1);
-        if (!live || t >= args.total) t = -1;
+        if (!live || t >= prog.total) t = -1;
         tq[slot] = t;
         st_shared_cluster(mapa_cluster(const_cast<int*>(&tq[slot]), 1), t);
         mbar_arrive_cluster(mapa_cluster(&qfull[slot], 0));
@@ -404,13 +426,13 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
         ended = t < 0;
         return live;
       };
-      if (rank == 0 && !publish(atomicAdd(args.tile_ctr, 1))) ok = false;
+      if (rank == 0 && !publish(atomicAdd(prog.tile_ctr, 1))) ok = false;
       for (int k = 0; ok; ++k) {
         int t;
         int fetched = -1;  // the next tile (leader), in flight during this tile's loads
         if (rank == 0) {
           t = tq[k % C::QD];  // this thread published it
-          if (t >= 0 && !ended) fetched = atomicAdd(args.tile_ctr, 1);
+          if (t >= 0 && !ended) fetched = atomicAdd(prog.tile_ctr, 1);
         } else {
           t = take_tile(k);
           if (t == -2) {
@@ -420,17 +442,24 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
           release_tile(k);
         }
         if (t < 0) break;
+        const int pi = phase_of(t);
+        const TcPhase& phs = prog.ph[pi];
         int b, p, j;
-        decode_pair(args, t, b, p, j);
+        decode_pair(phs, t - phs.first, b, p, j);
         const int m0 = (2 * p + rank) * C::BM, n0 = j * C::BN;
-        if (args.flag_wait && b != ready_b) {
-          if (!wait_counter(&args.done[b], args.wait_target)) {
+        if (phs.wait && (b != ready_b || pi != ready_pi)) {
+          if (!wait_counter(&prog.done[b], phs.wait_target)) {
             ok = false;
             break;
           }
           fence_proxy_async_global();  // the TMA loads below read what that matrix's writers stored
           ready_b = b;
+          ready_pi = pi;
         }
+        const int nk = phs.K / C::BK;         // k-blocks per segment
+        const int nks = nk * phs.nseg;        // k-blocks of the segments over K
+        const int nkb = nks + phs.diag_kb;    // k-blocks of this tile
+        const CUtensorMap* tm = phs.tm;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
@@ -444,41 +473,43 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
           if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * C::STAGE);
           uint8_t* sb = st + C::A_TILE;
           const int nb0 = n0 + rank * C::BNH;  // this CTA's half of the B tile: columns nb0 .. nb0 + 127
-          if (BMN && kb >= nks) {
+          if (kb >= nks) {
             // diagonal segment: this CTA's 128 rows of D, and the pair's own
             // rows of B's residual (256 p + 128 dk ..), MN-major
             const int dk = (kb - nks) * C::BK;
 #pragma unroll
             for (int g = 0; g < C::KATOMS; ++g)
-              tma_load_3d_pair(&tmD, fbar, st + g * C::KATOM_BYTES, dk + g * C::KA, rank * C::BM, 0);
+              tma_load_3d_pair(&tm[kMapD], fbar, st + g * C::KATOM_BYTES, dk + g * C::KA, rank * C::BM, 0);
 #pragma unroll
             for (int q = 0; q < C::BNH / C::MN_ATOM; ++q)
-              tma_load_3d_pair(&tmBl, fbar, sb + q * C::MN_BOX_BYTES, nb0 + q * C::MN_ATOM, 2 * p * C::BM + dk, b);
+              tma_load_3d_pair(&tm[kMapBl], fbar, sb + q * C::MN_BOX_BYTES, nb0 + q * C::MN_ATOM,
+                               2 * p * C::BM + dk, b);
             continue;
           }
           const int seg = kb / nk;
           const int k0 = (kb - seg * nk) * C::BK;
-          const bool alo = (args.seg_lo >> (2 * seg)) & 1;
-          const bool blo = (args.seg_lo >> (2 * seg + 1)) & 1;
+          const bool alo = (phs.seg_lo >> (2 * seg)) & 1;
+          const bool blo = (phs.seg_lo >> (2 * seg + 1)) & 1;
           // k-blocks above the diagonal of a block-lower symmetric operand come
           // from the stored lower block, read transposed
-          const bool a_up = args.a_sym && (k0 >> 8) > (m0 >> 8);
-          const bool b_up = !BMN && args.b_sym && (k0 >> 8) > (n0 >> 8);
+          const bool a_up = phs.a_sym && (k0 >> 8) > (m0 >> 8);
+          const bool b_up = !phs.bmn && phs.b_sym && (k0 >> 8) > (n0 >> 8);
           if (!a_up) {
 #pragma unroll
             for (int g = 0; g < C::KATOMS; ++g)
-              tma_load_3d_pair(alo ? &tmAl : &tmA, fbar, st + g * C::KATOM_BYTES, k0 + g * C::KA, m0, b);
+              tma_load_3d_pair(&tm[alo ? kMapAl : kMapA], fbar, st + g * C::KATOM_BYTES, k0 + g * C::KA, m0, b);
           } else {
 #pragma unroll
             for (int q = 0; q < C::BM / C::MN_ATOM; ++q)
-              tma_load_3d_pair(alo ? &tmAtl : &tmAt, fbar, st + q * C::MN_BOX_BYTES, m0 + q * C::MN_ATOM, k0, b);
+              tma_load_3d_pair(&tm[alo ? kMapAtl : kMapAt], fbar, st + q * C::MN_BOX_BYTES, m0 + q * C::MN_ATOM,
+                               k0, b);
           }
-          if (!BMN && !b_up) {
+          if (!phs.bmn && !b_up) {
 #pragma unroll
             for (int g = 0; g < C::KATOMS; ++g)
-              tma_load_3d_pair(blo ? &tmBl : &tmB, fbar, sb + g * C::KATOM_BYTES, k0 + g * C::KA, nb0, b);
+              tma_load_3d_pair(&tm[blo ? kMapBl : kMapB], fbar, sb + g * C::KATOM_BYTES, k0 + g * C::KA, nb0, b);
           } else {
-            const CUtensorMap* mb = BMN ? (blo ? &tmBl : &tmB) : (blo ? &tmBtl : &tmBt);
+            const CUtensorMap* mb = &tm[phs.bmn ? (blo ? kMapBl : kMapB) : (blo ? kMapBtl : kMapBt)];
 #pragma unroll
             for (int q = 0; q < C::BNH / C::MN_ATOM; ++q)
               tma_load_3d_pair(mb, fbar, sb + q * C::MN_BOX_BYTES, nb0 + q * C::MN_ATOM, k0, b);
@@ -487,7 +518,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
         if (rank == 0 && ok && !ended && !publish(fetched)) ok = false;
       }
       if (!ok) {
-        atomicOr(args.status, kStatusTimeout);
+        atomicOr(prog.status, kStatusTimeout);
         *abort_flag = 1;
         // Let the copies already issued land before the CTAs can exit (the
         // leader's barriers count the bytes of both CTAs).
@@ -510,9 +541,13 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
         }
         release_tile(k);
         if (t < 0) break;
+        const TcPhase& phs = prog.ph[phase_of(t)];
         int b, p, j;
-        decode_pair(args, t, b, p, j);
+        decode_pair(phs, t - phs.first, b, p, j);
         const int m0 = (2 * p + rank) * C::BM, n0 = j * C::BN;
+        const int nk = phs.K / C::BK;
+        const int nks = nk * phs.nseg;
+        const int nkb = nks + phs.diag_kb;
         const int abuf = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
         if (*abort_flag || !mbar_wait(&tempty[abuf], aph ^ 1)) {
@@ -532,10 +567,10 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
           // the diagonal segment's A (D) is K-major and its B MN-major
           const bool dseg = kb >= nks;
           const int k0 = dseg ? 0 : (kb % nk) * C::BK;
-          const bool a_mn = !dseg && args.a_sym && (k0 >> 8) > (m0 >> 8);
-          const bool b_mn = BMN || (!dseg && args.b_sym && (k0 >> 8) > (n0 >> 8));
+          const bool a_mn = !dseg && phs.a_sym && (k0 >> 8) > (m0 >> 8);
+          const bool b_mn = phs.bmn || (!dseg && phs.b_sym && (k0 >> 8) > (n0 >> 8));
           const uint32_t idesc =
-              make_idesc_f16kind(2 * C::BM, C::BN, b_mn, args.f16 == 0) | (a_mn ? (1u << 15) : 0u);
+              make_idesc_f16kind(2 * C::BM, C::BN, b_mn, phs.f16 == 0) | (a_mn ? (1u << 15) : 0u);
           const uint32_t a0 = smem_u32(tiles + s * C::STAGE);
           const uint32_t b0 = a0 + C::A_TILE;
 #pragma unroll
@@ -554,7 +589,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
         tc_commit_pair(&tfull[abuf], 0x3);  // both CTAs' accumulators ready for their epilogues
       }
       if (!ok) {
-        atomicOr(args.status, kStatusTimeout);
+        atomicOr(prog.status, kStatusTimeout);
         *abort_flag = 1;
       }
       // Every MMA issued by this thread completes before TMEM is released.
@@ -569,11 +604,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
     const int quarter = warp & 3;   // TMEM lanes this warp may read
     const int ew = warp - 2;
     const int jq = ew >> 2;         // this warp's index among the WPQ warps of its quarter
-    const EpiParams& e = args.epi;
+    const EpiFinal& f = prog.fin;
     uint8_t* box = staging + ew * C::ROWBOX;
-    const bool has_lo = e.Ol != nullptr;
-    const bool has_r = e.Rh != nullptr;
-    const bool has_rl = e.Rl != nullptr;
     const uint4 zero4 = make_uint4(0, 0, 0, 0);
     int tcount = 0;
     bool ok = true;
@@ -588,16 +620,21 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       __syncwarp();
       if (lane == 0) release_tile(k);
       if (t < 0) break;
+      const TcPhase& phs = prog.ph[phase_of(t)];
+      const EpiCore& e = phs.epi;
+      const bool has_lo = e.Ol != nullptr;
+      const bool has_r = e.Rh != nullptr;
+      const bool has_rl = e.Rl != nullptr;
       int b, p, j;
-      decode_pair(args, t, b, p, j);
+      decode_pair(phs, t - phs.first, b, p, j);
       const int m0 = (2 * p + rank) * C::BM;
       const int r0 = m0 + quarter * 32;
       const int r = r0 + lane;
       const int cb = j * C::BN;  // first column of the tile
-      if (args.flag_wait && has_r) {
-        // the residual may be the previous launch's output: acquire its
+      if (phs.wait && has_r) {
+        // the residual may be an earlier product's output: acquire its
         // counter before the first residual load below
-        if (lane == 0 && !wait_counter(&args.done[b], args.wait_target)) ok = false;
+        if (lane == 0 && !wait_counter(&prog.done[b], phs.wait_target)) ok = false;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
       }
@@ -607,17 +644,17 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       if (jq == 0) {
         if (has_r) bulk_prefetch_l2(static_cast<const uint16_t*>(e.Rh) + roff, C::BN * 2);
         if (has_rl) bulk_prefetch_l2(static_cast<const uint16_t*>(e.Rl) + roff, C::BN * 2);
-        if (e.final_mode == FINAL_APPLY && !e.tr[b] && args.final_vec && r < e.rows_valid &&
+        if (e.final_mode == FINAL_APPLY && !f.tr[b] && phs.final_vec && r < e.rows_valid &&
             cb + C::BN <= e.cols_valid) {
           const int esz = e.dst_fp32 ? 4 : 2;
           bulk_prefetch_l2(
-              static_cast<const uint8_t*>(e.dst[b]) + (static_cast<long long>(r) * e.cols_valid + cb) * esz,
+              static_cast<const uint8_t*>(f.dst[b]) + (static_cast<long long>(r) * e.cols_valid + cb) * esz,
               C::BN * esz);
         }
       }
       // Residual loads: through the read-only cache, unless the previous launch
       // may still be writing other matrices (chained), then from L2.
-      const bool coherent = args.flag_wait != 0;
+      const bool coherent = phs.wait != 0;
       auto ld16 = [&](const uint16_t* q) {
         return coherent ? __ldcg(reinterpret_cast<const uint4*>(q)) : __ldg(reinterpret_cast<const uint4*>(q));
       };
@@ -710,11 +747,11 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
         }
         if (e.final_mode != FINAL_NONE) {
           const bool full_block = r0 + 32 <= e.rows_valid && c0 + CH <= e.cols_valid;
-          if (!e.tr[b] && !e.dst_fp32 && args.final_vec && full_block) {
-            final_block_rows<bf16, CH>(e, b, r0, c0, lane, v, box);
+          if (!f.tr[b] && !e.dst_fp32 && phs.final_vec && full_block) {
+            final_block_rows<bf16, CH>(e, f, b, r0, c0, lane, v, box);
           } else {
 #pragma unroll
-            for (int u = 0; u < CH; ++u) epi_final_elem(e, b, r, c0 + u, v[u]);
+            for (int u = 0; u < CH; ++u) epi_final_elem(e, f, b, r, c0 + u, v[u]);
           }
         } else {
           uint32_t hw[CH / 2], lw[CH / 2];
@@ -728,17 +765,17 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_cluster(&tempty[abuf], 0));
-      if (args.done) {
-        // this warp's part of the tile is stored: publish it for the next
-        // launch, whose TMA (async proxy) and L2 loads read it
+      if (prog.done) {
+        // this warp's part of the tile is stored: publish it for the later
+        // products, whose TMA (async proxy) and L2 loads read it
         fence_proxy_async_global();
         __threadfence();
         __syncwarp();
-        if (lane == 0) red_release_gpu_add(&args.done[b], 1);
+        if (lane == 0) red_release_gpu_add(&prog.done[b], 1);
       }
     }
     if (!ok) {
-      if (lane == 0) atomicOr(args.status, kStatusTimeout);
+      if (lane == 0) atomicOr(prog.status, kStatusTimeout);
       *abort_flag = 1;
     }
     __syncwarp();
@@ -809,7 +846,7 @@ static cudaError_t launch_pair(void (*kernel)(KArgs...), int ncl, cudaStream_t s
 
 // The dynamic shared-memory limit is raised once per device and kernel, so a
 // later call (e.g. under stream capture) only enqueues launches.
-template <bool BMN>
+template <int NPH>
 static cudaError_t ensure_smem_attr() {
   static std::mutex mu;
   static bool done[64] = {false};
@@ -819,7 +856,7 @@ static cudaError_t ensure_smem_attr() {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(mu);
   if (!done[dev]) {
-    e = cudaFuncSetAttribute(tc_gemm_kernel<BMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg::SMEM);
+    e = cudaFuncSetAttribute(tc_gemm_kernel<NPH>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg::SMEM);
     if (e != cudaSuccess) return e;
     done[dev] = true;
   }
@@ -828,7 +865,7 @@ static cudaError_t ensure_smem_attr() {
 
 // Clusters of two that can be resident at once (queried once per device), so
 // the persistent grid never waits for a second wave of clusters.
-template <bool BMN>
+template <int NPH>
 static int max_clusters(int num_sms) {
   static std::mutex mu;
   static int cached[64] = {0};
@@ -848,7 +885,7 @@ static int max_clusters(int num_sms) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BMN>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<NPH>, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = num_sms / 2;
     }
@@ -857,45 +894,63 @@ static int max_clusters(int num_sms) {
   return cached[dev];
 }
 
-template <bool BMN>
-static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* status, cudaStream_t st,
-                               int num_sms, const char** why) {
+// Validates one product and fills its phase (tiles from `first` on).
+static bool build_phase(TcPhase& ph, const TcGemmDesc& d, const EpiParams& epi, int first, const char** why) {
   using C = TcCfg;
-  {
-    const cudaError_t e = ensure_smem_attr<BMN>();
-    if (e != cudaSuccess) return e;
+  if (d.split < 1 || d.split > 3 || (d.split == 2 && !d.b_mn)) {
+    *why = "unsupported operand split";
+    return false;
   }
-  CUtensorMap mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl;
+  if (d.M % 256 || d.N % 256 || d.K % 128) {
+    *why = "tensor-core GEMM needs M and N multiples of 256 (CTA pairs) and K a multiple of 128";
+    return false;
+  }
+  if ((d.split >= 2 && !d.A.lo) || (d.split == 3 && !d.Bop.lo)) {
+    *why = "split products need the residual operands";
+    return false;
+  }
+  if ((d.a_sym && d.K != d.M) || (d.b_sym && (d.b_mn || d.K != d.N)) || ((d.a_sym || d.b_sym) && d.K % 256)) {
+    *why = "symmetric operands must be square with K a multiple of 256";
+    return false;
+  }
+  if (d.diag && (d.split != 1 || !d.b_mn || d.K != d.M || !d.Bop.lo ||
+                 reinterpret_cast<uintptr_t>(d.diag) % 16)) {
+    *why = "a diagonal segment needs split 1, an MN-major B with its residual, K == M and an aligned D";
+    return false;
+  }
   const void* alo = d.A.lo ? d.A.lo : d.A.hi;
   const void* blo = d.Bop.lo ? d.Bop.lo : d.Bop.hi;
   const bool f = d.f16 != 0;
+  CUtensorMap* tm = ph.tm;
   // K-major boxes {64 k, rows}; transposed boxes {64 mn, 64 k} (symmetric operands: K == rows)
-  bool ok = make_map(&mA, d.A.hi, f, d.K, d.M, d.B, d.A.ld, d.A.bs, C::KA, C::BM, 128);
-  ok = ok && make_map(&mAl, alo, f, d.K, d.M, d.B, d.A.ld, d.A.bs, C::KA, C::BM, 128);
-  ok = ok && make_map(&mAt, d.A.hi, f, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
-  ok = ok && make_map(&mAtl, alo, f, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
-  if (!BMN) {
-    ok = ok && make_map(&mB, d.Bop.hi, f, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::KA, C::BNH, 128);
-    ok = ok && make_map(&mBl, blo, f, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::KA, C::BNH, 128);
-    ok = ok && make_map(&mBt, d.Bop.hi, f, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
-    ok = ok && make_map(&mBtl, blo, f, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
+  bool ok = make_map(&tm[kMapA], d.A.hi, f, d.K, d.M, d.B, d.A.ld, d.A.bs, C::KA, C::BM, 128);
+  ok = ok && make_map(&tm[kMapAl], alo, f, d.K, d.M, d.B, d.A.ld, d.A.bs, C::KA, C::BM, 128);
+  ok = ok && make_map(&tm[kMapAt], d.A.hi, f, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
+  ok = ok && make_map(&tm[kMapAtl], alo, f, d.K, d.M, d.B, d.A.ld, d.A.bs, C::MN_ATOM, C::BK, 128);
+  if (!d.b_mn) {
+    ok = ok && make_map(&tm[kMapB], d.Bop.hi, f, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::KA, C::BNH, 128);
+    ok = ok && make_map(&tm[kMapBl], blo, f, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::KA, C::BNH, 128);
+    ok = ok && make_map(&tm[kMapBt], d.Bop.hi, f, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
+    ok = ok && make_map(&tm[kMapBtl], blo, f, d.K, d.N, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
   } else {
-    ok = ok && make_map(&mB, d.Bop.hi, f, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
-    ok = ok && make_map(&mBl, blo, f, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
-    mBt = mB;
-    mBtl = mBl;
+    ok = ok && make_map(&tm[kMapB], d.Bop.hi, f, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
+    ok = ok && make_map(&tm[kMapBl], blo, f, d.N, d.K, d.B, d.Bop.ld, d.Bop.bs, C::MN_ATOM, C::BK, 128);
+    tm[kMapBt] = tm[kMapB];
+    tm[kMapBtl] = tm[kMapBl];
   }
   // D (the diagonal segment's A): one 256 x 256 matrix, K-major boxes like A's
-  CUtensorMap mD = mA;
-  if (d.diag) ok = ok && make_map(&mD, d.diag, f, kDiagDim, kDiagDim, 1, kDiagDim, kDiagDim * kDiagDim, C::KA, C::BM, 128);
-  const bool has_out = epi.Oh != nullptr;
+  tm[kMapD] = tm[kMapA];
+  if (d.diag)
+    ok = ok && make_map(&tm[kMapD], d.diag, f, kDiagDim, kDiagDim, 1, kDiagDim, kDiagDim * kDiagDim, C::KA, C::BM,
+                        128);
   if (!ok) {
     *why = "cuTensorMapEncodeTiled failed";
-    return cudaErrorInvalidValue;
+    return false;
   }
+  const bool has_out = epi.Oh != nullptr;
   if (epi.final_mode == FINAL_NONE && !has_out) {
     *why = "tensor-core epilogue needs a 16-bit output pair";
-    return cudaErrorInvalidValue;
+    return false;
   }
   // packed outputs and residuals are accessed with 16-byte row accesses
   if ((has_out || epi.Rh) && ((reinterpret_cast<uintptr_t>(epi.Oh) | reinterpret_cast<uintptr_t>(epi.Ol) |
@@ -903,88 +958,120 @@ static cudaError_t launch_impl(const TcGemmDesc& d, const EpiParams& epi, int* s
                                   16 ||
                               epi.ld % 8 || epi.bs % 8)) {
     *why = "tensor-core outputs and residuals need 16-byte aligned rows";
-    return cudaErrorInvalidValue;
+    return false;
   }
-  TcArgs a;
-  a.M = d.M;
-  a.N = d.N;
-  a.K = d.K;
-  a.sym = d.sym;
-  a.nI = d.M / C::BM;
-  a.nJ = d.N / C::BN;
+  ph.M = d.M;
+  ph.N = d.N;
+  ph.K = d.K;
+  ph.sym = d.sym;
+  ph.nI = d.M / C::BM;
+  ph.nJ = d.N / C::BN;
   if (d.sym) {
-    const int P = a.nI / 2;
-    a.tpm = P * (P + 1) / 2;
+    const int P = ph.nI / 2;
+    ph.tpm = P * (P + 1) / 2;
   } else {
-    a.tpm = (a.nI / 2) * a.nJ;
+    ph.tpm = (ph.nI / 2) * ph.nJ;
   }
-  a.total = a.tpm * d.B;
+  ph.first = first;
   // K segments of the split products (bit 2s: A residual, bit 2s+1: B residual)
   if (d.split == 1) {
-    a.nseg = 1;
-    a.seg_lo = 0;
+    ph.nseg = 1;
+    ph.seg_lo = 0;
   } else if (d.split == 2) {  // Ah B + Al B
-    a.nseg = 2;
-    a.seg_lo = 1 << 2;
+    ph.nseg = 2;
+    ph.seg_lo = 1 << 2;
   } else {  // Ah Bh + Ah Bl + Al Bh
-    a.nseg = 3;
-    a.seg_lo = (1 << 3) | (1 << 4);
+    ph.nseg = 3;
+    ph.seg_lo = (1 << 3) | (1 << 4);
   }
-  a.diag_kb = d.diag ? kDiagDim / C::BK : 0;
-  a.a_sym = d.a_sym;
-  a.b_sym = BMN ? 0 : d.b_sym;
-  a.f16 = d.f16 ? 1 : 0;
-  a.done = d.done;
-  a.wait_target = d.wait_target;
-  a.flag_wait = d.done && d.flag_wait ? 1 : 0;
-  a.tile_ctr = d.tile_ctr;
-  a.status = status;
-  a.epi = epi;
-  a.epi.sym = d.sym;
+  ph.diag_kb = d.diag ? kDiagDim / C::BK : 0;
+  ph.a_sym = d.a_sym;
+  ph.b_sym = d.b_mn ? 0 : d.b_sym;
+  ph.bmn = d.b_mn ? 1 : 0;
+  ph.f16 = d.f16 ? 1 : 0;
+  ph.wait = d.done && d.flag_wait ? 1 : 0;
+  ph.wait_target = d.wait_target;
+  ph.epi = epi;  // the scalars; the final tables travel once per launch
+  ph.epi.sym = d.sym;
   // 16-byte row accesses to the caller's matrices in final mode need aligned rows
-  a.final_vec = 1;
+  ph.final_vec = 1;
   if (epi.final_mode != FINAL_NONE) {
     const int esz = epi.dst_fp32 ? 4 : 2;
-    if ((static_cast<long long>(epi.cols_valid) * esz) % 16) a.final_vec = 0;
+    if ((static_cast<long long>(epi.cols_valid) * esz) % 16) ph.final_vec = 0;
     for (int q = 0; q < d.B; ++q)
-      if (reinterpret_cast<uintptr_t>(epi.dst[q]) % 16) a.final_vec = 0;
+      if (reinterpret_cast<uintptr_t>(epi.dst[q]) % 16) ph.final_vec = 0;
   }
-  const int nclusters = std::min(a.total, max_clusters<BMN>(num_sms));
+  return true;
+}
+
+// One launch over n products (n <= NPH) that share the batch's counters.
+template <int NPH>
+static cudaError_t launch_program(const TcGemmDesc* d, const EpiParams* const* epi, int n, int* status,
+                                  cudaStream_t st, int num_sms, const char** why) {
+  if (n < 1 || n > NPH) {
+    *why = "too many products for one launch";
+    return cudaErrorInvalidValue;
+  }
+  if (!d[0].tile_ctr) {
+    *why = "tensor-core GEMM needs a zeroed tile counter";
+    return cudaErrorInvalidValue;
+  }
+  {
+    const cudaError_t e = ensure_smem_attr<NPH>();
+    if (e != cudaSuccess) return e;
+  }
+  // The argument block is large (NPH tensor-map sets); build it on the heap.
+  static thread_local TcProgram<NPH>* prog = nullptr;
+  if (!prog) prog = new TcProgram<NPH>();
+  TcProgram<NPH>& a = *prog;
+  memset(&a, 0, sizeof(a));
+  const EpiParams* fin = nullptr;
+  int total = 0;
+  for (int q = 0; q < n; ++q) {
+    if (d[q].done != d[0].done) {
+      *why = "the products of one launch share one set of completion counters";
+      return cudaErrorInvalidValue;
+    }
+    if (q > 0 && !(d[q].done && d[q].flag_wait)) {
+      *why = "every product after a launch's first waits on the completion counters";
+      return cudaErrorInvalidValue;
+    }
+    if (epi[q]->final_mode != FINAL_NONE) {
+      if (fin) {
+        *why = "one final product per launch";
+        return cudaErrorInvalidValue;
+      }
+      fin = epi[q];
+    }
+    if (!build_phase(a.ph[q], d[q], *epi[q], total, why)) return cudaErrorInvalidValue;
+    total += a.ph[q].tpm * d[q].B;
+  }
+  a.nph = n;
+  a.total = total;
+  a.status = status;
+  a.done = d[0].done;
+  a.tile_ctr = d[0].tile_ctr;
+  if (fin) a.fin = static_cast<const EpiFinal&>(*fin);
+  const int nclusters = std::min(a.total, max_clusters<NPH>(num_sms));
   if (nclusters <= 0) return a.total > 0 ? cudaErrorLaunchOutOfResources : cudaSuccess;
-  return launch_pair(tc_gemm_kernel<BMN>, nclusters, st, mA, mAl, mAt, mAtl, mB, mBl, mBt, mBtl, mD, a);
+  return launch_pair(tc_gemm_kernel<NPH>, nclusters, st, a);
 }
 
 cudaError_t launch_tc_gemm(const TcGemmDesc& d, const EpiParams& epi, int* status, cudaStream_t st, int num_sms,
                            const char** why) {
   *why = nullptr;
-  if (d.split < 1 || d.split > 3 || (d.split == 2 && !d.b_mn)) {
-    *why = "unsupported operand split";
-    return cudaErrorInvalidValue;
-  }
-  if (!d.tile_ctr) {
-    *why = "tensor-core GEMM needs a zeroed tile counter";
-    return cudaErrorInvalidValue;
-  }
-  if (d.M % 256 || d.N % 256 || d.K % 128) {
-    *why = "tensor-core GEMM needs M and N multiples of 256 (CTA pairs) and K a multiple of 128";
-    return cudaErrorInvalidValue;
-  }
-  if ((d.split >= 2 && !d.A.lo) || (d.split == 3 && !d.Bop.lo)) {
-    *why = "split products need the residual operands";
-    return cudaErrorInvalidValue;
-  }
-  if ((d.a_sym && d.K != d.M) || (d.b_sym && (d.b_mn || d.K != d.N)) || ((d.a_sym || d.b_sym) && d.K % 256)) {
-    *why = "symmetric operands must be square with K a multiple of 256";
-    return cudaErrorInvalidValue;
-  }
-  if (d.diag && (d.split != 1 || !d.b_mn || d.K != d.M || !d.Bop.lo ||
-                 reinterpret_cast<uintptr_t>(d.diag) % 16)) {
-    *why = "a diagonal segment needs split 1, an MN-major B with its residual, K == M and an aligned D";
-    return cudaErrorInvalidValue;
-  }
-  return d.b_mn ? launch_impl<true>(d, epi, status, st, num_sms, why)
-                : launch_impl<false>(d, epi, status, st, num_sms, why);
+  const EpiParams* e = &epi;
+  return launch_program<1>(&d, &e, 1, status, st, num_sms, why);
 }
+
+cudaError_t launch_tc_program(const TcGemmDesc* d, const EpiParams* const* epi, int n, int* status,
+                              cudaStream_t st, int num_sms, const char** why) {
+  *why = nullptr;
+  if (n == 1) return launch_program<1>(d, epi, 1, status, st, num_sms, why);
+  return launch_program<kMaxPhases>(d, epi, n, status, st, num_sms, why);
+}
+
+int tc_max_products_per_launch() { return kMaxPhases; }
 
 int tc_signals_per_matrix(int M, int N, int sym) {
   const int P = M / 256;
