@@ -432,13 +432,16 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   const char* why = nullptr;
   Buffers bf;
   carve_buffers(ws, Bc, g.sp, g.lp, g.tiles, cx.dt, g.sc, cx.steps, bf);
-  // Chaining pays only when each product is a few waves of tiles: then the
-  // previous product's ragged last wave overlaps the next one's first.  On
-  // longer products the overlap only adds power next to a tail it cannot
-  // shorten (tiles are assigned statically), and the per-tile release fences
-  // cost more than the overlap gains (measured: c3 -13 %, 16x1024^2 +4 %).
+  // Chaining (and the shared launches below) pays when each product is a few
+  // waves of tiles: then one product's ragged last wave overlaps the next
+  // one's first, and a grid's fill and drain is a large part of a product.
+  // On longer products the overlap only adds power next to a tail it cannot
+  // shorten, and the per-tile signals cost more than it gains.  Measured
+  // with shared launches, against separate ones: 8 x 1024 x 4096 (8 pair-tiles
+  // per cluster in the update) 287 -> 360 TFLOP/s; the 512 small matrices of
+  // shapes 256 x 1024 .. 768 x 3072 (up to 75 per cluster) 293 -> 286.
   const long long pairs_rect = static_cast<long long>(Bc) * (g.sp / 256) * (g.lp / 256);
-  const bool chain = cx.dt == MUON_BF16 && pairs_rect <= 4LL * (cx.sms / 2);
+  const bool chain = cx.dt == MUON_BF16 && pairs_rect <= 8LL * (cx.sms / 2);
   // stream-ordered: runs after everything before this chunk, before its pack
   if (chain) CK(cudaMemsetAsync(bf.done, 0, sizeof(int) * Bc, cx.st));
   if (cx.dt == MUON_BF16 && cx.steps > 0) CK(cudaMemsetAsync(bf.tile_ctr, 0, sizeof(int) * kMaxTcLaunches, cx.st));

@@ -767,9 +767,10 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) tc_gemm_kernel(const __grid
       if (lane == 0) mbar_arrive_cluster(mapa_cluster(&tempty[abuf], 0));
       if (prog.done) {
         // this warp's part of the tile is stored: publish it for the later
-        // products, whose TMA (async proxy) and L2 loads read it
+        // products, whose TMA (async proxy) and L2 loads read it.  The warp
+        // barrier orders every lane's stores before lane 0's release, which
+        // is cumulative over them (no per-lane membar.gl).
         fence_proxy_async_global();
-        __threadfence();
         __syncwarp();
         if (lane == 0) red_release_gpu_add(&prog.done[b], 1);
       }
