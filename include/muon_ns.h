@@ -77,7 +77,7 @@ typedef enum {
     MUON_SCHED_GRAM_X3 = 1,  /* Gram space; symmetric products with split-bf16 operands (hi*hi + hi*lo + lo*hi) */
     MUON_SCHED_GRAM_X1 = 2,  /* Gram space; plain bf16 operands (fast mode, larger error) */
     MUON_SCHED_ORIG = 3,     /* original space (bf16: step 0 in bf16, later steps on fp16 operands, see below) */
-    MUON_SCHED_ORIG_BF16 = 4 /* original space on bf16 operands only; split A in A*A and B in B*X in the last two steps */
+    MUON_SCHED_ORIG_BF16 = 4 /* original space on bf16 operands only; split A in A*A and B in B*X in the last max(2, steps - 3) steps */
 } muon_sched;
 
 /*
@@ -95,7 +95,8 @@ typedef enum {
  *    do).  Coefficients that fail this check, or whose |b|, |c| could take B
  *    out of fp16's range, run as ORIG_BF16.
  *  - ORIG_BF16.  bf16 operands throughout, with X carried as a bf16 pair (about
- *    16 bits).  A*A and B*X use split operands in the last two steps.
+ *    16 bits).  A*A and B*X use split operands in the last max(2, steps - 3)
+ *    steps (every step from the fourth on when there are more than five).
  *  - GRAM_X3 / GRAM_X1.  The Gram recurrence on bf16 pairs (split products)
  *    or on plain bf16.  Gram space squares the condition number, so on
  *    ill-conditioned inputs it misses the 2e-2 target that ORIG meets.

@@ -105,6 +105,10 @@ static const float kEps = 1e-7f;
 #endif
 static const int kSplitA = MUON_SPLIT_A_STEPS;
 static const int kSplitB = MUON_SPLIT_B_STEPS;
+// Beyond five steps the rounding of the unsplit steps builds up (same
+// emulation, 256 x 512 Gaussian, quintic: 7 steps reach 3.0e-2 with two split
+// steps and 1.5e-2 with four), so every step from the fourth on is split.
+static int split_steps(int T, int base) { return std::max(base, T - 3); }
 
 static inline long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 
@@ -153,7 +157,8 @@ static muon_sched resolve(long long s, long long l, int steps, muon_dtype dt, mu
   //            2 s^3 per split A*A and 2 s^2 l per split B*X
   //   GRAM_X3  3 s^2 l (SYRK, split) + 3 (4T - 3) s^3 + 6 s^2 l (Q X0, split)
   const double S = static_cast<double>(s), L = static_cast<double>(l), T = steps;
-  const double na = std::min<double>(T, kSplitA), nb = std::min<double>(T, kSplitB);
+  const double na = std::min<double>(T, split_steps(steps, kSplitA));
+  const double nb = std::min<double>(T, split_steps(steps, kSplitB));
   const double orig = T * (3 * S * S * L + S * S * S) + na * 2 * S * S * S + nb * 2 * S * S * L;
   const double x3 = 9 * S * S * L + 3 * (4 * T - 3) * S * S * S;
   // Gram space squares the condition number, and the tensor cores' fp32
@@ -699,8 +704,8 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     // rounding of the last steps, where sigma ~ 1 and the b, c terms are large.
     int cur = 0;
     for (int k = 0; k < T; ++k) {
-      const bool split_a = k >= T - kSplitA;
-      const bool split = k >= T - kSplitB;
+      const bool split_a = k >= T - split_steps(T, kSplitA);
+      const bool split = k >= T - split_steps(T, kSplitB);
       const int nxt = cur ^ 1;
       // A = X X^T (k = 0: X = M / s, so scale by inv_norm^2)
       EpiParams e1 = epi_pair(g, bf, k == 0 ? 2 : 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, bf.Gl, sp, bss);
@@ -872,8 +877,8 @@ static double estimate_seconds(long long m, long long n, int steps, muon_dtype d
     const bool h16 = !fp32 && g.sc == MUON_SCHED_ORIG;
     const double sym1 = h16 ? sym_out / 2 : sym_out;
     for (int k = 0; k < steps; ++k) {
-      const double fa = (!fp32 && !h16 && k >= steps - kSplitA) ? 3.0 : 1.0;
-      const double fb = (!fp32 && !h16 && k >= steps - kSplitB) ? 2.0 : 1.0;
+      const double fa = (!fp32 && !h16 && k >= steps - split_steps(steps, kSplitA)) ? 3.0 : 1.0;
+      const double fb = (!fp32 && !h16 && k >= steps - split_steps(steps, kSplitB)) ? 2.0 : 1.0;
       launch(sym_tiles * tile * L, S * L * (fp32 ? 4.0 : 2.0) + sym1);
       launch(fa * sym_tiles * tile * S, 2.0 * sym1);
       const double out = k == steps - 1 ? apply : S * L * ssz;

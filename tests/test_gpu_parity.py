@@ -420,3 +420,17 @@ def test_each_product_through_few_steps(sched, dtype, steps):
     for i in range(2):
         e = rel(O[i].float().cpu(), oracle_O(X[i], steps))
         assert e < tol, (sched, dtype, steps, i, e)
+
+
+@pytest.mark.parametrize("sched,steps,coeffs", [("orig", 7, None), ("gram_x3", 7, None), ("orig_bf16", 7, None),
+                                                ("orig", 12, (1.5, -0.5, 0.0))])
+def test_more_products_than_one_shared_launch(sched, steps, coeffs):
+    """A short chunk runs up to 16 consecutive products in one launch; 7 or 12
+    steps need several such launches, chained on the same per-matrix counters."""
+    m = _m()
+    X = torch.stack([synth.random_matrix(256, 512, seed=820 + i) for i in range(3)]).to(torch.bfloat16).cuda()
+    O = m.ns_batched(X, steps=steps, schedule=sched, coeffs=coeffs)
+    torch.cuda.synchronize()
+    for i in range(3):
+        e = rel(O[i].float().cpu(), oracle_O(X[i], steps, coeffs or oracle.QUINTIC))
+        assert e < TOL_BF16, (sched, steps, i, e)

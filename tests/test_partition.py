@@ -176,7 +176,7 @@ def test_cost_estimate_properties():
     # square: five steps of SYRK + A A + B X on 4096^2 execute ~2e12 flops
     assert 0.3e-3 < c[0] < 3e-3
     more = m.cost_estimate([(4096, 4096)], steps=10)
-    assert more[0] > 1.5 * c[0]            # splits stay on the last two steps
+    assert more[0] > 1.5 * c[0]            # twice the steps, well over 1.5 times the work
     f32 = m.cost_estimate([(4096, 4096)], dtype=__import__("torch").float32)
     assert f32[0] > 10 * c[0]                # FFMA vs tensor cores
     zero = m.cost_estimate([(4096, 4096)], steps=0)
