@@ -442,11 +442,12 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   // one's first, and a grid's fill and drain is a large part of a product.
   // On longer products the overlap only adds power next to a tail it cannot
   // shorten, and the per-tile signals cost more than it gains.  Measured
-  // with shared launches, against separate ones: 8 x 1024 x 4096 (8 pair-tiles
-  // per cluster in the update) 287 -> 360 TFLOP/s; the 512 small matrices of
-  // shapes 256 x 1024 .. 768 x 3072 (up to 75 per cluster) 293 -> 286.
+  // with shared launches, against separate ones: 8 x 1024 x 4096 (7 pair-tiles
+  // per cluster in the update) 287 -> 360 TFLOP/s, 8 x 1024 x 8192 (13.5)
+  // 234 -> 270; the 512 small matrices of shapes 256 x 1024 .. 768 x 3072
+  // (10 to 75 per cluster) 293 -> 286 when every bucket shares launches.
   const long long pairs_rect = static_cast<long long>(Bc) * (g.sp / 256) * (g.lp / 256);
-  const bool chain = cx.dt == MUON_BF16 && pairs_rect <= 8LL * (cx.sms / 2);
+  const bool chain = cx.dt == MUON_BF16 && pairs_rect <= 16LL * (cx.sms / 2);
   // stream-ordered: runs after everything before this chunk, before its pack
   if (chain) CK(cudaMemsetAsync(bf.done, 0, sizeof(int) * Bc, cx.st));
   if (cx.dt == MUON_BF16 && cx.steps > 0) CK(cudaMemsetAsync(bf.tile_ctr, 0, sizeof(int) * kMaxTcLaunches, cx.st));
