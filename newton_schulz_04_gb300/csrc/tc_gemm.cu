@@ -10,9 +10,15 @@
 // Tile scheduling.  Each pair's leader takes tile indices in order from a
 // counter in global memory (atomicAdd) and publishes them to both CTAs through
 // a small shared-memory queue, so pairs that start early -- e.g. while the
-// previous launch on the stream drains -- take more tiles.  Optionally a launch
-// is chained to the previous one per matrix (TcArgs::done): it starts matrix b
-// once the previous launch's epilogues have published all of b's tiles.
+// previous launch on the stream drains -- take more tiles.
+//
+// Products per launch.  A launch runs one product, or up to kMaxPhases
+// consecutive products ("phases", tc_gemm_kernel<kMaxPhases>) whose tiles form
+// one sequence, product by product.  Ordering between products is per matrix
+// (TcProgram::done): every epilogue warp adds 1 to its matrix's counter once
+// its part of a tile is stored, and a tile of a later product (or of a
+// launch chained to the previous one) starts matrix b once the counter shows
+// every earlier product finished b -- no grid boundary in between.
 //
 // Symmetric storage.  A symmetric s x s matrix is stored "block-lower": only
 // its 256 x 256 blocks (I, J) with J <= I are written (diagonal blocks in
@@ -68,6 +74,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <memory>
 #include <mutex>
 #include <utility>
 
@@ -1021,9 +1028,10 @@ static cudaError_t launch_program(const TcGemmDesc* d, const EpiParams* const* e
     const cudaError_t e = ensure_smem_attr<NPH>();
     if (e != cudaSuccess) return e;
   }
-  // The argument block is large (NPH tensor-map sets); build it on the heap.
-  static thread_local TcProgram<NPH>* prog = nullptr;
-  if (!prog) prog = new TcProgram<NPH>();
+  // The argument block is large (NPH tensor-map sets); build it on the heap,
+  // once per thread (the launch copies it).
+  static thread_local std::unique_ptr<TcProgram<NPH>> prog;
+  if (!prog) prog.reset(new TcProgram<NPH>());
   TcProgram<NPH>& a = *prog;
   memset(&a, 0, sizeof(a));
   const EpiParams* fin = nullptr;
