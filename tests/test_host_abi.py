@@ -139,3 +139,24 @@ def test_step_argument_errors(lib):
 
 def test_empty_batch_is_a_noop(lib):
     assert _ns_call(lib, X=1 << 40, B=0, out=1 << 41, ws=1 << 42) == 0
+
+
+def _gemm_call(lib, split=4, dt=2, b_mn=1, M=256, N=256, K=256, B_lo=True, wsb=1024 + 131072, sym=0):
+    big = 1 << 40
+    p = ctypes.c_void_p
+    return lib.muon_debug_gemm(p(big), None, p(2 * big), p(3 * big) if B_lo else None, 1, M, N, K, split, b_mn, sym,
+                               dt, p(5 * big), None, p(6 * big), wsb, None)
+
+
+def test_debug_gemm_diagonal_segment_argument_errors(lib):
+    # every case is refused on the host, before any CUDA call
+    E = {"arg": 1, "shape": 2, "ws": 4}
+    assert _gemm_call(lib, dt=0) == E["arg"]             # bf16: the segment is fp16 only
+    assert _gemm_call(lib, B_lo=False) == E["arg"]       # needs B's low part
+    assert _gemm_call(lib, b_mn=0) == E["arg"]           # needs an MN-major B
+    assert _gemm_call(lib, K=512) == E["arg"]            # D is square: K must equal M
+    assert _gemm_call(lib, sym=1) == E["arg"]            # full outputs only
+    assert _gemm_call(lib, wsb=1024 + 1000) == E["ws"]   # room for the diagonal table
+    assert "workspace" in lib.muon_last_error().decode()
+    assert _gemm_call(lib, split=5) == E["arg"]
+    assert _gemm_call(lib, M=200, K=200) == E["shape"]   # tiles pair 256 rows
