@@ -7,7 +7,8 @@ apply W <- W - lr O, through the C ABI (muon_step).
 Default workload: 16 square 1024x1024 bf16 gradients N(0, 0.02^2), fp32
 momentum, bf16 weights (the square case where Gram space gives no reduction).
 Other workloads (--config): c3 (32-layer d=4096 / ffn=14336 model, every
-matrix), c4 (512 mixed small matrices), c5_n<N> (1024 x N, batch 8).
+matrix), c4 (512 mixed small matrices), c5_n<N>[_t<T>] and c5f32_n<N>[_t<T>]
+(1024 x N, batch 8, T NS steps, 5 by default).
 
 Prints one JSON line (rank 0).  `value` is algorithmic TFLOP/s over all ranks
 (symmetric Gram count 3 s^2 l + (4T - 3) s^3 per matrix), with inputs resident
@@ -95,6 +96,25 @@ def recorded_traffic(workload: str, kernel: str):
     return None
 
 
+def c5_params(name: str):
+    """(n, NS steps) of a c5 config name: c5[f32][_n<N>][_t<T>]."""
+    n, steps = 4096, 5
+    for part in name.split("_")[1:]:
+        if part.startswith("n"):
+            n = int(part[1:])
+        elif part.startswith("t"):
+            steps = int(part[1:])
+    return n, steps
+
+
+def workload_desc(name: str) -> str:
+    if name.startswith("c5"):
+        n, steps = c5_params(name)
+        dt = "fp32" if name.startswith("c5f32") else "bf16"
+        return f"8 x 1024x{n} {dt} grads N(0,1) with row 0 x100, fp32 momentum, {steps} NS steps quintic"
+    return WORKLOAD_DESC.get(name, name)
+
+
 def make_workload(name: str, device):
     if name == "c2":
         return synth.c2(device)
@@ -106,12 +126,10 @@ def make_workload(name: str, device):
         return synth.c4(device)
     if name == "c1":
         return synth.c1()
-    if name.startswith("c5f32"):
-        n = int(name.split("_n")[1]) if "_n" in name else 4096
-        return synth.c5(device, n=n, dtype=torch.float32)
     if name.startswith("c5"):
-        n = int(name.split("_n")[1]) if "_n" in name else 4096
-        return synth.c5(device, n=n)
+        n, steps = c5_params(name)
+        return synth.c5(device, n=n, dtype=torch.float32 if name.startswith("c5f32") else torch.bfloat16,
+                        steps=steps)
     raise SystemExit(f"unknown config {name}")
 
 
@@ -316,7 +334,7 @@ def run_reference(args, world, rank):
         "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_s / max(args.steps, 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC.get(args.config, args.config), "name": args.config,
+        "config": {"workload": workload_desc(args.config), "name": args.config,
                    "sample": vals[0]["sample"]},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": vals[0]["cores"], "kind": "oracle",
                          "sample": vals[0]["sample"]},
@@ -492,7 +510,7 @@ def run_ours(args, world, rank, local):
                      "bf16 in and out; NS products on bf16 (step 0) and fp16 (later steps) tensor-core operands, "
                      "fp32 accumulation"),
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC.get(args.config, args.config), "name": args.config,
+        "config": {"workload": workload_desc(args.config), "name": args.config,
                    "matrices_per_gpu": count, "l2": "flushed between timed steps" if flush is not None
                    else "inputs larger than L2",
                    "parallelism": "1 gpu" if world == 1 else
