@@ -33,9 +33,11 @@
  *  - Argument errors are detected before anything is launched, so a failed
  *    call writes nothing.  Nothing throws across the ABI.  The message of the
  *    last error on the calling thread is returned by muon_last_error().
- *  - A kernel that waits longer than its bound (about a second) on an
+ *  - A kernel that waits longer than its bound (4e9 SM clock cycles: about
+ *    2 s at the 2.07 GHz maximum clock, longer at lower clocks) on an
  *    internal barrier stops, records MUON_ERR_TIMEOUT in the workspace's
- *    status word and returns; muon_device_status() reports it.
+ *    status word and returns; muon_device_status() reports it.  The output
+ *    of such a call is incomplete.
  *  - NaN and Inf in the inputs propagate; they are not checked.
  *  - Calls that share a workspace must be ordered on one stream.
  */
@@ -242,18 +244,38 @@ MUON_API muon_status muon_profile_get(int i, const char** kind, float* ms, doubl
  *  - Problems whose single matrix needs more scratch than the array holds
  *    (e.g. a bf16 2048 x 2048 matrix) are rejected with MUON_ERR_WORKSPACE
  *    before anything is launched; larger batches are processed in chunks.
- *  - It calls no cudaMalloc, cudaFree or other allocating routine.  The first
- *    call on each device looks up the array's device address; make that first
- *    call before any stream capture.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.  Every call
+ *    looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress, which allocates nothing); the first call on a
+ *    device may load the library's device code, so make that first call
+ *    before any stream capture.
  *  - All calls share the one array: calls whose work overlaps on the GPU (two
  *    streams, two threads without ordering) race and give wrong results.
- *    Order them on one stream.  Each call resets the array's status word, so
- *    muon_device_status(scratch) is not available here.
+ *    Order them on one stream.
+ *  - A bounded-wait timeout inside one of its kernels is recorded in the
+ *    array's status word, which persists across calls until
+ *    muon_static_status() reads and clears it.
  */
 MUON_API muon_status muon_ns_batched_static(const void* X, int B, int m, int n, int steps,
                                             const float* coeffs, void* out, muon_dtype dt,
                                             muon_sched sc, void* stream);
 MUON_API size_t muon_static_scratch_bytes(void);
+
+/*
+ * muon_static_status -- muon_device_status for the static scratch: synchronise
+ * `stream`, then read and clear the status word of the array that
+ * muon_ns_batched_static runs in.  Returns MUON_ERR_TIMEOUT if one of its
+ * kernels gave up on a bounded wait since the last check (the output of that
+ * call is incomplete), MUON_ERR_CUDA on a CUDA error, else MUON_OK.
+ * Allocates nothing.
+ */
+MUON_API muon_status muon_static_status(void* stream);
+
+/*
+ * muon_debug_bounded_wait_static -- muon_debug_bounded_wait on the static
+ * scratch's status word (failure-detection self-test of muon_static_status).
+ */
+MUON_API muon_status muon_debug_bounded_wait_static(long long max_cycles, void* stream);
 
 /*
  * muon_adamw_tail -- one AdamW step over the non-matrix "tail" of a model

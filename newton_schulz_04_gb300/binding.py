@@ -78,6 +78,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.muon_ns_batched_static.restype = i32
     lib.muon_static_scratch_bytes.argtypes = []
     lib.muon_static_scratch_bytes.restype = sz
+    lib.muon_static_status.argtypes = [vp]
+    lib.muon_static_status.restype = i32
+    lib.muon_debug_bounded_wait_static.argtypes = [ctypes.c_longlong, vp]
+    lib.muon_debug_bounded_wait_static.restype = i32
     lib.muon_adamw_tail.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp),
                                     ctypes.POINTER(i64), i32, f32, f32, f32, f32, f32, i32, i32, vp]
     lib.muon_adamw_tail.restype = i32
@@ -334,6 +338,16 @@ def ns_batched_static(X: torch.Tensor, steps: int = 5, coeffs=None, schedule: st
     return out
 
 
+def static_status(stream=None) -> int:
+    """Synchronise and read/clear the status word of the static scratch that
+    ns_batched_static runs in (OK or ERR_TIMEOUT)."""
+    return load().muon_static_status(ctypes.c_void_p(_stream_ptr(stream)))
+
+
+def debug_bounded_wait_static(max_cycles: int, stream=None) -> None:
+    _check(load().muon_debug_bounded_wait_static(int(max_cycles), ctypes.c_void_p(_stream_ptr(stream))))
+
+
 def muon_step(weights: Sequence[torch.Tensor], grads: Sequence[torch.Tensor], moms: Sequence[torch.Tensor],
               beta: float = 0.95, lr: float = 0.02, steps: int = 5, coeffs=None, schedule: str = "auto",
               workspace: torch.Tensor | None = None, stream=None) -> None:
@@ -454,18 +468,23 @@ class MuonUpdater:
                   self.workspace, stream)
 
     def step(self, grads: Sequence[torch.Tensor], stream=None):
+        """One step on `stream` (the current stream if None)."""
         if not self.use_graph:
             self._eager(grads, stream)
             return
         key = tuple(g.data_ptr() for g in grads)
         graph = self._graphs.get(key)
         if graph is not None:
-            graph.replay()
+            if stream is None:
+                graph.replay()
+            else:
+                with torch.cuda.stream(stream):
+                    graph.replay()
             return
         # this call's update runs eagerly (and sets up per-device state); the same
         # launch sequence is then captured for the following calls
-        self._eager(grads)
-        torch.cuda.current_stream().synchronize()
+        self._eager(grads, stream)
+        (stream if stream is not None else torch.cuda.current_stream()).synchronize()
         graph = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
         with torch.cuda.graph(graph, stream=side):

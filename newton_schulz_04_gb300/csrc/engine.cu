@@ -5,17 +5,22 @@
 // run the Gram recurrence jointly), carve the caller's workspace, and enqueue one
 // schedule per group on the caller's stream:
 //
-//   ORIG     original space, bf16 tensor-core products, fp32 carry of X:
-//            A = X X^T (SYRK), B = b A + c A^2, X <- a X + B X
-//   GRAM_X3  Gram space with split-bf16 operands (hi*hi + hi*lo + lo*hi):
-//            G0 = X0 X0^T; P_k = a I + b G_k + c G_k^2; Q <- P_k Q;
-//            G_{k+1} = P_k (P_k G_k); O = Q X0
-//   GRAM_X1  the same recurrence with plain bf16 operands
-//   fp32     the ORIG or Gram recurrence with fp32 FFMA products
+//   ORIG       original space.  Step 0 multiplies the packed bf16 copy of M;
+//              later products take fp16 operands, with X carried between steps
+//              as an fp16 pair (hi + lo / 2^11):
+//              A = X X^T (SYRK), B' = a I + b A + c A^2, X <- B' X_hi + a X_lo
+//   ORIG_BF16  the same on bf16 operands only, X carried as a bf16 pair, with
+//              split products in the last steps
+//   GRAM_X3    Gram space with split-bf16 operands (hi*hi + hi*lo + lo*hi):
+//              G0 = X0 X0^T; P_k = a I + b G_k + c G_k^2; Q <- P_k Q;
+//              G_{k+1} = P_k (P_k G_k); O = Q X0
+//   GRAM_X1    the same recurrence with plain bf16 operands
+//   fp32       the ORIG or Gram recurrence with fp32 FFMA products
 //
 // Why these: the Gram recurrence squares the condition number, so plain bf16
 // products in Gram space exceed a 2e-2 relative error on ill-conditioned
-// inputs; split operands restore it at three products per product.
+// inputs; split operands restore it at three products per product.  fp16
+// operands (11 significant bits) in original space need no splits.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -23,7 +28,6 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
-#include <mutex>
 #include <string>
 #include <vector>
 
@@ -152,24 +156,15 @@ static muon_sched resolve(long long s, long long l, int steps, muon_dtype dt, mu
   }
   if (steps == 0) return MUON_SCHED_ORIG;  // only the packed fp32 copy is needed
   if (sc != MUON_SCHED_AUTO) return sc;
-  // Tensor-core work (symmetric products counted once):
-  //   ORIG     per step 3 s^2 l + s^3 (SYRK s^2 l, A*A s^3, B*X 2 s^2 l), plus
-  //            2 s^3 per split A*A and 2 s^2 l per split B*X
-  //   GRAM_X3  3 s^2 l (SYRK, split) + 3 (4T - 3) s^3 + 6 s^2 l (Q X0, split)
-  const double S = static_cast<double>(s), L = static_cast<double>(l), T = steps;
-  const double na = std::min<double>(T, split_steps(steps, kSplitA));
-  const double nb = std::min<double>(T, split_steps(steps, kSplitB));
-  const double orig = T * (3 * S * S * L + S * S * S) + na * 2 * S * S * S + nb * 2 * S * S * L;
-  const double x3 = 9 * S * S * L + 3 * (4 * T - 3) * S * S * S;
   // Gram space squares the condition number, and the tensor cores' fp32
   // accumulation is measurably coarser than IEEE fp32 (error ~1e-6 of the sum
   // of |products| per element, growing with K): on ill-conditioned inputs
-  // (rank-8 + noise) the split Gram recurrence exceeds the 2e-2 target even
-  // at aspect 1:8, where it would save ~30 % of the work, while the
-  // original-space schedule stays near 1e-2.  AUTO therefore runs bf16 in
-  // original space; GRAM_X3 / GRAM_X1 remain available on request.
-  (void)orig;
-  (void)x3;
+  // (rank-8 + noise) the split Gram recurrence exceeds the 2e-2 target, while
+  // the original-space schedule on fp16 operands stays near 1e-3.  AUTO
+  // therefore runs bf16 in original space; GRAM_X3 / GRAM_X1 remain available
+  // on request.
+  (void)s;
+  (void)l;
   return MUON_SCHED_ORIG;
 }
 
@@ -1243,50 +1238,76 @@ muon_status muon_profile_get(int i, const char** kind, float* ms, double* flops,
 // Device scratch for muon_ns_batched_static: one file-scope array, present on
 // every GPU that loads this library until the process exits.  Host code only
 // sees a host-side stand-in for this symbol, so its device address is looked
-// up once per device (cudaGetSymbolAddress) and passed to the kernels like any
-// caller workspace.
+// up (cudaGetSymbolAddress, on the current device) by every call that needs
+// it and passed to the kernels like any caller workspace.  The array starts
+// zeroed when the module loads; its first word is the status word, which
+// kernels set on a bounded-wait timeout and muon_static_status reads and
+// clears.
 static constexpr size_t kStaticScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
-static constexpr int kMaxDevices = 64;
-static void* g_static_addr[kMaxDevices] = {nullptr};
-static std::mutex g_static_mu;
+
+static muon_status static_scratch_addr(void** out) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess || !p) {
+    cudaGetLastError();
+    return fail(MUON_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s", cudaGetErrorString(e));
+  }
+  *out = p;
+  return MUON_OK;
+}
 
 muon_status muon_ns_batched_static(const void* X, int B, int m, int n, int steps, const float* coeffs, void* out,
                                    muon_dtype dt, muon_sched sc, void* stream) {
   g_last_error.clear();
-  if (B < 0) return fail(MUON_ERR_ARG, "B=%d < 0", B);
-  if (B > 0 && (!X || !out)) return fail(MUON_ERR_ARG, "X or out is NULL");
-  if (m <= 0 || n <= 0 || m > MUON_MAX_DIM || n > MUON_MAX_DIM) return fail(MUON_ERR_SHAPE, "bad shape %dx%d", m, n);
-  if (steps < 0 || steps > MUON_MAX_STEPS) return fail(MUON_ERR_ARG, "steps=%d out of [0, %d]", steps, MUON_MAX_STEPS);
-  if (!valid_dt(dt) || !valid_sc(sc)) return fail(MUON_ERR_ARG, "bad dtype or schedule");
-  // Reject problems whose single matrix does not fit the fixed scratch, before any CUDA call.
-  const Group g = make_group(m, n, steps, dt, sc);
-  const size_t need = group_bytes(g, 1, dt);
-  if (need > kStaticScratchBytes)
-    return fail(MUON_ERR_WORKSPACE,
-                "a %dx%d matrix needs %zu bytes of scratch; the static scratch of muon_ns_batched_static holds "
-                "%zu bytes (use muon_ns_batched with a caller workspace)",
-                m, n, need, kStaticScratchBytes);
-  if (B == 0) return MUON_OK;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return fail(MUON_ERR_UNSUPPORTED, "device %d out of range", dev);
-  void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_static_mu);
-    if (!g_static_addr[dev]) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_static_scratch);
-      if (e != cudaSuccess || !p) return fail(MUON_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-      g_static_addr[dev] = p;
-    }
-    scratch = g_static_addr[dev];
+  try {
+    if (B < 0) return fail(MUON_ERR_ARG, "B=%d < 0", B);
+    if (B > 0 && (!X || !out)) return fail(MUON_ERR_ARG, "X or out is NULL");
+    if (m <= 0 || n <= 0 || m > MUON_MAX_DIM || n > MUON_MAX_DIM)
+      return fail(MUON_ERR_SHAPE, "bad shape %dx%d", m, n);
+    if (steps < 0 || steps > MUON_MAX_STEPS)
+      return fail(MUON_ERR_ARG, "steps=%d out of [0, %d]", steps, MUON_MAX_STEPS);
+    if (!valid_dt(dt) || !valid_sc(sc)) return fail(MUON_ERR_ARG, "bad dtype or schedule");
+    // Reject problems whose single matrix does not fit the fixed scratch, before any CUDA call.
+    const Group g = make_group(m, n, steps, dt, sc);
+    const size_t need = group_bytes(g, 1, dt);
+    if (need > kStaticScratchBytes)
+      return fail(MUON_ERR_WORKSPACE,
+                  "a %dx%d matrix needs %zu bytes of scratch; the static scratch of muon_ns_batched_static holds "
+                  "%zu bytes (use muon_ns_batched with a caller workspace)",
+                  m, n, need, kStaticScratchBytes);
+    if (B == 0) return MUON_OK;
+    void* scratch = nullptr;
+    const muon_status st = static_scratch_addr(&scratch);
+    if (st != MUON_OK) return st;
+    return muon_ns_batched(X, B, m, n, steps, coeffs, out, dt, sc, scratch, kStaticScratchBytes, stream);
+  } catch (...) {
+    return fail(MUON_ERR_ARG, "internal exception");
   }
-  // The status word starts at zero for every call (the array keeps the last call's contents).
-  e = cudaMemsetAsync(scratch, 0, sizeof(int), static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return fail(MUON_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
-  return muon_ns_batched(X, B, m, n, steps, coeffs, out, dt, sc, scratch, kStaticScratchBytes, stream);
+}
+
+muon_status muon_static_status(void* stream) {
+  g_last_error.clear();
+  try {
+    void* scratch = nullptr;
+    const muon_status st = static_scratch_addr(&scratch);
+    if (st != MUON_OK) return st;
+    return muon_device_status(scratch, stream);
+  } catch (...) {
+    return fail(MUON_ERR_ARG, "internal exception");
+  }
+}
+
+muon_status muon_debug_bounded_wait_static(long long max_cycles, void* stream) {
+  g_last_error.clear();
+  try {
+    void* scratch = nullptr;
+    const muon_status st = static_scratch_addr(&scratch);
+    if (st != MUON_OK) return st;
+    return muon_debug_bounded_wait(scratch, max_cycles, stream);
+  } catch (...) {
+    return fail(MUON_ERR_ARG, "internal exception");
+  }
 }
 
 size_t muon_static_scratch_bytes(void) { return kStaticScratchBytes; }

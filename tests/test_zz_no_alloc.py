@@ -45,6 +45,26 @@ def test_static_scratch_matches_workspace_entry_point_twice():
 
 
 @pytest.mark.gpu
+def test_static_scratch_reports_a_timed_out_wait():
+    """A kernel that gives up on a bounded wait sets the static scratch's
+    status word; muon_static_status reports MUON_ERR_TIMEOUT once, clears the
+    word, and the next call on the same scratch is unaffected."""
+    import newton_schulz_04_gb300 as m
+    m.load(build_if_missing=True)
+    X = torch.stack([synth.random_matrix(256, 512, seed=74 + i) for i in range(2)]).to(torch.bfloat16).cuda()
+    ref = m.ns_batched(X, steps=5)
+    m.ns_batched_static(X, steps=5)
+    assert m.static_status() == 0  # MUON_OK after a normal call
+    m.debug_bounded_wait_static(2_000_000)  # ~1 ms of SM cycles; nothing arrives
+    assert m.static_status() == 6  # MUON_ERR_TIMEOUT
+    assert m.static_status() == 0  # read and cleared
+    got = m.ns_batched_static(X, steps=5)
+    torch.cuda.synchronize()
+    assert m.static_status() == 0
+    assert torch.equal(got, ref)
+
+
+@pytest.mark.gpu
 def test_static_scratch_refuses_oversized_problems_before_launch():
     import newton_schulz_04_gb300 as m
     lib = m.load(build_if_missing=True)
