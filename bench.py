@@ -4,11 +4,13 @@ One step = one pass of the whole update over a batch of synthetic matrices:
 momentum accumulate + pack + norm, Newton-Schulz (5 steps, quintic), and the
 apply W <- W - lr O, through the C ABI (muon_step).
 
-Default workload: 16 square 1024x1024 bf16 gradients N(0, 0.02^2), fp32
-momentum, bf16 weights (the square case where Gram space gives no reduction).
-Other workloads (--config): c3 (32-layer d=4096 / ffn=14336 model, every
-matrix), c4 (512 mixed small matrices), c5_n<N>[_t<T>] and c5f32_n<N>[_t<T>]
-(1024 x N, batch 8, T NS steps, 5 by default).
+Default workload: every 2-D matrix of a Llama-style 32-layer model with
+d = 4096 and ffn = 14336 (q, k, v, o 4096x4096; gate, up 4096x14336; down
+14336x4096; 7.78e9 parameters), bf16 gradients N(0, 1e-6) and weights, fp32
+momentum.  Other workloads (--config): c2 (16 square 1024x1024 bf16 matrices,
+the square case where Gram space gives no reduction), c4 (512 mixed small
+matrices), c5_n<N>[_t<T>] and c5f32_n<N>[_t<T>] (1024 x N, batch 8, T NS
+steps, 5 by default), c3_l<L> (the first L layers of the model).
 
 Prints one JSON line (rank 0).  `value` is algorithmic TFLOP/s over all ranks
 (symmetric Gram count 3 s^2 l + (4T - 3) s^3 per matrix), with inputs resident
@@ -16,6 +18,11 @@ in HBM; `e2e` is the same metric with the gradients copied from pinned host
 memory and the updated weights copied back inside the timed region.
 `--impl reference` times the fp64 CPU oracle on a bounded sample of the same
 workload instead.
+
+`--record-traffic CSV` reads an ncu log (`--csv --log-file` of the metrics
+dram__bytes_read.sum, dram__bytes_write.sum, gpu__time_duration.sum) taken on
+`--config`, and stores the mean DRAM bytes per launch of each kernel family
+in profiles/dram_traffic.json, from which `roofline.traffic` is taken.
 """
 from __future__ import annotations
 
@@ -72,28 +79,106 @@ def peaks():
     return dict(FALLBACK, source="fallback")
 
 
-KERNEL_SOURCES = {"pack": "elementwise.cu", "norm_finalize": "elementwise.cu", "final": "elementwise.cu",
-                  "adamw_tail": "adamw.cu"}
+# source file of each kernel family (a recorded traffic row is valid only while
+# its family's source is unchanged)
+FAMILY_SOURCES = {"tc_gemm": "tc_gemm.cu", "simt_gemm": "simt_gemm.cu", "pack": "elementwise.cu",
+                  "norm_finalize": "elementwise.cu", "final": "elementwise.cu", "adamw_tail": "adamw.cu"}
+TRAFFIC_JSON = os.path.join("profiles", "dram_traffic.json")
 
 
-def recorded_traffic(workload: str, kernel: str):
-    """Per-launch DRAM bytes (read + write) recorded by ncu in profiles/dram_traffic.md,
-    or None when there is no row for this workload and kernel class, or when the
-    kernel's source has changed since the row was taken (its sha256 no longer matches)."""
+def family_of(name: str) -> str:
+    """Kernel family of a launch label of the library's profiler ("tc_rect",
+    "tc_program", ...) or of an ncu kernel name ("void muon::tc_gemm_kernel<16>(...)")."""
+    n = name.lower()
+    for key, fam in (("tc_", "tc_gemm"), ("simt", "simt_gemm"), ("pack", "pack"), ("norm", "norm_finalize"),
+                     ("final", "final"), ("adamw", "adamw_tail"), ("fill_diag", "norm_finalize")):
+        if key in n:
+            return fam
+    return n
+
+
+def source_sha(family: str, root=None) -> str | None:
     import hashlib
-    src = KERNEL_SOURCES.get(kernel, "simt_gemm.cu" if kernel.startswith("simt") else "tc_gemm.cu")
+    src = FAMILY_SOURCES.get(family)
+    if src is None:
+        return None
     try:
-        sha = hashlib.sha256(open(os.path.join(ROOT, "newton_schulz_04_gb300", "csrc", src), "rb").read())
-        table = open(os.path.join(ROOT, "profiles", "dram_traffic.md")).read()
+        data = open(os.path.join(root or ROOT, "newton_schulz_04_gb300", "csrc", src), "rb").read()
     except OSError:
         return None
-    for line in table.splitlines():
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) == 8 and cells[0] == workload and cells[1] == kernel:
-            if not sha.hexdigest().startswith(cells[2]):
+    return hashlib.sha256(data).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, family: str):
+    """Mean DRAM bytes (read + write) per launch of a kernel family on a
+    workload, from profiles/dram_traffic.json, or None when there is no row, or
+    when the family's source has changed since the row was recorded."""
+    try:
+        rows = json.load(open(os.path.join(ROOT, TRAFFIC_JSON)))["rows"]
+    except (OSError, ValueError, KeyError):
+        return None
+    for r in rows:
+        if r.get("workload") == workload and r.get("family") == family:
+            if r.get("source_sha16") != source_sha(family):
                 return None
-            return float(cells[6]) * 1e6
+            return float(r["bytes_per_launch"])
     return None
+
+
+_UNITS = {"byte": 1.0, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12,
+          "nsecond": 1e-9, "usecond": 1e-6, "msecond": 1e-3, "second": 1.0}
+
+
+def parse_ncu_csv(path):
+    """{launch id: {"kernel": name, metric: value in bytes or seconds}} from an
+    ncu `--csv --log-file` metrics log (one row per launch and metric)."""
+    import csv
+    launches = {}
+    with open(path, newline="") as f:
+        lines = [ln for ln in f if ln.startswith('"')]  # ncu's own ==PROF== lines are not CSV
+    for row in csv.DictReader(lines):
+        try:
+            lid = int(row["ID"])
+            val = float(row["Metric Value"].replace(",", ""))
+        except (KeyError, ValueError):
+            continue
+        d = launches.setdefault(lid, {"kernel": row.get("Kernel Name", "")})
+        d[row["Metric Name"]] = val * _UNITS.get(row.get("Metric Unit", "").strip().lower(), 1.0)
+    return launches
+
+
+def record_traffic(csv_path, workload, command, scale=1.0, note=""):
+    """Average the captured launches per kernel family and store them (the
+    traffic per launch of `workload`, scaled by `scale` when the capture ran a
+    smaller case with the same launch structure) in profiles/dram_traffic.json."""
+    launches = parse_ncu_csv(csv_path)
+    fams = {}
+    for d in launches.values():
+        if "dram__bytes_read.sum" not in d or "dram__bytes_write.sum" not in d:
+            continue
+        f = fams.setdefault(family_of(d["kernel"]), [0, 0.0, 0.0, 0.0])
+        f[0] += 1
+        f[1] += d["dram__bytes_read.sum"]
+        f[2] += d["dram__bytes_write.sum"]
+        f[3] += d.get("gpu__time_duration.sum", 0.0)
+    path = os.path.join(ROOT, TRAFFIC_JSON)
+    try:
+        doc = json.load(open(path))
+    except (OSError, ValueError):
+        doc = {"rows": []}
+    doc["about"] = ("DRAM bytes per launch by kernel family, averaged over the captured launches "
+                    "(ncu dram__bytes_read.sum + dram__bytes_write.sum), written by bench.py --record-traffic")
+    rows = [r for r in doc.get("rows", []) if not (r.get("workload") == workload and r.get("family") in fams)]
+    for fam, (n, rd, wr, t) in sorted(fams.items()):
+        rows.append({"workload": workload, "family": fam, "source_sha16": source_sha(fam), "launches": n,
+                     "read_bytes_per_launch": scale * rd / n, "write_bytes_per_launch": scale * wr / n,
+                     "bytes_per_launch": scale * (rd + wr) / n, "ncu_us_per_launch": 1e6 * t / n,
+                     "scale": scale, "note": note, "command": command})
+    doc["rows"] = sorted(rows, key=lambda r: (r["workload"], r["family"]))
+    with open(path, "w") as f:
+        json.dump(doc, f, indent=1)
+        f.write("\n")
+    return doc
 
 
 def c5_params(name: str):
@@ -108,6 +193,9 @@ def c5_params(name: str):
 
 
 def workload_desc(name: str) -> str:
+    if name.startswith("c3_l") and name[4:].isdigit():
+        return (f"the first {name[4:]} layers of the d=4096 ffn=14336 model (per layer 4 x 4096^2, 2 x 4096x14336, "
+                f"14336x4096), bf16 grads N(0,1e-6), fp32 momentum, 5 NS steps")
     if name.startswith("c5"):
         n, steps = c5_params(name)
         dt = "fp32" if name.startswith("c5f32") else "bf16"
@@ -122,6 +210,8 @@ def make_workload(name: str, device):
         return synth.c3(device)
     if name == "c3_layer":  # one layer of c3 (same shapes), for profiling
         return synth.c3(device, layers=1)
+    if name.startswith("c3_l") and name[4:].isdigit():  # the first L layers of c3
+        return synth.c3(device, layers=int(name[4:]))
     if name == "c4":
         return synth.c4(device)
     if name == "c1":
@@ -143,6 +233,18 @@ WORKLOAD_DESC = {
 }
 
 
+def smi_id(local: int) -> str:
+    """nvidia-smi's name for CUDA device `local` of this process: its UUID (the
+    CUDA ordinal can name another GPU when CUDA_VISIBLE_DEVICES remaps)."""
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        if u:
+            return u if u.startswith("GPU-") else f"GPU-{u}"
+    except Exception:
+        pass
+    return str(local)
+
+
 class Clocks:
     """Samples nvidia-smi every 200 ms while running."""
 
@@ -156,7 +258,7 @@ class Clocks:
 
     def __enter__(self):
         try:
-            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={smi_id(self.index)}", f"--query-gpu={self.FIELDS}",
                                        "--format=csv,noheader,nounits", "-lms", "200"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
@@ -281,13 +383,16 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
-def cpu_baseline(work, budget_s=15.0, max_mats=None):
-    """The fp64 oracle, as it stands, on a bounded sample of the workload."""
+def cpu_baseline(work, budget_s=15.0, max_mats=None, start=0, of=None):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload
+    (matrices from index `start` on, cyclically; `of` describes the whole
+    workload the sample comes from)."""
     import oracle
     flops = 0.0
     done = 0
     t0 = time.perf_counter()
-    order = list(range(len(work.shapes)))
+    n_all = len(work.shapes)
+    order = [(start + k) % n_all for k in range(n_all)]
     for i in order:
         if max_mats is not None and done >= max_mats:
             break
@@ -308,22 +413,38 @@ def cpu_baseline(work, budget_s=15.0, max_mats=None):
     except Exception:
         pass
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} of {len(work.shapes)} matrices of the same workload, fp64 numpy, "
-                      f"{dt:.1f} s", "seconds": dt, "matrices": done}
+            "sample": f"{done} of {of or f'{n_all} matrices of the same workload'}, fp64 numpy, {dt:.1f} s",
+            "seconds": dt, "matrices": done}
+
+
+def c3_sample(work):
+    """One matrix of each bucket of the model: layer 0's q (4096x4096) and down
+    (14336x4096), drawn exactly as in the full workload (same seeded streams)."""
+    pick = [i for i in (0, 6) if i < len(work.shapes)]
+    return synth.Workload("c3_sample", [work.shapes[i] for i in pick], [work.grads[i].cpu() for i in pick],
+                          [work.weights[i].cpu() for i in pick])
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    work = make_workload(args.config, "cpu")
+    of = None
+    if args.config.startswith("c3"):
+        # the model's first layer holds one matrix of each bucket; the oracle
+        # takes one of them per step, in turn
+        work = c3_sample(synth.c3("cpu", layers=1))
+        of = f"sampled matrices (4096x4096 and 14336x4096) of {workload_desc(args.config)}"
+        per_step = dict(max_mats=1)
+    else:
+        work = make_workload(args.config, "cpu")
+        per_step = dict(budget_s=max(5.0, 60.0 / max(args.steps, 1)))
     steps = []
-    per_step_budget = max(5.0, 60.0 / max(args.steps, 1))
     for _ in range(args.warmup):
-        cpu_baseline(work, budget_s=1.0, max_mats=1)
+        cpu_baseline(synth.c1(), budget_s=1.0, max_mats=1)
     vals = []
     t_all = time.perf_counter()
-    for _ in range(args.steps):
-        r = cpu_baseline(work, budget_s=per_step_budget)
+    for k in range(args.steps):
+        r = cpu_baseline(work, start=k, of=of, **per_step)
         vals.append(r)
         steps.append(r["seconds"])
     tot_flops = sum(v["value"] * 1e12 * v["seconds"] for v in vals)
@@ -411,7 +532,8 @@ def run_ours(args, world, rank, local):
     ms_step = 1e3 * t_total / args.steps
     value = flops_all * args.steps / t_total / 1e12
     value_eager = flops_all * args.steps / max_over_ranks(sum(ms_eager) / 1e3, world) / 1e12
-    # dominant kernel kind by time in the profiled pass
+    # per-launch-label totals of the profiled pass, then per kernel family
+    # (tc_syrk / tc_sym / tc_rect / tc_program are launches of one kernel)
     by = {}
     for k, t, fl, byt in recs:
         d = by.setdefault(k, [0.0, 0, 0.0, 0.0])
@@ -419,36 +541,46 @@ def run_ours(args, world, rank, local):
         d[1] += 1
         d[2] += fl
         d[3] += byt
-    dom = max(by, key=lambda k: by[k][0])
+    fam = {}
+    for k, v in by.items():
+        d = fam.setdefault(family_of(k), [0.0, 0, 0.0, 0.0])
+        for i in range(4):
+            d[i] += v[i]
+    dom = max(fam, key=lambda k: fam[k][0])
     pk = peaks()
     # a kernel inside a seconds-long step runs under the power cap: sustained peak
     sustained = ms_step >= 100.0
     tc_peak = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
     traffic = recorded_traffic(args.config, dom)
     tot_launch_ms = sum(v[0] for v in by.values())
-    if dom.startswith("simt"):
-        achieved = by[dom][2] / (by[dom][0] / 1e3) / 1e12
-        mhz = clocks.get("sm_mhz") or 2070.0
-        alu_peak = fp32_alu_peak_tflops(mhz)
-        roof = {"bound": "alu", "kernel": dom, "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-                "frac": achieved / alu_peak, "traffic": traffic,
-                "peak_source": f"152 SMs x 128 FP32 lanes x 2 flops x {mhz:.0f} MHz (sampled median, else max)",
-                "launches": by[dom][1], "avg_launch_ms": by[dom][0] / by[dom][1],
-                "share_of_launch_time": by[dom][0] / tot_launch_ms}
-    elif dom.startswith("tc"):
-        achieved = by[dom][2] / (by[dom][0] / 1e3) / 1e12
-        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": tc_peak,
-                "unit": "TFLOP/s", "frac": achieved / tc_peak, "traffic": traffic,
-                "peak_source": pk["source"] + (" sustained" if sustained else " burst"), "launches": by[dom][1],
-                "avg_launch_ms": by[dom][0] / by[dom][1], "share_of_launch_time": by[dom][0] / tot_launch_ms}
+    t_dom = fam[dom][0] / 1e3
+    common = {"kernel": dom, "traffic": traffic, "launches": fam[dom][1], "avg_launch_ms": fam[dom][0] / fam[dom][1],
+              "share_of_launch_time": fam[dom][0] / tot_launch_ms,
+              "launch_labels": sorted(k for k in by if family_of(k) == dom)}
+    if dom in ("tc_gemm", "simt_gemm"):
+        # achieved: the method's algorithmic count (symmetric Gram form,
+        # 3 s^2 l + (4T - 3) s^3 per matrix) of the steps the profiled pass ran,
+        # over the family's summed launch time; executed: the products the
+        # schedule actually ran (lower tiles of symmetric outputs counted once)
+        achieved = flops_step * args.steps / t_dom / 1e12
+        executed = fam[dom][2] / t_dom / 1e12
+        if dom == "simt_gemm":
+            mhz = clocks.get("sm_mhz") or 2070.0
+            peak = fp32_alu_peak_tflops(mhz)
+            roof = dict(bound="alu", achieved=achieved, peak=peak, unit="TFLOP/s", frac=achieved / peak,
+                        executed_tflops=executed, executed_frac=executed / peak,
+                        peak_source=f"152 SMs x 128 FP32 lanes x 2 flops x {mhz:.0f} MHz (sampled median, else max)")
+        else:
+            roof = dict(bound="tensor", achieved=achieved, peak=tc_peak, unit="TFLOP/s", frac=achieved / tc_peak,
+                        executed_tflops=executed, executed_frac=executed / tc_peak,
+                        peak_source=pk["source"] + (" sustained" if sustained else " burst"))
     else:
-        achieved = by[dom][3] / (by[dom][0] / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "peak_source": pk["source"],
-                "launches": by[dom][1], "avg_launch_ms": by[dom][0] / by[dom][1],
-                "share_of_launch_time": by[dom][0] / tot_launch_ms}
+        achieved = fam[dom][3] / t_dom / 1e9
+        roof = dict(bound="hbm", achieved=achieved, peak=pk["hbm_gbs"], unit="GB/s", frac=achieved / pk["hbm_gbs"],
+                    peak_source=pk["source"])
+    roof.update(common)
     kernels = {k: {"launches": v[1], "ms_total": v[0], "share": v[0] / tot_launch_ms,
-                   "tflops": (v[2] / (v[0] / 1e3) / 1e12) if v[2] else None,
+                   "executed_tflops": (v[2] / (v[0] / 1e3) / 1e12) if v[2] else None,
                    "gbs": (v[3] / (v[0] / 1e3) / 1e9) if v[3] else None} for k, v in by.items()}
     # ---- end to end through the C ABI with host buffers (pinned).  Every step
     # copies its gradients in from pinned host memory and the updated weights
@@ -533,8 +665,10 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline and cpu_work is not None:
         line["cpu_baseline"] = cpu_baseline(cpu_work, budget_s=args.cpu_budget)
     elif rank == 0 and world == 1 and not args.no_cpu_baseline:
-        small = synth.Workload("c3_sample", [(4096, 4096)], [work.grads[0].cpu()], [work.weights[0].cpu()])
-        line["cpu_baseline"] = cpu_baseline(small, budget_s=args.cpu_budget, max_mats=1)
+        small = c3_sample(work)
+        line["cpu_baseline"] = cpu_baseline(small, budget_s=args.cpu_budget, max_mats=len(small.shapes),
+                                            of=f"2 sampled matrices (4096x4096 and 14336x4096) of the {count} "
+                                               f"matrices of the workload")
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -697,11 +831,23 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="c2")
+    ap.add_argument("--config", default="c3")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="call the C ABI per step instead of replaying a graph")
+    ap.add_argument("--record-traffic", metavar="CSV", help="store the DRAM traffic of an ncu metrics log taken on "
+                    "--config in profiles/dram_traffic.json (no GPU work)")
+    ap.add_argument("--traffic-scale", type=float, default=1.0, help="with --record-traffic: the factor from the "
+                    "captured workload's launches to --traffic-workload's")
+    ap.add_argument("--traffic-workload", help="with --record-traffic: the workload the rows are for (default --config)")
+    ap.add_argument("--traffic-command", default="", help="with --record-traffic: the command that made the log")
     args = ap.parse_args()
+    if args.record_traffic:
+        wl = args.traffic_workload or args.config
+        note = "" if wl == args.config else f"captured on {args.config}, scaled by {args.traffic_scale:g}"
+        doc = record_traffic(args.record_traffic, wl, args.traffic_command, args.traffic_scale, note)
+        print(json.dumps([r for r in doc["rows"] if r["workload"] == wl]))
+        return
     world, rank, local = dist_setup(args.gpus)
     tail = args.config in TAIL_DESC
     if args.impl == "reference":

@@ -1,5 +1,6 @@
 """Host-side pieces of bench.py that need no GPU: the roofline denominators and
 the recorded DRAM traffic, which must go null when its kernel source changes."""
+import json
 import os
 import sys
 
@@ -7,6 +8,14 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
 import bench  # noqa: E402
+
+NCU_HEADER = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size",'
+              '"Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"\n')
+
+
+def _row(i, kernel, metric, unit, value):
+    return (f'"{i}","1","python3","h","{kernel}","1","7","(320, 1, 1)","(152, 1, 1)","0","10.3",'
+            f'"Command line profiler metrics","{metric}","{unit}","{value}"\n')
 
 
 def test_peaks_have_every_denominator():
@@ -17,32 +26,63 @@ def test_peaks_have_every_denominator():
     assert pk["bf16_tflops_sustained"] <= pk["bf16_tflops"]
 
 
+def test_kernel_families():
+    for label in ("tc_rect", "tc_syrk_x3", "tc_program", "void muon::tc_gemm_kernel<16>(muon::TcProgram<16>)"):
+        assert bench.family_of(label) == "tc_gemm"
+    assert bench.family_of("simt_sym") == "simt_gemm"
+    assert bench.family_of("void muon::pack_vec_kernel<false>(muon::PackArgs)") == "pack"
+    assert bench.family_of("norm_finalize") == "norm_finalize"
+
+
 def test_recorded_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
-    # a private copy of the tree with the table and the two kernel sources
+    # a private copy of the tree with the kernel sources and an ncu metrics log
     csrc = tmp_path / "newton_schulz_04_gb300" / "csrc"
     csrc.mkdir(parents=True)
     (tmp_path / "profiles").mkdir()
-    src = b"// kernel v1\n"
-    (csrc / "tc_gemm.cu").write_bytes(src)
+    (csrc / "tc_gemm.cu").write_bytes(b"// kernel v1\n")
     (csrc / "elementwise.cu").write_bytes(b"// other\n")
-    import hashlib
-    sha = hashlib.sha256(src).hexdigest()[:16]
-    (tmp_path / "profiles" / "dram_traffic.md").write_text(
-        "| workload | kernel | sha | launches | read | write | traffic | us |\n|---|---|---|---|---|---|---|---|\n"
-        f"| c2 | tc_sym | {sha} | 8 | 36.77 | 0.30 | 37.07 | 33.3 |\n")
+    log = tmp_path / "traffic.csv"
+    k_tc = "void muon::tc_gemm_kernel<1>(muon::TcProgram<1>)"
+    k_pk = "void muon::pack_vec_kernel<false>(muon::PackArgs)"
+    log.write_text("==PROF== Connected to process 1\n" + NCU_HEADER +
+                   _row(0, k_pk, "dram__bytes_read.sum", "Mbyte", "100.5") +
+                   _row(0, k_pk, "dram__bytes_write.sum", "Mbyte", "75.5") +
+                   _row(0, k_pk, "gpu__time_duration.sum", "usecond", "35.9") +
+                   _row(1, k_tc, "dram__bytes_read.sum", "Gbyte", "1.5") +
+                   _row(1, k_tc, "dram__bytes_write.sum", "Mbyte", "500") +
+                   _row(1, k_tc, "gpu__time_duration.sum", "msecond", "2") +
+                   _row(2, k_tc, "dram__bytes_read.sum", "Gbyte", "0.5") +
+                   _row(2, k_tc, "dram__bytes_write.sum", "Mbyte", "1,500") +
+                   _row(2, k_tc, "gpu__time_duration.sum", "msecond", "4"))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.recorded_traffic("c2", "tc_sym") == 37.07e6
-    assert bench.recorded_traffic("c3", "tc_sym") is None       # no row for the workload
-    assert bench.recorded_traffic("c2", "pack") is None         # no row for the kernel
+    parsed = bench.parse_ncu_csv(str(log))
+    assert parsed[1]["dram__bytes_read.sum"] == 1.5e9 and parsed[2]["dram__bytes_write.sum"] == 1.5e9
+    bench.record_traffic(str(log), "c3", "ncu ...", scale=4.0, note="scaled")
+    doc = json.load(open(tmp_path / "profiles" / "dram_traffic.json"))
+    tc = [r for r in doc["rows"] if r["family"] == "tc_gemm"][0]
+    assert tc["launches"] == 2 and tc["bytes_per_launch"] == 4.0 * (2.0e9 + 2.0e9) / 2
+    assert abs(tc["ncu_us_per_launch"] - 3000.0) < 1e-6
+    assert bench.recorded_traffic("c3", "tc_gemm") == 8.0e9
+    assert bench.recorded_traffic("c3", "pack") == 4.0 * 176e6
+    assert bench.recorded_traffic("c2", "tc_gemm") is None       # no row for the workload
+    assert bench.recorded_traffic("c3", "simt_gemm") is None     # no row for the family
     (csrc / "tc_gemm.cu").write_bytes(b"// kernel v2\n")
-    assert bench.recorded_traffic("c2", "tc_sym") is None       # source changed since capture
+    assert bench.recorded_traffic("c3", "tc_gemm") is None       # source changed since capture
+    assert bench.recorded_traffic("c3", "pack") == 4.0 * 176e6   # its own source is unchanged
 
 
-def test_committed_traffic_rows_parse():
-    rows = 0
-    for line in open(os.path.join(ROOT, "profiles", "dram_traffic.md")):
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) == 8 and cells[0].startswith("c") and cells[3].isdigit():
-            rows += 1
-            assert abs(float(cells[6]) - (float(cells[4]) + float(cells[5]))) <= 0.011
-    assert rows >= 1
+def test_committed_traffic_rows_are_consistent():
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return
+    doc = json.load(open(path))
+    for r in doc["rows"]:
+        assert abs(r["bytes_per_launch"] - r["read_bytes_per_launch"] - r["write_bytes_per_launch"]) <= \
+            1e-9 * r["bytes_per_launch"] + 1
+        assert r["family"] in bench.FAMILY_SOURCES and r["command"]
+
+
+def test_c5_config_names():
+    assert bench.c5_params("c5f32_n4096_t10") == (4096, 10)
+    assert bench.c5_params("c5_n16384") == (16384, 5)
+    assert "layers" in bench.workload_desc("c3_l2")
