@@ -125,8 +125,9 @@ def recorded_traffic(workload: str, family: str):
     return None
 
 
-_UNITS = {"byte": 1.0, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12,
-          "nsecond": 1e-9, "usecond": 1e-6, "msecond": 1e-3, "second": 1.0}
+_UNITS = {"byte": 1.0, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12, "b": 1.0, "kb": 1e3, "mb": 1e6,
+          "gb": 1e9, "nsecond": 1e-9, "usecond": 1e-6, "msecond": 1e-3, "second": 1.0, "ns": 1e-9, "us": 1e-6,
+          "ms": 1e-3, "s": 1.0}
 
 
 def parse_ncu_csv(path):
@@ -201,6 +202,16 @@ def workload_desc(name: str) -> str:
         dt = "fp32" if name.startswith("c5f32") else "bf16"
         return f"8 x 1024x{n} {dt} grads N(0,1) with row 0 x100, fp32 momentum, {steps} NS steps quintic"
     return WORKLOAD_DESC.get(name, name)
+
+
+def operands_desc(dtype, schedule):
+    if schedule == "orig_f16x3":
+        return ("fp16-pair tensor-core operands (about 22 bits), three products per product, fp32 accumulation; "
+                f"{'fp32' if dtype == torch.float32 else 'bf16'} in and out")
+    if dtype == torch.float32:
+        return "fp32 FFMA on the CUDA cores"
+    return ("bf16 in and out; NS products on bf16 (step 0) and fp16 (later steps) tensor-core operands, "
+            "fp32 accumulation")
 
 
 def make_workload(name: str, device):
@@ -481,7 +492,7 @@ def run_ours(args, world, rank, local):
         cpu_work = work
     else:
         cpu_work = None
-    upd = pkg.MuonUpdater(W, work.beta, work.lr, work.steps, work.coeffs, "auto", use_graph=not args.no_graph)
+    upd = pkg.MuonUpdater(W, work.beta, work.lr, work.steps, work.coeffs, args.schedule, use_graph=not args.no_graph)
     Mo = upd.moms
     flops_step = work.flop_count()
     flops_all = sum_over_ranks(flops_step, world)  # = world x flops_step under weak scaling
@@ -495,7 +506,7 @@ def run_ours(args, world, rank, local):
         upd.step(G)
 
     def step_eager():
-        pkg.muon_step(W, G, Mo, work.beta, work.lr, work.steps, work.coeffs, "auto", upd.workspace, st)
+        pkg.muon_step(W, G, Mo, work.beta, work.lr, work.steps, work.coeffs, args.schedule, upd.workspace, st)
 
     def timed(fn, k):
         out = []
@@ -619,7 +630,8 @@ def run_ours(args, world, rank, local):
                 copy_in(1 - i)
             st.wait_event(ev_in[i])
             if args.no_graph:
-                pkg.muon_step(W, Gsets[i], Mo, work.beta, work.lr, work.steps, work.coeffs, "auto", upd.workspace, st)
+                pkg.muon_step(W, Gsets[i], Mo, work.beta, work.lr, work.steps, work.coeffs, args.schedule,
+                              upd.workspace, st)
             else:
                 upd.step(Gsets[i])
             for w, wh in zip(W, Wh):
@@ -637,10 +649,9 @@ def run_ours(args, world, rank, local):
         "metric": "Muon update TFLOP/s (algorithmic, symmetric Gram count)",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": scaling, "vs_baseline": None,
-        "dtype": "fp32" if work.dtype == torch.float32 else "bf16+fp16",
-        "operands": ("fp32 FFMA on the CUDA cores" if work.dtype == torch.float32 else
-                     "bf16 in and out; NS products on bf16 (step 0) and fp16 (later steps) tensor-core operands, "
-                     "fp32 accumulation"),
+        "dtype": ("fp16x2" if args.schedule == "orig_f16x3" else
+                  "fp32" if work.dtype == torch.float32 else "bf16+fp16"),
+        "operands": operands_desc(work.dtype, args.schedule),
         "data": "synthetic",
         "config": {"workload": workload_desc(args.config), "name": args.config,
                    "matrices_per_gpu": count, "l2": "flushed between timed steps" if flush is not None
@@ -648,6 +659,8 @@ def run_ours(args, world, rank, local):
                    "parallelism": "1 gpu" if world == 1 else
                    (f"owner placement over {world} ranks (LPT), no data-path collective" if scaling == "strong"
                     else f"one batch per rank x{world}")},
+        "schedules": {f"{a}x{b}": pkg.resolve_schedule(a, b, work.steps, work.dtype, args.schedule)
+                      for (a, b) in sorted({(min(x), max(x)) for x in shapes})},
         "matrices_per_s": count_all * args.steps / t_total,
         "pct_of_bf16_peak": 100.0 * value / pk["bf16_tflops"],
         "value_without_graph": value_eager,
@@ -835,6 +848,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="call the C ABI per step instead of replaying a graph")
+    ap.add_argument("--schedule", default="auto", help="NS schedule (auto, orig, gram_r2, orig_f16x3, ...)")
     ap.add_argument("--record-traffic", metavar="CSV", help="store the DRAM traffic of an ncu metrics log taken on "
                     "--config in profiles/dram_traffic.json (no GPU work)")
     ap.add_argument("--traffic-scale", type=float, default=1.0, help="with --record-traffic: the factor from the "

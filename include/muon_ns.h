@@ -79,13 +79,22 @@ typedef enum {
     MUON_SCHED_GRAM_X3 = 1,  /* Gram space; symmetric products with split-bf16 operands (hi*hi + hi*lo + lo*hi) */
     MUON_SCHED_GRAM_X1 = 2,  /* Gram space; plain bf16 operands (fast mode, larger error) */
     MUON_SCHED_ORIG = 3,     /* original space (bf16: step 0 in bf16, later steps on fp16 operands, see below) */
-    MUON_SCHED_ORIG_BF16 = 4 /* original space on bf16 operands only; split A in A*A and B in B*X in the last max(2, steps - 3) steps */
+    MUON_SCHED_ORIG_BF16 = 4, /* original space on bf16 operands only; split A in A*A and B in B*X in the last max(2, steps - 3) steps */
+    MUON_SCHED_ORIG_F16X3 = 5, /* original space; every operand an fp16 pair (~22 bits), three tensor-core products per product */
+    MUON_SCHED_GRAM_R2 = 6     /* Gram space restarted from X every two steps (bf16: fp16 operands; fp32: FFMA) */
 } muon_sched;
 
 /*
  * Schedules and precision.  Every tensor-core product accumulates in fp32.
- *  - bf16, AUTO: ORIG.  fp32, AUTO: Gram space when rows != cols (never more
- *    work), else ORIG; the fp32 path multiplies with fp32 FFMA.
+ *  - bf16, AUTO: GRAM_R2 where it executes at most 0.9x ORIG's tensor-core
+ *    work (the long side at least about 1.5x the short side, and 3 or more
+ *    steps), else ORIG.
+ *  - fp32, AUTO: up to 6 steps ORIG_F16X3 (tensor cores, below); longer runs
+ *    on fp32 FFMA (CUDA cores): GRAM_R2 where it saves at least a tenth of
+ *    ORIG's work, else ORIG.  Explicit GRAM_X3 / GRAM_X1 on fp32 data run
+ *    Gram space without restarts on FFMA, which is unstable on rank-deficient
+ *    inputs over many steps: rounding leaves G with small negative
+ *    eigenvalues that the recurrence grows by about a^2 per step.
  *  - ORIG (bf16).  Step 0 multiplies the packed bf16 copy of M (exact for bf16
  *    gradients from a zero momentum state) on bf16 operands.  Every later
  *    product takes fp16 operands (11 significant bits against bf16's 8).
@@ -102,7 +111,28 @@ typedef enum {
  *  - GRAM_X3 / GRAM_X1.  The Gram recurrence on bf16 pairs (split products)
  *    or on plain bf16.  Gram space squares the condition number, so on
  *    ill-conditioned inputs it misses the 2e-2 target that ORIG meets.
- * muon_workspace_bytes is the same for ORIG and ORIG_BF16.
+ *  - GRAM_R2 (bf16; fp32 runs the same segments with FFMA).  Step 0 is ORIG's bf16 step; the remaining steps run in
+ *    segments of two (a last single step when steps - 1 is odd).  A segment
+ *    forms A = X_hi X_hi^T once, runs two steps of the Gram recurrence on it
+ *    (P_0 = a I + b A + c A^2, G_1 = P_0 A P_0, P_1 likewise, Q = P_1 P_0,
+ *    fp16 operands) and restarts from X <- Q X_hi + a^2 X_lo.  Per two steps
+ *    that is one s x l SYRK, one s x s x l update and five s x s products,
+ *    against two SYRKs, two updates and two s x s products in ORIG.  Longer
+ *    Gram segments on fp16 operands lose the directions of small singular
+ *    values on low-rank inputs; two-step segments stay within about 1e-2 of
+ *    the fp64 result on them.  With coefficients outside fp16's range it runs
+ *    as ORIG_BF16.  Its workspace is ORIG's.
+ *  - ORIG_F16X3 (either dtype).  X0 = M / (||M||_F + eps) is formed in fp32
+ *    and split into an fp16 pair hi + lo / 2^11; every product takes pairs
+ *    (A, B' and X) and runs as hi*lo + lo*hi followed by hi*hi on an
+ *    accumulator the tensor core scales by 2^-11, in fp32.  About 22-bit
+ *    operands at three times the tensor-core work of one product: the
+ *    tensor-core form of the fp32 path, several times faster than FFMA.  Its
+ *    accuracy is set by the tensor cores' fp32 accumulation (about 1e-6 of
+ *    the sum of |products| per product, against 1e-7 for FFMA), so it is
+ *    fp32's AUTO choice only up to 6 steps (within 3e-5 there on Gaussian
+ *    and row-scaled inputs, about 9e-5 at 10 steps).
+ * muon_workspace_bytes is the same for ORIG, ORIG_BF16 and GRAM_R2 (bf16).
  */
 
 #define MUON_MAX_DIM 65536   /* largest accepted m or n */
@@ -204,6 +234,10 @@ MUON_API muon_status muon_debug_bounded_wait(void* ws, long long max_cycles, voi
  *   form the original-space update takes for the low part of X); the
  *   diagonal table is written into the workspace after the header, so
  *   ws_bytes must be at least 1024 + 131072.
+ *   split = 5 (fp16): A and B are fp16 pairs whose low parts are stored scaled,
+ *   A_lo = fp16((A_true - A) * 2^11) and likewise B_lo; C = A B + (A B_lo +
+ *   A_lo B) / 2^11, the low-part products accumulated first and the 2^-11
+ *   applied by the tensor core to the accumulator (about 22-bit operands).
  *   dt = MUON_FP32 runs the FFMA kernel on fp32 A, B and writes fp32 C to out.
  *   sym bit 0 (M == N): symmetric output; the bf16 kernel computes the tiles
  *   touching the lower triangle and stores the output "block-lower" (only the

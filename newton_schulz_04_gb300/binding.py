@@ -20,7 +20,7 @@ STATUS_NAMES = ["OK", "ERR_ARG", "ERR_SHAPE", "ERR_ALIGN", "ERR_WORKSPACE", "ERR
                 "ERR_UNSUPPORTED"]
 BF16, FP32, FP16 = 0, 1, 2  # FP16: muon_debug_gemm only
 F16_LO_SCALE = 2048.0  # an fp16 pair stores lo = fp16((v - hi) * 2^11)
-SCHED = {"auto": 0, "gram_x3": 1, "gram_x1": 2, "orig": 3, "orig_bf16": 4}
+SCHED = {"auto": 0, "gram_x3": 1, "gram_x1": 2, "orig": 3, "orig_bf16": 4, "orig_f16x3": 5, "gram_r2": 6}
 SCHED_NAMES = {v: k for k, v in SCHED.items()}
 WS_ALIGN = 256
 
@@ -396,8 +396,9 @@ def debug_gemm(A, B, A_lo=None, B_lo=None, split=1, b_mn=False, sym=False, a_sym
     value of the bf16 (fp16) head/residual pair it writes (with sym, only the
     256 x 256 blocks on or below the diagonal are written); a_sym / b_sym
     declare operands given in that block-lower storage.  split=4 (fp16,
-    b_mn, square A) adds B_lo / 2^11 through the diagonal K segment.  fp32
-    operands run the FFMA kernel."""
+    b_mn, square A) adds B_lo / 2^11 through the diagonal K segment; split=5
+    (fp16) multiplies the pairs A + A_lo / 2^11 and B + B_lo / 2^11 (the low
+    parts stored scaled by 2^11).  fp32 operands run the FFMA kernel."""
     lib = load()
     batch, M, K = A.shape
     N = B.shape[2] if b_mn else B.shape[1]

@@ -3,6 +3,8 @@
 // norm finalisation, the zero-step output, and the bounded-wait self test.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -253,6 +255,47 @@ cudaError_t launch_norm_finalize(const float* partial, int tiles, int B, float e
   if (B <= 0) return cudaSuccess;
   return launch_pdl(norm_finalize_kernel, dim3(B), dim3(256), 0, st, partial, tiles, eps, inv_norm,
                     static_cast<uint4*>(diag), diag_bits);
+}
+
+// X (an fp16 pair) = Xf * inv_norm[b], hi = fp16(x), lo = fp16((x - hi) * 2^11),
+// 8 elements per thread (n, the elements per matrix, is a multiple of 8 and
+// every buffer is 16-byte aligned).
+__global__ void __launch_bounds__(256) pair_from_f32_kernel(const float* Xf, const float* inv_norm, __half* Xh,
+                                                            __half* Xl, long long n) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int b = blockIdx.y;
+  const float sc = inv_norm[b];
+  const long long base = static_cast<long long>(b) * n;
+  for (long long i = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) * 8; i < n;
+       i += static_cast<long long>(gridDim.x) * 256 * 8) {
+    const float4* src = reinterpret_cast<const float4*>(Xf + base + i);
+    const float4 u0 = src[0], u1 = src[1];
+    const float x[8] = {u0.x * sc, u0.y * sc, u0.z * sc, u0.w * sc, u1.x * sc, u1.y * sc, u1.z * sc, u1.w * sc};
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 hh = __floats2half2_rn(x[2 * k], x[2 * k + 1]);
+      const float2 hf = __half22float2(hh);
+      const __half2 ll = __floats2half2_rn((x[2 * k] - hf.x) * kF16LoScale, (x[2 * k + 1] - hf.y) * kF16LoScale);
+      h[k] = *reinterpret_cast<const uint32_t*>(&hh);
+      l[k] = *reinterpret_cast<const uint32_t*>(&ll);
+    }
+    *reinterpret_cast<uint4*>(Xh + base + i) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(Xl + base + i) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+cudaError_t launch_pair_from_f32(const float* Xf, const float* inv_norm, void* Xh, void* Xl, long long n, int B,
+                                 int num_sms, cudaStream_t st) {
+  if (B <= 0 || n <= 0) return cudaSuccess;
+  if (n % 8 || (reinterpret_cast<uintptr_t>(Xf) | reinterpret_cast<uintptr_t>(Xh) | reinterpret_cast<uintptr_t>(Xl)) % 16)
+    return cudaErrorInvalidValue;
+  long long blocks = (n / 8 + 255) / 256;
+  const long long cap = std::max(1LL, 8LL * num_sms / B);  // about 8 blocks per SM over the batch
+  if (blocks > cap) blocks = cap;
+  return launch_pdl(pair_from_f32_kernel, dim3(static_cast<unsigned>(blocks), B), dim3(256), 0, st, Xf, inv_norm,
+                    static_cast<__half*>(Xh), static_cast<__half*>(Xl), n);
 }
 
 struct FinalArgs {

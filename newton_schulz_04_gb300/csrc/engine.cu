@@ -145,27 +145,24 @@ static int bucket_plan(const std::vector<std::pair<long long, long long>>& shape
 }
 
 // ------------------------------------------------------------------ schedules
-static muon_sched resolve(long long s, long long l, int steps, muon_dtype dt, muon_sched sc) {
-  if (dt == MUON_FP32) {
-    if (sc == MUON_SCHED_ORIG || sc == MUON_SCHED_ORIG_BF16) return MUON_SCHED_ORIG;  // one fp32 form
-    if (sc == MUON_SCHED_AUTO) {
-      // fp32 Gram costs 3 s^2 l + (4T - 3) s^3 vs T (3 s^2 l + s^3): never more, equal when square.
-      return (l > s && steps > 0) ? MUON_SCHED_GRAM_X3 : MUON_SCHED_ORIG;
-    }
-    return steps > 0 ? MUON_SCHED_GRAM_X3 : MUON_SCHED_ORIG;  // both Gram modes run in fp32 here
-  }
-  if (steps == 0) return MUON_SCHED_ORIG;  // only the packed fp32 copy is needed
-  if (sc != MUON_SCHED_AUTO) return sc;
-  // Gram space squares the condition number, and the tensor cores' fp32
-  // accumulation is measurably coarser than IEEE fp32 (error ~1e-6 of the sum
-  // of |products| per element, growing with K): on ill-conditioned inputs
-  // (rank-8 + noise) the split Gram recurrence exceeds the 2e-2 target, while
-  // the original-space schedule on fp16 operands stays near 1e-3.  AUTO
-  // therefore runs bf16 in original space; GRAM_X3 / GRAM_X1 remain available
-  // on request.
-  (void)s;
-  (void)l;
-  return MUON_SCHED_ORIG;
+// Lengths of the segments the steps run in (ORIG: every step alone; GRAM_R2:
+// step 0 alone, on the packed bf16 copy of M, then two steps per segment,
+// and a last single step when T - 1 is odd).
+static std::vector<int> segment_plan(int T, muon_sched sc) {
+  std::vector<int> plan;
+  if (T <= 0) return plan;
+  plan.push_back(1);
+  int left = T - 1;
+  if (sc == MUON_SCHED_GRAM_R2)
+    for (; left >= 2; left -= 2) plan.push_back(2);
+  for (; left > 0; --left) plan.push_back(1);
+  return plan;
+}
+
+static float ipow(float x, int k) {
+  float r = 1.f;
+  for (int i = 0; i < k; ++i) r *= x;
+  return r;
 }
 
 // ORIG on bf16 data multiplies fp16 operands from step 1 on.  That is safe when
@@ -187,6 +184,69 @@ static bool f16_coefficients_safe(float a, float b, float c) {
     pmax = std::max(pmax, std::fabs(x * (a + x2 * (b + x2 * c))));
   }
   return pmax + 0.5 * h * dmax <= 1.25;
+}
+
+
+// The coefficients as the schedules need them (the fp16 range check above).
+struct Coef {
+  float a, b, c;
+  bool f16_ok;
+};
+
+static Coef coef_of(const float* coeffs) {
+  const float* cf = coeffs ? coeffs : kQuintic;
+  return Coef{cf[0], cf[1], cf[2], f16_coefficients_safe(cf[0], cf[1], cf[2])};
+}
+
+static bool pair_sched(muon_sched sc) { return sc == MUON_SCHED_ORIG_F16X3; }
+
+// Tensor-core (or FFMA) work of a schedule's segment plan, with the padded
+// sizes: per segment of k steps one SYRK (S^2 L, lower tiles), 4k - 3
+// symmetric s x s products (S^3 each) and the update (2 S^2 L).
+static double plan_work(long long s, long long l, int steps, muon_sched sc) {
+  const double S = static_cast<double>(round_up(s, 256)), L = static_cast<double>(round_up(l, 256));
+  double w = 0.0;
+  for (int k : segment_plan(steps, sc)) w += 3.0 * S * S * L + (4.0 * k - 3.0) * S * S * S;
+  return w;
+}
+
+// fp32 runs up to this many steps take the tensor-core fp16-pair schedule:
+// measured on Gaussian and row-scaled fp32 inputs it stays within 3e-5 of
+// the fp64 result at 5 steps, but reaches about 9e-5 at 10 (the tensor cores'
+// fp32 accumulation, about 1e-6 of the sum of |products| per product, builds
+// up), too close to the 1e-4 tolerance; longer runs use FFMA.  (Gram space
+// without restarts is not used for them either: rounding leaves G with small
+// negative eigenvalues that the recurrence lambda <- (a + b lambda + c
+// lambda^2)^2 lambda grows by about a^2 per step until they overflow,
+// measured on rank-deficient fp32 inputs at 10 steps.)
+constexpr int kFp32PairMaxSteps = 6;
+
+static muon_sched resolve(long long s, long long l, int steps, muon_dtype dt, muon_sched sc, const Coef& k) {
+  if (steps == 0) return MUON_SCHED_ORIG;  // only the packed fp32 copy is needed
+  // two-step Gram segments where they save at least a tenth of the work
+  const bool r2_pays = plan_work(s, l, steps, MUON_SCHED_GRAM_R2) <= 0.9 * plan_work(s, l, steps, MUON_SCHED_ORIG);
+  if (sc == MUON_SCHED_AUTO) {
+    if (dt == MUON_FP32) {
+      // short runs: tensor-core fp16 pairs (FFMA Gram space if the
+      // coefficients leave fp16's range); long runs: FFMA in two-step Gram
+      // segments where they save work, else original space
+      if (steps <= kFp32PairMaxSteps)
+        sc = k.f16_ok ? MUON_SCHED_ORIG_F16X3 : (l > s ? MUON_SCHED_GRAM_X3 : MUON_SCHED_ORIG);
+      else
+        sc = r2_pays ? MUON_SCHED_GRAM_R2 : MUON_SCHED_ORIG;
+    } else {
+      // bf16: the Gram recurrence restarted every two steps (GRAM_R2) where it
+      // saves at least a tenth of the tensor-core work, else original space
+      sc = r2_pays ? MUON_SCHED_GRAM_R2 : MUON_SCHED_ORIG;
+    }
+  }
+  // fp16 pairs need coefficients that keep every operand in fp16's range
+  if (pair_sched(sc)) return k.f16_ok ? sc : (dt == MUON_FP32 ? MUON_SCHED_ORIG : MUON_SCHED_ORIG_BF16);
+  if (dt == MUON_FP32) {
+    if (sc == MUON_SCHED_ORIG || sc == MUON_SCHED_ORIG_BF16) return MUON_SCHED_ORIG;  // one fp32 form
+    return sc == MUON_SCHED_GRAM_R2 ? MUON_SCHED_GRAM_R2 : MUON_SCHED_GRAM_X3;       // both Gram modes: FFMA
+  }
+  return sc;
 }
 
 // Bump allocator over the workspace; with base == nullptr it only measures.
@@ -246,13 +306,30 @@ static size_t carve_buffers(char* base, int Bc, long long sp, long long lp, int 
   bf.partial = static_cast<float*>(c.take(sizeof(float) * Bc * static_cast<size_t>(tiles)));
   bf.done = static_cast<int*>(c.take(sizeof(int) * Bc));
   bf.tile_ctr = static_cast<int*>(c.take(sizeof(int) * kMaxTcLaunches));
+  if (steps > 0 && pair_sched(sc)) {
+    // fp32 copy of M, then fp16 pairs (stored in 16-bit buffers) of X (ping-pong), A and B'
+    bf.Xf = static_cast<float*>(c.take(4 * nx));
+    for (int q = 0; q < 2; ++q) {
+      bf.Xb[q] = static_cast<bf16*>(c.take(2 * nx));
+      bf.Xlo[q] = static_cast<bf16*>(c.take(2 * nx));
+    }
+    bf.Gh = static_cast<bf16*>(c.take(2 * ns));
+    bf.Gl = static_cast<bf16*>(c.take(2 * ns));
+    bf.Bh = static_cast<bf16*>(c.take(2 * ns));
+    bf.Bl = static_cast<bf16*>(c.take(2 * ns));
+    return c.off;
+  }
   if (dt == MUON_FP32 || steps == 0) {
     bf.Xf = static_cast<float*>(c.take(4 * nx));
     if (steps == 0) return c.off;
-    if (sc == MUON_SCHED_ORIG) {
+    if (sc == MUON_SCHED_ORIG || sc == MUON_SCHED_GRAM_R2) {
       bf.Xf2 = static_cast<float*>(c.take(4 * nx));
       bf.Af = static_cast<float*>(c.take(4 * ns));
       bf.Bf = static_cast<float*>(c.take(4 * ns));
+      if (sc == MUON_SCHED_GRAM_R2) {  // the two-step segments' H and P_1
+        bf.Hf = static_cast<float*>(c.take(4 * ns));
+        bf.Pf[0] = static_cast<float*>(c.take(4 * ns));
+      }
     } else {
       bf.Gf = static_cast<float*>(c.take(4 * ns));
       for (int q = 0; q < 2; ++q) bf.Pf[q] = static_cast<float*>(c.take(4 * ns));
@@ -261,7 +338,7 @@ static size_t carve_buffers(char* base, int Bc, long long sp, long long lp, int 
     }
     return c.off;
   }
-  if (sc == MUON_SCHED_ORIG || sc == MUON_SCHED_ORIG_BF16) {
+  if (sc == MUON_SCHED_ORIG || sc == MUON_SCHED_ORIG_BF16 || sc == MUON_SCHED_GRAM_R2) {
     // X carried as a 16-bit pair (bf16 pair ~16 significant bits, fp16 pair ~22), ping-ponged
     for (int q = 0; q < 2; ++q) {
       bf.Xb[q] = static_cast<bf16*>(c.take(2 * nx));
@@ -297,14 +374,15 @@ struct Group {
   int steps;
 };
 
-static Group make_group(long long m, long long n, int steps, muon_dtype dt, muon_sched sc) {
+static Group make_group(long long m, long long n, int steps, muon_dtype dt, muon_sched sc,
+                        const Coef& k = coef_of(nullptr)) {
   Group g;
   g.s = std::min(m, n);
   g.l = std::max(m, n);
   g.sp = round_up(g.s, 256);
   g.lp = round_up(g.l, 256);
   g.tiles = static_cast<int>((g.sp / 64) * (g.lp / 64));
-  g.sc = resolve(g.s, g.l, steps, dt, sc);
+  g.sc = resolve(g.s, g.l, steps, dt, sc, k);
   g.steps = steps;
   return g;
 }
@@ -442,15 +520,17 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   // 234 -> 270; the 512 small matrices of shapes 256 x 1024 .. 768 x 3072
   // (10 to 75 per cluster) 293 -> 286 when every bucket shares launches.
   const long long pairs_rect = static_cast<long long>(Bc) * (g.sp / 256) * (g.lp / 256);
-  const bool chain = cx.dt == MUON_BF16 && pairs_rect <= 16LL * (cx.sms / 2);
+  const bool pairs = cx.steps > 0 && pair_sched(g.sc);  // fp16-pair operands (either dtype)
+  const bool tensor = cx.dt == MUON_BF16 || pairs;       // the NS products run on the tensor cores
+  const bool chain = tensor && pairs_rect <= 16LL * (cx.sms / 2);
   // stream-ordered: runs after everything before this chunk, before its pack
   if (chain) CK(cudaMemsetAsync(bf.done, 0, sizeof(int) * Bc, cx.st));
-  if (cx.dt == MUON_BF16 && cx.steps > 0) CK(cudaMemsetAsync(bf.tile_ctr, 0, sizeof(int) * kMaxTcLaunches, cx.st));
+  if (tensor && cx.steps > 0) CK(cudaMemsetAsync(bf.tile_ctr, 0, sizeof(int) * kMaxTcLaunches, cx.st));
   const long long sp = g.sp, lp = g.lp;
   const long long bsx = sp * lp, bss = sp * sp;
   const bool fp32 = cx.dt == MUON_FP32;
   const bool x3 = g.sc == MUON_SCHED_GRAM_X3;
-  const bool h16 = !fp32 && g.sc == MUON_SCHED_ORIG && cx.f16_ok;
+  const bool h16 = !fp32 && (g.sc == MUON_SCHED_ORIG || g.sc == MUON_SCHED_GRAM_R2) && cx.f16_ok;
   const bool use_diag = h16 && cx.steps >= 2 && sp <= kDiagMaxK;
 
   // ---- momentum + pack + norm
@@ -466,10 +546,12 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   pa.bs = bsx;
   pa.partial = bf.partial;
   pa.tiles = g.tiles;
-  pa.Xf = bf.Xf;  // fp32 path, or zero steps
-  if (!fp32 && cx.steps > 0) {
+  pa.Xf = bf.Xf;  // fp32 path, pair schedules, or zero steps
+  if (!fp32 && !pairs && cx.steps > 0) {
     pa.Xh = bf.Xb[0];
-    pa.Xl = (g.sc == MUON_SCHED_ORIG || g.sc == MUON_SCHED_ORIG_BF16) ? bf.Xlo[0] : (x3 ? bf.Xl : nullptr);
+    pa.Xl = (g.sc == MUON_SCHED_ORIG || g.sc == MUON_SCHED_ORIG_BF16 || g.sc == MUON_SCHED_GRAM_R2)
+                ? bf.Xlo[0]
+                : (x3 ? bf.Xl : nullptr);
   }
   for (int q = 0; q < Bc; ++q) {
     // a bucket can mix m x n and n x m members: the pack kernel transposes per member
@@ -520,7 +602,12 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   const int T = cx.steps;
   const int S = static_cast<int>(sp), L = static_cast<int>(lp);
 
-  if (fp32) {
+  if (pairs) {
+    ProfScope ps("pair_split", 0.0, 12.0 * Bc * static_cast<double>(bsx), cx.st);
+    CK(launch_pair_from_f32(bf.Xf, bf.inv_norm, bf.Xb[0], g.sc == MUON_SCHED_ORIG_F16X3 ? bf.Xlo[0] : bf.Xl, bsx, Bc,
+                            cx.sms, cx.st));
+  }
+  if (fp32 && !pairs) {
     auto simt = [&](const float* A, long long lda, long long bsa, const float* Bm, long long ldb, long long bsb,
                     int M, int N, int K, int sym, int b_mn, const EpiParams& e) {
       SimtGemmDesc d{Bc, M, N, K, sym, b_mn, A, lda, bsa, Bm, ldb, bsb};
@@ -529,18 +616,41 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
       ProfScope ps(sym ? "simt_sym" : "simt_rect", fl, 0.0, cx.st);
       return launch_simt_gemm(d, e, cx.st);
     };
-    if (g.sc == MUON_SCHED_ORIG) {
+    if (g.sc == MUON_SCHED_ORIG || g.sc == MUON_SCHED_GRAM_R2) {
+      // Segments of one step (ORIG) or, after step 0, of two Gram steps
+      // (GRAM_R2): A = X X^T; then Q' = Q - a^k I with Q the segment's
+      // polynomial product (k = 1: b A + c A^2; k = 2: P_1 P_0 - a^2 I with
+      // P_j = a I + b G_j + c G_j^2, G_0 = A, G_1 = P_0 A P_0); X <- Q' X + a^k X.
       float* cur = bf.Xf;
       float* nxt = bf.Xf2;
-      for (int k = 0; k < T; ++k) {
-        EpiParams e1 = epi_packed(g, bf, k == 0 ? 2 : 0, 1.f, 0.f, 0.f, nullptr, bf.Af, sp, bss);
+      const std::vector<int> plan = segment_plan(T, g.sc);
+      for (size_t si = 0; si < plan.size(); ++si) {
+        const int k = plan[si];
+        const bool first = si == 0, last = si + 1 == plan.size();
+        EpiParams e1 = epi_packed(g, bf, first ? 2 : 0, 1.f, 0.f, 0.f, nullptr, bf.Af, sp, bss);
         CK(simt(cur, lp, bsx, cur, lp, bsx, S, S, L, 1, 0, e1));
-        EpiParams e2 = epi_packed(g, bf, 0, cx.c, cx.b, 0.f, bf.Af, bf.Bf, sp, bss);
-        CK(simt(bf.Af, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, e2));
-        EpiParams e3 = epi_packed(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, cur, nxt, lp, bsx);
+        const float* Qp = bf.Bf;
+        if (k == 1) {
+          EpiParams e2 = epi_packed(g, bf, 0, cx.c, cx.b, 0.f, bf.Af, bf.Bf, sp, bss);
+          CK(simt(bf.Af, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, e2));
+        } else {
+          // A in Af -> P_0 in Bf, H in Hf, G_1 in Af, P_1 in Pf[0], Q' in Af
+          EpiParams p0 = epi_packed(g, bf, 0, cx.c, cx.b, cx.a, bf.Af, bf.Bf, sp, bss);
+          CK(simt(bf.Af, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, p0));
+          EpiParams eh = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Hf, sp, bss);
+          CK(simt(bf.Bf, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, eh));
+          EpiParams eg = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Af, sp, bss);
+          CK(simt(bf.Bf, sp, bss, bf.Hf, sp, bss, S, S, S, 1, 0, eg));
+          EpiParams p1 = epi_packed(g, bf, 0, cx.c, cx.b, cx.a, bf.Af, bf.Pf[0], sp, bss);
+          CK(simt(bf.Af, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, p1));
+          EpiParams eq = epi_packed(g, bf, 0, 1.f, 0.f, -cx.a * cx.a, nullptr, bf.Af, sp, bss);
+          CK(simt(bf.Pf[0], sp, bss, bf.Bf, sp, bss, S, S, S, 1, 0, eq));
+          Qp = bf.Af;
+        }
+        EpiParams e3 = epi_packed(g, bf, first ? 1 : 0, 1.f, ipow(cx.a, k), 0.f, cur, nxt, lp, bsx);
         e3.cols_valid = static_cast<int>(g.l);
-        if (k == T - 1) epi_set_final(e3, cx, g, mats, Bc);
-        CK(simt(bf.Bf, sp, bss, cur, lp, bsx, S, L, S, 0, 1, e3));
+        if (last) epi_set_final(e3, cx, g, mats, Bc);
+        CK(simt(Qp, sp, bss, cur, lp, bsx, S, L, S, 0, 1, e3));
         std::swap(cur, nxt);
       }
       return MUON_OK;
@@ -630,9 +740,9 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     d.diag = diag;
     const double Kt = K == S ? static_cast<double>(g.s) : static_cast<double>(g.l);
     const double fl = d.sym ? Bc * static_cast<double>(g.s) * g.s * Kt : 2.0 * Bc * g.s * g.l * Kt;
-    static const char* const kSym[4] = {"", "tc_sym", "tc_sym_x2", "tc_sym_x3"};
-    static const char* const kSyrk[4] = {"", "tc_syrk", "tc_syrk_x2", "tc_syrk_x3"};
-    static const char* const kRect[4] = {"", "tc_rect", "tc_rect_x2", "tc_rect_x3"};
+    static const char* const kSym[6] = {"", "tc_sym", "tc_sym_x2", "tc_sym_x3", "", "tc_sym_p3"};
+    static const char* const kSyrk[6] = {"", "tc_syrk", "tc_syrk_x2", "tc_syrk_x3", "", "tc_syrk_p3"};
+    static const char* const kRect[6] = {"", "tc_rect", "tc_rect_x2", "tc_rect_x3", "", "tc_rect_p3"};
     const char* kind = d.sym ? (K == S ? kSym[split] : kSyrk[split]) : kRect[split];
     d.done = chain ? bf.done : nullptr;
     d.flag_wait = tc_launches > 0 ? 1 : 0;
@@ -651,42 +761,101 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     return launch_tc_gemm(d, e, cx.status, cx.st, cx.sms, &why);
   };
 
+  if (pairs) {
+    // Original space on fp16 pairs: X0 (normalised, fp32) was split above; A,
+    // B' = a I + b A + c A^2 and X are pairs, every product split 5.
+    int cur = 0;
+    for (int k = 0; k < T; ++k) {
+      const int nxt = cur ^ 1;
+      EpiParams e1 = epi_pair(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, bf.Gl, sp, bss);
+      e1.o_f16 = 1;
+      CK(tc(5, 0, 1, 1, S, S, L, bf.Xb[cur], bf.Xlo[cur], lp, bsx, bf.Xb[cur], bf.Xlo[cur], lp, bsx, e1));
+      EpiParams e2 = epi_pair(g, bf, 0, cx.c, cx.b, cx.a, bf.Gh, bf.Gl, bf.Bh, bf.Bl, sp, bss);
+      e2.r_f16 = 1;
+      e2.o_f16 = 1;
+      CK(tc(5, 0, 7, 1, S, S, S, bf.Gh, bf.Gl, sp, bss, bf.Gh, bf.Gl, sp, bss, e2));
+      EpiParams e3 = epi_pair(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Xb[nxt], bf.Xlo[nxt], lp, bsx);
+      e3.o_f16 = 1;
+      e3.cols_valid = static_cast<int>(g.l);
+      if (k == T - 1) epi_set_final(e3, cx, g, mats, Bc);
+      CK(tc(5, 1, 2, 1, S, L, S, bf.Bh, bf.Bl, sp, bss, bf.Xb[cur], bf.Xlo[cur], lp, bsx, e3));
+      cur = nxt;
+    }
+    CK(flush());
+    return MUON_OK;
+  }
   if (h16) {
     // Step 0 multiplies the packed bf16 copy of M (slot 0: hi, and lo for
     // the residual); A is stored as fp16, and B in the type of this step's X.
     // From step 1 on, X lives in the ping-pong slots as an fp16 pair and
     // every product takes fp16 operands.  Slot 0's bf16 copy is dead after
     // step 0, so step 1 writes its fp16 X there.
-    // The a X term is folded into the product: B' = a I + b A + c A^2, and
-    //   X <- B' X_hi + a X_lo = a X + B X_hi,
-    // so the update reads only the low part of X as its residual.  With the
-    // diagonal segment (use_diag) the low part written for the next step is
-    // 2^11 a (X - X_hi), and the next update adds 2^-11 I times it on the
-    // tensor cores instead of reading it in the epilogue.
+    // The steps run in segments (segment_plan): ORIG's are all one step long;
+    // GRAM_R2's are step 0 and then two steps each.  A segment of k steps
+    // starts from A = X_hi X_hi^T and ends with X <- Q X_hi + a^k X_lo, where
+    // Q = a^k I + ... is the product of the segment's polynomials: for k = 1
+    // Q = B' = a I + b A + c A^2, for k = 2 the Gram recurrence
+    //   P_0 = a I + b A + c A^2, G_1 = P_0 (P_0 A), P_1 = a I + b G_1 + c G_1^2,
+    //   Q = P_1 P_0
+    // on fp16 operands (all of them polynomials in A, so symmetric and stored
+    // block-lower).  Restarting from X every two steps keeps the Gram
+    // recurrence's fp16 rounding from building up in the directions of small
+    // singular values.  The a^k X_lo term keeps X's low part, which the
+    // products do not see: with the diagonal segment (use_diag) the low part
+    // written for the next segment is 2^11 a^k' (X - X_hi) (k' the next
+    // segment's length) and the next update adds 2^-11 I times it on the
+    // tensor cores; otherwise the epilogue reads it as a residual.
+    const std::vector<int> plan = segment_plan(T, g.sc);
     int cur = 0;
-    for (int k = 0; k < T; ++k) {
+    for (size_t si = 0; si < plan.size(); ++si) {
+      const int k = plan[si];
+      const bool first = si == 0, last = si + 1 == plan.size();
+      const float ak = ipow(cx.a, k), ak_next = last ? 1.f : ipow(cx.a, plan[si + 1]);
       const int nxt = cur ^ 1;
-      const int xf = k == 0 ? 0 : 1;  // 1: X (and so B) are fp16 this step
-      // A = X X^T (k = 0: X = M / s, so scale by inv_norm^2), fp16 out
-      EpiParams e1 = epi_pair(g, bf, k == 0 ? 2 : 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, nullptr, sp, bss);
+      const int xf = first ? 0 : 1;  // 1: X (and so Q) are fp16 in this segment
+      // A = X X^T (first segment: X = M / s, so scale by inv_norm^2), fp16 out
+      EpiParams e1 = epi_pair(g, bf, first ? 2 : 0, 1.f, 0.f, 0.f, nullptr, nullptr, bf.Gh, nullptr, sp, bss);
       e1.o_f16 = 1;
       CK(tc(1, 0, 1, xf, S, S, L, bf.Xb[cur], nullptr, lp, bsx, bf.Xb[cur], nullptr, lp, bsx, e1));
-      // B' = a I + b A + c A^2 on fp16 operands
-      EpiParams e2 = epi_pair(g, bf, 0, cx.c, cx.b, cx.a, bf.Gh, nullptr, bf.Bh, nullptr, sp, bss);
-      e2.r_f16 = 1;
-      e2.o_f16 = xf;
-      CK(tc(1, 0, 7, 1, S, S, S, bf.Gh, nullptr, sp, bss, bf.Gh, nullptr, sp, bss, e2));
-      // X <- B' X_hi + a X_lo (k = 0: both terms carry 1 / s), fp16 pair out
-      const bool dseg = use_diag && k > 0;
-      EpiParams e3 = epi_pair(g, bf, k == 0 ? 1 : 0, 1.f, cx.a, 0.f, dseg ? nullptr : bf.Xlo[cur], nullptr,
+      const bf16* Q = bf.Bh;
+      if (k == 1) {
+        // B' = a I + b A + c A^2 on fp16 operands
+        EpiParams e2 = epi_pair(g, bf, 0, cx.c, cx.b, cx.a, bf.Gh, nullptr, bf.Bh, nullptr, sp, bss);
+        e2.r_f16 = 1;
+        e2.o_f16 = xf;
+        CK(tc(1, 0, 7, 1, S, S, S, bf.Gh, nullptr, sp, bss, bf.Gh, nullptr, sp, bss, e2));
+      } else {
+        // two Gram steps; buffers: A and G_1 in Gh, P_0 in Bh, H = P_0 A in
+        // Gl, P_1 in Bl, Q in Gh (each written after its last reader)
+        auto poly = [&](const bf16* G, bf16* P) {
+          EpiParams e = epi_pair(g, bf, 0, cx.c, cx.b, cx.a, G, nullptr, P, nullptr, sp, bss);
+          e.r_f16 = 1;
+          e.o_f16 = 1;
+          return tc(1, 0, 7, 1, S, S, S, G, nullptr, sp, bss, G, nullptr, sp, bss, e);
+        };
+        auto mul = [&](const bf16* X1, const bf16* X2, bf16* out) {
+          EpiParams e = epi_pair(g, bf, 0, 1.f, 0.f, 0.f, nullptr, nullptr, out, nullptr, sp, bss);
+          e.o_f16 = 1;
+          return tc(1, 0, 7, 1, S, S, S, X1, nullptr, sp, bss, X2, nullptr, sp, bss, e);
+        };
+        CK(poly(bf.Gh, bf.Bh));        // P_0
+        CK(mul(bf.Bh, bf.Gh, bf.Gl));  // H = P_0 A
+        CK(mul(bf.Bh, bf.Gl, bf.Gh));  // G_1 = P_0 H
+        CK(poly(bf.Gh, bf.Bl));        // P_1
+        CK(mul(bf.Bl, bf.Bh, bf.Gh));  // Q = P_1 P_0
+        Q = bf.Gh;
+      }
+      // X <- Q X_hi + a^k X_lo (first segment: both terms carry 1 / s), fp16 pair out
+      const bool dseg = use_diag && !first;
+      EpiParams e3 = epi_pair(g, bf, first ? 1 : 0, 1.f, ak, 0.f, dseg ? nullptr : bf.Xlo[cur], nullptr,
                               bf.Xb[nxt], bf.Xlo[nxt], lp, bsx);
       e3.r_f16 = xf;
       e3.r_scale = xf ? 1.f / kF16LoScale : 1.f;  // an fp16 pair's low part is stored scaled by 2^11
       e3.o_f16 = 1;
-      if (use_diag) e3.lo_scale = kF16LoScale * cx.a;
+      if (use_diag) e3.lo_scale = kF16LoScale * ak_next;
       e3.cols_valid = static_cast<int>(g.l);
-      if (k == T - 1) epi_set_final(e3, cx, g, mats, Bc);
-      CK(tc(1, 1, 2, xf, S, L, S, bf.Bh, nullptr, sp, bss, bf.Xb[cur], dseg ? bf.Xlo[cur] : nullptr, lp, bsx, e3,
+      if (last) epi_set_final(e3, cx, g, mats, Bc);
+      CK(tc(1, 1, 2, xf, S, L, S, Q, nullptr, sp, bss, bf.Xb[cur], dseg ? bf.Xlo[cur] : nullptr, lp, bsx, e3,
             dseg ? bf.diag : nullptr));
       cur = nxt;
     }
@@ -694,7 +863,8 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     return MUON_OK;
   }
 
-  if (g.sc == MUON_SCHED_ORIG || g.sc == MUON_SCHED_ORIG_BF16) {
+  if (g.sc == MUON_SCHED_ORIG || g.sc == MUON_SCHED_ORIG_BF16 || g.sc == MUON_SCHED_GRAM_R2) {
+    // (GRAM_R2 with coefficients outside fp16's range runs this bf16 form.)
     // Operand splits (see kSplitA / kSplitB): plain bf16 products miss a 2e-2
     // relative error on Gaussian inputs of aspect >= 1:2, mostly through the
     // rounding of the last steps, where sigma ~ 1 and the b, c terms are large.
@@ -765,7 +935,7 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
 
 // ------------------------------------------------------------------ validation
 static bool valid_dt(int dt) { return dt == MUON_BF16 || dt == MUON_FP32; }
-static bool valid_sc(int sc) { return sc >= MUON_SCHED_AUTO && sc <= MUON_SCHED_ORIG_BF16; }
+static bool valid_sc(int sc) { return sc >= MUON_SCHED_AUTO && sc <= MUON_SCHED_GRAM_R2; }
 
 static muon_status check_common(int steps, const float* coeffs, int dt, int sc, void* ws, size_t ws_bytes) {
   if (steps < 0 || steps > MUON_MAX_STEPS) return fail(MUON_ERR_ARG, "steps=%d out of [0, %d]", steps, MUON_MAX_STEPS);
@@ -788,11 +958,12 @@ static muon_status run_all(std::vector<Mat>& mats, int steps, const float* coeff
   std::vector<int> order, start;
   const int groups = bucket_plan(shapes, order, start);
   // plan every group before launching anything
+  const Coef kc = coef_of(coeffs);
   std::vector<Group> gs(groups);
   std::vector<int> widths(groups);
   for (int gi = 0; gi < groups; ++gi) {
     const Mat& m0 = mats[order[start[gi]]];
-    gs[gi] = make_group(m0.m, m0.n, steps, dt, sc);
+    gs[gi] = make_group(m0.m, m0.n, steps, dt, sc, kc);
     widths[gi] = fit_batch(gs[gi], start[gi + 1] - start[gi], dt, ws_bytes);
     if (widths[gi] <= 0)
       return fail(MUON_ERR_WORKSPACE, "workspace of %zu bytes cannot hold one %lldx%lld matrix (needs %zu)", ws_bytes,
@@ -819,7 +990,7 @@ static muon_status run_all(std::vector<Mat>& mats, int steps, const float* coeff
   cx.lr = lr;
   cx.apply = apply;
   cx.has_mom = has_mom;
-  cx.f16_ok = f16_coefficients_safe(cx.a, cx.b, cx.c);
+  cx.f16_ok = kc.f16_ok;
   std::vector<Mat> chunk;
   for (int gi = 0; gi < groups; ++gi) {
     const int n = start[gi + 1] - start[gi];
@@ -851,8 +1022,9 @@ static double estimate_seconds(long long m, long long n, int steps, muon_dtype d
   const Group g = make_group(m, n, steps, dt, sc);
   const double S = static_cast<double>(g.sp), L = static_cast<double>(g.lp);
   const double el = static_cast<double>(g.s) * g.l;
+  const bool pairs = steps > 0 && pair_sched(g.sc);
   const bool fp32 = dt == MUON_FP32;
-  const double rate = fp32 ? kRateSimt : kRateTensor;
+  const double rate = fp32 && !pairs ? kRateSimt : kRateTensor;
   const double nb = S / 256.0, nl = L / 256.0;
   const double sym_tiles = nb * (nb + 1) / 2, rect_tiles = nb * nl, tile = 2.0 * 256.0 * 256.0;
   const double ssz = 4.0;  // bytes of a packed element: fp32, or a bf16 pair
@@ -867,6 +1039,28 @@ static double estimate_seconds(long long m, long long n, int steps, muon_dtype d
     return t;
   }
   const double sym_out = sym_tiles * 256.0 * 256.0 * ssz;  // a block-lower s x s output
+  if (pairs) {
+    // fp16 pairs: every product three times the tensor-core work, 4-byte operands
+    launch(0.0, S * L * 12.0);  // X0 split into its pair
+    for (int k = 0; k < steps; ++k) {
+      launch(3.0 * sym_tiles * tile * L, S * L * 4.0 + sym_out);
+      launch(3.0 * sym_tiles * tile * S, 2.0 * sym_out);
+      launch(3.0 * rect_tiles * tile * S, sym_out + S * L * 4.0 + (k == steps - 1 ? apply : S * L * 4.0));
+    }
+    return t;
+  }
+  if (g.sc == MUON_SCHED_GRAM_R2) {
+    // segments: SYRK, then A*A (one step) or five s x s products (two steps), then the update
+    const double sym1 = sym_out / 2;  // single fp16 values
+    const std::vector<int> plan = segment_plan(steps, g.sc);
+    for (size_t si = 0; si < plan.size(); ++si) {
+      launch(sym_tiles * tile * L, S * L * 2.0 + sym1);
+      for (int p = 0; p < 4 * plan[si] - 3; ++p) launch(sym_tiles * tile * S, 3.0 * sym1);
+      const double out = si + 1 == plan.size() ? apply : S * L * 4.0;
+      launch(rect_tiles * tile * S, sym1 + S * L * 4.0 + out);
+    }
+    return t;
+  }
   if (g.sc == MUON_SCHED_ORIG || g.sc == MUON_SCHED_ORIG_BF16) {
     // ORIG on bf16 data: fp16 operands, no splits, A and B single 16-bit values
     // (the default coefficients pass the fp16 range check)
@@ -1087,7 +1281,7 @@ size_t muon_workspace_bytes(const int64_t* shapes, int count, int steps, muon_dt
 }
 
 muon_sched muon_resolve_schedule(int64_t m, int64_t n, int steps, muon_dtype dt, muon_sched sc) {
-  return resolve(std::min<long long>(m, n), std::max<long long>(m, n), steps, dt, sc);
+  return resolve(std::min<long long>(m, n), std::max<long long>(m, n), steps, dt, sc, coef_of(nullptr));
 }
 
 int muon_bucket_plan(const int64_t* shapes, int count, int* order, int* group_start) {
@@ -1156,9 +1350,10 @@ muon_status muon_debug_gemm(const void* A, const void* A_lo, const void* B, cons
   const char* why = nullptr;
   if (dt == MUON_BF16 || dt == MUON_FP16) {
     if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 256 || K % 128) return fail(MUON_ERR_SHAPE, "16-bit sizes");
-    if (split < 1 || split > 4) return fail(MUON_ERR_ARG, "split must be 1, 2, 3 or 4");
-    if ((split == 2 || split == 3) && !A_lo) return fail(MUON_ERR_ARG, "split 2 and 3 need A_lo");
-    if (split >= 3 && !B_lo) return fail(MUON_ERR_ARG, "split 3 and 4 need B_lo");
+    if (split < 1 || split > 5) return fail(MUON_ERR_ARG, "split must be 1, 2, 3, 4 or 5");
+    if ((split == 2 || split == 3 || split == 5) && !A_lo) return fail(MUON_ERR_ARG, "split 2, 3 and 5 need A_lo");
+    if (split >= 3 && !B_lo) return fail(MUON_ERR_ARG, "split 3, 4 and 5 need B_lo");
+    if (split == 5 && dt != MUON_FP16) return fail(MUON_ERR_ARG, "split 5 needs fp16 operands");
     if (split == 4 && (dt != MUON_FP16 || !b_mn || M != K || (sym & 1)))
       return fail(MUON_ERR_ARG, "split 4 needs fp16, b_mn = 1, M == K and a full output");
     if (split == 4 && ws_bytes < kHeader + 2 * kDiagDim * kDiagDim)
@@ -1269,7 +1464,7 @@ muon_status muon_ns_batched_static(const void* X, int B, int m, int n, int steps
       return fail(MUON_ERR_ARG, "steps=%d out of [0, %d]", steps, MUON_MAX_STEPS);
     if (!valid_dt(dt) || !valid_sc(sc)) return fail(MUON_ERR_ARG, "bad dtype or schedule");
     // Reject problems whose single matrix does not fit the fixed scratch, before any CUDA call.
-    const Group g = make_group(m, n, steps, dt, sc);
+    const Group g = make_group(m, n, steps, dt, sc, coef_of(coeffs));
     const size_t need = group_bytes(g, 1, dt);
     if (need > kStaticScratchBytes)
       return fail(MUON_ERR_WORKSPACE,

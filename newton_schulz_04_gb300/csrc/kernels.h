@@ -48,7 +48,10 @@ struct TcGemmDesc {
   int B, M, N, K;  // M % 256 == 0, N % 256 == 0, K % 128 == 0 (K % 256 == 0 with symmetric operands)
   int sym;
   int a_sym, b_sym;
-  int split;  // 1, 2 or 3
+  // 1 plain; 2: (A + A_lo) B; 3: A B + A B_lo + A_lo B (bf16 pairs, same scale);
+  // 5: fp16 pairs with lo = (v - hi) * 2^11: A B_lo + A_lo B accumulated first,
+  // then A B on the accumulator scaled by 2^-11 (tcgen05 scale-input-d)
+  int split;
   int b_mn;
   int f16;    // 1: both operands are fp16, 0: both bf16 (one tcgen05 kind::f16 MMA takes one type)
   TcOperand A, Bop;
@@ -104,6 +107,10 @@ cudaError_t launch_norm_finalize(const float* partial, int tiles, int B, float e
                                  uint16_t diag_bits, cudaStream_t st);
 // D = d I on its own (muon_debug_gemm).
 cudaError_t launch_fill_diag(void* D, uint16_t bits, cudaStream_t st);
+// X = Xf * inv_norm[b] as an fp16 pair (hi, lo = (x - hi) * 2^11), n elements
+// per matrix (a multiple of 8; buffers 16-byte aligned), B matrices.
+cudaError_t launch_pair_from_f32(const float* Xf, const float* inv_norm, void* Xh, void* Xl, long long n, int B,
+                                 int num_sms, cudaStream_t st);
 // O = Xf * inv_norm written through a final-mode epilogue (zero NS steps).
 cudaError_t launch_final_from_packed(const float* Xf, long long ld, long long bs, int B, const EpiParams& e,
                                      cudaStream_t st);

@@ -183,6 +183,20 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uin
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] = A * B + D * 2^-SCALE (the tcgen05 scale-input-d operand, SCALE in
+// [0, 15]): accumulates onto a D that was built at 2^SCALE times the scale of
+// this product, e.g. the low-part products of fp16 pairs stored as
+// lo = (v - hi) * 2^11.
+template <int SCALE>
+__device__ __forceinline__ void tc_mma_pair_scale_d(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+  static_assert(SCALE >= 0 && SCALE <= 15, "scale-input-d takes 0..15");
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, 1, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p, %4;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "n"(SCALE)
+      : "memory");
+}
 // Arrive once on the barrier at `bar`'s offset in every CTA of `mask` when the
 // pair MMAs issued so far by this thread are done.  This is how a 2-SM MMA
 // reports completion to both CTAs; it moves no data (the kernels use no

@@ -49,6 +49,12 @@
 // pair of tensor maps, all accumulating into the same TMEM tile, so split
 // products run on the same 128-byte-swizzled pipeline as plain ones.
 //
+// Scaled fp16 pairs (split 5).  A value carried as an fp16 pair, hi = fp16(v)
+// and lo = fp16((v - hi) * 2^11) (about 22 significant bits), is multiplied as
+// hi*lo + lo*hi (two K segments, accumulated at 2^11 times their true scale)
+// followed by hi*hi, whose first MMA scales the accumulator by 2^-11 on input
+// (tcgen05 scale-input-d): D = hi*hi + (hi*lo + lo*hi) / 2^11 in one TMEM tile.
+//
 // Diagonal segment.  For C = A B + d B_lo with A square (K == M), B MN-major
 // and d a scalar, the term d B_lo runs on the tensor cores too: rows 256 p ..
 // 256 p + 255 of d B_lo are D B_lo[256 p .. 256 p + 255, :] with D = d I (256
@@ -149,6 +155,7 @@ struct TcPhase {
   int diag_kb;    // k-blocks of the diagonal segment (0, or 256 / BK: D times B's residual rows)
   int final_vec;  // final mode may use 16-byte accesses to the caller's rows
   int f16;        // operands are fp16 (else bf16)
+  int pair_scale; // 1: the last segment's first MMA scales the accumulator by 2^-11 (split 5)
   // With `wait`, a tile of matrix b starts once done[b] >= wait_target
   // instead of after the whole previous grid (griddepcontrol.wait).
   int wait;
@@ -588,7 +595,10 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) tc_gemm_kernel(const __grid
                                      : make_sdesc(a0 + koff, 16, SBO, C::SWZ);
             const uint64_t bd = b_mn ? make_sdesc(b0 + kk * 16 * 128, C::MN_BOX_BYTES, SBO, C::SWZ)
                                      : make_sdesc(b0 + koff, 16, SBO, C::SWZ);
-            tc_mma_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if (phs.pair_scale && kb == nks - nk && kk == 0)
+              tc_mma_pair_scale_d<11>(d, ad, bd, idesc);  // hi*hi + (cross terms) * 2^-11
+            else
+              tc_mma_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit_pair(&empty[s], 0x3);  // both CTAs' stage s is free once these MMAs have read it
         }
@@ -905,15 +915,19 @@ static int max_clusters(int num_sms) {
 // Validates one product and fills its phase (tiles from `first` on).
 static bool build_phase(TcPhase& ph, const TcGemmDesc& d, const EpiParams& epi, int first, const char** why) {
   using C = TcCfg;
-  if (d.split < 1 || d.split > 3 || (d.split == 2 && !d.b_mn)) {
+  if (d.split < 1 || d.split > 5 || d.split == 4 || (d.split == 2 && !d.b_mn)) {
     *why = "unsupported operand split";
+    return false;
+  }
+  if (d.split == 5 && (!d.f16 || !d.A.lo || !d.Bop.lo || d.diag)) {
+    *why = "scaled fp16-pair products need fp16 operands with both residuals and no diagonal segment";
     return false;
   }
   if (d.M % 256 || d.N % 256 || d.K % 128) {
     *why = "tensor-core GEMM needs M and N multiples of 256 (CTA pairs) and K a multiple of 128";
     return false;
   }
-  if ((d.split >= 2 && !d.A.lo) || (d.split == 3 && !d.Bop.lo)) {
+  if ((d.split >= 2 && !d.A.lo) || (d.split >= 3 && !d.Bop.lo)) {
     *why = "split products need the residual operands";
     return false;
   }
@@ -988,10 +1002,14 @@ static bool build_phase(TcPhase& ph, const TcGemmDesc& d, const EpiParams& epi, 
   } else if (d.split == 2) {  // Ah B + Al B
     ph.nseg = 2;
     ph.seg_lo = 1 << 2;
-  } else {  // Ah Bh + Ah Bl + Al Bh
+  } else if (d.split == 3) {  // Ah Bh + Ah Bl + Al Bh
     ph.nseg = 3;
     ph.seg_lo = (1 << 3) | (1 << 4);
+  } else {  // split 5: Ah Bl + Al Bh (scaled by 2^11), then Ah Bh on a 2^-11-scaled accumulator
+    ph.nseg = 3;
+    ph.seg_lo = (1 << 1) | (1 << 2);
   }
+  ph.pair_scale = d.split == 5 ? 1 : 0;
   ph.diag_kb = d.diag ? kDiagDim / C::BK : 0;
   ph.a_sym = d.a_sym;
   ph.b_sym = d.b_mn ? 0 : d.b_sym;

@@ -27,7 +27,8 @@ def test_peaks_have_every_denominator():
 
 
 def test_kernel_families():
-    for label in ("tc_rect", "tc_syrk_x3", "tc_program", "void muon::tc_gemm_kernel<16>(muon::TcProgram<16>)"):
+    for label in ("tc_rect", "tc_syrk_x3", "tc_program", "void muon::tc_gemm_kernel<16>(muon::TcProgram<16>)",
+                  "void tc_gemm_kernel<16>(TcProgram<T1>)"):
         assert bench.family_of(label) == "tc_gemm"
     assert bench.family_of("simt_sym") == "simt_gemm"
     assert bench.family_of("void muon::pack_vec_kernel<false>(muon::PackArgs)") == "pack"
@@ -53,7 +54,7 @@ def test_recorded_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
                    _row(1, k_tc, "gpu__time_duration.sum", "msecond", "2") +
                    _row(2, k_tc, "dram__bytes_read.sum", "Gbyte", "0.5") +
                    _row(2, k_tc, "dram__bytes_write.sum", "Mbyte", "1,500") +
-                   _row(2, k_tc, "gpu__time_duration.sum", "msecond", "4"))
+                   _row(2, k_tc, "gpu__time_duration.sum", "ns", "4000000"))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     parsed = bench.parse_ncu_csv(str(log))
     assert parsed[1]["dram__bytes_read.sum"] == 1.5e9 and parsed[2]["dram__bytes_write.sum"] == 1.5e9

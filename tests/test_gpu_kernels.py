@@ -230,6 +230,74 @@ def test_tc_fp16_symmetric_operands_in_block_lower_storage():
     assert _rel(out[:, mk], ref[:, mk]) < 2e-5
 
 
+# ---- scaled fp16 pairs (split 5): the low parts stored as (v - hi) * 2^11
+
+def _f16_pair(x64):
+    hi = x64.to(torch.float16)
+    lo = ((x64 - hi.double()) * 2048.0).to(torch.float16)
+    return hi, lo
+
+
+@pytest.mark.parametrize("M,N,K,b_mn", [(256, 256, 128, False), (256, 512, 384, True), (512, 768, 1024, False),
+                                        (768, 256, 512, True)])
+def test_tc_fp16_pair_products(M, N, K, b_mn):
+    """C = (A + A_lo/2^11)(B + B_lo/2^11) to about 22 bits: the two low-part
+    products accumulate at 2^11 times their scale, and the tensor core scales
+    that accumulator by 2^-11 before the high-part product adds to it."""
+    m = _lib()
+    g = torch.Generator().manual_seed(40 + M + K)
+    A64 = torch.randn(2, M, K, generator=g, dtype=torch.float64)
+    B64 = torch.randn(2, K, N, generator=g, dtype=torch.float64) if b_mn else \
+        torch.randn(2, N, K, generator=g, dtype=torch.float64)
+    Ah, Al = _f16_pair(A64)
+    Bh, Bl = _f16_pair(B64)
+    out = m.debug_gemm(Ah.cuda(), Bh.cuda(), A_lo=Al.cuda(), B_lo=Bl.cuda(), split=5, b_mn=b_mn)
+    torch.cuda.synchronize()
+    Ap = Ah.double() + Al.double() / 2048.0
+    Bp = Bh.double() + Bl.double() / 2048.0
+    ref = (Ap @ Bp if b_mn else Ap @ Bp.transpose(1, 2)).float()
+    out = out.cpu()
+    # about 22-bit operands; the tensor cores' fp32 accumulation (about 1e-6 of
+    # the sum of |products|) sets the bound
+    assert _rel(out, ref) < 5e-6
+    # the high parts alone are 2^-11-accurate, so the low-part terms are really in
+    hh = (Ah.double() @ Bh.double() if b_mn else Ah.double() @ Bh.double().transpose(1, 2)).float()
+    assert _rel(hh, ref) > 1e-4
+
+
+def test_tc_fp16_pair_symmetric_operands_in_block_lower_storage():
+    """Split 5 on symmetric operands given block-lower (the upper k-blocks of
+    both parts read as transposed boxes), with a symmetric output."""
+    m = _lib()
+    g = torch.Generator().manual_seed(47)
+    S = 768
+    X = torch.randn(1, S, S, generator=g, dtype=torch.float64)
+    G64 = (X @ X.transpose(1, 2)) / S
+    Gh, Gl = _f16_pair(G64)
+    mask = block_lower(S, "cpu")
+    Ghs, Gls = Gh.clone(), Gl.clone()
+    Ghs[:, ~mask] = float("nan")
+    Gls[:, ~mask] = float("nan")
+    out = m.debug_gemm(Ghs.cuda(), Ghs.cuda(), A_lo=Gls.cuda(), B_lo=Gls.cuda(), split=5, sym=True, a_sym=True,
+                       b_sym=True).cpu()
+    torch.cuda.synchronize()
+    Gp = Gh.double() + Gl.double() / 2048.0
+    ref = (Gp @ Gp).float()
+    assert torch.isfinite(out[:, mask]).all()
+    assert _rel(out[:, mask], ref[:, mask]) < 5e-6
+
+
+def test_tc_fp16_pair_rejects_bf16_and_missing_parts():
+    m = _lib()
+    A = _rand((1, 256, 128), 48, torch.float16)
+    B = _rand((1, 256, 128), 49, torch.float16)
+    with pytest.raises(m.MuonError):
+        m.debug_gemm(A, B, A_lo=A, split=5)  # no B_lo
+    with pytest.raises(m.MuonError):
+        m.debug_gemm(A.to(torch.bfloat16), B.to(torch.bfloat16), A_lo=A.to(torch.bfloat16),
+                     B_lo=B.to(torch.bfloat16), split=5)
+
+
 # ---- diagonal K segment: C = A B + B_lo / 2^11 with the second term on the tensor cores
 
 @pytest.mark.parametrize("M,N,batch,a_sym", [(256, 256, 1, False), (512, 768, 2, False), (1024, 256, 3, True),

@@ -60,7 +60,7 @@ def oracle_O(x, steps=5, coeffs=oracle.QUINTIC):
 SHAPES_BF16 = [(256, 512), (512, 256), (200, 328), (328, 200), (256, 256), (130, 1000)]
 
 
-@pytest.mark.parametrize("sched", ["orig", "orig_bf16", "gram_x3"])
+@pytest.mark.parametrize("sched", ["orig", "orig_bf16", "gram_x3", "gram_r2", "orig_f16x3"])
 @pytest.mark.parametrize("shape", SHAPES_BF16)
 def test_ns_batched_bf16(sched, shape):
     m = _m()
@@ -81,7 +81,8 @@ def test_ill_conditioned_low_rank_bf16(shape):
     # accumulation precision: its error here is bounded, not held to 2e-2.
     m = _m()
     X = torch.stack([synth.low_rank(*shape, 8, 1e-4, seed=60 + i) for i in range(2)]).to(torch.bfloat16).cuda()
-    for sched, tol in [("auto", TOL_BF16), ("orig", TOL_BF16), ("orig_bf16", TOL_BF16), ("gram_x3", 0.1)]:
+    for sched, tol in [("auto", TOL_BF16), ("orig", TOL_BF16), ("orig_bf16", TOL_BF16), ("gram_r2", TOL_BF16),
+                       ("orig_f16x3", TOL_BF16), ("gram_x3", 0.1)]:
         O = m.ns_batched(X, steps=5, schedule=sched)
         torch.cuda.synchronize()
         for i in range(2):
@@ -110,6 +111,30 @@ def test_orig_fp16_operands_keep_a_wide_margin():
         ebf = rel(m.ns_batched(X, steps=5, schedule="orig_bf16")[0].float().cpu(), ref)
         assert e16 < 5e-3, (name, e16)
         assert ebf < TOL_BF16, (name, ebf)
+
+
+def test_gram_r2_keeps_a_margin():
+    """The Gram recurrence restarted every two steps on fp16 operands: a CPU
+    emulation (fp32-exact accumulation, which the tensor cores match on these
+    products) puts its worst error over rank-1 to rank-32, Gaussian,
+    row-scaled and fp32-momentum inputs at 8.2e-3 before the bf16 output
+    rounding, against 4.1e-3 for ORIG.  It must stay within 1.2e-2 here."""
+    m = _m()
+    for name, x in _inputs_of_every_kind():
+        X = x[None].to(torch.bfloat16).cuda()
+        e = rel(m.ns_batched(X, steps=5, schedule="gram_r2")[0].float().cpu(), oracle_O(X[0]))
+        assert e < 1.2e-2, (name, e)
+
+
+def test_auto_runs_gram_r2_where_it_saves_work():
+    m = _m()
+    assert m.resolve_schedule(4096, 14336) == "gram_r2"
+    assert m.resolve_schedule(4096, 4096) == "orig"
+    X = torch.stack([synth.random_matrix(256, 1024, seed=830 + i) for i in range(2)]).to(torch.bfloat16).cuda()
+    a = m.ns_batched(X, steps=5)
+    b = m.ns_batched(X, steps=5, schedule="gram_r2")
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
 
 
 def test_coefficients_outside_the_fp16_range_run_the_bf16_schedule():
@@ -145,7 +170,7 @@ def test_gram_x1_fast_mode_error_is_bounded_and_larger():
         assert e3 < e1
 
 
-@pytest.mark.parametrize("sched", ["orig", "gram_x3"])
+@pytest.mark.parametrize("sched", ["orig", "gram_x3", "gram_r2", "orig_f16x3"])
 @pytest.mark.parametrize("shape", [(128, 256), (256, 128), (200, 328), (384, 384)])
 def test_ns_batched_fp32(sched, shape):
     m = _m()
@@ -360,7 +385,7 @@ def test_custom_coefficients_cubic():
 def test_determinism_bitwise():
     m = _m()
     X = torch.stack([synth.random_matrix(512, 1024, seed=97 + i) for i in range(3)]).to(torch.bfloat16).cuda()
-    for sched in ["orig", "orig_bf16", "gram_x3"]:
+    for sched in ["orig", "orig_bf16", "gram_x3", "gram_r2", "orig_f16x3"]:
         a = m.ns_batched(X, steps=5, schedule=sched)
         b = m.ns_batched(X, steps=5, schedule=sched)
         torch.cuda.synchronize()
@@ -468,18 +493,55 @@ def test_c4_many_small_matrices_sampled():
         _check_apply(w.weights[i].double().numpy(), W[i].cpu().double().numpy(), O_gpu, w.lr, torch.bfloat16)
 
 
-@pytest.mark.parametrize("n", [1024, 2048])
-def test_c5_aspect_sweep_fp32(n):
+@pytest.mark.parametrize("sched", ["auto", "gram_r2", "orig_f16x3"])
+@pytest.mark.parametrize("n", [1024, 2048, 4096])
+def test_c5_aspect_sweep_fp32(n, sched):
     """The aspect-ratio sweep on the fp32 path (m = 1024, row 0 scaled by 100),
-    2 of the 8 matrices per shape, 5 and 10 steps."""
+    2 of the 8 matrices per shape, 5 and 10 steps: FFMA (AUTO: Gram space at
+    5 steps, two-step Gram segments or original space at 10) and the
+    tensor-core fp16-pair schedule."""
     m = _m()
     for steps in (5, 10):
         w = synth.c5(n=n, batch=2, dtype=torch.float32, steps=steps)
         X = torch.stack(w.grads).cuda()
-        O = m.ns_batched(X, steps=steps)
+        O = m.ns_batched(X, steps=steps, schedule=sched)
         torch.cuda.synchronize()
         for i in range(2):
-            assert rel(O[i].cpu(), oracle_O(w.grads[i], steps)) < TOL_FP32, (n, steps, i)
+            e = rel(O[i].cpu(), oracle_O(w.grads[i], steps))
+            assert e < TOL_FP32, (n, steps, i, e)
+
+
+@pytest.mark.parametrize("sched", ["auto", "orig", "gram_r2"])
+@pytest.mark.parametrize("steps", [5, 10])
+def test_fp32_rank_deficient_inputs_stay_bounded(sched, steps):
+    """fp32 rank-1 and rank-8 + noise inputs (not rounded to bf16).  fp32
+    rounding of A = X X^T is far above the squared noise singular values here,
+    so even FFMA in original space misses 1e-4 (measured: up to 2.2e-4 at 5
+    steps, 3.3e-3 at 10).  Every fp32 schedule AUTO uses must stay finite and
+    within 5e-4 (5 steps) or 5e-3 (10 steps).  (Gram space without restarts
+    diverged on these inputs at 10 steps, which is why AUTO never runs it
+    beyond 6.)"""
+    m = _m()
+    for shape, r in [((256, 1024), 8), ((768, 3072), 8), ((768, 3072), 1)]:
+        X = torch.stack([synth.low_rank(*shape, r, 1e-4, seed=860 + i) for i in range(2)]).cuda()
+        O = m.ns_batched(X, steps=steps, schedule=sched)
+        torch.cuda.synchronize()
+        assert torch.isfinite(O).all(), (sched, shape, r)
+        for i in range(2):
+            e = rel(O[i].cpu(), oracle_O(X[i], steps))
+            assert e < (5e-4 if steps <= 6 else 5e-3), (sched, shape, r, i, e)
+
+
+def test_fp32_pair_schedule_full_step():
+    """muon_step on fp32 data through the tensor-core fp32 schedule: the c1
+    matrix and both orientations of a ragged shape, momentum within one fp32
+    ulp, weights elementwise against W0 - lr O_gpu."""
+    _check_step([(128, 256), (256, 128), (200, 328)], dtype=torch.float32, seed=17, sched="orig_f16x3")
+    _check_step([(256, 512)], dtype=torch.float32, seed=19, sched="orig_f16x3", mom_init=True)
+
+
+def test_fp32_restarted_gram_full_step():
+    _check_step([(128, 512), (512, 128), (200, 600)], dtype=torch.float32, seed=23, sched="gram_r2", steps=10)
 
 
 def test_updater_graphs_for_alternating_gradient_buffers():
@@ -508,7 +570,9 @@ def test_updater_graphs_for_alternating_gradient_buffers():
 
 
 @pytest.mark.parametrize("sched,dtype", [("orig", torch.bfloat16), ("gram_x3", torch.bfloat16),
-                                         ("orig", torch.float32), ("gram_x3", torch.float32)])
+                                         ("gram_r2", torch.bfloat16), ("orig", torch.float32),
+                                         ("gram_x3", torch.float32), ("orig_f16x3", torch.float32),
+                                         ("gram_r2", torch.float32)])
 @pytest.mark.parametrize("steps", [1, 2, 3])
 def test_each_product_through_few_steps(sched, dtype, steps):
     """One step is O = P_0 X_0 with P_0 = a I + b G_0 + c G_0^2 (the SYRK, the
@@ -526,7 +590,8 @@ def test_each_product_through_few_steps(sched, dtype, steps):
 
 
 @pytest.mark.parametrize("sched,steps,coeffs", [("orig", 7, None), ("gram_x3", 7, None), ("orig_bf16", 7, None),
-                                                ("orig", 12, (1.5, -0.5, 0.0))])
+                                                ("orig", 12, (1.5, -0.5, 0.0)), ("gram_r2", 7, None),
+                                                ("gram_r2", 10, None), ("gram_r2", 12, (1.5, -0.5, 0.0))])
 def test_more_products_than_one_shared_launch(sched, steps, coeffs):
     """A short chunk runs up to 16 consecutive products in one launch; 7 or 12
     steps need several such launches, chained on the same per-matrix counters."""

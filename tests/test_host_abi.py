@@ -65,15 +65,39 @@ def test_bucket_plan_llama_shapes(lib):
 
 def test_schedule_choice(lib):
     import newton_schulz_04_gb300 as m
-    # bf16 AUTO runs original space (split Gram misses 2e-2 on ill-conditioned
-    # inputs with the tensor cores' accumulation); fp32 AUTO takes Gram space
-    # whenever l > s, where it never costs more
-    for shp in [(1024, 1024), (1024, 4096), (1024, 8192), (16384, 1024), (4096, 14336), (256, 1024)]:
-        assert m.resolve_schedule(*shp) == "orig"
+    # bf16 AUTO runs the Gram recurrence restarted every two steps where it
+    # executes at most 0.9x ORIG's tensor-core work, else original space;
+    # fp32 AUTO takes Gram space whenever l > s, where it never costs more
+    for shp in [(1024, 1024), (4096, 4096), (1000, 1100), (1024, 1280)]:
+        assert m.resolve_schedule(*shp) == "orig", shp
+    for shp in [(1024, 4096), (1024, 8192), (16384, 1024), (4096, 14336), (256, 1024), (1024, 2048)]:
+        assert m.resolve_schedule(*shp) == "gram_r2", shp
+    assert m.resolve_schedule(4096, 14336, steps=2) == "orig"  # no two-step segment to run
+    assert m.resolve_schedule(4096, 14336, steps=3) == "gram_r2"
     assert m.resolve_schedule(1024, 8192, steps=0) == "orig"
     assert m.resolve_schedule(1024, 8192, schedule="gram_x1") == "gram_x1"
-    assert m.resolve_schedule(128, 256, dtype=torch.float32) == "gram_x3"
-    assert m.resolve_schedule(128, 128, dtype=torch.float32) == "orig"
+    assert m.resolve_schedule(128, 256, dtype=torch.float32) == "orig_f16x3"
+    assert m.resolve_schedule(128, 128, dtype=torch.float32) == "orig_f16x3"
+    assert m.resolve_schedule(128, 256, dtype=torch.float32, schedule="gram_x3") == "gram_x3"
+    assert m.resolve_schedule(128, 128, dtype=torch.float32, schedule="orig") == "orig"
+    assert m.resolve_schedule(128, 128, dtype=torch.float32, schedule="gram_r2") == "gram_r2"  # FFMA segments
+    assert m.resolve_schedule(128, 256, dtype=torch.float32, schedule="orig_f16x3") == "orig_f16x3"
+    assert m.resolve_schedule(128, 256, schedule="orig_f16x3") == "orig_f16x3"
+    # fp32 beyond 6 steps: Gram space only in restarted segments
+    assert m.resolve_schedule(1024, 2048, steps=6, dtype=torch.float32) == "orig_f16x3"
+    assert m.resolve_schedule(1024, 2048, steps=10, dtype=torch.float32) == "gram_r2"
+    assert m.resolve_schedule(1024, 1100, steps=10, dtype=torch.float32) == "orig"
+    assert m.resolve_schedule(1024, 2048, steps=10, dtype=torch.float32, schedule="gram_r2") == "gram_r2"
+
+
+def test_gram_r2_work_against_orig(lib):
+    """The segment plan's tensor-core work as AUTO counts it: per segment of k
+    steps S^2 L (SYRK) + (4k - 3) S^3 + 2 S^2 L; ORIG is k = 1 throughout."""
+    def work(plan, S, L):
+        return sum(3 * S * S * L + (4 * k - 3) * S ** 3 for k in plan)
+    S, L = 4096, 14336
+    assert work([1, 2, 2], S, L) / work([1] * 5, S, L) < 0.75  # the c3 rectangular bucket: 26 % less
+    assert work([1, 2, 2], S, S) == work([1] * 5, S, S)          # square: the same
 
 
 def test_workspace_sizes(lib):
