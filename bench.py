@@ -205,7 +205,7 @@ def workload_desc(name: str) -> str:
 
 
 def operands_desc(dtype, schedule):
-    if schedule == "orig_f16x3":
+    if schedule.startswith("orig_f16x3"):
         return ("fp16-pair tensor-core operands (about 22 bits), three products per product, fp32 accumulation; "
                 f"{'fp32' if dtype == torch.float32 else 'bf16'} in and out")
     if dtype == torch.float32:
@@ -492,7 +492,9 @@ def run_ours(args, world, rank, local):
         cpu_work = work
     else:
         cpu_work = None
+    t_tune = time.perf_counter()
     upd = pkg.MuonUpdater(W, work.beta, work.lr, work.steps, work.coeffs, args.schedule, use_graph=not args.no_graph)
+    t_tune = time.perf_counter() - t_tune
     Mo = upd.moms
     flops_step = work.flop_count()
     flops_all = sum_over_ranks(flops_step, world)  # = world x flops_step under weak scaling
@@ -506,7 +508,7 @@ def run_ours(args, world, rank, local):
         upd.step(G)
 
     def step_eager():
-        pkg.muon_step(W, G, Mo, work.beta, work.lr, work.steps, work.coeffs, args.schedule, upd.workspace, st)
+        upd._eager(G, st)
 
     def timed(fn, k):
         out = []
@@ -630,8 +632,7 @@ def run_ours(args, world, rank, local):
                 copy_in(1 - i)
             st.wait_event(ev_in[i])
             if args.no_graph:
-                pkg.muon_step(W, Gsets[i], Mo, work.beta, work.lr, work.steps, work.coeffs, args.schedule,
-                              upd.workspace, st)
+                upd._eager(Gsets[i], st)
             else:
                 upd.step(Gsets[i])
             for w, wh in zip(W, Wh):
@@ -649,9 +650,9 @@ def run_ours(args, world, rank, local):
         "metric": "Muon update TFLOP/s (algorithmic, symmetric Gram count)",
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": scaling, "vs_baseline": None,
-        "dtype": ("fp16x2" if args.schedule == "orig_f16x3" else
+        "dtype": ("fp16x2" if any(c.startswith("orig_f16x3") for c in upd.chosen.values()) else
                   "fp32" if work.dtype == torch.float32 else "bf16+fp16"),
-        "operands": operands_desc(work.dtype, args.schedule),
+        "operands": operands_desc(work.dtype, next(iter(upd.chosen.values()))),
         "data": "synthetic",
         "config": {"workload": workload_desc(args.config), "name": args.config,
                    "matrices_per_gpu": count, "l2": "flushed between timed steps" if flush is not None
@@ -659,8 +660,8 @@ def run_ours(args, world, rank, local):
                    "parallelism": "1 gpu" if world == 1 else
                    (f"owner placement over {world} ranks (LPT), no data-path collective" if scaling == "strong"
                     else f"one batch per rank x{world}")},
-        "schedules": {f"{a}x{b}": pkg.resolve_schedule(a, b, work.steps, work.dtype, args.schedule)
-                      for (a, b) in sorted({(min(x), max(x)) for x in shapes})},
+        "schedules": {f"{a}x{b}": sc for (a, b), sc in sorted(upd.chosen.items())},
+        "schedule_arg": args.schedule,
         "matrices_per_s": count_all * args.steps / t_total,
         "pct_of_bf16_peak": 100.0 * value / pk["bf16_tflops"],
         "value_without_graph": value_eager,
@@ -675,6 +676,8 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "peaks": pk,
     }
+    if args.schedule == "tuned":
+        line["tuning_s"] = t_tune
     if rank == 0 and world == 1 and not args.no_cpu_baseline and cpu_work is not None:
         line["cpu_baseline"] = cpu_baseline(cpu_work, budget_s=args.cpu_budget)
     elif rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -848,7 +851,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="call the C ABI per step instead of replaying a graph")
-    ap.add_argument("--schedule", default="auto", help="NS schedule (auto, orig, gram_r2, orig_f16x3, ...)")
+    ap.add_argument("--schedule", default="auto", help="NS schedule (auto, orig, gram_r2, orig_f16x3, ..., with an "
+                    "optional +shared / +separate launch mode), or tuned: the fastest per shape group, measured")
     ap.add_argument("--record-traffic", metavar="CSV", help="store the DRAM traffic of an ncu metrics log taken on "
                     "--config in profiles/dram_traffic.json (no GPU work)")
     ap.add_argument("--traffic-scale", type=float, default=1.0, help="with --record-traffic: the factor from the "

@@ -135,6 +135,20 @@ typedef enum {
  * muon_workspace_bytes is the same for ORIG, ORIG_BF16 and GRAM_R2 (bf16).
  */
 
+/*
+ * Launch-mode flags, OR'ed into a muon_sched argument (its low 8 bits are the
+ * schedule).  By default the tensor-core products of a batch chunk share
+ * persistent launches (up to 16 consecutive products per launch, ordered per
+ * matrix by completion counters) when the chunk is small -- at most 16
+ * 256 x 256 tile pairs per CTA pair in its largest product -- and run one
+ * launch per product otherwise.  These flags force one of the two; the
+ * numerics are the same either way (every tile is computed identically).
+ * Measured per shape by the binding's tune_schedules.
+ */
+#define MUON_SCHED_SHARED_LAUNCH 0x100
+#define MUON_SCHED_SEPARATE_LAUNCH 0x200
+#define MUON_SCHED_MASK 0xff
+
 #define MUON_MAX_DIM 65536   /* largest accepted m or n */
 #define MUON_MAX_STEPS 100   /* largest accepted number of NS steps */
 #define MUON_WS_ALIGN 256    /* required alignment of the workspace pointer */
@@ -188,8 +202,9 @@ MUON_API size_t muon_workspace_bytes(const int64_t* shapes, int count, int steps
                             muon_dtype dt, muon_sched sc);
 
 /*
- * muon_resolve_schedule -- the schedule AUTO picks for one s x l group
- * (s <= l) with `steps` iterations.  Host only.
+ * muon_resolve_schedule -- the schedule AUTO picks for one m x n group with
+ * `steps` iterations and the quintic coefficients (launch-mode flags in `sc`
+ * are ignored; the result has none).  Host only.
  */
 MUON_API muon_sched muon_resolve_schedule(int64_t m, int64_t n, int steps, muon_dtype dt, muon_sched sc);
 

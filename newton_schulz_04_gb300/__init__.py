@@ -8,5 +8,5 @@ from .binding import (  # noqa: F401
     AdamwTail, MuonError, MuonUpdater, adamw_tail, bucket_plan, cost_estimate, debug_bounded_wait,
     debug_bounded_wait_static, debug_gemm, device_status, library_path, load, measure_costs, muon_step, new_workspace,
     ns_batched, ns_batched_static, owned, partition, profile_enable, profile_records, resolve_schedule,
-    static_status, workspace_bytes,
+    sched_code, schedule_candidates, static_status, tune_schedules, workspace_bytes,
 )

@@ -22,6 +22,16 @@ BF16, FP32, FP16 = 0, 1, 2  # FP16: muon_debug_gemm only
 F16_LO_SCALE = 2048.0  # an fp16 pair stores lo = fp16((v - hi) * 2^11)
 SCHED = {"auto": 0, "gram_x3": 1, "gram_x1": 2, "orig": 3, "orig_bf16": 4, "orig_f16x3": 5, "gram_r2": 6}
 SCHED_NAMES = {v: k for k, v in SCHED.items()}
+LAUNCH = {"": 0, "shared": 0x100, "separate": 0x200}  # "+shared" / "+separate" suffixes of a schedule name
+
+
+def sched_code(name: str) -> int:
+    """C-ABI value of a schedule name, optionally with a launch-mode suffix
+    ("gram_r2+shared", "orig+separate")."""
+    base, _, mode = name.partition("+")
+    if base not in SCHED or mode not in LAUNCH:
+        raise ValueError(f"unknown schedule {name!r}")
+    return SCHED[base] | LAUNCH[mode]
 WS_ALIGN = 256
 
 _lib = None
@@ -130,7 +140,7 @@ def _stream_ptr(stream) -> int:
 
 def workspace_bytes(shapes, steps=5, dtype=torch.bfloat16, schedule="auto") -> int:
     lib = load()
-    n = lib.muon_workspace_bytes(_shapes_arr(shapes), len(shapes), int(steps), _dtype_code(dtype), SCHED[schedule])
+    n = lib.muon_workspace_bytes(_shapes_arr(shapes), len(shapes), int(steps), _dtype_code(dtype), sched_code(schedule))
     if n == 0:
         raise MuonError(ERR_ARG, lib.muon_last_error().decode())
     return int(n)
@@ -138,7 +148,7 @@ def workspace_bytes(shapes, steps=5, dtype=torch.bfloat16, schedule="auto") -> i
 
 def resolve_schedule(m, n, steps=5, dtype=torch.bfloat16, schedule="auto") -> str:
     return SCHED_NAMES[load().muon_resolve_schedule(int(m), int(n), int(steps), _dtype_code(dtype),
-                                                    SCHED[schedule])]
+                                                    sched_code(schedule))]
 
 
 def bucket_plan(shapes):
@@ -224,7 +234,7 @@ def cost_estimate(shapes, steps=5, dtype=torch.bfloat16, schedule="auto") -> lis
     lib = load()
     n = len(shapes)
     out = (ctypes.c_double * max(n, 1))()
-    _check(lib.muon_cost_estimate(_shapes_arr(shapes), n, int(steps), _dtype_code(dtype), SCHED[schedule], out))
+    _check(lib.muon_cost_estimate(_shapes_arr(shapes), n, int(steps), _dtype_code(dtype), sched_code(schedule), out))
     return list(out[:n])
 
 
@@ -283,6 +293,67 @@ def measure_costs(shapes, steps=5, dtype=torch.bfloat16, schedule="auto", repeat
     return out
 
 
+def schedule_candidates(dtype=torch.bfloat16, steps=5):
+    """What a measured choice may pick from: schedules whose accuracy meets
+    the dtype's tolerance on every input kind measured (bf16: original space,
+    or the Gram recurrence restarted every two steps; fp32: the tensor-core
+    fp16-pair schedule up to 6 steps, FFMA restarted Gram or original space),
+    each tensor-core one with shared or separate launches."""
+    if dtype == torch.bfloat16:
+        base = ["orig", "gram_r2"] if steps >= 3 else ["orig"]
+        return [f"{b}+{mode}" for b in base for mode in ("shared", "separate")]
+    if steps <= 6:
+        return ["orig_f16x3+shared", "orig_f16x3+separate", "orig", "gram_r2"]
+    return ["gram_r2", "orig"]
+
+
+def tune_schedules(shapes, steps=5, dtype=torch.bfloat16, candidates=None, repeats=3, cache=None, device=None):
+    """Measured schedule choice per shape group.
+
+    For each distinct (short, long) group of `shapes`, at its real batch width,
+    every candidate schedule (schedule_candidates by default) runs muon_step on
+    one set of synthetic tensors drawn on the device (one warm-up call, then
+    `repeats` calls timed with CUDA events), and the fastest wins.  Returns
+    {(s, l): schedule}.  `cache` (a dict, e.g. loaded from and saved to JSON by
+    the caller) keeps, per key "s,l,dtype,steps,width", the chosen schedule and
+    every candidate's milliseconds, so later calls measure nothing.
+    """
+    dev = device or torch.device("cuda")
+    cands = list(candidates or schedule_candidates(dtype, steps))
+    groups = {}
+    for (m, n) in shapes:
+        key = (min(m, n), max(m, n))
+        groups[key] = groups.get(key, 0) + 1
+    out = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    for (s_, l_), width in sorted(groups.items()):
+        key = f"{s_},{l_},{str(dtype).split('.')[-1]},{steps},{width}"
+        if cache is not None and key in cache:
+            out[(s_, l_)] = cache[key]["best"]
+            continue
+        W = [torch.zeros(s_, l_, dtype=dtype, device=dev) for _ in range(width)]
+        G = [torch.randn(s_, l_, generator=gen, device=dev).to(dtype) for _ in range(width)]
+        M = [torch.zeros(s_, l_, dtype=torch.float32, device=dev) for _ in range(width)]
+        ws = new_workspace(max(workspace_bytes([(s_, l_)] * width, steps, dtype, sc) for sc in cands), dev)
+        ms = {}
+        for sc in cands:
+            muon_step(W, G, M, 0.0, 0.0, steps, None, sc, ws)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(repeats):
+                muon_step(W, G, M, 0.0, 0.0, steps, None, sc, ws)
+            b.record()
+            b.synchronize()
+            ms[sc] = a.elapsed_time(b) / repeats
+        del W, G, M, ws
+        entry = {"best": min(ms, key=ms.get), "ms": ms}
+        if cache is not None:
+            cache[key] = entry
+        out[(s_, l_)] = entry["best"]
+    return out
+
+
 def owned(shapes, rank: int, world: int, costs=None, steps=5, dtype=torch.bfloat16, schedule="auto",
           exact_limit: int = 12):
     """Indices of the matrices `rank` owns out of `world` owners (model costs
@@ -315,7 +386,7 @@ def ns_batched(X: torch.Tensor, steps: int = 5, coeffs=None, schedule: str = "au
     if workspace is None:
         workspace = new_workspace(workspace_bytes([(m, n)] * max(B, 1), steps, X.dtype, schedule), X.device)
     st = lib.muon_ns_batched(ctypes.c_void_p(X.data_ptr()), B, m, n, int(steps), _coeffs(coeffs),
-                             ctypes.c_void_p(out.data_ptr()), dt, SCHED[schedule],
+                             ctypes.c_void_p(out.data_ptr()), dt, sched_code(schedule),
                              ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                              ctypes.c_void_p(_stream_ptr(stream)))
     _check(st)
@@ -333,7 +404,7 @@ def ns_batched_static(X: torch.Tensor, steps: int = 5, coeffs=None, schedule: st
     if out is None:
         out = torch.empty_like(X)
     _check(lib.muon_ns_batched_static(ctypes.c_void_p(X.data_ptr()), B, m, n, int(steps), _coeffs(coeffs),
-                                      ctypes.c_void_p(out.data_ptr()), _dtype_code(X.dtype), SCHED[schedule],
+                                      ctypes.c_void_p(out.data_ptr()), _dtype_code(X.dtype), sched_code(schedule),
                                       ctypes.c_void_p(_stream_ptr(stream))))
     return out
 
@@ -372,7 +443,7 @@ def muon_step(weights: Sequence[torch.Tensor], grads: Sequence[torch.Tensor], mo
     P = ctypes.c_void_p * count
     st = lib.muon_step(P(*[w.data_ptr() for w in weights]), P(*[g.data_ptr() for g in grads]),
                        P(*[m.data_ptr() for m in moms]), _shapes_arr(shapes), count, float(beta), float(lr),
-                       int(steps), _coeffs(coeffs), _dtype_code(dtype), SCHED[schedule],
+                       int(steps), _coeffs(coeffs), _dtype_code(dtype), sched_code(schedule),
                        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                        ctypes.c_void_p(_stream_ptr(stream)))
     _check(st)
@@ -444,6 +515,9 @@ class MuonUpdater:
 
     Holds the fp32 momentum buffers and one caller-side workspace sized for the
     parameter shapes; `step(grads)` calls the C ABI once.  With
+    `schedule="tuned"` each shape group runs the schedule that measured fastest
+    for it (tune_schedules, at construction; `tune_cache` is passed through),
+    one C-ABI call per group, in the library's group order.  With
     `use_graph=True` the first step with a given set of gradient tensors runs
     eagerly and is captured into a CUDA graph; later steps with the same
     tensors replay it (one launch of the whole kernel sequence).  Graphs are
@@ -452,11 +526,26 @@ class MuonUpdater:
     """
 
     def __init__(self, params: Sequence[torch.Tensor], beta=0.95, lr=0.02, steps=5, coeffs=None,
-                 schedule="auto", workspace_limit: int | None = None, use_graph: bool = False, max_graphs: int = 4):
+                 schedule="auto", workspace_limit: int | None = None, use_graph: bool = False, max_graphs: int = 4,
+                 tune_cache=None):
         self.params = list(params)
         self.beta, self.lr, self.steps, self.coeffs, self.schedule = beta, lr, steps, coeffs, schedule
         self.moms = [torch.zeros(p.shape, dtype=torch.float32, device=p.device) for p in self.params]
-        need = workspace_bytes([tuple(p.shape) for p in self.params], steps, self.params[0].dtype, schedule)
+        shapes = [tuple(p.shape) for p in self.params]
+        dtype = self.params[0].dtype
+        if schedule == "tuned":
+            self.chosen = tune_schedules(shapes, steps, dtype, cache=tune_cache, device=self.params[0].device)
+            order, start = bucket_plan(shapes)
+            self._groups = []
+            for k in range(len(start) - 1):
+                idx = order[start[k]:start[k + 1]]
+                s_, l_ = min(shapes[idx[0]]), max(shapes[idx[0]])
+                self._groups.append((idx, self.chosen[(s_, l_)]))
+            need = max(workspace_bytes([shapes[i] for i in idx], steps, dtype, sc) for idx, sc in self._groups)
+        else:
+            self.chosen = {(min(sh), max(sh)): resolve_schedule(sh[0], sh[1], steps, dtype, schedule) for sh in shapes}
+            self._groups = None
+            need = workspace_bytes(shapes, steps, dtype, schedule)
         if workspace_limit is not None:
             need = min(need, int(workspace_limit))
         self.workspace = new_workspace(need, self.params[0].device)
@@ -465,8 +554,13 @@ class MuonUpdater:
         self._graphs = {}  # tuple of gradient data pointers -> CUDAGraph
 
     def _eager(self, grads, stream=None):
-        muon_step(self.params, grads, self.moms, self.beta, self.lr, self.steps, self.coeffs, self.schedule,
-                  self.workspace, stream)
+        if self._groups is None:
+            muon_step(self.params, grads, self.moms, self.beta, self.lr, self.steps, self.coeffs, self.schedule,
+                      self.workspace, stream)
+            return
+        for idx, sc in self._groups:
+            muon_step([self.params[i] for i in idx], [grads[i] for i in idx], [self.moms[i] for i in idx], self.beta,
+                      self.lr, self.steps, self.coeffs, sc, self.workspace, stream)
 
     def step(self, grads: Sequence[torch.Tensor], stream=None):
         """One step on `stream` (the current stream if None)."""

@@ -222,6 +222,7 @@ static double plan_work(long long s, long long l, int steps, muon_sched sc) {
 constexpr int kFp32PairMaxSteps = 6;
 
 static muon_sched resolve(long long s, long long l, int steps, muon_dtype dt, muon_sched sc, const Coef& k) {
+  sc = static_cast<muon_sched>(sc & MUON_SCHED_MASK);  // launch-mode flags are the Group's
   if (steps == 0) return MUON_SCHED_ORIG;  // only the packed fp32 copy is needed
   // two-step Gram segments where they save at least a tenth of the work
   const bool r2_pays = plan_work(s, l, steps, MUON_SCHED_GRAM_R2) <= 0.9 * plan_work(s, l, steps, MUON_SCHED_ORIG);
@@ -372,6 +373,7 @@ struct Group {
   int tiles;  // pack tiles per matrix
   muon_sched sc;
   int steps;
+  int launch;  // 0: shared launches for small chunks, else one per product; or the forcing flag
 };
 
 static Group make_group(long long m, long long n, int steps, muon_dtype dt, muon_sched sc,
@@ -383,6 +385,7 @@ static Group make_group(long long m, long long n, int steps, muon_dtype dt, muon
   g.lp = round_up(g.l, 256);
   g.tiles = static_cast<int>((g.sp / 64) * (g.lp / 64));
   g.sc = resolve(g.s, g.l, steps, dt, sc, k);
+  g.launch = sc & ~MUON_SCHED_MASK;
   g.steps = steps;
   return g;
 }
@@ -522,7 +525,8 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   const long long pairs_rect = static_cast<long long>(Bc) * (g.sp / 256) * (g.lp / 256);
   const bool pairs = cx.steps > 0 && pair_sched(g.sc);  // fp16-pair operands (either dtype)
   const bool tensor = cx.dt == MUON_BF16 || pairs;       // the NS products run on the tensor cores
-  const bool chain = tensor && pairs_rect <= 16LL * (cx.sms / 2);
+  const bool chain = tensor && (g.launch == MUON_SCHED_SHARED_LAUNCH ||
+                                (g.launch == 0 && pairs_rect <= 16LL * (cx.sms / 2)));
   // stream-ordered: runs after everything before this chunk, before its pack
   if (chain) CK(cudaMemsetAsync(bf.done, 0, sizeof(int) * Bc, cx.st));
   if (tensor && cx.steps > 0) CK(cudaMemsetAsync(bf.tile_ctr, 0, sizeof(int) * kMaxTcLaunches, cx.st));
@@ -935,7 +939,11 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
 
 // ------------------------------------------------------------------ validation
 static bool valid_dt(int dt) { return dt == MUON_BF16 || dt == MUON_FP32; }
-static bool valid_sc(int sc) { return sc >= MUON_SCHED_AUTO && sc <= MUON_SCHED_GRAM_R2; }
+static bool valid_sc(int sc) {
+  const int base = sc & MUON_SCHED_MASK, flags = sc & ~MUON_SCHED_MASK;
+  return base >= MUON_SCHED_AUTO && base <= MUON_SCHED_GRAM_R2 &&
+         (flags == 0 || flags == MUON_SCHED_SHARED_LAUNCH || flags == MUON_SCHED_SEPARATE_LAUNCH);
+}
 
 static muon_status check_common(int steps, const float* coeffs, int dt, int sc, void* ws, size_t ws_bytes) {
   if (steps < 0 || steps > MUON_MAX_STEPS) return fail(MUON_ERR_ARG, "steps=%d out of [0, %d]", steps, MUON_MAX_STEPS);

@@ -156,6 +156,7 @@ struct TcPhase {
   int final_vec;  // final mode may use 16-byte accesses to the caller's rows
   int f16;        // operands are fp16 (else bf16)
   int pair_scale; // 1: the last segment's first MMA scales the accumulator by 2^-11 (split 5)
+  int rgroup;     // rectangular products: row-block pairs per column-major group of tiles
   // With `wait`, a tile of matrix b starts once done[b] >= wait_target
   // instead of after the whole previous grid (griddepcontrol.wait).
   int wait;
@@ -196,8 +197,9 @@ __device__ __forceinline__ void decode_pair(const TcPhase& a, int t, int& b, int
     p = q;
     j = u - q * (q + 1) / 2;
   } else {
-    // Groups of 4 row-block pairs walked column by column keep a wave's operands in L2.
-    constexpr int G = 4;
+    // Groups of rgroup row-block pairs walked column by column: the group's
+    // rows of A stay in L2 while each column block of B is read once per group.
+    const int G = a.rgroup;
     const int nP = a.nI / 2;
     const int per = G * a.nJ;
     const int g = u / per;
@@ -1010,6 +1012,11 @@ static bool build_phase(TcPhase& ph, const TcGemmDesc& d, const EpiParams& epi, 
     ph.seg_lo = (1 << 1) | (1 << 2);
   }
   ph.pair_scale = d.split == 5 ? 1 : 0;
+  // A rectangular product walks its tiles column by column within groups of
+  // row-block pairs, so that a group's rows of A (rgroup * 256 rows x K) stay
+  // in L2 while every column block of B is fetched once per group: as many
+  // pairs as keep that panel within 32 MiB of the 126 MiB L2, at least 4.
+  ph.rgroup = std::min(std::max(ph.nI / 2, 1), std::max(4, static_cast<int>((32LL << 20) / (512LL * d.K))));
   ph.diag_kb = d.diag ? kDiagDim / C::BK : 0;
   ph.a_sym = d.a_sym;
   ph.b_sym = d.b_mn ? 0 : d.b_sym;

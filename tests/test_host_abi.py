@@ -90,6 +90,20 @@ def test_schedule_choice(lib):
     assert m.resolve_schedule(1024, 2048, steps=10, dtype=torch.float32, schedule="gram_r2") == "gram_r2"
 
 
+def test_launch_mode_flags(lib):
+    import newton_schulz_04_gb300 as m
+    assert m.sched_code("gram_r2+shared") == 6 | 0x100
+    assert m.sched_code("orig+separate") == 3 | 0x200
+    assert m.resolve_schedule(4096, 14336, schedule="orig+separate") == "orig"
+    assert m.workspace_bytes([(512, 2048)] * 3, schedule="gram_r2+shared") == m.workspace_bytes([(512, 2048)] * 3)
+    big = 1 << 40
+    # both flags at once, or an unknown flag, are argument errors
+    assert _ns_call(lib, X=big, out=2 * big, sc=6 | 0x300) == 1
+    assert _ns_call(lib, X=big, out=2 * big, sc=6 | 0x400) == 1
+    with pytest.raises(ValueError):
+        m.sched_code("orig+sideways")
+
+
 def test_gram_r2_work_against_orig(lib):
     """The segment plan's tensor-core work as AUTO counts it: per segment of k
     steps S^2 L (SYRK) + (4k - 3) S^3 + 2 S^2 L; ORIG is k = 1 throughout."""
