@@ -572,9 +572,12 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     const double esz = fp32 ? 4.0 : 2.0;
     const double pbytes = el * (esz + (cx.has_mom ? 8.0 : 0.0) + (pa.Xf ? 4.0 : 0.0) + (pa.Xh ? 2.0 : 0.0) +
                                 (pa.Xl ? 2.0 : 0.0));
-    ProfScope ps("pack", 0.0, pbytes * Bc, cx.st);
-    CK(launch_pack(pa, q, cx.st));
+    {
+      ProfScope ps("pack", 0.0, pbytes * q, cx.st);
+      CK(launch_pack(pa, q, cx.st));
+    }
     if (q < Bc) {
+      ProfScope ps("pack", 0.0, pbytes * (Bc - q), cx.st);
       PackArgs pb = pa;
       pb.m = mats[q].m;
       pb.n = mats[q].n;

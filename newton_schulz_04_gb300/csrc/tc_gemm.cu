@@ -153,7 +153,8 @@ struct TcPhase {
   int bmn;        // 1: B is MN-major ([K, N] row-major), 0: K-major ([N, K])
   int seg_lo;     // bit 2s: segment s reads A's residual map; bit 2s+1: B's residual map
   int diag_kb;    // k-blocks of the diagonal segment (0, or 256 / BK: D times B's residual rows)
-  int final_vec;  // final mode may use 16-byte accesses to the caller's rows
+  int final_vec;    // final mode may use 16-byte accesses to the caller's rows (matrices stored as packed)
+  int final_vec_t;  // the same for matrices stored transposed (rows of length rows_valid)
   int f16;        // operands are fp16 (else bf16)
   int pair_scale; // 1: the last segment's first MMA scales the accumulator by 2^-11 (split 5)
   int rgroup;     // rectangular products: row-block pairs per column-major group of tiles
@@ -334,6 +335,49 @@ __device__ __forceinline__ void final_block_rows(const EpiCore& e, const EpiFina
   for (int it = 0; it < PIECES; ++it) {
     const int row = it * ROWS_PER + lane / PIECES, pc = lane % PIECES;
     *reinterpret_cast<uint4*>(dst + (r0 + row) * cols + c0 + pc * EPP) =
+        *reinterpret_cast<const uint4*>(box + row * STRIDE + pc * 16);
+  }
+  __syncwarp();
+}
+
+// Final write of a full 32 x CH block to a caller's bf16 matrix stored
+// transposed (dst[b] is [cols_valid, rows_valid]): the block is CH rows of dst
+// (packed columns c0 ..) by 32 columns (packed rows r0 .., one per lane).
+// Rows of dst are read and written 16 bytes at a time through the warp's box
+// (CH rows of 64 bytes, 16 bytes of padding each); in between, lane t updates
+// column t of the box, 2 bytes per row (lanes t and t + 1 share a 4-byte word,
+// so a warp's accesses fall in 16 distinct banks).
+template <int CH>
+__device__ __forceinline__ void final_block_cols(const EpiCore& e, const EpiFinal& f, int b, int r0, int c0,
+                                                 int lane, const float (&v)[CH], uint8_t* box) {
+  constexpr int STRIDE = 32 * 2 + 16;         // one dst row of the block: 32 bf16 values, padded
+  constexpr int PIECES = CH * 4;              // 16-byte pieces of the block (4 per row)
+  static_assert(PIECES % 32 == 0 && CH * STRIDE <= 32 * (2 * CH + 16), "block fits the warp's box");
+  const long long ldd = e.rows_valid;         // dst row length
+  uint16_t* dst = static_cast<uint16_t*>(f.dst[b]);
+  const bool apply = e.final_mode == FINAL_APPLY;
+  if (apply) {
+#pragma unroll
+    for (int it = 0; it < PIECES / 32; ++it) {
+      const int k = it * 32 + lane, row = k >> 2, pc = k & 3;
+      *reinterpret_cast<uint4*>(box + row * STRIDE + pc * 16) =
+          *reinterpret_cast<const uint4*>(dst + (c0 + row) * ldd + r0 + pc * 8);
+    }
+    __syncwarp();
+  }
+#pragma unroll
+  for (int u = 0; u < CH; ++u) {
+    uint16_t* q = reinterpret_cast<uint16_t*>(box + u * STRIDE) + lane;
+    float w = v[u];
+    if (apply) w = __uint_as_float(static_cast<uint32_t>(*q) << 16) - e.lr * v[u];
+    const bf16 h = __float2bfloat16_rn(w);
+    *q = *reinterpret_cast<const uint16_t*>(&h);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < PIECES / 32; ++it) {
+    const int k = it * 32 + lane, row = k >> 2, pc = k & 3;
+    *reinterpret_cast<uint4*>(dst + (c0 + row) * ldd + r0 + pc * 8) =
         *reinterpret_cast<const uint4*>(box + row * STRIDE + pc * 16);
   }
   __syncwarp();
@@ -716,15 +760,24 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) tc_gemm_kernel(const __grid
       const float sc = epi_scale(e, b);
       const float ka = sc * e.c_acc, kr = sc * e.c_res * e.r_scale;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + abuf * C::BN;
-      constexpr int MAXIT = (C::NCHT + C::WPQ - 1) / C::WPQ;  // chunks of the busiest warp of a quarter
+      constexpr int MAXIT = C::NCHT / C::WPQ;  // chunks of each warp of a quarter
+      static_assert(C::NCHT % C::WPQ == 0 && CH == 32, "every warp takes the same number of 32-column chunks");
+      // The TMEM load of chunk i + 1 is issued once chunk i's values are in
+      // their output form, so it runs while chunk i is stored (one buffer of
+      // registers: two would not fit this kernel's 168 per thread)
+      uint32_t tb[CH];
+      tmem_ld_32x32b_x32_issue(tbase + jq * CH, tb);
 #pragma unroll
       for (int i = 0; i < MAXIT; ++i) {
         const int cc = jq + i * C::WPQ;
-        if (cc >= C::NCHT) break;
         const int c0 = cb + cc * CH;
+        const bool more = i + 1 < MAXIT;
+        const uint32_t tnext = tbase + (cc + C::WPQ) * CH;
         __syncwarp();
+        tmem_ld_wait_x32(tb);
         float v[CH];
-        tmem_ld_rows(tbase + cc * CH, v);
+#pragma unroll
+        for (int u = 0; u < CH; ++u) v[u] = __uint_as_float(tb[u]);
         uint32_t rhw[CH / 2], rlw[CH / 2];
         if (has_r) to_rows(nh, rhw);
         if (has_rl) {
@@ -768,13 +821,19 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) tc_gemm_kernel(const __grid
           const bool full_block = r0 + 32 <= e.rows_valid && c0 + CH <= e.cols_valid;
           if (!f.tr[b] && !e.dst_fp32 && phs.final_vec && full_block) {
             final_block_rows<bf16, CH>(e, f, b, r0, c0, lane, v, box);
+          } else if (f.tr[b] && !e.dst_fp32 && phs.final_vec_t && full_block) {
+            final_block_cols<CH>(e, f, b, r0, c0, lane, v, box);
           } else {
 #pragma unroll
             for (int u = 0; u < CH; ++u) epi_final_elem(e, f, b, r, c0 + u, v[u]);
           }
+          __syncwarp();  // tcgen05.ld is warp-aligned: reconverge after the per-lane branches
+          if (more) tmem_ld_32x32b_x32_issue(tnext, tb);
         } else {
           uint32_t hw[CH / 2], lw[CH / 2];
           split_words<CH>(v, hw, lw, has_lo, e.o_f16 != 0, e.lo_scale);
+          __syncwarp();  // tcgen05.ld is warp-aligned: reconverge after the per-lane branches
+          if (more) tmem_ld_32x32b_x32_issue(tnext, tb);
           const long long off = static_cast<long long>(b) * e.bs + static_cast<long long>(r0) * e.ld + c0;
           store_block16<CH>(static_cast<uint16_t*>(e.Oh) + off, e.ld, lane, hw, box);
           if (has_lo) store_block16<CH>(static_cast<uint16_t*>(e.Ol) + off, e.ld, lane, lw, box);
@@ -1028,11 +1087,13 @@ static bool build_phase(TcPhase& ph, const TcGemmDesc& d, const EpiParams& epi, 
   ph.epi.sym = d.sym;
   // 16-byte row accesses to the caller's matrices in final mode need aligned rows
   ph.final_vec = 1;
+  ph.final_vec_t = 1;
   if (epi.final_mode != FINAL_NONE) {
     const int esz = epi.dst_fp32 ? 4 : 2;
     if ((static_cast<long long>(epi.cols_valid) * esz) % 16) ph.final_vec = 0;
+    if ((static_cast<long long>(epi.rows_valid) * esz) % 16) ph.final_vec_t = 0;
     for (int q = 0; q < d.B; ++q)
-      if (reinterpret_cast<uintptr_t>(epi.dst[q]) % 16) ph.final_vec = 0;
+      if (reinterpret_cast<uintptr_t>(epi.dst[q]) % 16) ph.final_vec = ph.final_vec_t = 0;
   }
   return true;
 }
