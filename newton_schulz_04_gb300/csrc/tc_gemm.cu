@@ -520,6 +520,8 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) tc_gemm_kernel(const __grid
         const int nks = nk * phs.nseg;        // k-blocks of the segments over K
         const int nkb = nks + phs.diag_kb;    // k-blocks of this tile
         const CUtensorMap* tm = phs.tm;
+        // the phase's flags, read once per tile from the kernel-parameter block
+        const int seg_lo = phs.seg_lo, pa_sym = phs.a_sym, pb_sym = phs.b_sym, pbmn = phs.bmn;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
@@ -548,12 +550,12 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) tc_gemm_kernel(const __grid
           }
           const int seg = kb / nk;
           const int k0 = (kb - seg * nk) * C::BK;
-          const bool alo = (phs.seg_lo >> (2 * seg)) & 1;
-          const bool blo = (phs.seg_lo >> (2 * seg + 1)) & 1;
+          const bool alo = (seg_lo >> (2 * seg)) & 1;
+          const bool blo = (seg_lo >> (2 * seg + 1)) & 1;
           // k-blocks above the diagonal of a block-lower symmetric operand come
           // from the stored lower block, read transposed
-          const bool a_up = phs.a_sym && (k0 >> 8) > (m0 >> 8);
-          const bool b_up = !phs.bmn && phs.b_sym && (k0 >> 8) > (n0 >> 8);
+          const bool a_up = pa_sym && (k0 >> 8) > (m0 >> 8);
+          const bool b_up = !pbmn && pb_sym && (k0 >> 8) > (n0 >> 8);
           if (!a_up) {
 #pragma unroll
             for (int g = 0; g < C::KATOMS; ++g)
@@ -564,12 +566,12 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) tc_gemm_kernel(const __grid
               tma_load_3d_pair(&tm[alo ? kMapAtl : kMapAt], fbar, st + q * C::MN_BOX_BYTES, m0 + q * C::MN_ATOM,
                                k0, b);
           }
-          if (!phs.bmn && !b_up) {
+          if (!pbmn && !b_up) {
 #pragma unroll
             for (int g = 0; g < C::KATOMS; ++g)
               tma_load_3d_pair(&tm[blo ? kMapBl : kMapB], fbar, sb + g * C::KATOM_BYTES, k0 + g * C::KA, nb0, b);
           } else {
-            const CUtensorMap* mb = &tm[phs.bmn ? (blo ? kMapBl : kMapB) : (blo ? kMapBtl : kMapBt)];
+            const CUtensorMap* mb = &tm[pbmn ? (blo ? kMapBl : kMapB) : (blo ? kMapBtl : kMapBt)];
 #pragma unroll
             for (int q = 0; q < C::BNH / C::MN_ATOM; ++q)
               tma_load_3d_pair(mb, fbar, sb + q * C::MN_BOX_BYTES, nb0 + q * C::MN_ATOM, k0, b);
@@ -608,6 +610,9 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) tc_gemm_kernel(const __grid
         const int nk = phs.K / C::BK;
         const int nks = nk * phs.nseg;
         const int nkb = nks + phs.diag_kb;
+        // the phase's flags, read once per tile from the kernel-parameter block
+        const int pa_sym = phs.a_sym, pb_sym = phs.b_sym, pbmn = phs.bmn, pf16 = phs.f16;
+        const int pscale = phs.pair_scale;
         const int abuf = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1;
         if (*abort_flag || !mbar_wait(&tempty[abuf], aph ^ 1)) {
@@ -627,10 +632,10 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) tc_gemm_kernel(const __grid
           // the diagonal segment's A (D) is K-major and its B MN-major
           const bool dseg = kb >= nks;
           const int k0 = dseg ? 0 : (kb % nk) * C::BK;
-          const bool a_mn = !dseg && phs.a_sym && (k0 >> 8) > (m0 >> 8);
-          const bool b_mn = phs.bmn || (!dseg && phs.b_sym && (k0 >> 8) > (n0 >> 8));
+          const bool a_mn = !dseg && pa_sym && (k0 >> 8) > (m0 >> 8);
+          const bool b_mn = pbmn || (!dseg && pb_sym && (k0 >> 8) > (n0 >> 8));
           const uint32_t idesc =
-              make_idesc_f16kind(2 * C::BM, C::BN, b_mn, phs.f16 == 0) | (a_mn ? (1u << 15) : 0u);
+              make_idesc_f16kind(2 * C::BM, C::BN, b_mn, pf16 == 0) | (a_mn ? (1u << 15) : 0u);
           const uint32_t a0 = smem_u32(tiles + s * C::STAGE);
           const uint32_t b0 = a0 + C::A_TILE;
 #pragma unroll
@@ -641,7 +646,7 @@ __global__ void __launch_bounds__(TcCfg::THREADS, 1) tc_gemm_kernel(const __grid
                                      : make_sdesc(a0 + koff, 16, SBO, C::SWZ);
             const uint64_t bd = b_mn ? make_sdesc(b0 + kk * 16 * 128, C::MN_BOX_BYTES, SBO, C::SWZ)
                                      : make_sdesc(b0 + koff, 16, SBO, C::SWZ);
-            if (phs.pair_scale && kb == nks - nk && kk == 0)
+            if (pscale && kb == nks - nk && kk == 0)
               tc_mma_pair_scale_d<11>(d, ad, bd, idesc);  // hi*hi + (cross terms) * 2^-11
             else
               tc_mma_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
