@@ -76,8 +76,8 @@ typedef enum {
 
 typedef enum {
     MUON_SCHED_AUTO = 0,     /* cheapest schedule that meets the dtype's accuracy (see below) */
-    MUON_SCHED_GRAM_X3 = 1,  /* Gram space; symmetric products with split-bf16 operands (hi*hi + hi*lo + lo*hi) */
-    MUON_SCHED_GRAM_X1 = 2,  /* Gram space; plain bf16 operands (fast mode, larger error) */
+    MUON_SCHED_GRAM_X3 = 1,  /* Gram space without restarts; split-bf16 operands (hi*hi + hi*lo + lo*hi) */
+    MUON_SCHED_GRAM_X1 = 2,  /* Gram space without restarts; plain bf16 operands (diverges on rank-deficient inputs) */
     MUON_SCHED_ORIG = 3,     /* original space (bf16: step 0 in bf16, later steps on fp16 operands, see below) */
     MUON_SCHED_ORIG_BF16 = 4, /* original space on bf16 operands only; split A in A*A and B in B*X in the last max(2, steps - 3) steps */
     MUON_SCHED_ORIG_F16X3 = 5, /* original space; every operand an fp16 pair (~22 bits), three tensor-core products per product */
@@ -108,9 +108,14 @@ typedef enum {
  *  - ORIG_BF16.  bf16 operands throughout, with X carried as a bf16 pair (about
  *    16 bits).  A*A and B*X use split operands in the last max(2, steps - 3)
  *    steps (every step from the fourth on when there are more than five).
- *  - GRAM_X3 / GRAM_X1.  The Gram recurrence on bf16 pairs (split products)
- *    or on plain bf16.  Gram space squares the condition number, so on
- *    ill-conditioned inputs it misses the 2e-2 target that ORIG meets.
+ *  - GRAM_X3 / GRAM_X1.  The Gram recurrence for all steps, without restarts,
+ *    on bf16 pairs (split products) or on plain bf16: the pages' form, kept
+ *    for comparison.  Over several Gram steps the rounding of G (and the
+ *    symmetric storage of products that commute only up to rounding) is
+ *    amplified in the directions of small singular values.  Measured on
+ *    rank-8 + noise inputs at 5 steps: GRAM_X3 reaches 2.1e-2, and GRAM_X1
+ *    diverges (relative errors of 9 to 45).  On full-rank inputs GRAM_X3
+ *    stays at the bf16 output rounding (1.7e-3).  Use GRAM_R2 for Gram space.
  *  - GRAM_R2 (bf16; fp32 runs the same segments with FFMA).  Step 0 is ORIG's bf16 step; the remaining steps run in
  *    segments of two (a last single step when steps - 1 is odd).  A segment
  *    forms A = X_hi X_hi^T once, runs two steps of the Gram recurrence on it
@@ -140,8 +145,8 @@ typedef enum {
  * schedule).  By default the tensor-core products of a batch chunk share
  * persistent launches (up to 16 consecutive products per launch, ordered per
  * matrix by completion counters) when the chunk is small -- at most 16
- * 256 x 256 tile pairs per CTA pair in its largest product -- and run one
- * launch per product otherwise.  These flags force one of the two; the
+ * 256 x 256 tile pairs per CTA pair in its largest product, or at most 4 in
+ * its s x s products -- and run one launch per product otherwise.  These flags force one of the two; the
  * numerics are the same either way (every tile is computed identically).
  * Measured per shape by the binding's tune_schedules.
  */

@@ -522,11 +522,18 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
   // per cluster in the update) 287 -> 360 TFLOP/s, 8 x 1024 x 8192 (13.5)
   // 234 -> 270; the 512 small matrices of shapes 256 x 1024 .. 768 x 3072
   // (10 to 75 per cluster) 293 -> 286 when every bucket shares launches.
+  // Also when the s x s products alone are about a wave (at most 4 tile pairs
+  // per CTA pair, e.g. 8 x 1024 x 16384): each is then a short launch whose
+  // fill and drain dominate, and the SYRK's last partial wave leaves most of
+  // the GPU idle; sharing launches overlaps them across matrices.  Measured on
+  // 8 x 1024 x 16384: 1.95 -> 1.77 ms per step.
   const long long pairs_rect = static_cast<long long>(Bc) * (g.sp / 256) * (g.lp / 256);
+  const long long nbs = g.sp / 256;
+  const long long pairs_sym = static_cast<long long>(Bc) * nbs * (nbs + 1) / 2;
   const bool pairs = cx.steps > 0 && pair_sched(g.sc);  // fp16-pair operands (either dtype)
   const bool tensor = cx.dt == MUON_BF16 || pairs;       // the NS products run on the tensor cores
-  const bool chain = tensor && (g.launch == MUON_SCHED_SHARED_LAUNCH ||
-                                (g.launch == 0 && pairs_rect <= 16LL * (cx.sms / 2)));
+  const bool small = pairs_rect <= 16LL * (cx.sms / 2) || pairs_sym <= 4LL * (cx.sms / 2);
+  const bool chain = tensor && (g.launch == MUON_SCHED_SHARED_LAUNCH || (g.launch == 0 && small));
   // stream-ordered: runs after everything before this chunk, before its pack
   if (chain) CK(cudaMemsetAsync(bf.done, 0, sizeof(int) * Bc, cx.st));
   if (tensor && cx.steps > 0) CK(cudaMemsetAsync(bf.tile_ctr, 0, sizeof(int) * kMaxTcLaunches, cx.st));
