@@ -618,3 +618,61 @@ def test_more_products_than_one_shared_launch(sched, steps, coeffs):
     for i in range(3):
         e = rel(O[i].float().cpu(), oracle_O(X[i], steps, coeffs or oracle.QUINTIC))
         assert e < TOL_BF16, (sched, steps, i, e)
+
+
+def test_longest_side_at_the_maximum():
+    """The largest accepted dimension (65536) as the long side, in both
+    orientations, through muon_step with the default schedule (the restarted
+    Gram recurrence at this aspect); W checked elementwise against
+    W0 - lr O_gpu and O_gpu against the oracle on each matrix."""
+    m = _m()
+    shapes = [(256, 65536), (65536, 256)]
+    Gs = [synth.random_matrix(a, b, seed=2700 + i).to(torch.bfloat16) for i, (a, b) in enumerate(shapes)]
+    Ws = [synth.random_matrix(a, b, seed=2800 + i, std=0.02).to(torch.bfloat16) for i, (a, b) in enumerate(shapes)]
+    W = [w.cuda() for w in Ws]
+    G = [g.cuda() for g in Gs]
+    M = [torch.zeros(g.shape, dtype=torch.float32, device="cuda") for g in Gs]
+    assert m.resolve_schedule(256, 65536) == "gram_r2"
+    m.muon_step(W, G, M, beta=0.95, lr=0.02, steps=5)
+    torch.cuda.synchronize()
+    for i in range(2):
+        O_gpu = m.ns_batched(G[i][None], steps=5)[0].double().cpu().numpy()
+        e = rel(O_gpu, oracle_O(Gs[i]))
+        assert e < TOL_BF16, (i, e)
+        _check_apply(Ws[i].double().numpy(), W[i].cpu().double().numpy(), O_gpu, 0.02, torch.bfloat16)
+
+
+def test_transposed_apply_with_unaligned_rows():
+    """A matrix stored transposed to its packed form whose rows (the short
+    side, 130 bf16 values = 260 bytes) are not 16-byte multiples takes the
+    per-element final path; its neighbour with aligned rows (the block path)
+    runs in the same call."""
+    _check_step([(1000, 130), (600, 200)], seed=31)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_pair_schedule_falls_back_outside_the_fp16_range(dtype):
+    """Coefficients whose polynomial leaves [-1.25, 1.25] on [0, 1.25] (the
+    quintic scaled by 1.05) cannot run on fp16 pairs: ORIG_F16X3 then runs
+    the bf16 split schedule (bf16 data) or FFMA original space (fp32 data),
+    bit for bit."""
+    m = _m()
+    co = tuple(1.05 * c for c in oracle.QUINTIC)
+    X = torch.stack([synth.random_matrix(256, 512, seed=2900 + i) for i in range(2)]).to(dtype).cuda()
+    a = m.ns_batched(X, steps=5, coeffs=co, schedule="orig_f16x3")
+    b = m.ns_batched(X, steps=5, coeffs=co, schedule="orig_bf16" if dtype == torch.bfloat16 else "orig")
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("steps", [4, 6])
+def test_restarted_gram_plans_with_a_final_single_step(steps):
+    """GRAM_R2 splits T steps as 1, 2, 2, ..., with a last single step when
+    T - 1 is odd (4 steps: 1, 2, 1; 6 steps: 1, 2, 2, 1)."""
+    m = _m()
+    X = torch.stack([synth.random_matrix(256, 1024, seed=2950 + i) for i in range(2)]).to(torch.bfloat16).cuda()
+    O = m.ns_batched(X, steps=steps, schedule="gram_r2")
+    torch.cuda.synchronize()
+    for i in range(2):
+        e = rel(O[i].float().cpu(), oracle_O(X[i], steps))
+        assert e < 1.2e-2, (steps, i, e)
