@@ -493,7 +493,10 @@ def run_ours(args, world, rank, local):
     else:
         cpu_work = None
     t_tune = time.perf_counter()
-    upd = pkg.MuonUpdater(W, work.beta, work.lr, work.steps, work.coeffs, args.schedule, use_graph=not args.no_graph)
+    # largest groups first: the end-to-end pass copies each group's weights out
+    # while the groups after it compute
+    upd = pkg.MuonUpdater(W, work.beta, work.lr, work.steps, work.coeffs, args.schedule, use_graph=not args.no_graph,
+                          group_order="largest_first")
     t_tune = time.perf_counter() - t_tune
     Mo = upd.moms
     flops_step = work.flop_count()
@@ -598,18 +601,23 @@ def run_ours(args, world, rank, local):
     # ---- end to end through the C ABI with host buffers (pinned).  Every step
     # copies its gradients in from pinned host memory and the updated weights
     # back out.  The copy of step k+1's gradients runs on a second stream into
-    # the other of two device gradient buffers while step k computes; W's copy
-    # out follows its step on the compute stream.
+    # the other of two device gradient buffers while step k computes.  Each
+    # shape group's weights are copied out on a third stream as soon as that
+    # group's update is done, while the groups after it compute; the group's
+    # next update waits for that copy.
     Gh = [g.to("cpu").pin_memory() for g in G]
     Wh = [torch.empty(w.shape, dtype=w.dtype).pin_memory() for w in W]
     h2d = sum(g.numel() * g.element_size() for g in Gh)
     d2h = sum(w.numel() * w.element_size() for w in Wh)
     Gsets = [G, [g.clone() for g in G]]
     cs = torch.cuda.Stream(dev)
+    cs_out = torch.cuda.Stream(dev)
+    ngroups = len(upd.groups)
 
     def e2e_run(k):
         ev_in = [torch.cuda.Event(), torch.cuda.Event()]
         ev_used = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_out = [torch.cuda.Event() for _ in range(ngroups)]  # group g's weights are copied out
 
         def copy_in(i):
             with torch.cuda.stream(cs):
@@ -618,6 +626,18 @@ def run_ours(args, world, rank, local):
                     g.copy_(gh, non_blocking=True)
                 ev_in[i].record(cs)
 
+        def before_group(gi, idx, s):
+            s.wait_event(ev_out[gi])  # the previous copy of these weights has left
+
+        def after_group(gi, idx, s):
+            done = torch.cuda.Event()
+            done.record(s)
+            with torch.cuda.stream(cs_out):
+                cs_out.wait_event(done)
+                for q in idx:
+                    Wh[q].copy_(W[q], non_blocking=True)
+                ev_out[gi].record(cs_out)
+
         if flush is not None:
             flush.zero_()
         torch.cuda.synchronize()
@@ -625,6 +645,8 @@ def run_ours(args, world, rank, local):
         a.record(st)
         for i in (0, 1):
             ev_used[i].record(st)
+        for e in ev_out:
+            e.record(st)
         copy_in(0)
         for s_ in range(k):
             i = s_ % 2
@@ -632,12 +654,12 @@ def run_ours(args, world, rank, local):
                 copy_in(1 - i)
             st.wait_event(ev_in[i])
             if args.no_graph:
-                upd._eager(Gsets[i], st)
+                upd._eager(Gsets[i], st, before_group, after_group)
             else:
-                upd.step(Gsets[i])
-            for w, wh in zip(W, Wh):
-                wh.copy_(w, non_blocking=True)
+                upd.step(Gsets[i], st, before_group, after_group)
             ev_used[i].record(st)
+        for e in ev_out:  # the last step's weights are all on the host
+            st.wait_event(e)
         b.record(st)
         torch.cuda.synchronize()
         return a.elapsed_time(b)
@@ -671,7 +693,9 @@ def run_ours(args, world, rank, local):
         "roofline": roof,
         "kernels": kernels,
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipelining": "step k+1's gradient copy-in overlaps step k on a second stream",
+                "pipelining": "step k+1's gradient copy-in overlaps step k on a second stream; each shape group's "
+                              "weights are copied out on a third stream while the later groups compute (largest "
+                              "groups first)",
                 "ms_per_step": 1e3 * e2e_t / args.steps},
         "clocks": clocks,
         "peaks": pk,

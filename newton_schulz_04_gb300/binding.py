@@ -514,20 +514,25 @@ class MuonUpdater:
     """Owner-side Muon step over a fixed list of 2-D parameters.
 
     Holds the fp32 momentum buffers and one caller-side workspace sized for the
-    parameter shapes; `step(grads)` calls the C ABI once.  With
-    `schedule="tuned"` each shape group runs the schedule that measured fastest
-    for it (tune_schedules, at construction; `tune_cache` is passed through),
-    one C-ABI call per group, in the library's group order.  With
-    `use_graph=True` the first step with a given set of gradient tensors runs
-    eagerly and is captured into a CUDA graph; later steps with the same
-    tensors replay it (one launch of the whole kernel sequence).  Graphs are
-    kept for up to `max_graphs` sets of gradient tensors (e.g. two buffers
-    that alternate while the next step's gradients are copied in).
+    parameter shapes.  `step(grads)` makes one C-ABI call per shape group (the
+    library's bucket grouping); the groups are independent, so their order
+    does not change any result.  `group_order="largest_first"` runs the groups
+    with the most parameter bytes first, which lets a caller that copies each
+    group's weights out (the `after_group` hook of `step`) overlap those copies
+    with the groups that follow.  With `schedule="tuned"` each group runs the
+    schedule that measured fastest for it (tune_schedules, at construction;
+    `tune_cache` is passed through).  With `use_graph=True` the first step
+    with a given set of gradient tensors runs eagerly and is captured, one
+    CUDA graph per group; later steps with the same tensors replay them.
+    Graphs are kept for up to `max_graphs` sets of gradient tensors (e.g. two
+    buffers that alternate while the next step's gradients are copied in).
     """
 
     def __init__(self, params: Sequence[torch.Tensor], beta=0.95, lr=0.02, steps=5, coeffs=None,
                  schedule="auto", workspace_limit: int | None = None, use_graph: bool = False, max_graphs: int = 4,
-                 tune_cache=None):
+                 tune_cache=None, group_order: str = "library"):
+        if group_order not in ("library", "largest_first"):
+            raise ValueError("group_order is 'library' or 'largest_first'")
         self.params = list(params)
         self.beta, self.lr, self.steps, self.coeffs, self.schedule = beta, lr, steps, coeffs, schedule
         self.moms = [torch.zeros(p.shape, dtype=torch.float32, device=p.device) for p in self.params]
@@ -535,55 +540,78 @@ class MuonUpdater:
         dtype = self.params[0].dtype
         if schedule == "tuned":
             self.chosen = tune_schedules(shapes, steps, dtype, cache=tune_cache, device=self.params[0].device)
-            order, start = bucket_plan(shapes)
-            self._groups = []
-            for k in range(len(start) - 1):
-                idx = order[start[k]:start[k + 1]]
-                s_, l_ = min(shapes[idx[0]]), max(shapes[idx[0]])
-                self._groups.append((idx, self.chosen[(s_, l_)]))
-            need = max(workspace_bytes([shapes[i] for i in idx], steps, dtype, sc) for idx, sc in self._groups)
         else:
             self.chosen = {(min(sh), max(sh)): resolve_schedule(sh[0], sh[1], steps, dtype, schedule) for sh in shapes}
-            self._groups = None
-            need = workspace_bytes(shapes, steps, dtype, schedule)
+        order, start = bucket_plan(shapes)
+        self._groups = []
+        for k in range(len(start) - 1):
+            idx = order[start[k]:start[k + 1]]
+            s_, l_ = min(shapes[idx[0]]), max(shapes[idx[0]])
+            self._groups.append((idx, self.chosen[(s_, l_)] if schedule == "tuned" else schedule))
+        if group_order == "largest_first":
+            nbytes = [sum(self.params[i].numel() * self.params[i].element_size() for i in idx) for idx, _ in self._groups]
+            self._groups = [g for _, g in sorted(zip(nbytes, self._groups), key=lambda t: -t[0])]
+        need = max((workspace_bytes([shapes[i] for i in idx], steps, dtype, sc) for idx, sc in self._groups), default=0)
         if workspace_limit is not None:
             need = min(need, int(workspace_limit))
         self.workspace = new_workspace(need, self.params[0].device)
         self.use_graph = use_graph
         self.max_graphs = max_graphs
-        self._graphs = {}  # tuple of gradient data pointers -> CUDAGraph
+        self._graphs = {}  # tuple of gradient data pointers -> one CUDAGraph per group
 
-    def _eager(self, grads, stream=None):
-        if self._groups is None:
-            muon_step(self.params, grads, self.moms, self.beta, self.lr, self.steps, self.coeffs, self.schedule,
-                      self.workspace, stream)
-            return
-        for idx, sc in self._groups:
-            muon_step([self.params[i] for i in idx], [grads[i] for i in idx], [self.moms[i] for i in idx], self.beta,
-                      self.lr, self.steps, self.coeffs, sc, self.workspace, stream)
+    @property
+    def groups(self):
+        """The shape groups in the order `step` runs them: (parameter indices, schedule)."""
+        return [(list(idx), sc) for idx, sc in self._groups]
 
-    def step(self, grads: Sequence[torch.Tensor], stream=None):
-        """One step on `stream` (the current stream if None)."""
+    def _run_group(self, gi, grads, stream):
+        idx, sc = self._groups[gi]
+        muon_step([self.params[i] for i in idx], [grads[i] for i in idx], [self.moms[i] for i in idx], self.beta,
+                  self.lr, self.steps, self.coeffs, sc, self.workspace, stream)
+
+    def _eager(self, grads, stream=None, before_group=None, after_group=None):
+        st = stream if stream is not None else torch.cuda.current_stream()
+        for gi, (idx, _) in enumerate(self._groups):
+            if before_group is not None:
+                before_group(gi, idx, st)
+            self._run_group(gi, grads, st)
+            if after_group is not None:
+                after_group(gi, idx, st)
+
+    def step(self, grads: Sequence[torch.Tensor], stream=None, before_group=None, after_group=None):
+        """One step on `stream` (the current stream if None).
+
+        `before_group(gi, indices, stream)` and `after_group(gi, indices,
+        stream)`, if given, are called on the host just before and just after
+        group `gi`'s work is enqueued on the stream, e.g. to make the stream
+        wait for an earlier copy of those weights, or to record an event and
+        start copying them out."""
         if not self.use_graph:
-            self._eager(grads, stream)
+            self._eager(grads, stream, before_group, after_group)
             return
         key = tuple(g.data_ptr() for g in grads)
-        graph = self._graphs.get(key)
-        if graph is not None:
-            if stream is None:
-                graph.replay()
-            else:
-                with torch.cuda.stream(stream):
-                    graph.replay()
+        graphs = self._graphs.get(key)
+        if graphs is not None:
+            st = stream if stream is not None else torch.cuda.current_stream()
+            with torch.cuda.stream(st):
+                for gi, (idx, _) in enumerate(self._groups):
+                    if before_group is not None:
+                        before_group(gi, idx, st)
+                    graphs[gi].replay()
+                    if after_group is not None:
+                        after_group(gi, idx, st)
             return
         # this call's update runs eagerly (and sets up per-device state); the same
-        # launch sequence is then captured for the following calls
-        self._eager(grads, stream)
+        # launch sequence is then captured, group by group, for the following calls
+        self._eager(grads, stream, before_group, after_group)
         (stream if stream is not None else torch.cuda.current_stream()).synchronize()
-        graph = torch.cuda.CUDAGraph()
+        graphs = []
         side = torch.cuda.Stream()
-        with torch.cuda.graph(graph, stream=side):
-            self._eager(grads, side)
+        for gi in range(len(self._groups)):
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                self._run_group(gi, grads, side)
+            graphs.append(graph)
         if len(self._graphs) >= self.max_graphs:
             self._graphs.pop(next(iter(self._graphs)))
-        self._graphs[key] = graph
+        self._graphs[key] = graphs

@@ -585,6 +585,56 @@ def test_updater_graphs_for_alternating_gradient_buffers():
         assert torch.equal(a, b)
 
 
+def test_updater_group_order_and_hooks():
+    """Running the shape groups largest first, with a per-group copy-out of the
+    weights on another stream (the end-to-end pattern), gives the same weights
+    and momentum, bit for bit, as the library order without hooks; the hooks
+    see every group once, in the order the updater reports."""
+    m = _m()
+    shapes = [(256, 512), (1024, 256), (256, 768), (512, 256), (256, 1024)]
+    W0 = [synth.random_matrix(a, b, seed=900 + i, std=0.02).to(torch.bfloat16) for i, (a, b) in enumerate(shapes)]
+    Gs = [[synth.random_matrix(a, b, seed=950 + 10 * k + i).to(torch.bfloat16).cuda() for i, (a, b) in enumerate(shapes)]
+          for k in range(2)]
+    Wa = [w.clone().cuda() for w in W0]
+    Wb = [w.clone().cuda() for w in W0]
+    upd = m.MuonUpdater(Wa, 0.95, 0.02, 5, use_graph=True, group_order="largest_first")
+    ref = m.MuonUpdater(Wb, 0.95, 0.02, 5, use_graph=False)
+    sizes = [sum(shapes[i][0] * shapes[i][1] for i in idx) for idx, _ in upd.groups]
+    assert sizes == sorted(sizes, reverse=True)
+    assert sorted(i for idx, _ in upd.groups for i in idx) == list(range(len(shapes)))
+    host = [torch.empty(w.shape, dtype=w.dtype).pin_memory() for w in Wa]
+    out = torch.cuda.Stream()
+    copied = [torch.cuda.Event() for _ in upd.groups]
+    for e in copied:
+        e.record()
+    seen = []
+
+    def before(gi, idx, st):
+        st.wait_event(copied[gi])  # the previous copy of these weights has left
+
+    def after(gi, idx, st):
+        seen.append((gi, list(idx)))
+        ev = torch.cuda.Event()
+        ev.record(st)
+        with torch.cuda.stream(out):
+            out.wait_event(ev)
+            for q in idx:
+                host[q].copy_(Wa[q], non_blocking=True)
+            copied[gi].record(out)
+
+    for k in range(3):
+        upd.step(Gs[k % 2], before_group=before, after_group=after)
+        ref.step(Gs[k % 2])
+    torch.cuda.synchronize()
+    assert seen[:len(upd.groups)] == [(gi, idx) for gi, (idx, _) in enumerate(upd.groups)]
+    assert len(seen) == 3 * len(upd.groups)
+    for a, b, h in zip(Wa, Wb, host):
+        assert torch.equal(a, b)
+        assert torch.equal(h, a.cpu())
+    for a, b in zip(upd.moms, ref.moms):
+        assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("sched,dtype", [("orig", torch.bfloat16), ("gram_x3", torch.bfloat16),
                                          ("gram_r2", torch.bfloat16), ("orig", torch.float32),
                                          ("gram_x3", torch.float32), ("orig_f16x3", torch.float32),

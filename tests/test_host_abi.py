@@ -198,3 +198,21 @@ def test_debug_gemm_diagonal_segment_argument_errors(lib):
     assert "workspace" in lib.muon_last_error().decode()
     assert _gemm_call(lib, split=5) == E["arg"]
     assert _gemm_call(lib, M=200, K=200) == E["shape"]   # tiles pair 256 rows
+
+
+def test_updater_groups_on_the_host(lib):
+    """The updater's groups are the library's bucket grouping; largest_first
+    orders them by parameter bytes (stable for ties), and an unknown order is
+    an argument error.  Built on CPU tensors: nothing here launches."""
+    import newton_schulz_04_gb300 as m
+    shapes = [(64, 128), (512, 1024), (128, 64), (256, 256), (1024, 512), (64, 64)]
+    params = [torch.zeros(s, dtype=torch.bfloat16) for s in shapes]
+    lib_order = m.MuonUpdater(params, use_graph=False)
+    order, start = m.bucket_plan(shapes)
+    assert [idx for idx, _ in lib_order.groups] == [order[start[k]:start[k + 1]] for k in range(len(start) - 1)]
+    big = m.MuonUpdater(params, use_graph=False, group_order="largest_first")
+    nbytes = [sum(shapes[i][0] * shapes[i][1] for i in idx) for idx, _ in big.groups]
+    assert nbytes == sorted(nbytes, reverse=True)
+    assert sorted(map(tuple, (idx for idx, _ in big.groups))) == sorted(map(tuple, (idx for idx, _ in lib_order.groups)))
+    with pytest.raises(ValueError):
+        m.MuonUpdater(params, group_order="smallest_first")
