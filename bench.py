@@ -394,6 +394,27 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
+def host_copy_gbs(dev, nbytes=1 << 30):
+    """This box's pinned host <-> device copy rates (GB/s, best of 3 single
+    copies of 1 GiB, each direction alone): the end-to-end figure is bound by
+    them when a step's copies take longer than its compute."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, fn in (("h2d", lambda: d.copy_(h, non_blocking=True)), ("d2h", lambda: h.copy_(d, non_blocking=True))):
+        best = float("inf")
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            best = min(best, a.elapsed_time(b) / 1e3)
+        out[name] = nbytes / best / 1e9
+    del h, d
+    return out
+
+
 def cpu_baseline(work, budget_s=15.0, max_mats=None, start=0, of=None):
     """The fp64 oracle, as it stands, on a bounded sample of the workload
     (matrices from index `start` on, cyclically; `of` describes the whole
@@ -613,6 +634,7 @@ def run_ours(args, world, rank, local):
     cs = torch.cuda.Stream(dev)
     cs_out = torch.cuda.Stream(dev)
     ngroups = len(upd.groups)
+    link = host_copy_gbs(dev)
 
     def e2e_run(k):
         ev_in = [torch.cuda.Event(), torch.cuda.Event()]
@@ -696,7 +718,8 @@ def run_ours(args, world, rank, local):
                 "pipelining": "step k+1's gradient copy-in overlaps step k on a second stream; each shape group's "
                               "weights are copied out on a third stream while the later groups compute (largest "
                               "groups first)",
-                "ms_per_step": 1e3 * e2e_t / args.steps},
+                "ms_per_step": 1e3 * e2e_t / args.steps,
+                "host_copy_gbs": link},
         "clocks": clocks,
         "peaks": pk,
     }
