@@ -622,9 +622,13 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
                             cx.sms, cx.st));
   }
   if (fp32 && !pairs) {
+    // Every operand here but the SYRK's X is symmetric and stored in full (the
+    // symmetric products mirror their lower tiles), so it is read MN-major
+    // (`sym_ops`): both operands then go straight into shared memory.
     auto simt = [&](const float* A, long long lda, long long bsa, const float* Bm, long long ldb, long long bsb,
-                    int M, int N, int K, int sym, int b_mn, const EpiParams& e) {
-      SimtGemmDesc d{Bc, M, N, K, sym, b_mn, A, lda, bsa, Bm, ldb, bsb};
+                    int M, int N, int K, int sym, int b_mn, const EpiParams& e, bool sym_ops = false) {
+      SimtGemmDesc d{Bc, M, N, K, sym, sym_ops ? 1 : b_mn, A, lda, bsa, Bm, ldb, bsb};
+      d.a_mn = sym_ops ? 1 : 0;
       const double Kt = K == S ? static_cast<double>(g.s) : static_cast<double>(g.l);
       const double fl = sym ? Bc * static_cast<double>(g.s) * g.s * Kt : 2.0 * Bc * g.s * g.l * Kt;
       ProfScope ps(sym ? "simt_sym" : "simt_rect", fl, 0.0, cx.st);
@@ -646,25 +650,25 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
         const float* Qp = bf.Bf;
         if (k == 1) {
           EpiParams e2 = epi_packed(g, bf, 0, cx.c, cx.b, 0.f, bf.Af, bf.Bf, sp, bss);
-          CK(simt(bf.Af, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, e2));
+          CK(simt(bf.Af, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, e2, true));
         } else {
           // A in Af -> P_0 in Bf, H in Hf, G_1 in Af, P_1 in Pf[0], Q' in Af
           EpiParams p0 = epi_packed(g, bf, 0, cx.c, cx.b, cx.a, bf.Af, bf.Bf, sp, bss);
-          CK(simt(bf.Af, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, p0));
+          CK(simt(bf.Af, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, p0, true));
           EpiParams eh = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Hf, sp, bss);
-          CK(simt(bf.Bf, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, eh));
+          CK(simt(bf.Bf, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, eh, true));
           EpiParams eg = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Af, sp, bss);
-          CK(simt(bf.Bf, sp, bss, bf.Hf, sp, bss, S, S, S, 1, 0, eg));
+          CK(simt(bf.Bf, sp, bss, bf.Hf, sp, bss, S, S, S, 1, 0, eg, true));
           EpiParams p1 = epi_packed(g, bf, 0, cx.c, cx.b, cx.a, bf.Af, bf.Pf[0], sp, bss);
-          CK(simt(bf.Af, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, p1));
+          CK(simt(bf.Af, sp, bss, bf.Af, sp, bss, S, S, S, 1, 0, p1, true));
           EpiParams eq = epi_packed(g, bf, 0, 1.f, 0.f, -cx.a * cx.a, nullptr, bf.Af, sp, bss);
-          CK(simt(bf.Pf[0], sp, bss, bf.Bf, sp, bss, S, S, S, 1, 0, eq));
+          CK(simt(bf.Pf[0], sp, bss, bf.Bf, sp, bss, S, S, S, 1, 0, eq, true));
           Qp = bf.Af;
         }
         EpiParams e3 = epi_packed(g, bf, first ? 1 : 0, 1.f, ipow(cx.a, k), 0.f, cur, nxt, lp, bsx);
         e3.cols_valid = static_cast<int>(g.l);
         if (last) epi_set_final(e3, cx, g, mats, Bc);
-        CK(simt(Qp, sp, bss, cur, lp, bsx, S, L, S, 0, 1, e3));
+        CK(simt(Qp, sp, bss, cur, lp, bsx, S, L, S, 0, 1, e3, true));
         std::swap(cur, nxt);
       }
       return MUON_OK;
@@ -677,26 +681,26 @@ static muon_status run_chunk(const Ctx& cx, const Group& g, const Mat* mats, int
     for (int k = 0; k < T; ++k) {
       float* P = bf.Pf[k & 1];
       EpiParams ep = epi_packed(g, bf, 0, cx.c, cx.b, cx.a, bf.Gf, P, sp, bss);
-      CK(simt(bf.Gf, sp, bss, bf.Gf, sp, bss, S, S, S, 1, 0, ep));
+      CK(simt(bf.Gf, sp, bss, bf.Gf, sp, bss, S, S, S, 1, 0, ep, true));
       if (k == 0) {
         Q = P;
       } else {
         float* Qn = bf.Qf[qi];
         qi ^= 1;
         EpiParams eq = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, Qn, sp, bss);
-        CK(simt(P, sp, bss, Q, sp, bss, S, S, S, 1, 0, eq));
+        CK(simt(P, sp, bss, Q, sp, bss, S, S, S, 1, 0, eq, true));
         Q = Qn;
       }
       if (k + 1 < T) {
         EpiParams eh = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Hf, sp, bss);
-        CK(simt(P, sp, bss, bf.Gf, sp, bss, S, S, S, 1, 0, eh));
+        CK(simt(P, sp, bss, bf.Gf, sp, bss, S, S, S, 1, 0, eh, true));
         EpiParams eg = epi_packed(g, bf, 0, 1.f, 0.f, 0.f, nullptr, bf.Gf, sp, bss);
-        CK(simt(P, sp, bss, bf.Hf, sp, bss, S, S, S, 1, 0, eg));
+        CK(simt(P, sp, bss, bf.Hf, sp, bss, S, S, S, 1, 0, eg, true));
       }
     }
     EpiParams ef = epi_packed(g, bf, 1, 1.f, 0.f, 0.f, nullptr, nullptr, lp, bsx);
     epi_set_final(ef, cx, g, mats, Bc);
-    CK(simt(Q, sp, bss, bf.Xf, lp, bsx, S, L, S, 0, 1, ef));
+    CK(simt(Q, sp, bss, bf.Xf, lp, bsx, S, L, S, 0, 1, ef, true));
     return MUON_OK;
   }
 

@@ -96,6 +96,11 @@ struct SimtGemmDesc {
   long long lda, bsa;
   const float* Bm;
   long long ldb, bsb;
+  // A given MN-major: element (m, k) at A[k * lda + m].  For a symmetric A
+  // stored in full this is the same buffer as K-major.  With a_mn and b_mn
+  // both set, the operand tiles are copied straight into shared memory
+  // (cp.async, three stages) instead of through registers.
+  int a_mn = 0;
 };
 cudaError_t launch_simt_gemm(const SimtGemmDesc& d, const EpiParams& epi, cudaStream_t st);
 

@@ -26,7 +26,8 @@ constexpr int SK = 16;   // k per smem stage
 
 // Two blocks per SM (at most 128 registers a thread): at 129 registers only one
 // block fitted, and 8 warps per SM hid the shared-memory latency poorly (8 x
-// 1024x4096 fp32, 10 steps: 24.7 ms per call with one block, 18.8 with two).
+// 1024x4096 fp32, 10 steps: 24.7 ms per call with one block, 18.8 with two,
+// 16.3 once the symmetric-operand products moved to simt_gemm_mn_kernel).
 __global__ void __launch_bounds__(256, 2) simt_gemm_kernel(const __grid_constant__ SimtArgs a) {
   __shared__ __align__(16) float As[2][SK][SB];
   __shared__ __align__(16) float Bs[2][SK][SB];
@@ -128,6 +129,98 @@ __global__ void __launch_bounds__(256, 2) simt_gemm_kernel(const __grid_constant
   }
 }
 
+// Both operands MN-major (a_mn and b_mn): every stage is 16 rows of 128
+// contiguous floats per operand, so each thread copies two 16-byte pieces of
+// each straight into shared memory with cp.async, three stages deep (48 KB),
+// and no registers stage the tiles or transpose them.  The inner product and
+// the epilogue are those of simt_gemm_kernel.
+constexpr int MN_STAGES = 3;
+constexpr int MN_STAGE_FLOATS = 2 * SK * SB;  // A then B
+
+__global__ void __launch_bounds__(256, 2) simt_gemm_mn_kernel(const __grid_constant__ SimtArgs a) {
+  extern __shared__ __align__(16) float smem[];  // [MN_STAGES][A, B][SK][SB]
+  pdl_launch_dependents();
+  pdl_wait();
+  const SimtGemmDesc& d = a.d;
+  const int b = blockIdx.y;
+  const int u = blockIdx.x;
+  int i, j;
+  if (d.sym) {  // lower-triangular square tiles: row i holds i + 1 tiles
+    i = static_cast<int>((sqrtf(8.f * static_cast<float>(u) + 1.f) - 1.f) * 0.5f);
+    while (i > 0 && i * (i + 1) / 2 > u) --i;
+    while ((i + 1) * (i + 2) / 2 <= u) ++i;
+    j = u - i * (i + 1) / 2;
+  } else {
+    i = u % a.nI;
+    j = u / a.nI;
+  }
+  const int m0 = i * SB, n0 = j * SB;
+  const int tid = threadIdx.x;
+  const float* A = d.A + static_cast<long long>(b) * d.bsa;
+  const float* Bm = d.Bm + static_cast<long long>(b) * d.bsb;
+  // piece c = tid + 256 h (h = 0, 1) of a stage: row c / 32, floats 4 (c % 32) ..
+  auto issue = [&](int kb, int stg) {
+    float* As = smem + stg * MN_STAGE_FLOATS;
+    float* Bs = As + SK * SB;
+    const int k0 = kb * SK;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = tid + h * 256, kr = c >> 5, col = (c & 31) * 4;
+      cp_async16(As + kr * SB + col, A + static_cast<long long>(k0 + kr) * d.lda + m0 + col);
+      cp_async16(Bs + kr * SB + col, Bm + static_cast<long long>(k0 + kr) * d.ldb + n0 + col);
+    }
+  };
+
+  const int ty = tid >> 4, tx = tid & 15;
+  float acc[8][8];
+#pragma unroll
+  for (int p = 0; p < 8; ++p)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[p][q] = 0.f;
+
+  const int nk = d.K / SK;
+#pragma unroll
+  for (int s0 = 0; s0 < MN_STAGES - 1; ++s0) {
+    if (s0 < nk) issue(s0, s0);
+    cp_async_commit();  // one group per stage, empty past the end, so the counts below hold
+  }
+  for (int kb = 0; kb < nk; ++kb) {
+    cp_async_wait<MN_STAGES - 2>();  // this thread's pieces of stage kb have landed
+    __syncthreads();                 // everyone's have, and stage kb - 1 is no longer read
+    const int nxt = kb + MN_STAGES - 1;
+    if (nxt < nk) issue(nxt, nxt % MN_STAGES);
+    cp_async_commit();
+    const float* As = smem + (kb % MN_STAGES) * MN_STAGE_FLOATS;
+    const float* Bs = As + SK * SB;
+#pragma unroll
+    for (int k = 0; k < SK; ++k) {
+      const float4 a0 = *reinterpret_cast<const float4*>(As + k * SB + ty * 4);
+      const float4 a1 = *reinterpret_cast<const float4*>(As + k * SB + 64 + ty * 4);
+      const float4 b0 = *reinterpret_cast<const float4*>(Bs + k * SB + tx * 4);
+      const float4 b1 = *reinterpret_cast<const float4*>(Bs + k * SB + 64 + tx * 4);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int p = 0; p < 8; ++p)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[p][q] = fmaf(av[p], bv[q], acc[p][q]);
+    }
+  }
+  cp_async_wait<0>();
+
+  const EpiParams& e = a.epi;
+  const float sc = epi_scale(e, b);
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const int r = m0 + (p < 4 ? ty * 4 + p : 64 + ty * 4 + (p - 4));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int c = n0 + (q < 4 ? tx * 4 + q : 64 + tx * 4 + (q - 4));
+      epi_elem(e, b, r, c, acc[p][q], sc);
+    }
+  }
+}
+
 cudaError_t launch_simt_gemm(const SimtGemmDesc& d, const EpiParams& epi, cudaStream_t st) {
   SimtArgs a;
   a.d = d;
@@ -137,6 +230,10 @@ cudaError_t launch_simt_gemm(const SimtGemmDesc& d, const EpiParams& epi, cudaSt
   a.epi = epi;
   a.epi.sym = d.sym;
   if (d.B <= 0 || a.tpm <= 0) return cudaSuccess;
+  if (d.a_mn && d.b_mn)
+    return launch_pdl(simt_gemm_mn_kernel, dim3(a.tpm, d.B), dim3(256),
+                      static_cast<size_t>(MN_STAGES) * MN_STAGE_FLOATS * sizeof(float), st, a);
+  if (d.a_mn) return cudaErrorInvalidValue;  // an MN-major A is only taken with an MN-major B
   return launch_pdl(simt_gemm_kernel, dim3(a.tpm, d.B), dim3(256), 0, st, a);
 }
 

@@ -726,3 +726,38 @@ def test_restarted_gram_plans_with_a_final_single_step(steps):
     for i in range(2):
         e = rel(O[i].float().cpu(), oracle_O(X[i], steps))
         assert e < 1.2e-2, (steps, i, e)
+
+
+@pytest.mark.parametrize("bad", [float("nan"), float("inf")])
+@pytest.mark.parametrize("sched", ["auto", "orig", "gram_r2"])
+def test_nonfinite_input_stays_in_its_matrix(bad, sched):
+    """A NaN or Inf in one matrix of a batch is not checked: it propagates into
+    that matrix's output (its norm is not finite), and the other matrices of
+    the same launches come out bit for bit as without it."""
+    m = _m()
+    X = torch.stack([synth.random_matrix(256, 768, seed=3000 + i) for i in range(3)]).to(torch.bfloat16).cuda()
+    ref = m.ns_batched(X, steps=5, schedule=sched)
+    Xb = X.clone()
+    Xb[1, 17, 100] = bad
+    out = m.ns_batched(Xb, steps=5, schedule=sched)
+    torch.cuda.synchronize()
+    assert not torch.isfinite(out[1].float()).all()
+    assert torch.equal(out[0], ref[0]) and torch.equal(out[2], ref[2])
+
+
+@pytest.mark.parametrize("sched", ["auto", "orig"])
+def test_rows_spanning_six_decades(sched):
+    """Row norms spread log-uniformly over 1e-3 .. 1e3 (bf16 data): after the
+    Frobenius normalisation most rows sit far below fp16's normal range, where
+    the fp16 pair keeps their low part; the result must still meet the bf16
+    tolerance."""
+    m = _m()
+    g = torch.Generator().manual_seed(3100)
+    X = torch.randn(2, 512, 2048, generator=g)
+    X *= (10.0 ** (6.0 * torch.rand(2, 512, 1, generator=g) - 3.0))
+    X = X.to(torch.bfloat16).cuda()
+    O = m.ns_batched(X, steps=5, schedule=sched)
+    torch.cuda.synchronize()
+    for i in range(2):
+        e = rel(O[i].float().cpu(), oracle_O(X[i]))
+        assert e < TOL_BF16, (sched, i, e)
