@@ -129,13 +129,15 @@ __global__ void __launch_bounds__(256, 2) simt_gemm_kernel(const __grid_constant
   }
 }
 
-// Both operands MN-major (a_mn and b_mn): every stage is 16 rows of 128
-// contiguous floats per operand, so each thread copies two 16-byte pieces of
-// each straight into shared memory with cp.async, three stages deep (48 KB),
+// Both operands MN-major (a_mn and b_mn): every stage is MN_SK rows of 128
+// contiguous floats per operand, so each thread copies MN_SK / 8 16-byte
+// pieces of each straight into shared memory with cp.async, three stages deep,
 // and no registers stage the tiles or transpose them.  The inner product and
 // the epilogue are those of simt_gemm_kernel.
 constexpr int MN_STAGES = 3;
-constexpr int MN_STAGE_FLOATS = 2 * SK * SB;  // A then B
+constexpr int MN_SK = 16;                        // k per stage
+constexpr int MN_STAGE_FLOATS = 2 * MN_SK * SB;  // A then B
+constexpr size_t MN_SMEM = static_cast<size_t>(MN_STAGES) * MN_STAGE_FLOATS * sizeof(float);
 
 __global__ void __launch_bounds__(256, 2) simt_gemm_mn_kernel(const __grid_constant__ SimtArgs a) {
   extern __shared__ __align__(16) float smem[];  // [MN_STAGES][A, B][SK][SB]
@@ -158,13 +160,13 @@ __global__ void __launch_bounds__(256, 2) simt_gemm_mn_kernel(const __grid_const
   const int tid = threadIdx.x;
   const float* A = d.A + static_cast<long long>(b) * d.bsa;
   const float* Bm = d.Bm + static_cast<long long>(b) * d.bsb;
-  // piece c = tid + 256 h (h = 0, 1) of a stage: row c / 32, floats 4 (c % 32) ..
+  // piece c = tid + 256 h of a stage: row c / 32, floats 4 (c % 32) ..
   auto issue = [&](int kb, int stg) {
     float* As = smem + stg * MN_STAGE_FLOATS;
-    float* Bs = As + SK * SB;
-    const int k0 = kb * SK;
+    float* Bs = As + MN_SK * SB;
+    const int k0 = kb * MN_SK;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < MN_SK / 8; ++h) {
       const int c = tid + h * 256, kr = c >> 5, col = (c & 31) * 4;
       cp_async16(As + kr * SB + col, A + static_cast<long long>(k0 + kr) * d.lda + m0 + col);
       cp_async16(Bs + kr * SB + col, Bm + static_cast<long long>(k0 + kr) * d.ldb + n0 + col);
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(256, 2) simt_gemm_mn_kernel(const __grid_const
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[p][q] = 0.f;
 
-  const int nk = d.K / SK;
+  const int nk = d.K / MN_SK;
 #pragma unroll
   for (int s0 = 0; s0 < MN_STAGES - 1; ++s0) {
     if (s0 < nk) issue(s0, s0);
@@ -191,9 +193,9 @@ __global__ void __launch_bounds__(256, 2) simt_gemm_mn_kernel(const __grid_const
     if (nxt < nk) issue(nxt, nxt % MN_STAGES);
     cp_async_commit();
     const float* As = smem + (kb % MN_STAGES) * MN_STAGE_FLOATS;
-    const float* Bs = As + SK * SB;
+    const float* Bs = As + MN_SK * SB;
 #pragma unroll
-    for (int k = 0; k < SK; ++k) {
+    for (int k = 0; k < MN_SK; ++k) {
       const float4 a0 = *reinterpret_cast<const float4*>(As + k * SB + ty * 4);
       const float4 a1 = *reinterpret_cast<const float4*>(As + k * SB + 64 + ty * 4);
       const float4 b0 = *reinterpret_cast<const float4*>(Bs + k * SB + tx * 4);
@@ -230,9 +232,18 @@ cudaError_t launch_simt_gemm(const SimtGemmDesc& d, const EpiParams& epi, cudaSt
   a.epi = epi;
   a.epi.sym = d.sym;
   if (d.B <= 0 || a.tpm <= 0) return cudaSuccess;
-  if (d.a_mn && d.b_mn)
-    return launch_pdl(simt_gemm_mn_kernel, dim3(a.tpm, d.B), dim3(256),
-                      static_cast<size_t>(MN_STAGES) * MN_STAGE_FLOATS * sizeof(float), st, a);
+  if (d.a_mn && d.b_mn) {
+    if (MN_SMEM > 48 * 1024) {
+      static bool opted = false;  // per process: the attribute belongs to the kernel
+      if (!opted) {
+        const cudaError_t e = cudaFuncSetAttribute(simt_gemm_mn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(MN_SMEM));
+        if (e != cudaSuccess) return e;
+        opted = true;
+      }
+    }
+    return launch_pdl(simt_gemm_mn_kernel, dim3(a.tpm, d.B), dim3(256), MN_SMEM, st, a);
+  }
   if (d.a_mn) return cudaErrorInvalidValue;  // an MN-major A is only taken with an MN-major B
   return launch_pdl(simt_gemm_kernel, dim3(a.tpm, d.B), dim3(256), 0, st, a);
 }

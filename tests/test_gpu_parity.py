@@ -761,3 +761,12 @@ def test_rows_spanning_six_decades(sched):
     for i in range(2):
         e = rel(O[i].float().cpu(), oracle_O(X[i]))
         assert e < TOL_BF16, (sched, i, e)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_degenerate_shapes(dtype):
+    """Single rows, single columns, 1 x 1 and tiny matrices: a 1 x n matrix has
+    one singular value, so O is x / |x| mapped by the scalar polynomial; each
+    pads to one 256 x 256 tile pair.  Checked through muon_step against the
+    oracle, in one call with every shape."""
+    _check_step([(1, 1), (1, 300), (300, 1), (2, 2), (17, 5), (5, 17), (1, 4096)], dtype=dtype, seed=41)

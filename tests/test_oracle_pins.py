@@ -151,6 +151,16 @@ def test_diagonal_reduces_to_scalar_map():
     assert np.max(np.abs(O - E)) < 1e-14
 
 
+@pytest.mark.parametrize("shape", [(1, 300), (300, 1), (1, 1)])
+def test_single_row_or_column_reduces_to_scalar_map(shape):
+    """A 1 x n (or n x 1) matrix has one singular value, |x| / (|x| + eps):
+    O is x / |x| times the scalar map of it, whichever side is short."""
+    x = np.random.default_rng(12).standard_normal(shape)
+    nx = np.linalg.norm(x)
+    O = oracle.newton_schulz(x, 5)
+    assert np.max(np.abs(O - x / nx * scalar_map(np.array([nx / (nx + 1e-7)]), 5)[0])) < 1e-14
+
+
 def test_worked_example_by_hand():
     # M = [[3,0,0],[0,4,0]]: ||M||_F = 5, singular values 0.6 and 0.8 after
     # normalisation.  One quintic step by hand:
