@@ -395,23 +395,39 @@ def max_over_ranks(x, world):
 
 
 def host_copy_gbs(dev, nbytes=1 << 30):
-    """This box's pinned host <-> device copy rates (GB/s, best of 3 single
-    copies of 1 GiB, each direction alone): the end-to-end figure is bound by
-    them when a step's copies take longer than its compute."""
-    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
-    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    """This box's pinned host <-> device copy rates in GB/s, best of 3 copies of
+    1 GiB: each direction alone, and the total of both directions at once (as
+    the end-to-end pass runs them).  The end-to-end figure is bound by them
+    when a step's copies take longer than its compute."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def h2d():
+        d_in.copy_(h_in, non_blocking=True)
+
+    def d2h():
+        h_out.copy_(d_out, non_blocking=True)
+
+    def both():
+        with torch.cuda.stream(s_in):
+            h2d()
+        with torch.cuda.stream(s_out):
+            d2h()
+
     out = {}
-    for name, fn in (("h2d", lambda: d.copy_(h, non_blocking=True)), ("d2h", lambda: h.copy_(d, non_blocking=True))):
+    for name, fn, moved in (("h2d", h2d, nbytes), ("d2h", d2h, nbytes), ("both_total", both, 2 * nbytes)):
         best = float("inf")
         for _ in range(3):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
             fn()
-            b.record()
-            b.synchronize()
-            best = min(best, a.elapsed_time(b) / 1e3)
-        out[name] = nbytes / best / 1e9
-    del h, d
+            torch.cuda.synchronize(dev)
+            best = min(best, time.perf_counter() - t0)
+        out[name] = moved / best / 1e9
+    del h_in, h_out, d_in, d_out
     return out
 
 
