@@ -9,18 +9,28 @@
 //              later products take fp16 operands, with X carried between steps
 //              as an fp16 pair (hi + lo / 2^11):
 //              A = X X^T (SYRK), B' = a I + b A + c A^2, X <- B' X_hi + a X_lo
-//   ORIG_BF16  the same on bf16 operands only, X carried as a bf16 pair, with
-//              split products in the last steps
-//   GRAM_X3    Gram space with split-bf16 operands (hi*hi + hi*lo + lo*hi):
-//              G0 = X0 X0^T; P_k = a I + b G_k + c G_k^2; Q <- P_k Q;
+//   GRAM_R2    the Gram recurrence (DMuon technical summary, §2.2) restarted
+//              from X every two steps: step 0 as in ORIG, then segments
+//              A = X_hi X_hi^T; P_0 = a I + b A + c A^2; G_1 = P_0 (P_0 A);
+//              P_1 = a I + b G_1 + c G_1^2; X <- (P_1 P_0) X_hi + a^2 X_lo,
+//              on fp16 operands (the bf16 default where it saves work)
+//   ORIG_BF16  ORIG on bf16 operands only, X carried as a bf16 pair, with
+//              split products in the last steps (the fallback for coefficients
+//              outside fp16's range)
+//   ORIG_F16X3 ORIG on fp16 pairs, three MMAs per product (fp32 data, up to
+//              6 steps)
+//   GRAM_X3    Gram space for all steps, split-bf16 operands (hi*hi + hi*lo +
+//              lo*hi): G0 = X0 X0^T; P_k = a I + b G_k + c G_k^2; Q <- P_k Q;
 //              G_{k+1} = P_k (P_k G_k); O = Q X0
 //   GRAM_X1    the same recurrence with plain bf16 operands
-//   fp32       the ORIG or Gram recurrence with fp32 FFMA products
+//   fp32       ORIG, GRAM_R2 or the Gram recurrence with fp32 FFMA products
 //
-// Why these: the Gram recurrence squares the condition number, so plain bf16
-// products in Gram space exceed a 2e-2 relative error on ill-conditioned
-// inputs; split operands restore it at three products per product.  fp16
-// operands (11 significant bits) in original space need no splits.
+// Why these: the Gram recurrence squares the condition number, and without
+// restarts the rounding of G grows in the directions of small singular values
+// (GRAM_X1 diverges on rank-deficient inputs, GRAM_X3 reaches ~2e-2).
+// Re-forming G from X every two steps keeps it within a third of the bf16
+// tolerance.  fp16 operands (11 significant bits) in original space need no
+// splits.  GRAM_X3 and GRAM_X1 are kept on request for comparison.
 #include <cuda_runtime.h>
 
 #include <algorithm>
