@@ -22,9 +22,9 @@
 //
 // Symmetric storage.  A symmetric s x s matrix is stored "block-lower": only
 // its 256 x 256 blocks (I, J) with J <= I are written (diagonal blocks in
-// full).  When such a matrix is an operand, a 64-wide k-block that falls in an
-// upper block is read as the transposed (MN-major) box of the stored lower
-// block and the MMA instruction descriptor switches that operand's major-ness
+// full).  When such a matrix is an operand, a 128-deep k-block (one stage)
+// that falls in an upper block is read as the transposed (MN-major) boxes of
+// the stored lower block and the MMA instruction descriptor switches that operand's major-ness
 // for it; so no mirror is ever written.
 //
 // Warp roles (320 threads):
