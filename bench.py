@@ -725,7 +725,8 @@ def run_ours(args, world, rank, local):
         "matrices_per_s": count_all * args.steps / t_total,
         "pct_of_bf16_peak": 100.0 * value / pk["bf16_tflops"],
         "value_without_graph": value_eager,
-        "launch_path": "CUDA graph replay of the C-ABI call sequence" if not args.no_graph else "direct C-ABI calls",
+        "launch_path": "CUDA graph replay of the C-ABI calls, one graph per shape group" if not args.no_graph
+                       else "direct C-ABI calls",
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "roofline_timing": "per-launch CUDA events in a second pass of the same steps",
         "roofline": roof,
