@@ -87,3 +87,17 @@ def test_c5_config_names():
     assert bench.c5_params("c5f32_n4096_t10") == (4096, 10)
     assert bench.c5_params("c5_n16384") == (16384, 5)
     assert "layers" in bench.workload_desc("c3_l2")
+
+
+def test_clock_records_that_are_rejected():
+    """hw/thermal slowdowns, or a clock stuck far below its maximum without a
+    power-cap reason, reject a timed region; the power cap alone does not."""
+    import bench
+    ok = {"sm_mhz": 1600.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    assert not bench.clocks_rejected(ok)
+    assert not bench.clocks_rejected({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []})
+    assert bench.clocks_rejected(dict(ok, reasons=["sw_power_cap", "hw_slowdown"]))
+    assert bench.clocks_rejected(dict(ok, reasons=["sw_thermal_slowdown"]))
+    assert bench.clocks_rejected({"sm_mhz": 900.0, "sm_max_mhz": 2070.0, "reasons": []})
+    assert not bench.clocks_rejected({"sm_mhz": 900.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]})
+    assert not bench.clocks_rejected({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]})
