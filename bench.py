@@ -663,12 +663,19 @@ def run_ours(args, world, rank, local):
     # ---- end to end through the C ABI with host buffers (pinned).  Every step
     # copies its gradients in from pinned host memory and the updated weights
     # back out.  The copy of step k+1's gradients runs on a second stream into
-    # the other of two device gradient buffers while step k computes.  Each
-    # shape group's weights are copied out on a third stream as soon as that
-    # group's update is done, while the groups after it compute; the group's
-    # next update waits for that copy.
+    # the other of two device gradient buffers while step k computes.  As soon
+    # as a shape group's update is done, a third stream copies its weights out
+    # to the host while the later groups compute; the group's next update
+    # waits for that copy (or, with a single group, only for a device
+    # snapshot that the host copy then reads).
     Gh = [g.to("cpu").pin_memory() for g in G]
     Wh = [torch.empty(w.shape, dtype=w.dtype).pin_memory() for w in W]
+    # With one shape group nothing else computes while its weights leave, so
+    # the copy-out reads a device snapshot and the next step starts at once.
+    # With several groups the later groups cover the copy-out, and a snapshot
+    # only adds work (measured: c3 1025 -> 996 TFLOP/s end to end, c4 244 -> 215).
+    snapshot = len(upd.groups) == 1
+    Ws = [torch.empty_like(w) for w in W] if snapshot else W
     h2d = sum(g.numel() * g.element_size() for g in Gh)
     d2h = sum(w.numel() * w.element_size() for w in Wh)
     Gsets = [G, [g.clone() for g in G]]
@@ -680,7 +687,8 @@ def run_ours(args, world, rank, local):
     def e2e_run(k):
         ev_in = [torch.cuda.Event(), torch.cuda.Event()]
         ev_used = [torch.cuda.Event(), torch.cuda.Event()]
-        ev_out = [torch.cuda.Event() for _ in range(ngroups)]  # group g's weights are copied out
+        ev_snap = [torch.cuda.Event() for _ in range(ngroups)]  # group g's weights are snapshotted
+        ev_out = [torch.cuda.Event() for _ in range(ngroups)]  # group g's weights are on the host
 
         def copy_in(i):
             with torch.cuda.stream(cs):
@@ -690,15 +698,21 @@ def run_ours(args, world, rank, local):
                 ev_in[i].record(cs)
 
         def before_group(gi, idx, s):
-            s.wait_event(ev_out[gi])  # the previous copy of these weights has left
+            s.wait_event(ev_snap[gi])  # the previous step's weights of this group are snapshotted
 
         def after_group(gi, idx, s):
             done = torch.cuda.Event()
             done.record(s)
             with torch.cuda.stream(cs_out):
                 cs_out.wait_event(done)
+                if snapshot:
+                    for q in idx:
+                        Ws[q].copy_(W[q], non_blocking=True)
+                    ev_snap[gi].record(cs_out)
                 for q in idx:
-                    Wh[q].copy_(W[q], non_blocking=True)
+                    Wh[q].copy_(Ws[q], non_blocking=True)
+                if not snapshot:
+                    ev_snap[gi].record(cs_out)  # the group's next update waits for the copy itself
                 ev_out[gi].record(cs_out)
 
         if flush is not None:
@@ -708,7 +722,7 @@ def run_ours(args, world, rank, local):
         a.record(st)
         for i in (0, 1):
             ev_used[i].record(st)
-        for e in ev_out:
+        for e in ev_snap + ev_out:
             e.record(st)
         copy_in(0)
         for s_ in range(k):
@@ -759,7 +773,8 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipelining": "step k+1's gradient copy-in overlaps step k on a second stream; each shape group's "
                               "weights are copied out on a third stream while the later groups compute (largest "
-                              "groups first)",
+                              "groups first); with a single group, from a device snapshot while the next step "
+                              "computes",
                 "ms_per_step": 1e3 * e2e_t / args.steps,
                 "host_copy_gbs": link},
         "clocks": clocks,
