@@ -286,7 +286,7 @@ class Clocks:
                 self.p.kill()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in (getattr(self, "out", "") or "").splitlines():
             f = [x.strip() for x in line.split(",")]
@@ -297,13 +297,19 @@ class Clocks:
                 mx.append(float(f[2]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(f[3]))
+            except ValueError:
+                pass
             for nm, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
+        if pw:
+            out["power_w"] = float(np.median(pw))
+        return out
 
 
 REJECTED_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
@@ -456,6 +462,36 @@ def host_copy_gbs(dev, nbytes=1 << 30):
     return out
 
 
+def step_copy_gbs(dev, host_in, dev_in, host_out, dev_out):
+    """The copy rates of one step's own buffers (all gradients in, all weights
+    out), each direction alone and both at once, in GB/s: what the
+    end-to-end pass can reach on this machine and these allocations."""
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    nin = sum(t.numel() * t.element_size() for t in host_in)
+    nout = sum(t.numel() * t.element_size() for t in host_out)
+
+    def h2d():
+        with torch.cuda.stream(s_in):
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s_out):
+            for h, d in zip(host_out, dev_out):
+                h.copy_(d, non_blocking=True)
+
+    out = {}
+    for name, fns, moved in (("step_h2d", (h2d,), nin), ("step_d2h", (d2h,), nout), ("step_both_total", (h2d, d2h),
+                                                                                       nin + nout)):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for fn in fns:
+            fn()
+        torch.cuda.synchronize(dev)
+        out[name] = moved / (time.perf_counter() - t0) / 1e9
+    return out
+
+
 def cpu_baseline(work, budget_s=15.0, max_mats=None, start=0, of=None):
     """The fp64 oracle, as it stands, on a bounded sample of the workload
     (matrices from index `start` on, cyclically; `of` describes the whole
@@ -550,6 +586,21 @@ def run_ours(args, world, rank, local):
     count = len(shapes)
     W = [w.to(dev) for w in work.weights]
     G = [g.to(dev) for g in work.grads]
+    # The end-to-end pass's buffers come first, before the workspace and the
+    # timed work: on a box whose GPU memory earlier processes have used, host
+    # copies into and out of buffers allocated later ran slower (c3 end to end
+    # 785-794 TFLOP/s against 879-932 allocated here; the same on a fresh box).
+    G2 = [g.clone() for g in G]  # the second gradient buffer of the end-to-end pass
+    Gh = [torch.empty(g.shape, dtype=g.dtype).pin_memory() for g in G]
+    for gh, g in zip(Gh, G):
+        gh.copy_(g)
+    Wh = [torch.empty(w.shape, dtype=w.dtype).pin_memory() for w in W]
+    # With one shape group nothing else computes while its weights leave, so
+    # the copy-out reads a device snapshot and the next step starts at once.
+    # With several groups the later groups cover the copy-out, and a snapshot
+    # only adds work (measured: c3 1025 -> 996 TFLOP/s end to end, c4 244 -> 215).
+    snapshot = len({(min(a, b), max(a, b)) for a, b in work.shapes}) == 1
+    Ws = [torch.empty_like(w) for w in W] if snapshot else W
     if not args.config.startswith("c3"):
         cpu_work = work
     else:
@@ -668,21 +719,14 @@ def run_ours(args, world, rank, local):
     # to the host while the later groups compute; the group's next update
     # waits for that copy (or, with a single group, only for a device
     # snapshot that the host copy then reads).
-    Gh = [g.to("cpu").pin_memory() for g in G]
-    Wh = [torch.empty(w.shape, dtype=w.dtype).pin_memory() for w in W]
-    # With one shape group nothing else computes while its weights leave, so
-    # the copy-out reads a device snapshot and the next step starts at once.
-    # With several groups the later groups cover the copy-out, and a snapshot
-    # only adds work (measured: c3 1025 -> 996 TFLOP/s end to end, c4 244 -> 215).
-    snapshot = len(upd.groups) == 1
-    Ws = [torch.empty_like(w) for w in W] if snapshot else W
     h2d = sum(g.numel() * g.element_size() for g in Gh)
     d2h = sum(w.numel() * w.element_size() for w in Wh)
-    Gsets = [G, [g.clone() for g in G]]
+    Gsets = [G, G2]
     cs = torch.cuda.Stream(dev)
     cs_out = torch.cuda.Stream(dev)
     ngroups = len(upd.groups)
     link = host_copy_gbs(dev)
+    link.update(step_copy_gbs(dev, Gh, Gsets[1], Wh, W))
 
     def e2e_run(k):
         ev_in = [torch.cuda.Event(), torch.cuda.Event()]
@@ -742,7 +786,9 @@ def run_ours(args, world, rank, local):
         return a.elapsed_time(b)
 
     e2e_run(max(args.warmup, 2))  # both gradient buffers get their graphs here
-    e2e_t = max_over_ranks(e2e_run(args.steps) / 1e3, world)
+    with Clocks(local) as e2e_clk:  # the copies draw power too: the clocks of this pass, reported beside it
+        e2e_ms = e2e_run(args.steps)
+    e2e_t = max_over_ranks(e2e_ms / 1e3, world)
     e2e_val = flops_all * args.steps / e2e_t / 1e12
     launches_per_step = len(recs) / args.steps
     line = {
@@ -776,7 +822,7 @@ def run_ours(args, world, rank, local):
                               "groups first); with a single group, from a device snapshot while the next step "
                               "computes",
                 "ms_per_step": 1e3 * e2e_t / args.steps,
-                "host_copy_gbs": link},
+                "host_copy_gbs": link, "clocks": e2e_clk.summary()},
         "clocks": clocks,
         "peaks": pk,
     }
