@@ -772,3 +772,25 @@ def test_degenerate_shapes(dtype):
     pads to one 256 x 256 tile pair.  Checked through muon_step against the
     oracle, in one call with every shape."""
     _check_step([(1, 1), (1, 300), (300, 1), (2, 2), (17, 5), (5, 17), (1, 4096)], dtype=dtype, seed=41)
+
+
+def test_muon_step_more_matrices_than_one_chunk():
+    """300 matrices of one shape group (both orientations) exceed the 256
+    matrices a chunk takes: the group runs as two chunks through the same
+    workspace, and every matrix's update still matches the oracle."""
+    shapes = [(64, 128) if i % 3 else (128, 64) for i in range(300)]
+    _check_step(shapes, seed=47)
+
+
+def test_ns_batched_more_matrices_than_one_chunk():
+    """muon_ns_batched with B = 300 (over the 256 a chunk takes): sampled
+    matrices from both chunks against the oracle, and every output finite."""
+    m = _m()
+    g = torch.Generator().manual_seed(49)
+    X = torch.randn(300, 64, 128, generator=g).to(torch.bfloat16).cuda()
+    O = m.ns_batched(X, steps=5)
+    torch.cuda.synchronize()
+    assert torch.isfinite(O.float()).all()
+    for i in (0, 131, 255, 256, 299):
+        e = rel(O[i].float().cpu(), oracle_O(X[i]))
+        assert e < TOL_BF16, (i, e)
