@@ -794,3 +794,36 @@ def test_ns_batched_more_matrices_than_one_chunk():
     for i in (0, 131, 255, 256, 299):
         e = rel(O[i].float().cpu(), oracle_O(X[i]))
         assert e < TOL_BF16, (i, e)
+
+
+@pytest.mark.parametrize("steps", [6, 7])
+def test_fp32_at_the_pair_schedule_threshold(steps):
+    """fp32 AUTO runs the tensor-core fp16 pairs up to 6 steps and FFMA from
+    7: both sides of the switch meet 1e-4 on Gaussian and row-scaled inputs."""
+    m = _m()
+    assert m.resolve_schedule(512, 2048, steps=steps, dtype=torch.float32) == ("orig_f16x3" if steps <= 6 else "gram_r2")
+    x = synth.random_matrix(512, 2048, seed=53)
+    y = synth.random_matrix(512, 2048, seed=54)
+    y[0] *= 100
+    X = torch.stack([x, y]).cuda()
+    O = m.ns_batched(X, steps=steps)
+    torch.cuda.synchronize()
+    for i in range(2):
+        e = rel(O[i].cpu(), oracle_O(X[i], steps))
+        assert e < TOL_FP32, (steps, i, e)
+
+
+@pytest.mark.parametrize("sched", ["auto", "orig", "gram_r2", "orig_bf16"])
+def test_identity_coefficients_return_the_normalised_input(sched):
+    """With (a, b, c) = (1, 0, 0) every step maps X to itself, so O is
+    X / (||X||_F + eps) whatever the schedule: the polynomial epilogues, the
+    Gram segments and the low-part bookkeeping must add nothing."""
+    m = _m()
+    X = torch.stack([synth.random_matrix(256, 768, seed=57 + i) for i in range(2)]).to(torch.bfloat16).cuda()
+    O = m.ns_batched(X, steps=3, coeffs=(1.0, 0.0, 0.0), schedule=sched)
+    torch.cuda.synchronize()
+    for i in range(2):
+        x = X[i].double().cpu().numpy()
+        ref = x / (np.linalg.norm(x) + oracle.EPS)
+        assert rel(O[i].float().cpu(), ref) < 2e-3, (sched, i)  # the bf16 output rounding only
+        assert rel(oracle_O(X[i], 3, (1.0, 0.0, 0.0)), ref) < 1e-12
