@@ -49,22 +49,30 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackA
         x = g;
       }
     }
-    ss = fmaf(x, x, ss);
     S[ri][cj] = x;
   }
   __syncthreads();
   const long long base = static_cast<long long>(b) * a.bs;
-#pragma unroll 4
-  for (int rr = 0; rr < (PT * PT) / 256; ++rr) {
-    const int idx = rr * 256 + tid;
-    const int pr = idx >> 6, pc = idx & 63;
-    const float x = tr ? S[pc][pr] : S[pr][pc];
-    const long long off = base + static_cast<long long>(P0 + pr) * a.lp + (Q0 + pc);
-    if (a.Xf) a.Xf[off] = x;
-    if (a.Xh) {
-      const bf16 h = __float2bfloat16_rn(x);
-      a.Xh[off] = h;
-      if (a.Xl) a.Xl[off] = __float2bfloat16_rn(x - __bfloat162float(h));
+  // Packed order, 8 consecutive packed elements per thread as in
+  // pack_vec_kernel, and the sum of squares taken here in that order: the
+  // partial sums (and so the norm) of a packed tile are the same whichever
+  // way the matrix is stored and whichever kernel packs it.
+#pragma unroll
+  for (int rep = 0; rep < 2; ++rep) {
+    const int c = rep * 256 + tid;
+    const int pr = c >> 3, pc0 = (c & 7) * 8;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int pc = pc0 + k;
+      const float x = tr ? S[pc][pr] : S[pr][pc];
+      ss = fmaf(x, x, ss);
+      const long long off = base + static_cast<long long>(P0 + pr) * a.lp + (Q0 + pc);
+      if (a.Xf) a.Xf[off] = x;
+      if (a.Xh) {
+        const bf16 h = __float2bfloat16_rn(x);
+        a.Xh[off] = h;
+        if (a.Xl) a.Xl[off] = __float2bfloat16_rn(x - __bfloat162float(h));
+      }
     }
   }
   // fixed-shape reduction: warp shuffle tree, then 8 warp sums in order
@@ -157,9 +165,10 @@ __global__ void __launch_bounds__(256) pack_vec_kernel(const __grid_constant__ P
 #pragma unroll
       for (int k = 0; k < 8; ++k) x[k] = 0.f;
     }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) ss = fmaf(x[k], x[k], ss);
     if (!tr) {
+      // packed order is source order here: the sum of squares goes in that order
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ss = fmaf(x[k], x[k], ss);
       store8(base + static_cast<long long>(P0 + ri) * a.lp + (Q0 + cj), x);
     } else {
 #pragma unroll
@@ -175,6 +184,9 @@ __global__ void __launch_bounds__(256) pack_vec_kernel(const __grid_constant__ P
       float x[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) x[k] = S[pc + k][pr];
+      // in packed order, so the tile's partial sum equals the untransposed one's
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ss = fmaf(x[k], x[k], ss);
       store8(base + static_cast<long long>(P0 + pr) * a.lp + (Q0 + pc), x);
     }
   }
