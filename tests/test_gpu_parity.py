@@ -844,3 +844,28 @@ def test_transpose_equivariance_bitwise(shape):
     Ot = m.ns_batched(Xt, steps=5)
     torch.cuda.synchronize()
     assert torch.equal(Ot, O.transpose(1, 2))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_result_independent_of_batch_company(dtype):
+    """A matrix's output does not depend on what else is in the call: alone,
+    in a batch of 7 (another launch mode and tile schedule), or in a muon_step
+    with other shape groups, it is bit for bit the same."""
+    m = _m()
+    X = synth.random_matrix(256, 1024, seed=61).to(dtype).cuda()
+    others = torch.stack([synth.random_matrix(256, 1024, seed=62 + i) for i in range(6)]).to(dtype).cuda()
+    alone = m.ns_batched(X[None], steps=5)[0]
+    batch = m.ns_batched(torch.cat([others[:3], X[None], others[3:]]), steps=5)[3]
+    torch.cuda.synchronize()
+    assert torch.equal(alone, batch)
+    # through muon_step: W = 0, lr = 2^-5, so W = -lr O exactly (see the apply tests)
+    shapes = [(256, 1024), (512, 512), (1024, 256), (300, 200)]
+    Ws = [torch.zeros(s, dtype=dtype, device="cuda") for s in shapes]
+    Gs = [X] + [synth.random_matrix(*s, seed=70 + i).to(dtype).cuda() for i, s in enumerate(shapes[1:])]
+    Ms = [torch.zeros(s, dtype=torch.float32, device="cuda") for s in shapes]
+    m.muon_step(Ws, Gs, Ms, beta=0.95, lr=2.0 ** -5, steps=5)
+    W1 = torch.zeros_like(X)
+    m.muon_step([W1], [X], [torch.zeros(X.shape, dtype=torch.float32, device="cuda")], beta=0.95, lr=2.0 ** -5,
+                steps=5)
+    torch.cuda.synchronize()
+    assert torch.equal(Ws[0], W1)
