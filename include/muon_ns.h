@@ -86,9 +86,13 @@ typedef enum {
 
 /*
  * Schedules and precision.  Every tensor-core product accumulates in fp32.
- *  - bf16, AUTO: GRAM_R2 where it executes at most 0.9x ORIG's tensor-core
- *    work (the long side at least about 1.5x the short side, and 3 or more
- *    steps), else ORIG.
+ *  - bf16, AUTO: up to 10 steps GRAM_R2 where it executes at most 0.9x
+ *    ORIG's tensor-core work (the long side at least about 1.5x the short
+ *    side, and 3 or more steps), else ORIG.  Past 10 steps ORIG_F16X3: the
+ *    quintic does not contract inside the band it maps singular values into,
+ *    so single fp16 operands drift with the step count (at most 8.9e-3 at 10
+ *    steps, 2.1e-2 at 15, up to 3.7e-2 at 20-100), where fp16 pairs stay at
+ *    the bf16 output rounding.
  *  - fp32, AUTO: up to 6 steps ORIG_F16X3 (tensor cores, below); longer runs
  *    on fp32 FFMA (CUDA cores): GRAM_R2 where it saves at least a tenth of
  *    ORIG's work, else ORIG.  Explicit GRAM_X3 / GRAM_X1 on fp32 data run

@@ -296,11 +296,15 @@ def measure_costs(shapes, steps=5, dtype=torch.bfloat16, schedule="auto", repeat
 def schedule_candidates(dtype=torch.bfloat16, steps=5):
     """What a measured choice may pick from: schedules whose accuracy meets
     the dtype's tolerance on every input kind measured (bf16: original space,
-    or the Gram recurrence restarted every two steps; fp32: the tensor-core
-    fp16-pair schedule up to 6 steps, FFMA restarted Gram or original space),
-    each tensor-core one with shared or separate launches."""
+    or the Gram recurrence restarted every two steps, and past 10 steps the
+    fp16-pair schedule; fp32: the tensor-core fp16-pair schedule up to 6
+    steps, FFMA restarted Gram or original space), each tensor-core one with
+    shared or separate launches."""
     if dtype == torch.bfloat16:
-        base = ["orig", "gram_r2"] if steps >= 3 else ["orig"]
+        if steps > 10:
+            base = ["orig_f16x3"]
+        else:
+            base = ["orig", "gram_r2"] if steps >= 3 else ["orig"]
         return [f"{b}+{mode}" for b in base for mode in ("shared", "separate")]
     if steps <= 6:
         return ["orig_f16x3+shared", "orig_f16x3+separate", "orig", "gram_r2"]

@@ -231,6 +231,15 @@ static double plan_work(long long s, long long l, int steps, muon_sched sc) {
 // measured on rank-deficient fp32 inputs at 10 steps.)
 constexpr int kFp32PairMaxSteps = 6;
 
+// bf16 runs up to this many steps take single fp16 operands (ORIG, GRAM_R2);
+// longer ones take fp16 pairs (ORIG_F16X3).  The quintic does not contract
+// inside the band it maps the singular values into, so each step's operand
+// rounding (fp16: 2^-11) is carried forward and the error grows with the step
+// count.  Measured on Gaussian, row-scaled and rank-8 inputs: at most 8.9e-3
+// at 10 steps, 1.3e-2 at 12, 2.1e-2 at 15 and 2.3-3.7e-2 at 20 to 100, where
+// the fp16 pairs stay at the bf16 output rounding (1.7e-3; 4.7e-3 at most).
+constexpr int kBf16SingleMaxSteps = 10;
+
 static muon_sched resolve(long long s, long long l, int steps, muon_dtype dt, muon_sched sc, const Coef& k) {
   sc = static_cast<muon_sched>(sc & MUON_SCHED_MASK);  // launch-mode flags are the Group's
   if (steps == 0) return MUON_SCHED_ORIG;  // only the packed fp32 copy is needed
@@ -245,6 +254,9 @@ static muon_sched resolve(long long s, long long l, int steps, muon_dtype dt, mu
         sc = k.f16_ok ? MUON_SCHED_ORIG_F16X3 : (l > s ? MUON_SCHED_GRAM_X3 : MUON_SCHED_ORIG);
       else
         sc = r2_pays ? MUON_SCHED_GRAM_R2 : MUON_SCHED_ORIG;
+    } else if (steps > kBf16SingleMaxSteps && k.f16_ok) {
+      // bf16, long runs: fp16 pairs
+      sc = MUON_SCHED_ORIG_F16X3;
     } else {
       // bf16: the Gram recurrence restarted every two steps (GRAM_R2) where it
       // saves at least a tenth of the tensor-core work, else original space

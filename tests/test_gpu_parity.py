@@ -869,3 +869,20 @@ def test_result_independent_of_batch_company(dtype):
                 steps=5)
     torch.cuda.synchronize()
     assert torch.equal(Ws[0], W1)
+
+
+@pytest.mark.parametrize("steps", [12, 20, 100])
+def test_bf16_long_runs_meet_the_tolerance(steps):
+    """The quintic does not contract inside its band, so single fp16 operands
+    drift past 2e-2 beyond about 12 steps; AUTO then runs fp16 pairs, which
+    stay near the bf16 output rounding.  Checked up to the maximum step count
+    on the inputs where the drift was largest."""
+    m = _m()
+    y = synth.random_matrix(512, 2048, seed=84)
+    y[0] *= 100
+    for name, x in (("gauss 256x512", synth.random_matrix(256, 512, seed=80)), ("rowx100 512x2048", y)):
+        X = x[None].to(torch.bfloat16).cuda()
+        O = m.ns_batched(X, steps=steps)
+        torch.cuda.synchronize()
+        e = rel(O[0].float().cpu(), oracle_O(X[0], steps))
+        assert e < 1e-2, (steps, name, e)

@@ -75,6 +75,13 @@ def test_schedule_choice(lib):
     assert m.resolve_schedule(4096, 14336, steps=2) == "orig"  # no two-step segment to run
     assert m.resolve_schedule(4096, 14336, steps=3) == "gram_r2"
     assert m.resolve_schedule(1024, 8192, steps=0) == "orig"
+    # bf16 past 10 steps: fp16 pairs, whatever the shape
+    for shp in [(1024, 1024), (4096, 14336), (256, 1024)]:
+        assert m.resolve_schedule(*shp, steps=10) != "orig_f16x3", shp
+        assert m.resolve_schedule(*shp, steps=11) == "orig_f16x3", shp
+        assert m.resolve_schedule(*shp, steps=100) == "orig_f16x3", shp
+    assert m.resolve_schedule(1024, 1024, steps=20, schedule="orig") == "orig"
+    assert m.schedule_candidates(torch.bfloat16, 20) == ["orig_f16x3+shared", "orig_f16x3+separate"]
     assert m.resolve_schedule(1024, 8192, schedule="gram_x1") == "gram_x1"
     assert m.resolve_schedule(128, 256, dtype=torch.float32) == "orig_f16x3"
     assert m.resolve_schedule(128, 128, dtype=torch.float32) == "orig_f16x3"
