@@ -886,3 +886,11 @@ def test_bf16_long_runs_meet_the_tolerance(steps):
         torch.cuda.synchronize()
         e = rel(O[0].float().cpu(), oracle_O(X[0], steps))
         assert e < 1e-2, (steps, name, e)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_large_ragged_shapes(dtype):
+    """Large shapes that are not multiples of the 256 tile: 2000 x 3000 pads to
+    2048 x 3072, so every product's last tile row and column, the symmetric
+    products' diagonal tiles and the apply all run partly on padding."""
+    _check_step([(2000, 3000), (3000, 2000)], dtype=dtype, seed=91)
