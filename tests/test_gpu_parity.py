@@ -894,3 +894,43 @@ def test_large_ragged_shapes(dtype):
     2048 x 3072, so every product's last tile row and column, the symmetric
     products' diagonal tiles and the apply all run partly on padding."""
     _check_step([(2000, 3000), (3000, 2000)], dtype=dtype, seed=91)
+
+
+def test_seeded_fuzz_of_shapes_steps_and_schedules():
+    """150 seeded draws of (m, n) in [1, 1200], dtype, 1-14 steps and an
+    accurate schedule (or AUTO), each through muon_ns_batched with a batch of
+    1-3 matrices, against the oracle at the dtype's tolerance (Gaussian
+    inputs)."""
+    m = _m()
+    rng = np.random.default_rng(2024)
+    bf16_scheds = ["auto", "orig", "gram_r2", "orig_f16x3"]
+    fp32_scheds = ["auto", "orig", "gram_r2", "orig_f16x3"]
+    for case in range(150):
+        a, b = (int(v) for v in rng.integers(1, 1201, size=2))
+        dtype = torch.bfloat16 if rng.random() < 0.6 else torch.float32
+        steps = int(rng.integers(1, 15))
+        scheds = bf16_scheds if dtype == torch.bfloat16 else fp32_scheds
+        sched = scheds[int(rng.integers(0, len(scheds)))]
+        if dtype == torch.bfloat16 and steps > 10 and sched in ("orig", "gram_r2"):
+            sched = "auto"  # single fp16 operands are documented to drift past 10 steps
+        if dtype == torch.float32 and steps > 6 and sched == "orig_f16x3":
+            sched = "auto"  # fp16 pairs on fp32 data are for up to 6 steps
+        B = int(rng.integers(1, 4))
+        X = torch.stack([synth.random_matrix(a, b, seed=5000 + 10 * case + i) for i in range(B)]).to(dtype).cuda()
+        O = m.ns_batched(X, steps=steps, schedule=sched)
+        torch.cuda.synchronize()
+        tol = TOL_BF16 if dtype == torch.bfloat16 else TOL_FP32
+        for i in range(B):
+            e = rel(O[i].float().cpu(), oracle_O(X[i], steps))
+            assert e < tol, (case, (a, b), str(dtype), steps, sched, i, e)
+
+
+def test_seeded_fuzz_of_muon_step_calls():
+    """12 seeded muon_step calls, each over 2-6 matrices of random shapes (so
+    several shape groups, both orientations) in one dtype, checked matrix by
+    matrix: momentum to one fp32 ulp, O against the oracle, W elementwise."""
+    rng = np.random.default_rng(2025)
+    for call in range(12):
+        dtype = torch.bfloat16 if call % 3 else torch.float32
+        shapes = [tuple(int(v) for v in rng.integers(1, 700, size=2)) for _ in range(int(rng.integers(2, 7)))]
+        _check_step(shapes, dtype=dtype, seed=6000 + 100 * call, steps=int(rng.integers(1, 9)))
