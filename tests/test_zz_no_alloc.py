@@ -45,6 +45,33 @@ def test_static_scratch_matches_workspace_entry_point_twice():
 
 
 @pytest.mark.gpu
+def test_static_scratch_seeded_fuzz():
+    """30 seeded problems that fit the scratch (random shapes up to 700, both
+    dtypes, 1-12 steps, AUTO), one after another: each equals the workspace
+    entry point bit for bit, and nothing is carried over between calls."""
+    import newton_schulz_04_gb300 as m
+    m.load(build_if_missing=True)
+    lib = m.load()
+    cap = lib.muon_static_scratch_bytes()
+    rng = np.random.default_rng(77)
+    done = 0
+    while done < 30:
+        a, b = (int(v) for v in rng.integers(1, 701, size=2))
+        dtype = torch.bfloat16 if rng.random() < 0.6 else torch.float32
+        steps = int(rng.integers(1, 13))
+        B = int(rng.integers(1, 4))
+        if m.workspace_bytes([(a, b)] * B, steps, dtype) + 4096 > cap:
+            continue
+        X = torch.stack([synth.random_matrix(a, b, seed=7000 + 10 * done + i) for i in range(B)]).to(dtype).cuda()
+        ref = m.ns_batched(X, steps=steps)
+        got = m.ns_batched_static(X, steps=steps)
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref), (done, (a, b), str(dtype), steps, B)
+        assert m.static_status() == 0
+        done += 1
+
+
+@pytest.mark.gpu
 def test_static_scratch_reports_a_timed_out_wait():
     """A kernel that gives up on a bounded wait sets the static scratch's
     status word; muon_static_status reports MUON_ERR_TIMEOUT once, clears the
